@@ -1,0 +1,189 @@
+/*
+ * h3enc — Qwen3-VL text-decoder prefill ("layer-50 encoder" of MiniMax H3) on
+ * one GB300 (sm_103a).  C ABI: plain pointers and sizes, no torch types.
+ *
+ * What one encode computes (page "vllm-omni vllm_omni/diffusion/models/
+ * minimax_h3/encoder.py", MiniMaxH3Qwen3VLTextModel.forward and the classes it
+ * calls; the module docstring states the contract):
+ *   x = embed_tokens[input_ids]
+ *   cos/sin = interleaved 3-D M-RoPE tables of positions[3,S], computed once
+ *   for each kept layer l:
+ *     x = x + o_proj(attn(rope(q_norm(q)), rope(k_norm(k)), v))      q,k,v of input_layernorm(x)
+ *     x = x + down_proj(silu(gate_proj(y)) * up_proj(y)),  y = post_attention_layernorm(x)
+ *     if l < num_deepstack: x[visual rows] += deepstack[l]   (row j -> j-th visual row)
+ *   out = x  (unnormalised hidden_states[num_layers], bf16 [S, hidden])
+ * Attention is causal within each packed sequence (cu_seqlens), GQA with
+ * q head h reading kv head h / (n_heads / n_kv_heads), scale 1/sqrt(head_dim).
+ *
+ * Ownership: the caller owns every input/output buffer and the stream.  The
+ * handle owns a copy of the weights (packed for the kernels) and a workspace
+ * sized at create from max_tokens; encode calls allocate nothing and never
+ * synchronise the host (h3enc_encode_host excepted).
+ *
+ * Errors: every argument, shape and completeness error is detected on the
+ * host before any launch and returned as a status (h3enc_last_error() has the
+ * message).  Errors that only the device can see (token id >= vocab, visual
+ * mask count != n_vis, a bounded device wait that ran out) are recorded in a
+ * device status word; h3enc_get_status() synchronises and reports them.
+ */
+#ifndef H3ENC_H
+#define H3ENC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    H3ENC_OK = 0,
+    H3ENC_WARN_IGNORED = 1,        /* load_weights: name not used by the kept layers (lm_head, final norm,
+                                      layers >= num_layers, vision tower, unknown names) */
+    H3ENC_ERR_INVALID_ARG = 2,     /* null pointer, bad size, bad cu_seqlens, bad config */
+    H3ENC_ERR_SHAPE = 3,           /* weight shape mismatch; visual-mask count != n_vis (device) */
+    H3ENC_ERR_NOT_LOADED = 4,      /* encode before h3enc_finalize_weights succeeded */
+    H3ENC_ERR_MISSING_WEIGHTS = 5, /* finalize: a parameter or a fused shard (q/k/v, gate/up) was never loaded */
+    H3ENC_ERR_UNSUPPORTED = 6,     /* dtype other than bf16 (e.g. serialized FP8), head_dim not 64/128, ... */
+    H3ENC_ERR_CUDA = 7,            /* a CUDA runtime/driver call failed (no device, launch failure) */
+    H3ENC_ERR_OOM = 8,             /* device allocation failed */
+    H3ENC_ERR_DEVICE_TIMEOUT = 9,  /* a bounded device-side wait ran out (reported by h3enc_get_status) */
+    H3ENC_ERR_DEVICE_BOUNDS = 10   /* token id outside [0, vocab) (reported by h3enc_get_status) */
+} h3enc_status;
+
+enum { H3ENC_DTYPE_BF16 = 0, H3ENC_DTYPE_F32 = 1, H3ENC_DTYPE_FP8_E4M3 = 2 };
+
+/* Model and capacity.  Shapes of the Qwen3-VL text config (hidden_size,
+ * num_attention_heads, num_key_value_heads, head_dim, intermediate_size,
+ * vocab_size, rms_norm_eps, rope_theta, mrope_section).  num_layers is the
+ * number of decoder layers kept (50 for the layer-50 contract).
+ * Requirements of this implementation: head_dim in {64, 128}; hidden and
+ * n_heads*head_dim multiples of 64; (n_heads + 2*n_kv_heads)*head_dim and hidden
+ * multiples of 256; intermediate a multiple of 128; n_heads % n_kv_heads == 0.
+ * vocab == 0 builds an embeddings-only model (h3enc_encode_embeds only). */
+typedef struct {
+    int32_t num_layers;
+    int32_t hidden;
+    int32_t n_heads;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t intermediate;
+    int32_t vocab;
+    float rms_eps;
+    float rope_theta;
+    int32_t mrope_section[3];
+    int32_t max_tokens;     /* largest S of one encode (workspace sizing) */
+    int32_t max_seqs;       /* largest number of packed sequences, <= 1024 */
+    int32_t num_deepstack;  /* largest number of DeepStack levels accepted */
+} h3enc_config;
+
+typedef struct h3enc h3enc;
+
+/* Validate cfg, allocate the weight arena and the workspace on the current
+ * CUDA device.  *out is NULL on failure. */
+h3enc_status h3enc_create(const h3enc_config *cfg, h3enc **out);
+
+/* Load one checkpoint tensor by its HF name (page "vllm-omni ... encoder.py",
+ * MiniMaxH3Qwen3VLEncoder._map_weight_name / load_weights):
+ *   model.language_model.embed_tokens.weight                   [vocab, hidden]
+ *   model.language_model.layers.{l}.input_layernorm.weight     [hidden]
+ *   model.language_model.layers.{l}.post_attention_layernorm.weight [hidden]
+ *   model.language_model.layers.{l}.self_attn.{q,k,v}_proj.weight   [n*head_dim, hidden]
+ *   model.language_model.layers.{l}.self_attn.o_proj.weight    [hidden, n_heads*head_dim]
+ *   model.language_model.layers.{l}.self_attn.{q,k}_norm.weight [head_dim]
+ *   model.language_model.layers.{l}.mlp.{gate,up}_proj.weight  [intermediate, hidden]
+ *   model.language_model.layers.{l}.mlp.down_proj.weight       [hidden, intermediate]
+ * q/k/v are packed into one QKV weight and gate/up into one interleaved
+ * weight here.  data: bf16, row-major, host memory (data_on_device=0) or
+ * device memory of the handle's device (1); copied, so the caller may free it
+ * on return.  Returns H3ENC_WARN_IGNORED for names the kept layers do not use,
+ * H3ENC_ERR_SHAPE for a shape mismatch, H3ENC_ERR_UNSUPPORTED for a dtype
+ * other than bf16 (the pages accept online FP8 only, never serialized FP8). */
+h3enc_status h3enc_load_weights(h3enc *h, const char *name, const void *data, int32_t dtype,
+                                const int64_t *shape, int32_t ndim, int32_t data_on_device);
+
+/* Check that every parameter and every fused shard was loaded (page
+ * "... encoder.py", _verify_fused_shards_complete and the missing-parameter
+ * check of load_weights) and prepare the kernels' weight descriptors.
+ * H3ENC_ERR_MISSING_WEIGHTS lists what is missing in h3enc_last_error(). */
+h3enc_status h3enc_finalize_weights(h3enc *h);
+
+/* One encode, asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *   input_ids    device int32 [S]
+ *   positions    device int32 [3, S]  (t, h, w rows)
+ *   visual_mask  device uint8 [S] (nonzero = visual token) or NULL
+ *   deepstack    device bf16 [num_deepstack, n_vis, hidden] or NULL; level l is
+ *                added after layer l at the visual rows, row j to the j-th visual row
+ *   cu_seqlens   HOST int32 [n_seqs + 1], 0 = cu[0] <= ... <= cu[n_seqs] = S, or NULL
+ *                (one sequence); attention is causal within each sequence
+ *   out          device bf16 [S, hidden]; the hidden state lives here during the encode
+ * S == 0 is a no-op.  Inputs are read-only; the buffers must not overlap out. */
+h3enc_status h3enc_encode(h3enc *h, const int32_t *input_ids, const int32_t *positions,
+                          const uint8_t *visual_mask, const void *deepstack, int32_t num_deepstack,
+                          int32_t n_vis, const int32_t *cu_seqlens, int32_t n_seqs, int32_t seq_len,
+                          void *out, void *stream);
+
+/* As h3enc_encode, from hidden states instead of token ids, over the layer
+ * range [layer_begin, layer_end) (global layer indices: DeepStack level l still
+ * follows layer l).  inputs_embeds: device bf16 [S, hidden]; it may equal out. */
+h3enc_status h3enc_encode_embeds(h3enc *h, const void *inputs_embeds, int32_t layer_begin,
+                                 int32_t layer_end, const int32_t *positions,
+                                 const uint8_t *visual_mask, const void *deepstack,
+                                 int32_t num_deepstack, int32_t n_vis, const int32_t *cu_seqlens,
+                                 int32_t n_seqs, int32_t seq_len, void *out, void *stream);
+
+/* As h3enc_encode with HOST buffers (ids, positions, mask, deepstack, out):
+ * copies the inputs to the handle's device staging buffers, encodes, copies
+ * the result back and synchronises `stream`.  Host buffers may be pageable;
+ * pinned buffers copy faster. */
+h3enc_status h3enc_encode_host(h3enc *h, const int32_t *input_ids, const int32_t *positions,
+                               const uint8_t *visual_mask, const void *deepstack,
+                               int32_t num_deepstack, int32_t n_vis, const int32_t *cu_seqlens,
+                               int32_t n_seqs, int32_t seq_len, void *out, void *stream);
+
+/* Record the state after every executed layer: per_layer[l] is a device bf16
+ * [max_tokens, hidden] buffer (or NULL to skip layer l), n == num_layers.
+ * n == 0 disables capture.  The pointers are kept until changed. */
+h3enc_status h3enc_set_layer_capture(h3enc *h, void *const *per_layer, int32_t n);
+
+/* Synchronise the device, read and clear the device status word.  Returns
+ * H3ENC_OK, H3ENC_ERR_DEVICE_TIMEOUT, H3ENC_ERR_DEVICE_BOUNDS or H3ENC_ERR_SHAPE
+ * (the first that applies, in that order). */
+h3enc_status h3enc_get_status(h3enc *h);
+
+/* Message of the last error on this handle (or of the last failed create when
+ * h is NULL).  Valid until the next call on the handle. */
+const char *h3enc_last_error(const h3enc *h);
+
+void h3enc_destroy(h3enc *h);
+
+/* Kernel classes timed by the optional profiler. */
+enum {
+    H3ENC_K_PREP = 0,     /* embedding gather / input copy, M-RoPE tables, visual ranks */
+    H3ENC_K_RMSNORM = 1,
+    H3ENC_K_GEMM_QKV = 2,
+    H3ENC_K_QK_ROPE = 3,
+    H3ENC_K_ATTN = 4,
+    H3ENC_K_GEMM_O = 5,
+    H3ENC_K_GEMM_GATE_UP = 6,
+    H3ENC_K_GEMM_DOWN = 7,
+    H3ENC_K_COUNT = 8
+};
+
+/* enable != 0: record a CUDA event pair around every kernel launch (on the
+ * launching stream) and accumulate per-class device time.  Resets totals. */
+h3enc_status h3enc_set_profiling(h3enc *h, int32_t enable);
+
+/* Synchronise and return per-class totals since the last reset:
+ * ms[k], launches[k] for k < n (n <= H3ENC_K_COUNT).  Resets totals. */
+h3enc_status h3enc_get_profile(h3enc *h, double *ms, int64_t *launches, int32_t n);
+
+/* Number of kernels this handle has launched since create. */
+int64_t h3enc_launch_count(const h3enc *h);
+
+/* Number of streaming multiprocessors the handle's kernels size their grids by. */
+int32_t h3enc_num_sms(const h3enc *h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* H3ENC_H */

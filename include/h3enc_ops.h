@@ -1,0 +1,97 @@
+/*
+ * h3enc op-level entry points: each step of the encode as its own call, for
+ * parity tests and kernel benchmarks.  The encode (h3enc.h) launches exactly
+ * these kernels.  All pointers are device pointers unless marked HOST; all
+ * matrices are row-major bf16 with the stated leading dimension; `stream` is
+ * a cudaStream_t (NULL = legacy default).  `status` is an optional device
+ * int32 that kernels OR error bits into (1 = bounded wait ran out, 2 = index
+ * out of bounds, 4 = visual count mismatch); NULL disables recording.
+ * Return: H3ENC_OK, H3ENC_ERR_INVALID_ARG (checked before launch) or
+ * H3ENC_ERR_CUDA (launch failed).
+ */
+#ifndef H3ENC_OPS_H
+#define H3ENC_OPS_H
+
+#include <stdint.h>
+#include "h3enc.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* GEMM epilogues of the projection kernel C = A * W^T (fp32 accumulation). */
+enum {
+    H3ENC_EPI_STORE = 0,       /* C = bf16(acc)                                   (QKV projection) */
+    H3ENC_EPI_RESIDUAL = 1,    /* C = bf16(R + acc); R may equal C                (o_proj + residual) */
+    H3ENC_EPI_SWIGLU = 2,      /* W packed by h3enc_op_pack_gate_up (N = 2*I rows):
+                                  C[:, i] = bf16(silu(gate_i) * up_i), C has I columns (gate/up + SwiGLU) */
+    H3ENC_EPI_RESIDUAL_DS = 3  /* C = bf16(R + acc), then at rows with vis_rank[r] = j in [0, n_vis):
+                                  C = bf16(C + DS[j])                             (down_proj + residual + DeepStack) */
+};
+
+/* Projection GEMM on the tcgen05 tensor cores (page "vllm-omni ... encoder.py":
+ * F.linear of the QKV, o, gate/up and down projections, plus the residual adds
+ * of MiniMaxH3Qwen3VLTextDecoderLayer.forward and _deepstack_process).
+ *   A [M, K] (lda = K), W [N, K] (ldw = K), C [M, ldc]: ldc = N, or N/2 for SWIGLU.
+ *   R [M, ldc] residual (RESIDUAL*), DS [n_vis, ldc] and vis_rank [M] (RESIDUAL_DS).
+ * Requires K % 8 == 0, N % 256 == 0 (of the packed weight for SWIGLU), A and W
+ * 16-byte aligned.  M may be any size >= 0. */
+h3enc_status h3enc_op_gemm(const void *A, const void *W, void *C, int32_t M, int32_t N, int32_t K,
+                           int32_t epilogue, const void *R, const void *DS, const int32_t *vis_rank,
+                           int32_t n_vis, int32_t *status, void *stream);
+
+/* Pack gate [I, K] and up [I, K] into W [2I, K] for H3ENC_EPI_SWIGLU: rows
+ * [256b, 256b+128) = gate rows [128b, 128b+128), rows [256b+128, 256b+256) =
+ * up rows [128b, 128b+128).  Requires I % 128 == 0. */
+h3enc_status h3enc_op_pack_gate_up(const void *gate, const void *up, void *W, int32_t I, int32_t K,
+                                   void *stream);
+
+/* y = bf16(w * x / sqrt(mean(x^2) + eps)) per row, fp32 math (page "...
+ * encoder.py", MiniMaxH3Qwen3VLRMSNorm).  x, y [rows, cols]; cols % 8 == 0,
+ * cols <= 8192; y may equal x. */
+h3enc_status h3enc_op_rmsnorm(const void *x, const void *w, void *y, int32_t rows, int32_t cols,
+                              float eps, void *stream);
+
+/* M-RoPE tables (page "... encoder.py", MiniMaxH3Qwen3VLTextRotaryEmbedding and
+ * _apply_interleaved_mrope): for j < head_dim/2,
+ *   ang = float(positions[axis(j)][s]) * inv_freq[j],  inv_freq[j] = theta^(-2j/head_dim) (fp32),
+ *   axis(j) = 1 if j%3==1 and j < 3*section[1]; 2 if j%3==2 and j < 3*section[2]; else 0,
+ *   cos_tab[s][j] = cos(ang), sin_tab[s][j] = sin(ang)   (fp32, [S, head_dim/2]). */
+h3enc_status h3enc_op_rope_table(const int32_t *positions, int32_t S, int32_t head_dim, float theta,
+                                 const int32_t *section_host, float *cos_tab, float *sin_tab,
+                                 void *stream);
+
+/* In place on qkv [S, (nq + 2*nkv)*head_dim]: every q head (columns h*d) and k
+ * head (columns (nq + g)*d) becomes rope(rmsnorm(x, w_q or w_k)) with
+ * rope(x)[j] = x[j]*cos[j] - x[j+d/2]*sin[j], rope(x)[j+d/2] = x[j+d/2]*cos[j] + x[j]*sin[j]
+ * (page "... encoder.py", q_norm/k_norm then _apply_rotary_pos_emb).  v heads untouched. */
+h3enc_status h3enc_op_qk_norm_rope(void *qkv, int32_t S, int32_t n_heads, int32_t n_kv_heads,
+                                   int32_t head_dim, const void *w_q, const void *w_k, float eps,
+                                   const float *cos_tab, const float *sin_tab, void *stream);
+
+/* Causal GQA attention over packed sequences (page "... encoder.py",
+ * MiniMaxH3Qwen3VLTextAttention.forward: repeat_interleave of K/V, SDPA with
+ * is_causal=True, scale 1/sqrt(d)).  Reads q/k/v from qkv [S, (nq+2nkv)*d]
+ * (q head h at column h*d, k head g at (nq+g)*d, v head g at (nq+nkv+g)*d),
+ * writes o [S, nq*d] (head h at column h*d).  cu_seqlens HOST int32 [n_seqs+1]
+ * or NULL (one sequence); n_seqs <= 1024. */
+h3enc_status h3enc_op_attention(const void *qkv, void *o, int32_t S, int32_t n_heads,
+                                int32_t n_kv_heads, int32_t head_dim, const int32_t *cu_seqlens,
+                                int32_t n_seqs, void *stream);
+
+/* out[s] = table[ids[s]] (bit-exact row copy; page "... encoder.py",
+ * embed_tokens / F.embedding).  Ids outside [0, vocab) give a zero row and
+ * set status bit 2.  hidden % 8 == 0. */
+h3enc_status h3enc_op_embed(const int32_t *ids, const void *table, int32_t vocab, int32_t hidden,
+                            void *out, int32_t S, int32_t *status, void *stream);
+
+/* vis_rank[s] = number of visual rows before s if mask[s] != 0, else -1 (the
+ * row of the DeepStack features that boolean-mask assignment gives row s).
+ * Sets status bit 4 if the mask holds a count other than n_vis. */
+h3enc_status h3enc_op_vis_rank(const uint8_t *mask, int32_t S, int32_t n_vis, int32_t *vis_rank,
+                               int32_t *status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* H3ENC_OPS_H */
