@@ -31,6 +31,12 @@
 
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define H3ENC_API __attribute__((visibility("default")))
+#else
+#define H3ENC_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -80,7 +86,7 @@ typedef struct h3enc h3enc;
 
 /* Validate cfg, allocate the weight arena and the workspace on the current
  * CUDA device.  *out is NULL on failure. */
-h3enc_status h3enc_create(const h3enc_config *cfg, h3enc **out);
+H3ENC_API h3enc_status h3enc_create(const h3enc_config *cfg, h3enc **out);
 
 /* Load one checkpoint tensor by its HF name (page "vllm-omni ... encoder.py",
  * MiniMaxH3Qwen3VLEncoder._map_weight_name / load_weights):
@@ -98,14 +104,14 @@ h3enc_status h3enc_create(const h3enc_config *cfg, h3enc **out);
  * on return.  Returns H3ENC_WARN_IGNORED for names the kept layers do not use,
  * H3ENC_ERR_SHAPE for a shape mismatch, H3ENC_ERR_UNSUPPORTED for a dtype
  * other than bf16 (the pages accept online FP8 only, never serialized FP8). */
-h3enc_status h3enc_load_weights(h3enc *h, const char *name, const void *data, int32_t dtype,
+H3ENC_API h3enc_status h3enc_load_weights(h3enc *h, const char *name, const void *data, int32_t dtype,
                                 const int64_t *shape, int32_t ndim, int32_t data_on_device);
 
 /* Check that every parameter and every fused shard was loaded (page
  * "... encoder.py", _verify_fused_shards_complete and the missing-parameter
  * check of load_weights) and prepare the kernels' weight descriptors.
  * H3ENC_ERR_MISSING_WEIGHTS lists what is missing in h3enc_last_error(). */
-h3enc_status h3enc_finalize_weights(h3enc *h);
+H3ENC_API h3enc_status h3enc_finalize_weights(h3enc *h);
 
 /* One encode, asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
  *   input_ids    device int32 [S]
@@ -117,7 +123,7 @@ h3enc_status h3enc_finalize_weights(h3enc *h);
  *                (one sequence); attention is causal within each sequence
  *   out          device bf16 [S, hidden]; the hidden state lives here during the encode
  * S == 0 is a no-op.  Inputs are read-only; the buffers must not overlap out. */
-h3enc_status h3enc_encode(h3enc *h, const int32_t *input_ids, const int32_t *positions,
+H3ENC_API h3enc_status h3enc_encode(h3enc *h, const int32_t *input_ids, const int32_t *positions,
                           const uint8_t *visual_mask, const void *deepstack, int32_t num_deepstack,
                           int32_t n_vis, const int32_t *cu_seqlens, int32_t n_seqs, int32_t seq_len,
                           void *out, void *stream);
@@ -125,7 +131,7 @@ h3enc_status h3enc_encode(h3enc *h, const int32_t *input_ids, const int32_t *pos
 /* As h3enc_encode, from hidden states instead of token ids, over the layer
  * range [layer_begin, layer_end) (global layer indices: DeepStack level l still
  * follows layer l).  inputs_embeds: device bf16 [S, hidden]; it may equal out. */
-h3enc_status h3enc_encode_embeds(h3enc *h, const void *inputs_embeds, int32_t layer_begin,
+H3ENC_API h3enc_status h3enc_encode_embeds(h3enc *h, const void *inputs_embeds, int32_t layer_begin,
                                  int32_t layer_end, const int32_t *positions,
                                  const uint8_t *visual_mask, const void *deepstack,
                                  int32_t num_deepstack, int32_t n_vis, const int32_t *cu_seqlens,
@@ -135,7 +141,7 @@ h3enc_status h3enc_encode_embeds(h3enc *h, const void *inputs_embeds, int32_t la
  * copies the inputs to the handle's device staging buffers, encodes, copies
  * the result back and synchronises `stream`.  Host buffers may be pageable;
  * pinned buffers copy faster. */
-h3enc_status h3enc_encode_host(h3enc *h, const int32_t *input_ids, const int32_t *positions,
+H3ENC_API h3enc_status h3enc_encode_host(h3enc *h, const int32_t *input_ids, const int32_t *positions,
                                const uint8_t *visual_mask, const void *deepstack,
                                int32_t num_deepstack, int32_t n_vis, const int32_t *cu_seqlens,
                                int32_t n_seqs, int32_t seq_len, void *out, void *stream);
@@ -143,18 +149,18 @@ h3enc_status h3enc_encode_host(h3enc *h, const int32_t *input_ids, const int32_t
 /* Record the state after every executed layer: per_layer[l] is a device bf16
  * [max_tokens, hidden] buffer (or NULL to skip layer l), n == num_layers.
  * n == 0 disables capture.  The pointers are kept until changed. */
-h3enc_status h3enc_set_layer_capture(h3enc *h, void *const *per_layer, int32_t n);
+H3ENC_API h3enc_status h3enc_set_layer_capture(h3enc *h, void *const *per_layer, int32_t n);
 
 /* Synchronise the device, read and clear the device status word.  Returns
  * H3ENC_OK, H3ENC_ERR_DEVICE_TIMEOUT, H3ENC_ERR_DEVICE_BOUNDS or H3ENC_ERR_SHAPE
  * (the first that applies, in that order). */
-h3enc_status h3enc_get_status(h3enc *h);
+H3ENC_API h3enc_status h3enc_get_status(h3enc *h);
 
 /* Message of the last error on this handle (or of the last failed create when
  * h is NULL).  Valid until the next call on the handle. */
-const char *h3enc_last_error(const h3enc *h);
+H3ENC_API const char *h3enc_last_error(const h3enc *h);
 
-void h3enc_destroy(h3enc *h);
+H3ENC_API void h3enc_destroy(h3enc *h);
 
 /* Kernel classes timed by the optional profiler. */
 enum {
@@ -171,17 +177,17 @@ enum {
 
 /* enable != 0: record a CUDA event pair around every kernel launch (on the
  * launching stream) and accumulate per-class device time.  Resets totals. */
-h3enc_status h3enc_set_profiling(h3enc *h, int32_t enable);
+H3ENC_API h3enc_status h3enc_set_profiling(h3enc *h, int32_t enable);
 
 /* Synchronise and return per-class totals since the last reset:
  * ms[k], launches[k] for k < n (n <= H3ENC_K_COUNT).  Resets totals. */
-h3enc_status h3enc_get_profile(h3enc *h, double *ms, int64_t *launches, int32_t n);
+H3ENC_API h3enc_status h3enc_get_profile(h3enc *h, double *ms, int64_t *launches, int32_t n);
 
 /* Number of kernels this handle has launched since create. */
-int64_t h3enc_launch_count(const h3enc *h);
+H3ENC_API int64_t h3enc_launch_count(const h3enc *h);
 
 /* Number of streaming multiprocessors the handle's kernels size their grids by. */
-int32_t h3enc_num_sms(const h3enc *h);
+H3ENC_API int32_t h3enc_num_sms(const h3enc *h);
 
 #ifdef __cplusplus
 }

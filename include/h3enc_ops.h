@@ -36,20 +36,20 @@ enum {
  *   R [M, ldc] residual (RESIDUAL*), DS [n_vis, ldc] and vis_rank [M] (RESIDUAL_DS).
  * Requires K % 8 == 0, N % 256 == 0 (of the packed weight for SWIGLU), A and W
  * 16-byte aligned.  M may be any size >= 0. */
-h3enc_status h3enc_op_gemm(const void *A, const void *W, void *C, int32_t M, int32_t N, int32_t K,
+H3ENC_API h3enc_status h3enc_op_gemm(const void *A, const void *W, void *C, int32_t M, int32_t N, int32_t K,
                            int32_t epilogue, const void *R, const void *DS, const int32_t *vis_rank,
                            int32_t n_vis, int32_t *status, void *stream);
 
 /* Pack gate [I, K] and up [I, K] into W [2I, K] for H3ENC_EPI_SWIGLU: rows
  * [256b, 256b+128) = gate rows [128b, 128b+128), rows [256b+128, 256b+256) =
  * up rows [128b, 128b+128).  Requires I % 128 == 0. */
-h3enc_status h3enc_op_pack_gate_up(const void *gate, const void *up, void *W, int32_t I, int32_t K,
+H3ENC_API h3enc_status h3enc_op_pack_gate_up(const void *gate, const void *up, void *W, int32_t I, int32_t K,
                                    void *stream);
 
 /* y = bf16(w * x / sqrt(mean(x^2) + eps)) per row, fp32 math (page "...
  * encoder.py", MiniMaxH3Qwen3VLRMSNorm).  x, y [rows, cols]; cols % 8 == 0,
  * cols <= 8192; y may equal x. */
-h3enc_status h3enc_op_rmsnorm(const void *x, const void *w, void *y, int32_t rows, int32_t cols,
+H3ENC_API h3enc_status h3enc_op_rmsnorm(const void *x, const void *w, void *y, int32_t rows, int32_t cols,
                               float eps, void *stream);
 
 /* M-RoPE tables (page "... encoder.py", MiniMaxH3Qwen3VLTextRotaryEmbedding and
@@ -57,7 +57,7 @@ h3enc_status h3enc_op_rmsnorm(const void *x, const void *w, void *y, int32_t row
  *   ang = float(positions[axis(j)][s]) * inv_freq[j],  inv_freq[j] = theta^(-2j/head_dim) (fp32),
  *   axis(j) = 1 if j%3==1 and j < 3*section[1]; 2 if j%3==2 and j < 3*section[2]; else 0,
  *   cos_tab[s][j] = cos(ang), sin_tab[s][j] = sin(ang)   (fp32, [S, head_dim/2]). */
-h3enc_status h3enc_op_rope_table(const int32_t *positions, int32_t S, int32_t head_dim, float theta,
+H3ENC_API h3enc_status h3enc_op_rope_table(const int32_t *positions, int32_t S, int32_t head_dim, float theta,
                                  const int32_t *section_host, float *cos_tab, float *sin_tab,
                                  void *stream);
 
@@ -65,7 +65,7 @@ h3enc_status h3enc_op_rope_table(const int32_t *positions, int32_t S, int32_t he
  * head (columns (nq + g)*d) becomes rope(rmsnorm(x, w_q or w_k)) with
  * rope(x)[j] = x[j]*cos[j] - x[j+d/2]*sin[j], rope(x)[j+d/2] = x[j+d/2]*cos[j] + x[j]*sin[j]
  * (page "... encoder.py", q_norm/k_norm then _apply_rotary_pos_emb).  v heads untouched. */
-h3enc_status h3enc_op_qk_norm_rope(void *qkv, int32_t S, int32_t n_heads, int32_t n_kv_heads,
+H3ENC_API h3enc_status h3enc_op_qk_norm_rope(void *qkv, int32_t S, int32_t n_heads, int32_t n_kv_heads,
                                    int32_t head_dim, const void *w_q, const void *w_k, float eps,
                                    const float *cos_tab, const float *sin_tab, void *stream);
 
@@ -75,20 +75,20 @@ h3enc_status h3enc_op_qk_norm_rope(void *qkv, int32_t S, int32_t n_heads, int32_
  * (q head h at column h*d, k head g at (nq+g)*d, v head g at (nq+nkv+g)*d),
  * writes o [S, nq*d] (head h at column h*d).  cu_seqlens HOST int32 [n_seqs+1]
  * or NULL (one sequence); n_seqs <= 1024. */
-h3enc_status h3enc_op_attention(const void *qkv, void *o, int32_t S, int32_t n_heads,
+H3ENC_API h3enc_status h3enc_op_attention(const void *qkv, void *o, int32_t S, int32_t n_heads,
                                 int32_t n_kv_heads, int32_t head_dim, const int32_t *cu_seqlens,
                                 int32_t n_seqs, void *stream);
 
 /* out[s] = table[ids[s]] (bit-exact row copy; page "... encoder.py",
  * embed_tokens / F.embedding).  Ids outside [0, vocab) give a zero row and
  * set status bit 2.  hidden % 8 == 0. */
-h3enc_status h3enc_op_embed(const int32_t *ids, const void *table, int32_t vocab, int32_t hidden,
+H3ENC_API h3enc_status h3enc_op_embed(const int32_t *ids, const void *table, int32_t vocab, int32_t hidden,
                             void *out, int32_t S, int32_t *status, void *stream);
 
 /* vis_rank[s] = number of visual rows before s if mask[s] != 0, else -1 (the
  * row of the DeepStack features that boolean-mask assignment gives row s).
  * Sets status bit 4 if the mask holds a count other than n_vis. */
-h3enc_status h3enc_op_vis_rank(const uint8_t *mask, int32_t S, int32_t n_vis, int32_t *vis_rank,
+H3ENC_API h3enc_status h3enc_op_vis_rank(const uint8_t *mask, int32_t S, int32_t n_vis, int32_t *vis_rank,
                                int32_t *status, void *stream);
 
 #ifdef __cplusplus

@@ -1,0 +1,289 @@
+"""qwen3_vl_text_gb300 — Qwen3-VL text-decoder prefill (MiniMax H3 layer-50
+encoder) on one GB300.
+
+Thin ctypes binding over ``libh3enc.so`` (C ABI in ``include/h3enc.h`` and
+``include/h3enc_ops.h``): the functions below carry the C names and only
+marshal arguments (device pointers from torch tensors, the current CUDA
+stream).  Every step of the encode runs in the library's CUDA kernels; if the
+library cannot be loaded, importing the binding raises — there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "lib", "H3encError", "Config", "STATUS", "EPI_STORE", "EPI_RESIDUAL", "EPI_SWIGLU", "EPI_RESIDUAL_DS",
+    "h3enc_create", "h3enc_load_weights", "h3enc_finalize_weights", "h3enc_encode", "h3enc_encode_embeds",
+    "h3enc_encode_host", "h3enc_set_layer_capture", "h3enc_get_status", "h3enc_last_error", "h3enc_destroy",
+    "h3enc_set_profiling", "h3enc_get_profile", "h3enc_launch_count", "h3enc_num_sms",
+    "h3enc_op_gemm", "h3enc_op_pack_gate_up", "h3enc_op_rmsnorm", "h3enc_op_rope_table",
+    "h3enc_op_qk_norm_rope", "h3enc_op_attention", "h3enc_op_embed", "h3enc_op_vis_rank", "Encoder",
+    "KERNEL_CLASSES",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libh3enc.so")
+
+STATUS = {0: "OK", 1: "WARN_IGNORED", 2: "ERR_INVALID_ARG", 3: "ERR_SHAPE", 4: "ERR_NOT_LOADED",
+          5: "ERR_MISSING_WEIGHTS", 6: "ERR_UNSUPPORTED", 7: "ERR_CUDA", 8: "ERR_OOM",
+          9: "ERR_DEVICE_TIMEOUT", 10: "ERR_DEVICE_BOUNDS"}
+EPI_STORE, EPI_RESIDUAL, EPI_SWIGLU, EPI_RESIDUAL_DS = 0, 1, 2, 3
+KERNEL_CLASSES = ["prep", "rmsnorm", "gemm_qkv", "qk_rope", "attention", "gemm_o", "gemm_gate_up", "gemm_down"]
+
+
+class H3encError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"h3enc {STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("hidden", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("intermediate", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
+                ("mrope_section", ctypes.c_int32 * 3), ("max_tokens", ctypes.c_int32),
+                ("max_seqs", ctypes.c_int32), ("num_deepstack", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with qwen3_vl_text_gb300.build.build()")
+    return ctypes.CDLL(LIB_PATH)
+
+
+lib = _load()
+
+_P, _I32, _I64, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+_SIGS = {
+    "h3enc_create": ([ctypes.POINTER(Config), ctypes.POINTER(_P)], _I32),
+    "h3enc_load_weights": ([_P, ctypes.c_char_p, _P, _I32, ctypes.POINTER(_I64), _I32, _I32], _I32),
+    "h3enc_finalize_weights": ([_P], _I32),
+    "h3enc_encode": ([_P, _P, _P, _P, _P, _I32, _I32, _P, _I32, _I32, _P, _P], _I32),
+    "h3enc_encode_embeds": ([_P, _P, _I32, _I32, _P, _P, _P, _I32, _I32, _P, _I32, _I32, _P, _P], _I32),
+    "h3enc_encode_host": ([_P, _P, _P, _P, _P, _I32, _I32, _P, _I32, _I32, _P, _P], _I32),
+    "h3enc_set_layer_capture": ([_P, ctypes.POINTER(_P), _I32], _I32),
+    "h3enc_get_status": ([_P], _I32),
+    "h3enc_last_error": ([_P], ctypes.c_char_p),
+    "h3enc_destroy": ([_P], None),
+    "h3enc_set_profiling": ([_P, _I32], _I32),
+    "h3enc_get_profile": ([_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I64), _I32], _I32),
+    "h3enc_launch_count": ([_P], _I64),
+    "h3enc_num_sms": ([_P], _I32),
+    "h3enc_op_gemm": ([_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _P], _I32),
+    "h3enc_op_pack_gate_up": ([_P, _P, _P, _I32, _I32, _P], _I32),
+    "h3enc_op_rmsnorm": ([_P, _P, _P, _I32, _I32, _F, _P], _I32),
+    "h3enc_op_rope_table": ([_P, _I32, _I32, _F, ctypes.POINTER(_I32), _P, _P, _P], _I32),
+    "h3enc_op_qk_norm_rope": ([_P, _I32, _I32, _I32, _I32, _P, _P, _F, _P, _P, _P], _I32),
+    "h3enc_op_attention": ([_P, _P, _I32, _I32, _I32, _I32, _P, _I32, _P], _I32),
+    "h3enc_op_embed": ([_P, _P, _I32, _I32, _P, _I32, _P, _P], _I32),
+    "h3enc_op_vis_rank": ([_P, _I32, _I32, _P, _P, _P], _I32),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _fn = getattr(lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _res
+
+
+# ---------------------------------------------------------------- marshalling helpers
+
+def _ptr(t):
+    """Device/host address of a tensor, an int address, or None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def _host_i32(a):
+    """ctypes int32 array from a sequence (HOST cu_seqlens / sections)."""
+    if a is None:
+        return None
+    vals = [int(x) for x in a]
+    return (ctypes.c_int32 * len(vals))(*vals)
+
+
+def _check(code, handle=None):
+    if code not in (0, 1):
+        msg = lib.h3enc_last_error(handle)
+        raise H3encError(code, msg.decode() if msg else "")
+    return code
+
+
+# ---------------------------------------------------------------- C-named calls
+
+def h3enc_create(cfg: Config):
+    h = _P()
+    _check(lib.h3enc_create(ctypes.byref(cfg), ctypes.byref(h)))
+    return h.value
+
+
+def h3enc_load_weights(h, name: str, tensor, data_on_device: bool = True):
+    shape = (_I64 * tensor.dim())(*tensor.shape)
+    return _check(lib.h3enc_load_weights(h, name.encode(), _ptr(tensor), 0, shape, tensor.dim(),
+                                         1 if data_on_device else 0), h)
+
+
+def h3enc_finalize_weights(h):
+    return _check(lib.h3enc_finalize_weights(h), h)
+
+
+def h3enc_encode(h, input_ids, positions, visual_mask, deepstack, num_deepstack, n_vis, cu_seqlens, seq_len,
+                 out, stream=None):
+    cu = _host_i32(cu_seqlens)
+    n_seqs = len(cu) - 1 if cu is not None else 0
+    return _check(lib.h3enc_encode(h, _ptr(input_ids), _ptr(positions), _ptr(visual_mask), _ptr(deepstack),
+                                   num_deepstack, n_vis, cu, n_seqs, seq_len, _ptr(out), _stream(stream)), h)
+
+
+def h3enc_encode_embeds(h, inputs_embeds, layer_begin, layer_end, positions, visual_mask, deepstack,
+                        num_deepstack, n_vis, cu_seqlens, seq_len, out, stream=None):
+    cu = _host_i32(cu_seqlens)
+    n_seqs = len(cu) - 1 if cu is not None else 0
+    return _check(lib.h3enc_encode_embeds(h, _ptr(inputs_embeds), layer_begin, layer_end, _ptr(positions),
+                                          _ptr(visual_mask), _ptr(deepstack), num_deepstack, n_vis, cu, n_seqs,
+                                          seq_len, _ptr(out), _stream(stream)), h)
+
+
+def h3enc_encode_host(h, input_ids, positions, visual_mask, deepstack, num_deepstack, n_vis, cu_seqlens, seq_len,
+                      out, stream=None):
+    cu = _host_i32(cu_seqlens)
+    n_seqs = len(cu) - 1 if cu is not None else 0
+    return _check(lib.h3enc_encode_host(h, _ptr(input_ids), _ptr(positions), _ptr(visual_mask), _ptr(deepstack),
+                                        num_deepstack, n_vis, cu, n_seqs, seq_len, _ptr(out), _stream(stream)), h)
+
+
+def h3enc_set_layer_capture(h, tensors):
+    ptrs = (_P * len(tensors))(*[_ptr(t) for t in tensors]) if tensors else None
+    return _check(lib.h3enc_set_layer_capture(h, ptrs, len(tensors) if tensors else 0), h)
+
+
+def h3enc_get_status(h):
+    return lib.h3enc_get_status(h)
+
+
+def h3enc_last_error(h=None) -> str:
+    m = lib.h3enc_last_error(h)
+    return m.decode() if m else ""
+
+
+def h3enc_destroy(h):
+    lib.h3enc_destroy(h)
+
+
+def h3enc_set_profiling(h, enable: bool):
+    return _check(lib.h3enc_set_profiling(h, 1 if enable else 0), h)
+
+
+def h3enc_get_profile(h):
+    n = len(KERNEL_CLASSES)
+    ms = (ctypes.c_double * n)()
+    cnt = (_I64 * n)()
+    _check(lib.h3enc_get_profile(h, ms, cnt, n), h)
+    return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_CLASSES)}
+
+
+def h3enc_launch_count(h) -> int:
+    return lib.h3enc_launch_count(h)
+
+
+def h3enc_num_sms(h) -> int:
+    return lib.h3enc_num_sms(h)
+
+
+def h3enc_op_gemm(A, W, C, M, N, K, epilogue, R=None, DS=None, vis_rank=None, n_vis=0, status=None, stream=None):
+    return _check(lib.h3enc_op_gemm(_ptr(A), _ptr(W), _ptr(C), M, N, K, epilogue, _ptr(R), _ptr(DS),
+                                    _ptr(vis_rank), n_vis, _ptr(status), _stream(stream)))
+
+
+def h3enc_op_pack_gate_up(gate, up, W, I, K, stream=None):
+    return _check(lib.h3enc_op_pack_gate_up(_ptr(gate), _ptr(up), _ptr(W), I, K, _stream(stream)))
+
+
+def h3enc_op_rmsnorm(x, w, y, rows, cols, eps, stream=None):
+    return _check(lib.h3enc_op_rmsnorm(_ptr(x), _ptr(w), _ptr(y), rows, cols, eps, _stream(stream)))
+
+
+def h3enc_op_rope_table(positions, S, head_dim, theta, section, cos_tab, sin_tab, stream=None):
+    return _check(lib.h3enc_op_rope_table(_ptr(positions), S, head_dim, theta, _host_i32(section), _ptr(cos_tab),
+                                          _ptr(sin_tab), _stream(stream)))
+
+
+def h3enc_op_qk_norm_rope(qkv, S, n_heads, n_kv_heads, head_dim, w_q, w_k, eps, cos_tab, sin_tab, stream=None):
+    return _check(lib.h3enc_op_qk_norm_rope(_ptr(qkv), S, n_heads, n_kv_heads, head_dim, _ptr(w_q), _ptr(w_k), eps,
+                                            _ptr(cos_tab), _ptr(sin_tab), _stream(stream)))
+
+
+def h3enc_op_attention(qkv, o, S, n_heads, n_kv_heads, head_dim, cu_seqlens=None, stream=None):
+    cu = _host_i32(cu_seqlens)
+    n_seqs = len(cu) - 1 if cu is not None else 0
+    return _check(lib.h3enc_op_attention(_ptr(qkv), _ptr(o), S, n_heads, n_kv_heads, head_dim, cu, n_seqs,
+                                         _stream(stream)))
+
+
+def h3enc_op_embed(ids, table, vocab, hidden, out, S, status=None, stream=None):
+    return _check(lib.h3enc_op_embed(_ptr(ids), _ptr(table), vocab, hidden, _ptr(out), S, _ptr(status),
+                                     _stream(stream)))
+
+
+def h3enc_op_vis_rank(mask, S, n_vis, vis_rank, status=None, stream=None):
+    return _check(lib.h3enc_op_vis_rank(_ptr(mask), S, n_vis, _ptr(vis_rank), _ptr(status), _stream(stream)))
+
+
+# ---------------------------------------------------------------- convenience wrapper
+
+class Encoder:
+    """Owns one h3enc handle.  ``model`` is any object with the Qwen3-VL text
+    config attributes (num_layers, hidden, n_heads, n_kv_heads, head_dim,
+    intermediate, vocab, rms_eps, rope_theta, mrope_section)."""
+
+    def __init__(self, model, max_tokens: int, max_seqs: int = 64, num_deepstack: int = 3):
+        c = Config()
+        c.num_layers, c.hidden, c.n_heads = model.num_layers, model.hidden, model.n_heads
+        c.n_kv_heads, c.head_dim, c.intermediate = model.n_kv_heads, model.head_dim, model.intermediate
+        c.vocab, c.rms_eps, c.rope_theta = model.vocab, model.rms_eps, model.rope_theta
+        c.mrope_section = (ctypes.c_int32 * 3)(*model.mrope_section)
+        c.max_tokens, c.max_seqs, c.num_deepstack = max_tokens, max_seqs, num_deepstack
+        self.model = model
+        self.handle = h3enc_create(c)
+
+    def load(self, name, tensor):
+        return h3enc_load_weights(self.handle, name, tensor, tensor.is_cuda)
+
+    def finalize(self):
+        return h3enc_finalize_weights(self.handle)
+
+    def encode(self, input_ids, positions, out, visual_mask=None, deepstack=None, n_vis=0, cu_seqlens=None,
+               stream=None):
+        nds = 0 if deepstack is None else int(deepstack.shape[0])
+        return h3enc_encode(self.handle, input_ids, positions, visual_mask, deepstack, nds, n_vis, cu_seqlens,
+                            int(positions.shape[1]), out, stream)
+
+    def encode_embeds(self, inputs_embeds, positions, out, layer_begin=0, layer_end=None, visual_mask=None,
+                      deepstack=None, n_vis=0, cu_seqlens=None, stream=None):
+        nds = 0 if deepstack is None else int(deepstack.shape[0])
+        le = self.model.num_layers if layer_end is None else layer_end
+        return h3enc_encode_embeds(self.handle, inputs_embeds, layer_begin, le, positions, visual_mask, deepstack,
+                                   nds, n_vis, cu_seqlens, int(positions.shape[1]), out, stream)
+
+    def status(self):
+        return h3enc_get_status(self.handle)
+
+    def close(self):
+        if self.handle:
+            h3enc_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,726 @@
+// C ABI of the encoder: handle, weight loading and packing, encode orchestration.
+//
+// One encode enqueues, on the caller's stream and without host synchronisation:
+//   embedding gather (or input copy) -> M-RoPE tables -> visual ranks (if DeepStack)
+//   per layer: RMSNorm -> QKV GEMM -> q/k RMSNorm + M-RoPE -> attention ->
+//              o GEMM (+residual) -> RMSNorm -> gate/up GEMM (SwiGLU) ->
+//              down GEMM (+residual, +DeepStack for layers < levels)
+// following MiniMaxH3Qwen3VLTextModel.forward and MiniMaxH3Qwen3VLTextDecoderLayer.
+// forward (page "vllm-omni vllm_omni/diffusion/models/minimax_h3/encoder.py").
+// The hidden state lives in the caller's output buffer for the whole encode.
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/h3enc.h"
+#include "../../include/h3enc_ops.h"
+#include "kernels.h"
+
+using h3::bf16;
+
+namespace {
+
+enum { T_IN = 0, T_Q, T_K, T_V, T_QN, T_KN, T_O, T_POST, T_GATE, T_UP, T_DOWN, T_COUNT };
+const char *kSuffix[T_COUNT] = {
+    "input_layernorm.weight", "self_attn.q_proj.weight", "self_attn.k_proj.weight", "self_attn.v_proj.weight",
+    "self_attn.q_norm.weight", "self_attn.k_norm.weight", "self_attn.o_proj.weight",
+    "post_attention_layernorm.weight", "mlp.gate_proj.weight", "mlp.up_proj.weight", "mlp.down_proj.weight"};
+
+struct LayerW {
+    bf16 *qkv = nullptr, *o = nullptr, *gu = nullptr, *down = nullptr;
+    bf16 *in_norm = nullptr, *post_norm = nullptr, *q_norm = nullptr, *k_norm = nullptr;
+    CUtensorMap tm_qkv, tm_o, tm_gu, tm_down;
+    uint32_t loaded = 0;
+};
+
+thread_local std::string g_create_error;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+struct h3enc {
+    h3enc_config cfg;
+    int device = 0;
+    int num_sms = 0;
+    int qkv_out = 0;
+    h3::RopeParams rope;
+    char *arena = nullptr;
+    bf16 *embed = nullptr;
+    bool embed_loaded = false;
+    std::vector<LayerW> layers;
+    char *ws = nullptr;
+    bf16 *y = nullptr, *qkv = nullptr, *attn = nullptr, *act = nullptr;
+    float *cos_t = nullptr, *sin_t = nullptr;
+    int32_t *vis_rank = nullptr, *status = nullptr;
+    int32_t *st_ids = nullptr, *st_pos = nullptr;
+    uint8_t *st_mask = nullptr;
+    bf16 *st_ds = nullptr, *st_out = nullptr;
+    CUtensorMap tm_y, tm_attn, tm_act;
+    bool finalized = false;
+    std::string err;
+    std::vector<void *> capture;
+    bool prof = false;
+    std::vector<cudaEvent_t> ev_pool;
+    std::vector<int> ev_class;
+    size_t ev_used = 0;
+    double ms[H3ENC_K_COUNT] = {0};
+    int64_t launches[H3ENC_K_COUNT] = {0};
+    int64_t launch_count = 0;
+};
+
+namespace {
+
+h3enc_status fail(h3enc *h, h3enc_status s, const char *fmt, ...) {
+    char buf[2048];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    if (h) h->err = buf; else g_create_error = buf;
+    return s;
+}
+
+h3enc_status cuda_fail(h3enc *h, cudaError_t e, const char *what) {
+    return fail(h, e == cudaErrorMemoryAllocation ? H3ENC_ERR_OOM : H3ENC_ERR_CUDA, "%s: %s", what,
+                cudaGetErrorString(e));
+}
+
+// Run one kernel launch, timed per class when profiling is on.
+template <class F>
+cudaError_t run(h3enc *h, int cls, cudaStream_t st, F &&launch) {
+    size_t e0 = 0;
+    if (h->prof) {
+        if (h->ev_used + 2 > h->ev_pool.size()) {
+            for (int i = 0; i < 256; ++i) {
+                cudaEvent_t ev;
+                if (cudaEventCreate(&ev) != cudaSuccess) break;
+                h->ev_pool.push_back(ev);
+                h->ev_class.push_back(0);
+            }
+        }
+        if (h->ev_used + 2 <= h->ev_pool.size()) {
+            e0 = h->ev_used;
+            cudaEventRecord(h->ev_pool[e0], st);
+        } else {
+            e0 = (size_t)-1;
+        }
+    }
+    cudaError_t e = launch();
+    if (h->prof && e0 != (size_t)-1) {
+        cudaEventRecord(h->ev_pool[e0 + 1], st);
+        h->ev_class[e0] = cls;
+        h->ev_used += 2;
+    }
+    h->launch_count++;
+    h->launches[cls]++;
+    return e;
+}
+
+h3enc_status validate_config(const h3enc_config *c) {
+    if (!c) return fail(nullptr, H3ENC_ERR_INVALID_ARG, "config is NULL");
+    if (c->num_layers < 1 || c->hidden < 1 || c->n_heads < 1 || c->n_kv_heads < 1 || c->intermediate < 1 ||
+        c->vocab < 0 || c->max_tokens < 1 || c->max_seqs < 1 || c->max_seqs > h3::kMaxSeqs ||
+        c->num_deepstack < 0)
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "config: sizes out of range");
+    if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f))
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "config: rms_eps and rope_theta must be > 0");
+    if (c->mrope_section[0] < 0 || c->mrope_section[1] < 0 || c->mrope_section[2] < 0)
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "config: negative mrope_section");
+    if (c->head_dim != 64 && c->head_dim != 128)
+        return fail(nullptr, H3ENC_ERR_UNSUPPORTED, "config: head_dim %d not in {64, 128}", c->head_dim);
+    if (c->n_heads % c->n_kv_heads)
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "config: n_heads %% n_kv_heads != 0");
+    const long long qkv = (long long)(c->n_heads + 2 * c->n_kv_heads) * c->head_dim;
+    if (c->hidden % 256 || qkv % 256 || (c->n_heads * c->head_dim) % 64 || c->intermediate % 128 ||
+        c->hidden > 8192)
+        return fail(nullptr, H3ENC_ERR_UNSUPPORTED,
+                    "config: need hidden %% 256 == 0 (<= 8192), qkv width %% 256 == 0, n_heads*head_dim %% 64 "
+                    "== 0, intermediate %% 128 == 0");
+    return H3ENC_OK;
+}
+
+struct Sizes {
+    size_t qkv, o, gu, down, norm_h, norm_d, layer, embed;
+};
+
+Sizes weight_sizes(const h3enc_config &c) {
+    Sizes s;
+    const size_t H = c.hidden, d = c.head_dim;
+    s.qkv = align256((size_t)(c.n_heads + 2 * c.n_kv_heads) * d * H * 2);
+    s.o = align256(H * c.n_heads * d * 2);
+    s.gu = align256((size_t)2 * c.intermediate * H * 2);
+    s.down = align256(H * (size_t)c.intermediate * 2);
+    s.norm_h = align256(H * 2);
+    s.norm_d = align256(d * 2);
+    s.layer = s.qkv + s.o + s.gu + s.down + 2 * s.norm_h + 2 * s.norm_d;
+    s.embed = align256((size_t)c.vocab * H * 2);
+    return s;
+}
+
+bool parse_layer_name(const char *name, int *layer, int *which) {
+    static const char kPre[] = "model.language_model.layers.";
+    const size_t n = sizeof(kPre) - 1;
+    if (strncmp(name, kPre, n) != 0) return false;
+    const char *p = name + n;
+    if (*p < '0' || *p > '9') return false;
+    long l = 0;
+    while (*p >= '0' && *p <= '9') {
+        l = l * 10 + (*p - '0');
+        if (l > 1000000) return false;
+        ++p;
+    }
+    if (*p != '.') return false;
+    ++p;
+    for (int t = 0; t < T_COUNT; ++t)
+        if (strcmp(p, kSuffix[t]) == 0) {
+            *layer = (int)l;
+            *which = t;
+            return true;
+        }
+    *layer = (int)l;
+    *which = -1;
+    return true;
+}
+
+h3enc_status check_seqs(h3enc *h, const int32_t *cu, int n_seqs, int S) {
+    if (!cu) return H3ENC_OK;
+    if (n_seqs < 1 || n_seqs > h->cfg.max_seqs)
+        return fail(h, H3ENC_ERR_INVALID_ARG, "n_seqs %d outside [1, %d]", n_seqs, h->cfg.max_seqs);
+    if (cu[0] != 0 || cu[n_seqs] != S)
+        return fail(h, H3ENC_ERR_INVALID_ARG, "cu_seqlens must start at 0 and end at seq_len %d", S);
+    for (int i = 0; i < n_seqs; ++i)
+        if (cu[i + 1] < cu[i]) return fail(h, H3ENC_ERR_INVALID_ARG, "cu_seqlens decreases at %d", i);
+    return H3ENC_OK;
+}
+
+h3enc_status check_encode_args(h3enc *h, const void *positions, const uint8_t *mask, const void *ds, int nds,
+                               int n_vis, const int32_t *cu, int n_seqs, int S, const void *out) {
+    if (!h->finalized) return fail(h, H3ENC_ERR_NOT_LOADED, "weights not finalized (call h3enc_finalize_weights)");
+    if (S < 0 || S > h->cfg.max_tokens)
+        return fail(h, H3ENC_ERR_INVALID_ARG, "seq_len %d outside [0, max_tokens=%d]", S, h->cfg.max_tokens);
+    if (S > 0 && (!positions || !out)) return fail(h, H3ENC_ERR_INVALID_ARG, "positions and out must be non-NULL");
+    if (nds < 0 || nds > h->cfg.num_deepstack)
+        return fail(h, H3ENC_ERR_INVALID_ARG, "num_deepstack %d outside [0, %d]", nds, h->cfg.num_deepstack);
+    if (n_vis < 0 || n_vis > S) return fail(h, H3ENC_ERR_INVALID_ARG, "n_vis %d outside [0, seq_len]", n_vis);
+    if (nds > 0 && n_vis > 0 && (!mask || !ds))
+        return fail(h, H3ENC_ERR_INVALID_ARG, "DeepStack features need visual_mask and deepstack pointers");
+    return check_seqs(h, cu, n_seqs, S);
+}
+
+h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int lb, int le, const int32_t *pos,
+                         const uint8_t *mask, const bf16 *ds, int nds, int n_vis, const int32_t *cu, int n_seqs,
+                         int S, bf16 *out, cudaStream_t st) {
+    if (S == 0) return H3ENC_OK;
+    const h3enc_config &c = h->cfg;
+    const int H = c.hidden, d = c.head_dim, nq = c.n_heads, nkv = c.n_kv_heads, I = c.intermediate;
+    cudaError_t e;
+    if (ids) {
+        e = run(h, H3ENC_K_PREP, st, [&] {
+            return h3::launch_embed(ids, h->embed, c.vocab, H, out, S, h->status, st);
+        });
+        if (e != cudaSuccess) return cuda_fail(h, e, "embedding gather");
+    } else if (embeds != out) {
+        e = cudaMemcpyAsync(out, embeds, (size_t)S * H * 2, cudaMemcpyDeviceToDevice, st);
+        if (e != cudaSuccess) return cuda_fail(h, e, "input copy");
+    }
+    e = run(h, H3ENC_K_PREP, st, [&] { return h3::launch_rope_table(pos, S, h->rope, h->cos_t, h->sin_t, st); });
+    if (e != cudaSuccess) return cuda_fail(h, e, "rope table");
+    const bool use_ds = nds > 0 && n_vis > 0;
+    if (use_ds) {
+        e = run(h, H3ENC_K_PREP, st,
+                [&] { return h3::launch_vis_rank(mask, S, n_vis, h->vis_rank, h->status, st); });
+        if (e != cudaSuccess) return cuda_fail(h, e, "visual ranks");
+    }
+    for (int l = lb; l < le; ++l) {
+        LayerW &w = h->layers[l];
+        e = run(h, H3ENC_K_RMSNORM, st,
+                [&] { return h3::launch_rmsnorm(out, w.in_norm, h->y, S, H, c.rms_eps, st); });
+        if (e != cudaSuccess) return cuda_fail(h, e, "input_layernorm");
+        h3::GemmPlan p{};
+        p.num_sms = h->num_sms;
+        p.status = h->status;
+        p.M = S;
+        p.tmA = &h->tm_y; p.tmW = &w.tm_qkv; p.N = h->qkv_out; p.K = H; p.epi = h3::EPI_STORE;
+        p.C = h->qkv; p.ldc = h->qkv_out;
+        e = run(h, H3ENC_K_GEMM_QKV, st, [&] { return h3::launch_gemm(p, st); });
+        if (e != cudaSuccess) return cuda_fail(h, e, "qkv gemm");
+        e = run(h, H3ENC_K_QK_ROPE, st, [&] {
+            return h3::launch_qk_norm_rope(h->qkv, S, nq, nkv, d, w.q_norm, w.k_norm, c.rms_eps, h->cos_t,
+                                           h->sin_t, st);
+        });
+        if (e != cudaSuccess) return cuda_fail(h, e, "q/k norm + rope");
+        e = run(h, H3ENC_K_ATTN, st,
+                [&] { return h3::launch_attention(h->qkv, h->attn, S, nq, nkv, d, cu, n_seqs, st); });
+        if (e != cudaSuccess) return cuda_fail(h, e, "attention");
+        p.tmA = &h->tm_attn; p.tmW = &w.tm_o; p.N = H; p.K = nq * d; p.epi = h3::EPI_RESIDUAL;
+        p.C = out; p.ldc = H; p.R = out;
+        e = run(h, H3ENC_K_GEMM_O, st, [&] { return h3::launch_gemm(p, st); });
+        if (e != cudaSuccess) return cuda_fail(h, e, "o_proj gemm");
+        e = run(h, H3ENC_K_RMSNORM, st,
+                [&] { return h3::launch_rmsnorm(out, w.post_norm, h->y, S, H, c.rms_eps, st); });
+        if (e != cudaSuccess) return cuda_fail(h, e, "post_attention_layernorm");
+        p.tmA = &h->tm_y; p.tmW = &w.tm_gu; p.N = 2 * I; p.K = H; p.epi = h3::EPI_SWIGLU;
+        p.C = h->act; p.ldc = I; p.R = nullptr;
+        e = run(h, H3ENC_K_GEMM_GATE_UP, st, [&] { return h3::launch_gemm(p, st); });
+        if (e != cudaSuccess) return cuda_fail(h, e, "gate/up gemm");
+        p.tmA = &h->tm_act; p.tmW = &w.tm_down; p.N = H; p.K = I; p.C = out; p.ldc = H; p.R = out;
+        if (use_ds && l < nds) {
+            p.epi = h3::EPI_RESIDUAL_DS;
+            p.DS = ds + (size_t)l * n_vis * H;
+            p.vis_rank = h->vis_rank;
+            p.n_vis = n_vis;
+        } else {
+            p.epi = h3::EPI_RESIDUAL;
+        }
+        e = run(h, H3ENC_K_GEMM_DOWN, st, [&] { return h3::launch_gemm(p, st); });
+        if (e != cudaSuccess) return cuda_fail(h, e, "down gemm");
+        if (l < (int)h->capture.size() && h->capture[l]) {
+            e = cudaMemcpyAsync(h->capture[l], out, (size_t)S * H * 2, cudaMemcpyDeviceToDevice, st);
+            if (e != cudaSuccess) return cuda_fail(h, e, "layer capture");
+        }
+    }
+    return H3ENC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+h3enc_status h3enc_create(const h3enc_config *cfg, h3enc **out) {
+    if (!out) return fail(nullptr, H3ENC_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    h3enc_status s = validate_config(cfg);
+    if (s != H3ENC_OK) return s;
+    h3enc *h = new h3enc();
+    h->cfg = *cfg;
+    const h3enc_config &c = h->cfg;
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e != cudaSuccess) {
+        delete h;
+        return fail(nullptr, H3ENC_ERR_CUDA, "no CUDA device: %s", cudaGetErrorString(e));
+    }
+    h->num_sms = h3::device_num_sms();
+    h->qkv_out = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+    h3::make_rope_params(&h->rope, c.head_dim, c.rope_theta, c.mrope_section);
+    const Sizes ws = weight_sizes(c);
+    const size_t arena = ws.embed + ws.layer * (size_t)c.num_layers;
+    e = cudaMalloc(&h->arena, arena);
+    if (e != cudaSuccess) {
+        delete h;
+        return fail(nullptr, H3ENC_ERR_OOM, "weight arena of %zu bytes: %s", arena, cudaGetErrorString(e));
+    }
+    char *p = h->arena;
+    h->embed = c.vocab ? reinterpret_cast<bf16 *>(p) : nullptr;
+    p += ws.embed;
+    h->layers.resize(c.num_layers);
+    for (auto &w : h->layers) {
+        w.qkv = reinterpret_cast<bf16 *>(p); p += ws.qkv;
+        w.o = reinterpret_cast<bf16 *>(p); p += ws.o;
+        w.gu = reinterpret_cast<bf16 *>(p); p += ws.gu;
+        w.down = reinterpret_cast<bf16 *>(p); p += ws.down;
+        w.in_norm = reinterpret_cast<bf16 *>(p); p += ws.norm_h;
+        w.post_norm = reinterpret_cast<bf16 *>(p); p += ws.norm_h;
+        w.q_norm = reinterpret_cast<bf16 *>(p); p += ws.norm_d;
+        w.k_norm = reinterpret_cast<bf16 *>(p); p += ws.norm_d;
+    }
+    const size_t T = c.max_tokens, H = c.hidden;
+    const size_t b_y = align256(T * H * 2), b_qkv = align256(T * h->qkv_out * 2),
+                 b_attn = align256(T * c.n_heads * c.head_dim * 2), b_act = align256(T * c.intermediate * 2),
+                 b_cs = align256(T * (c.head_dim / 2) * 4), b_rank = align256(T * 4), b_stat = 256,
+                 b_ids = align256(T * 4), b_pos = align256(3 * T * 4), b_mask = align256(T),
+                 b_ds = align256((size_t)c.num_deepstack * T * H * 2), b_out = b_y;
+    const size_t wsz = b_y + b_qkv + b_attn + b_act + 2 * b_cs + b_rank + b_stat + b_ids + b_pos + b_mask + b_ds + b_out;
+    e = cudaMalloc(&h->ws, wsz);
+    if (e != cudaSuccess) {
+        cudaFree(h->arena);
+        delete h;
+        return fail(nullptr, H3ENC_ERR_OOM, "workspace of %zu bytes: %s", wsz, cudaGetErrorString(e));
+    }
+    p = h->ws;
+    h->y = reinterpret_cast<bf16 *>(p); p += b_y;
+    h->qkv = reinterpret_cast<bf16 *>(p); p += b_qkv;
+    h->attn = reinterpret_cast<bf16 *>(p); p += b_attn;
+    h->act = reinterpret_cast<bf16 *>(p); p += b_act;
+    h->cos_t = reinterpret_cast<float *>(p); p += b_cs;
+    h->sin_t = reinterpret_cast<float *>(p); p += b_cs;
+    h->vis_rank = reinterpret_cast<int32_t *>(p); p += b_rank;
+    h->status = reinterpret_cast<int32_t *>(p); p += b_stat;
+    h->st_ids = reinterpret_cast<int32_t *>(p); p += b_ids;
+    h->st_pos = reinterpret_cast<int32_t *>(p); p += b_pos;
+    h->st_mask = reinterpret_cast<uint8_t *>(p); p += b_mask;
+    h->st_ds = reinterpret_cast<bf16 *>(p); p += b_ds;
+    h->st_out = reinterpret_cast<bf16 *>(p); p += b_out;
+    e = cudaMemset(h->ws, 0, wsz);
+    if (e != cudaSuccess) {
+        h3enc_destroy(h);
+        return fail(nullptr, H3ENC_ERR_CUDA, "workspace clear: %s", cudaGetErrorString(e));
+    }
+    const uint32_t ba = (uint32_t)h3::gemm_box_rows_a();
+    if (!h3::make_tmap_rows(&h->tm_y, h->y, T, H, ba) ||
+        !h3::make_tmap_rows(&h->tm_attn, h->attn, T, (size_t)c.n_heads * c.head_dim, ba) ||
+        !h3::make_tmap_rows(&h->tm_act, h->act, T, c.intermediate, ba)) {
+        h3enc_destroy(h);
+        return fail(nullptr, H3ENC_ERR_CUDA, "cuTensorMapEncodeTiled refused a workspace operand");
+    }
+    *out = h;
+    return H3ENC_OK;
+}
+
+h3enc_status h3enc_load_weights(h3enc *h, const char *name, const void *data, int32_t dtype,
+                                const int64_t *shape, int32_t ndim, int32_t data_on_device) {
+    if (!h || !name || !data || !shape || ndim < 1) return fail(h, H3ENC_ERR_INVALID_ARG, "NULL argument");
+    const h3enc_config &c = h->cfg;
+    if (strcmp(name, "lm_head.weight") == 0 || strcmp(name, "model.language_model.norm.weight") == 0 ||
+        strncmp(name, "model.visual.", 13) == 0)
+        return H3ENC_WARN_IGNORED;
+    int layer = -1, which = -1;
+    const bool is_embed = strcmp(name, "model.language_model.embed_tokens.weight") == 0;
+    if (!is_embed) {
+        if (!parse_layer_name(name, &layer, &which)) {
+            fail(h, H3ENC_WARN_IGNORED, "weight %s has no target parameter", name);
+            return H3ENC_WARN_IGNORED;
+        }
+        if (layer >= c.num_layers) return H3ENC_WARN_IGNORED;
+        if (which < 0) {
+            fail(h, H3ENC_WARN_IGNORED, "weight %s has no target parameter", name);
+            return H3ENC_WARN_IGNORED;
+        }
+    } else if (c.vocab == 0) {
+        return H3ENC_WARN_IGNORED;
+    }
+    if (dtype == H3ENC_DTYPE_FP8_E4M3)
+        return fail(h, H3ENC_ERR_UNSUPPORTED, "%s: serialized FP8 weights are not supported (online FP8 only)", name);
+    if (dtype != H3ENC_DTYPE_BF16) return fail(h, H3ENC_ERR_UNSUPPORTED, "%s: dtype %d is not bf16", name, dtype);
+    const int64_t H = c.hidden, d = c.head_dim, nq = c.n_heads, nkv = c.n_kv_heads, I = c.intermediate;
+    int64_t want[2] = {0, 0};
+    int want_nd = 2;
+    if (is_embed) { want[0] = c.vocab; want[1] = H; }
+    else switch (which) {
+        case T_IN: case T_POST: want_nd = 1; want[0] = H; break;
+        case T_QN: case T_KN: want_nd = 1; want[0] = d; break;
+        case T_Q: want[0] = nq * d; want[1] = H; break;
+        case T_K: case T_V: want[0] = nkv * d; want[1] = H; break;
+        case T_O: want[0] = H; want[1] = nq * d; break;
+        case T_GATE: case T_UP: want[0] = I; want[1] = H; break;
+        case T_DOWN: want[0] = H; want[1] = I; break;
+    }
+    if (ndim != want_nd || shape[0] != want[0] || (want_nd == 2 && shape[1] != want[1]))
+        return fail(h, H3ENC_ERR_SHAPE, "%s: shape mismatch (expected [%lld%s%lld])", name, (long long)want[0],
+                    want_nd == 2 ? ", " : "", want_nd == 2 ? (long long)want[1] : 0LL);
+    const cudaMemcpyKind kind = data_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+    const bf16 *src = static_cast<const bf16 *>(data);
+    cudaError_t e = cudaSuccess;
+    const size_t n = (size_t)want[0] * (want_nd == 2 ? (size_t)want[1] : 1);
+    if (is_embed) {
+        e = cudaMemcpy(h->embed, src, n * 2, kind);
+        if (e == cudaSuccess) h->embed_loaded = true;
+    } else {
+        LayerW &w = h->layers[layer];
+        bf16 *dst = nullptr;
+        switch (which) {
+            case T_IN: dst = w.in_norm; break;
+            case T_POST: dst = w.post_norm; break;
+            case T_QN: dst = w.q_norm; break;
+            case T_KN: dst = w.k_norm; break;
+            case T_Q: dst = w.qkv; break;
+            case T_K: dst = w.qkv + nq * d * H; break;
+            case T_V: dst = w.qkv + (nq + nkv) * d * H; break;
+            case T_O: dst = w.o; break;
+            case T_DOWN: dst = w.down; break;
+            default: break;
+        }
+        if (which == T_GATE || which == T_UP) {
+            e = h3::pack_gate_up_rows(src, w.gu, (int)I, (int)H, which == T_UP, kind, 0);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(0);
+        } else {
+            e = cudaMemcpy(dst, src, n * 2, kind);
+        }
+        if (e == cudaSuccess) w.loaded |= 1u << which;
+    }
+    if (e != cudaSuccess) return cuda_fail(h, e, name);
+    h->finalized = false;
+    return H3ENC_OK;
+}
+
+h3enc_status h3enc_finalize_weights(h3enc *h) {
+    if (!h) return fail(h, H3ENC_ERR_INVALID_ARG, "NULL handle");
+    const h3enc_config &c = h->cfg;
+    std::string missing, shards;
+    int n_missing = 0;
+    if (c.vocab && !h->embed_loaded) {
+        missing += "model.language_model.embed_tokens.weight";
+        ++n_missing;
+    }
+    for (int l = 0; l < c.num_layers; ++l) {
+        const uint32_t m = h->layers[l].loaded;
+        for (int t = 0; t < T_COUNT; ++t)
+            if (!(m & (1u << t))) {
+                if (n_missing < 40) {
+                    if (!missing.empty()) missing += ", ";
+                    missing += "model.language_model.layers." + std::to_string(l) + "." + kSuffix[t];
+                }
+                ++n_missing;
+            }
+        const bool q = m & (1u << T_Q), k = m & (1u << T_K), v = m & (1u << T_V);
+        if ((q || k || v) && !(q && k && v))
+            shards += " layers." + std::to_string(l) + ".qkv_proj: [" + (q ? "" : "q ") + (k ? "" : "k ") +
+                      (v ? "" : "v") + "]";
+        const bool g = m & (1u << T_GATE), u = m & (1u << T_UP);
+        if ((g || u) && !(g && u))
+            shards += " layers." + std::to_string(l) + ".gate_up_proj: [" + (g ? "" : "gate") + (u ? "" : "up") + "]";
+    }
+    if (n_missing)
+        return fail(h, H3ENC_ERR_MISSING_WEIGHTS, "weights not loaded: %d params: %s%s; fused shards missing:%s",
+                    n_missing, missing.c_str(), n_missing > 40 ? ", ..." : "", shards.empty() ? " none" : shards.c_str());
+    const uint32_t bw = (uint32_t)h3::gemm_box_rows_w();
+    const size_t H = c.hidden, d = c.head_dim;
+    for (auto &w : h->layers) {
+        if (!h3::make_tmap_rows(&w.tm_qkv, w.qkv, h->qkv_out, H, bw) ||
+            !h3::make_tmap_rows(&w.tm_o, w.o, H, c.n_heads * d, bw) ||
+            !h3::make_tmap_rows(&w.tm_gu, w.gu, 2 * (size_t)c.intermediate, H, bw) ||
+            !h3::make_tmap_rows(&w.tm_down, w.down, H, c.intermediate, bw))
+            return fail(h, H3ENC_ERR_CUDA, "cuTensorMapEncodeTiled refused a weight operand");
+    }
+    h->finalized = true;
+    return H3ENC_OK;
+}
+
+h3enc_status h3enc_encode(h3enc *h, const int32_t *input_ids, const int32_t *positions, const uint8_t *visual_mask,
+                          const void *deepstack, int32_t num_deepstack, int32_t n_vis, const int32_t *cu_seqlens,
+                          int32_t n_seqs, int32_t seq_len, void *out, void *stream) {
+    if (!h) return fail(h, H3ENC_ERR_INVALID_ARG, "NULL handle");
+    h3enc_status s = check_encode_args(h, positions, visual_mask, deepstack, num_deepstack, n_vis, cu_seqlens,
+                                       n_seqs, seq_len, out);
+    if (s != H3ENC_OK) return s;
+    if (h->cfg.vocab == 0) return fail(h, H3ENC_ERR_UNSUPPORTED, "model has no embedding table (vocab 0)");
+    if (seq_len > 0 && !input_ids) return fail(h, H3ENC_ERR_INVALID_ARG, "input_ids is NULL");
+    return encode_core(h, input_ids, nullptr, 0, h->cfg.num_layers, positions, visual_mask,
+                       static_cast<const bf16 *>(deepstack), num_deepstack, n_vis, cu_seqlens, n_seqs, seq_len,
+                       static_cast<bf16 *>(out), static_cast<cudaStream_t>(stream));
+}
+
+h3enc_status h3enc_encode_embeds(h3enc *h, const void *inputs_embeds, int32_t layer_begin, int32_t layer_end,
+                                 const int32_t *positions, const uint8_t *visual_mask, const void *deepstack,
+                                 int32_t num_deepstack, int32_t n_vis, const int32_t *cu_seqlens, int32_t n_seqs,
+                                 int32_t seq_len, void *out, void *stream) {
+    if (!h) return fail(h, H3ENC_ERR_INVALID_ARG, "NULL handle");
+    h3enc_status s = check_encode_args(h, positions, visual_mask, deepstack, num_deepstack, n_vis, cu_seqlens,
+                                       n_seqs, seq_len, out);
+    if (s != H3ENC_OK) return s;
+    if (layer_begin < 0 || layer_end > h->cfg.num_layers || layer_begin > layer_end)
+        return fail(h, H3ENC_ERR_INVALID_ARG, "layer range [%d, %d) outside [0, %d]", layer_begin, layer_end,
+                    h->cfg.num_layers);
+    if (seq_len > 0 && !inputs_embeds) return fail(h, H3ENC_ERR_INVALID_ARG, "inputs_embeds is NULL");
+    return encode_core(h, nullptr, static_cast<const bf16 *>(inputs_embeds), layer_begin, layer_end, positions,
+                       visual_mask, static_cast<const bf16 *>(deepstack), num_deepstack, n_vis, cu_seqlens, n_seqs,
+                       seq_len, static_cast<bf16 *>(out), static_cast<cudaStream_t>(stream));
+}
+
+h3enc_status h3enc_encode_host(h3enc *h, const int32_t *input_ids, const int32_t *positions,
+                               const uint8_t *visual_mask, const void *deepstack, int32_t num_deepstack,
+                               int32_t n_vis, const int32_t *cu_seqlens, int32_t n_seqs, int32_t seq_len, void *out,
+                               void *stream) {
+    if (!h) return fail(h, H3ENC_ERR_INVALID_ARG, "NULL handle");
+    h3enc_status s = check_encode_args(h, positions, visual_mask, deepstack, num_deepstack, n_vis, cu_seqlens,
+                                       n_seqs, seq_len, out);
+    if (s != H3ENC_OK) return s;
+    if (h->cfg.vocab == 0) return fail(h, H3ENC_ERR_UNSUPPORTED, "model has no embedding table (vocab 0)");
+    if (seq_len == 0) return H3ENC_OK;
+    if (!input_ids) return fail(h, H3ENC_ERR_INVALID_ARG, "input_ids is NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t S = seq_len, H = h->cfg.hidden;
+    cudaError_t e = cudaMemcpyAsync(h->st_ids, input_ids, S * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h->st_pos, positions, 3 * S * 4, cudaMemcpyHostToDevice, st);
+    const bool use_ds = num_deepstack > 0 && n_vis > 0;
+    if (e == cudaSuccess && visual_mask) e = cudaMemcpyAsync(h->st_mask, visual_mask, S, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && use_ds)
+        e = cudaMemcpyAsync(h->st_ds, deepstack, (size_t)num_deepstack * n_vis * H * 2, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "host-to-device copy");
+    s = encode_core(h, h->st_ids, nullptr, 0, h->cfg.num_layers, h->st_pos, visual_mask ? h->st_mask : nullptr,
+                    use_ds ? h->st_ds : nullptr, num_deepstack, n_vis, cu_seqlens, n_seqs, seq_len, h->st_out, st);
+    if (s != H3ENC_OK) return s;
+    e = cudaMemcpyAsync(out, h->st_out, S * H * 2, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "device-to-host copy");
+    return H3ENC_OK;
+}
+
+h3enc_status h3enc_set_layer_capture(h3enc *h, void *const *per_layer, int32_t n) {
+    if (!h) return fail(h, H3ENC_ERR_INVALID_ARG, "NULL handle");
+    if (n == 0) {
+        h->capture.clear();
+        return H3ENC_OK;
+    }
+    if (n != h->cfg.num_layers || !per_layer)
+        return fail(h, H3ENC_ERR_INVALID_ARG, "capture needs num_layers=%d pointers", h->cfg.num_layers);
+    h->capture.assign(per_layer, per_layer + n);
+    return H3ENC_OK;
+}
+
+h3enc_status h3enc_get_status(h3enc *h) {
+    if (!h) return fail(h, H3ENC_ERR_INVALID_ARG, "NULL handle");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(h, e, "device synchronise");
+    int32_t st = 0;
+    e = cudaMemcpy(&st, h->status, 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(h->status, 0, 4);
+    if (e != cudaSuccess) return cuda_fail(h, e, "status read");
+    if (st & 1) return fail(h, H3ENC_ERR_DEVICE_TIMEOUT, "a bounded device wait ran out");
+    if (st & 2) return fail(h, H3ENC_ERR_DEVICE_BOUNDS, "token id outside [0, vocab)");
+    if (st & 4) return fail(h, H3ENC_ERR_SHAPE, "visual mask count differs from n_vis");
+    return H3ENC_OK;
+}
+
+const char *h3enc_last_error(const h3enc *h) { return h ? h->err.c_str() : g_create_error.c_str(); }
+
+void h3enc_destroy(h3enc *h) {
+    if (!h) return;
+    for (cudaEvent_t ev : h->ev_pool) cudaEventDestroy(ev);
+    if (h->ws) cudaFree(h->ws);
+    if (h->arena) cudaFree(h->arena);
+    delete h;
+}
+
+h3enc_status h3enc_set_profiling(h3enc *h, int32_t enable) {
+    if (!h) return fail(h, H3ENC_ERR_INVALID_ARG, "NULL handle");
+    h->prof = enable != 0;
+    h->ev_used = 0;
+    for (int k = 0; k < H3ENC_K_COUNT; ++k) {
+        h->ms[k] = 0;
+        h->launches[k] = 0;
+    }
+    return H3ENC_OK;
+}
+
+h3enc_status h3enc_get_profile(h3enc *h, double *ms, int64_t *launches, int32_t n) {
+    if (!h || n < 0 || n > H3ENC_K_COUNT) return fail(h, H3ENC_ERR_INVALID_ARG, "bad arguments");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(h, e, "device synchronise");
+    for (size_t i = 0; i + 1 < h->ev_used; i += 2) {
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, h->ev_pool[i], h->ev_pool[i + 1]) == cudaSuccess) h->ms[h->ev_class[i]] += t;
+    }
+    h->ev_used = 0;
+    for (int k = 0; k < n; ++k) {
+        if (ms) ms[k] = h->ms[k];
+        if (launches) launches[k] = h->launches[k];
+    }
+    for (int k = 0; k < H3ENC_K_COUNT; ++k) {
+        h->ms[k] = 0;
+        h->launches[k] = 0;
+    }
+    return H3ENC_OK;
+}
+
+int64_t h3enc_launch_count(const h3enc *h) { return h ? h->launch_count : 0; }
+int32_t h3enc_num_sms(const h3enc *h) { return h ? h->num_sms : 0; }
+
+// ---------------------------------------------------------------- op-level entries
+
+h3enc_status h3enc_op_gemm(const void *A, const void *W, void *C, int32_t M, int32_t N, int32_t K, int32_t epilogue,
+                           const void *R, const void *DS, const int32_t *vis_rank, int32_t n_vis, int32_t *status,
+                           void *stream) {
+    if (M < 0 || N <= 0 || K <= 0 || N % 256 || K % 8 || epilogue < 0 || epilogue > 3)
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm: bad sizes or epilogue");
+    if (M == 0) return H3ENC_OK;
+    if (!A || !W || !C || ((epilogue == H3ENC_EPI_RESIDUAL || epilogue == H3ENC_EPI_RESIDUAL_DS) && !R) ||
+        (epilogue == H3ENC_EPI_RESIDUAL_DS && DS && !vis_rank))
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm: NULL operand");
+    CUtensorMap ta, tw;
+    if (!h3::make_tmap_rows(&ta, A, M, K, h3::gemm_box_rows_a()) ||
+        !h3::make_tmap_rows(&tw, W, N, K, h3::gemm_box_rows_w()))
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm: operands not 16-byte aligned or driver refused the map");
+    h3::GemmPlan p{};
+    p.tmA = &ta; p.tmW = &tw; p.M = M; p.N = N; p.K = K; p.epi = epilogue;
+    p.C = static_cast<bf16 *>(C);
+    p.ldc = epilogue == H3ENC_EPI_SWIGLU ? N / 2 : N;
+    p.R = static_cast<const bf16 *>(R);
+    p.DS = static_cast<const bf16 *>(DS);
+    p.vis_rank = vis_rank;
+    p.n_vis = n_vis;
+    p.status = status;
+    p.num_sms = h3::device_num_sms();
+    cudaError_t e = h3::launch_gemm(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "gemm launch");
+}
+
+h3enc_status h3enc_op_pack_gate_up(const void *gate, const void *up, void *W, int32_t I, int32_t K, void *stream) {
+    if (!gate || !up || !W || I <= 0 || K <= 0 || I % 128) return fail(nullptr, H3ENC_ERR_INVALID_ARG, "pack: bad args");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = h3::pack_gate_up_rows(static_cast<const bf16 *>(gate), static_cast<bf16 *>(W), I, K, 0,
+                                          cudaMemcpyDeviceToDevice, st);
+    if (e == cudaSuccess)
+        e = h3::pack_gate_up_rows(static_cast<const bf16 *>(up), static_cast<bf16 *>(W), I, K, 1,
+                                  cudaMemcpyDeviceToDevice, st);
+    return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "pack gate/up");
+}
+
+h3enc_status h3enc_op_rmsnorm(const void *x, const void *w, void *y, int32_t rows, int32_t cols, float eps,
+                              void *stream) {
+    if (!x || !w || !y || rows < 0 || cols <= 0 || cols % 8 || cols > 8192)
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "rmsnorm: bad args");
+    cudaError_t e = h3::launch_rmsnorm(static_cast<const bf16 *>(x), static_cast<const bf16 *>(w),
+                                       static_cast<bf16 *>(y), rows, cols, eps, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "rmsnorm launch");
+}
+
+h3enc_status h3enc_op_rope_table(const int32_t *positions, int32_t S, int32_t head_dim, float theta,
+                                 const int32_t *section_host, float *cos_tab, float *sin_tab, void *stream) {
+    if (!positions || !section_host || !cos_tab || !sin_tab || S < 0 || head_dim < 2 || head_dim > 128 ||
+        head_dim % 2 || !(theta > 0.f))
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "rope_table: bad args");
+    h3::RopeParams rp;
+    h3::make_rope_params(&rp, head_dim, theta, section_host);
+    cudaError_t e = h3::launch_rope_table(positions, S, rp, cos_tab, sin_tab, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "rope_table launch");
+}
+
+h3enc_status h3enc_op_qk_norm_rope(void *qkv, int32_t S, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                   const void *w_q, const void *w_k, float eps, const float *cos_tab,
+                                   const float *sin_tab, void *stream) {
+    if (!qkv || !w_q || !w_k || !cos_tab || !sin_tab || S < 0 || n_heads < 1 || n_kv_heads < 1 ||
+        (head_dim != 64 && head_dim != 128))
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "qk_norm_rope: bad args");
+    cudaError_t e = h3::launch_qk_norm_rope(static_cast<bf16 *>(qkv), S, n_heads, n_kv_heads, head_dim,
+                                            static_cast<const bf16 *>(w_q), static_cast<const bf16 *>(w_k), eps,
+                                            cos_tab, sin_tab, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "qk_norm_rope launch");
+}
+
+h3enc_status h3enc_op_attention(const void *qkv, void *o, int32_t S, int32_t n_heads, int32_t n_kv_heads,
+                                int32_t head_dim, const int32_t *cu_seqlens, int32_t n_seqs, void *stream) {
+    if (!qkv || !o || S < 0 || n_heads < 1 || n_kv_heads < 1 || n_heads % n_kv_heads ||
+        (head_dim != 64 && head_dim != 128))
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "attention: bad args");
+    if (cu_seqlens) {
+        if (n_seqs < 1 || n_seqs > h3::kMaxSeqs || cu_seqlens[0] != 0 || cu_seqlens[n_seqs] != S)
+            return fail(nullptr, H3ENC_ERR_INVALID_ARG, "attention: bad cu_seqlens");
+        for (int i = 0; i < n_seqs; ++i)
+            if (cu_seqlens[i + 1] < cu_seqlens[i]) return fail(nullptr, H3ENC_ERR_INVALID_ARG, "attention: bad cu_seqlens");
+    }
+    cudaError_t e = h3::launch_attention(static_cast<const bf16 *>(qkv), static_cast<bf16 *>(o), S, n_heads,
+                                         n_kv_heads, head_dim, cu_seqlens, n_seqs, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "attention launch");
+}
+
+h3enc_status h3enc_op_embed(const int32_t *ids, const void *table, int32_t vocab, int32_t hidden, void *out, int32_t S,
+                            int32_t *status, void *stream) {
+    if (!ids || !table || !out || vocab < 1 || hidden < 8 || hidden % 8 || S < 0)
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "embed: bad args");
+    cudaError_t e = h3::launch_embed(ids, static_cast<const bf16 *>(table), vocab, hidden, static_cast<bf16 *>(out), S,
+                                     status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "embed launch");
+}
+
+h3enc_status h3enc_op_vis_rank(const uint8_t *mask, int32_t S, int32_t n_vis, int32_t *vis_rank, int32_t *status,
+                               void *stream) {
+    if (!mask || !vis_rank || S < 0) return fail(nullptr, H3ENC_ERR_INVALID_ARG, "vis_rank: bad args");
+    cudaError_t e = h3::launch_vis_rank(mask, S, n_vis, vis_rank, status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "vis_rank launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+// Host-side launchers of the device kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace h3 {
+
+using bf16 = __nv_bfloat16;
+
+enum { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_RESIDUAL_DS = 3 };
+
+constexpr int kMaxSeqs = 1024;
+constexpr int kMaxHalfDim = 64;
+
+// ---- projection GEMM (gemm.cu)
+struct GemmPlan {
+    const CUtensorMap *tmA;   // A [rows >= M, K], box 128 x 64
+    const CUtensorMap *tmW;   // W [N, K], box 256 x 64
+    int M, N, K, epi;
+    bf16 *C;
+    int ldc;
+    const bf16 *R;
+    const bf16 *DS;
+    const int32_t *vis_rank;
+    int n_vis;
+    int32_t *status;
+    int num_sms;
+};
+// Tensor map of a row-major bf16 matrix [rows, cols] read in boxes of
+// box_rows x 64 with 128-byte swizzle.  False if the driver refuses it.
+bool make_tmap_rows(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
+int gemm_box_rows_a();
+int gemm_box_rows_w();
+cudaError_t launch_gemm(const GemmPlan &p, cudaStream_t stream);
+
+// ---- norms and rotary embedding (norm_rope.cu)
+struct RopeParams {
+    int half_dim;
+    float inv_freq[kMaxHalfDim];
+    int8_t axis[kMaxHalfDim];
+};
+void make_rope_params(RopeParams *p, int head_dim, float theta, const int32_t section[3]);
+cudaError_t launch_rmsnorm(const bf16 *x, const bf16 *w, bf16 *y, int rows, int cols, float eps, cudaStream_t st);
+cudaError_t launch_rope_table(const int32_t *positions, int S, const RopeParams &rp, float *cos_t, float *sin_t,
+                              cudaStream_t st);
+cudaError_t launch_qk_norm_rope(bf16 *qkv, int S, int nq, int nkv, int d, const bf16 *wq, const bf16 *wk,
+                                float eps, const float *cos_t, const float *sin_t, cudaStream_t st);
+
+// ---- attention (attention.cu)
+cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, int d, const int32_t *cu_host,
+                             int n_seqs, cudaStream_t st);
+
+// ---- embedding gather, visual ranks, weight packing (embed.cu)
+cudaError_t launch_embed(const int32_t *ids, const bf16 *table, int vocab, int hidden, bf16 *out, int S,
+                         int32_t *status, cudaStream_t st);
+cudaError_t launch_vis_rank(const uint8_t *mask, int S, int n_vis, int32_t *rank, int32_t *status,
+                            cudaStream_t st);
+cudaError_t pack_gate_up_rows(const bf16 *src, bf16 *W, int I, int K, int which, cudaMemcpyKind kind,
+                              cudaStream_t st);
+
+int device_num_sms();
+
+}  // namespace h3
