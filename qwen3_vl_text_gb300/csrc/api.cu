@@ -589,6 +589,14 @@ h3enc_status h3enc_set_profiling(h3enc *h, int32_t enable) {
     if (!h) return fail(h, H3ENC_ERR_INVALID_ARG, "NULL handle");
     h->prof = enable != 0;
     h->ev_used = 0;
+    // reserve event pairs up front so a timed region never creates events
+    while (h->prof && h->ev_pool.size() < 16384) {
+        cudaEvent_t ev;
+        cudaError_t e = cudaEventCreate(&ev);
+        if (e != cudaSuccess) return cuda_fail(h, e, "profiling events");
+        h->ev_pool.push_back(ev);
+        h->ev_class.push_back(0);
+    }
     for (int k = 0; k < H3ENC_K_COUNT; ++k) {
         h->ms[k] = 0;
         h->launches[k] = 0;

@@ -1,0 +1,90 @@
+"""Shared helpers of the GPU parity tests: build an encoder from the seeded
+generator (weights drawn on the device), the matching CPU oracle run (same
+weights drawn on the host), and the comparison metrics."""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+import oracle as O
+import workloads as W
+
+
+def rel_l2(a, b) -> float:
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def max_abs_over_rms(a, b) -> float:
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.max(np.abs(a - b)) / max(np.sqrt(np.mean(b * b)), 1e-30))
+
+
+def bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> float32 (multithreaded via torch; exact)."""
+    import torch
+    return W.bf16_bits_to_torch(np.ascontiguousarray(bits)).float().numpy()
+
+
+def t2f(t) -> np.ndarray:
+    """torch bf16 tensor (any device) -> float32 numpy."""
+    return t.detach().float().cpu().numpy()
+
+
+def f2bf16_torch(x: np.ndarray, device="cuda"):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).to(device)
+
+
+def model_of(wl: W.Workload, num_layers=None):
+    m = wl.model
+    return m if num_layers is None else dataclasses.replace(m, num_layers=num_layers)
+
+
+def oracle_layer_getter(wl: W.Workload, cfg):
+    def get(l):
+        lw = O.LayerWeights()
+        for name, shape, mean, sigma in W.layer_weight_specs(cfg, l):
+            lw[name.split(".")[-2]] = bits_to_f32(W.gen_weight(wl.seed, name, shape, mean, sigma))
+        return lw
+    return get
+
+
+def oracle_embed(wl: W.Workload, cfg, ids: np.ndarray) -> np.ndarray:
+    return bits_to_f32(W.gen_weight(wl.seed, W.embed_name(), (cfg.vocab, cfg.hidden), 0.0, 0.02, rows=ids))
+
+
+def make_encoder(wl: W.Workload, cfg, max_tokens: int, max_seqs: int = 64):
+    import torch
+    from qwen3_vl_text_gb300 import Encoder
+    enc = Encoder(cfg, max_tokens=max_tokens, max_seqs=max_seqs, num_deepstack=max(3, wl.deepstack_levels))
+    for l in range(cfg.num_layers):
+        for name, shape, mean, sigma in W.layer_weight_specs(cfg, l):
+            enc.load(name, W.gen_weight(wl.seed, name, shape, mean, sigma, device="cuda"))
+    if cfg.vocab:
+        enc.load(W.embed_name(), W.gen_weight(wl.seed, W.embed_name(), (cfg.vocab, cfg.hidden), 0.0, 0.02,
+                                              device="cuda"))
+    torch.cuda.synchronize()
+    enc.finalize()
+    return enc
+
+
+def device_inputs(inp: dict):
+    """Workload inputs as device tensors (ids, positions, mask, deepstack, embeds)."""
+    import torch
+    dev = {}
+    dev["positions"] = torch.from_numpy(inp["positions"]).cuda()
+    dev["input_ids"] = None if inp["input_ids"] is None else torch.from_numpy(inp["input_ids"]).cuda()
+    dev["visual_mask"] = torch.from_numpy(inp["visual_mask"]).cuda() if inp["n_vis"] else None
+    dev["deepstack"] = None if inp["deepstack"] is None else W.bf16_bits_to_torch(inp["deepstack"]).cuda()
+    dev["inputs_embeds"] = (None if inp.get("inputs_embeds") is None
+                            else W.bf16_bits_to_torch(inp["inputs_embeds"]).cuda())
+    return dev
+
+
+def cu_or_none(inp: dict):
+    cu = inp["cu_seqlens"]
+    return None if len(cu) == 2 else [int(x) for x in cu]

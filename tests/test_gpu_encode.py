@@ -1,0 +1,275 @@
+"""Whole-encode parity through the C ABI against the CPU oracle.
+
+Bars (from the encoder's contract): per-layer hidden state relative L2 <= 5e-3
+when the layer is fed the oracle's bf16-rounded input ("teacher-forced");
+final output relative L2 <= 2e-2 and max |diff| <= 0.05 * RMS(out) for free
+runs; bit-exact for the properties that hold at any size (determinism, causal
+prefix, packing, zero DeepStack).
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+from _harness import (bits_to_f32, cu_or_none, device_inputs, make_encoder, max_abs_over_rms, model_of,
+                      oracle_embed, oracle_layer_getter, rel_l2, t2f)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import qwen3_vl_text_gb300 as Q  # noqa: E402
+
+LAYER_TOL = 5e-3
+FINAL_TOL = 2e-2
+MAXABS_TOL = 0.05
+
+
+def _oracle_inputs(wl, cfg, inp):
+    if inp["input_ids"] is not None:
+        x0 = oracle_embed(wl, cfg, inp["input_ids"])
+    else:
+        x0 = bits_to_f32(inp["inputs_embeds"])
+    ds = None if inp["deepstack"] is None else bits_to_f32(inp["deepstack"])
+    return x0, ds
+
+
+def _run_gpu(enc, dev, inp, S, capture=None, layer_range=None, embeds=None):
+    out = torch.empty(S, enc.model.hidden, dtype=torch.bfloat16, device="cuda")
+    if capture is not None:
+        Q.h3enc_set_layer_capture(enc.handle, capture)
+    nds = 0 if dev["deepstack"] is None else dev["deepstack"].shape[0]
+    if embeds is not None or dev["input_ids"] is None:
+        lb, le = layer_range if layer_range else (0, enc.model.num_layers)
+        Q.h3enc_encode_embeds(enc.handle, embeds if embeds is not None else dev["inputs_embeds"], lb, le,
+                              dev["positions"], dev["visual_mask"], dev["deepstack"], nds, inp["n_vis"],
+                              cu_or_none(inp), S, out)
+    else:
+        Q.h3enc_encode(enc.handle, dev["input_ids"], dev["positions"], dev["visual_mask"], dev["deepstack"], nds,
+                       inp["n_vis"], cu_or_none(inp), S, out)
+    if capture is not None:
+        Q.h3enc_set_layer_capture(enc.handle, [])
+    assert enc.status() == 0, Q.h3enc_last_error(enc.handle)
+    return out
+
+
+def _check_layers_and_final(wl, cfg, enc, inp, per_layer=True):
+    """Free run vs oracle free run, then every layer teacher-forced."""
+    S = inp["seq_len"]
+    dev = device_inputs(inp)
+    x0, ds = _oracle_inputs(wl, cfg, inp)
+    get = oracle_layer_getter(wl, cfg)
+    cu = list(inp["cu_seqlens"])
+    cap = []
+    ref = O.forward(x0, inp["positions"], cfg, get, inp["visual_mask"], ds, cu, capture=cap)
+    out = t2f(_run_gpu(enc, dev, inp, S))
+    r, m = rel_l2(out, ref), max_abs_over_rms(out, ref)
+    assert r <= FINAL_TOL and m <= MAXABS_TOL, f"final rel {r:.3g} max/rms {m:.3g}"
+    if not per_layer:
+        return
+    ins = [x0] + cap[:-1]
+    for l in range(cfg.num_layers):
+        xin = O.round_to_bf16(ins[l])
+        want = O.forward(xin, inp["positions"], cfg, get, inp["visual_mask"], ds, cu, layers=[l])
+        got = t2f(_run_gpu(enc, dev, inp, S, layer_range=(l, l + 1),
+                           embeds=torch.from_numpy(xin).to(torch.bfloat16).cuda()))
+        assert rel_l2(got, want) <= LAYER_TOL, f"layer {l}: rel {rel_l2(got, want):.3g}"
+
+
+def test_tiny_two_layer_model():
+    wl = W.workload(0)
+    cfg = wl.model
+    enc = make_encoder(wl, cfg, max_tokens=64)
+    try:
+        _check_layers_and_final(wl, cfg, enc, W.gen_inputs(wl))
+    finally:
+        enc.close()
+
+
+def test_tiny_layer_capture_and_host_entry_match_device_encode():
+    wl = W.workload(0)
+    cfg = wl.model
+    inp = W.gen_inputs(wl)
+    S = inp["seq_len"]
+    enc = make_encoder(wl, cfg, max_tokens=64)
+    try:
+        dev = device_inputs(inp)
+        caps = [torch.zeros(64, cfg.hidden, dtype=torch.bfloat16, device="cuda") for _ in range(cfg.num_layers)]
+        out = _run_gpu(enc, dev, inp, S, capture=caps)
+        assert torch.equal(caps[-1][:S], out)
+        host_out = torch.empty(S, cfg.hidden, dtype=torch.bfloat16).pin_memory()
+        ids = torch.from_numpy(inp["input_ids"])
+        pos = torch.from_numpy(inp["positions"])
+        mask = torch.from_numpy(inp["visual_mask"])
+        ds = W.bf16_bits_to_torch(inp["deepstack"])
+        Q.h3enc_encode_host(enc.handle, ids, pos, mask, ds, ds.shape[0], inp["n_vis"], None, S, host_out)
+        assert torch.equal(host_out, out.cpu())
+        # run twice: deterministic, bit for bit
+        assert torch.equal(_run_gpu(enc, dev, inp, S), out)
+        # zero DeepStack features equal no DeepStack at all
+        z = dict(dev)
+        z["deepstack"] = torch.zeros_like(dev["deepstack"])
+        nods = dict(dev)
+        nods["deepstack"] = None
+        assert torch.equal(_run_gpu(enc, z, inp, S), _run_gpu(enc, nods, dict(inp, n_vis=0), S))
+        # S = 0 is a no-op
+        Q.h3enc_encode(enc.handle, dev["input_ids"], dev["positions"], None, None, 0, 0, None, 0, out)
+    finally:
+        enc.close()
+
+
+def test_one_full_width_layer():
+    wl = W.workload(1)
+    cfg = wl.model
+    inp = W.gen_inputs(wl)
+    enc = make_encoder(wl, cfg, max_tokens=inp["seq_len"])
+    try:
+        _check_layers_and_final(wl, cfg, enc, inp, per_layer=False)
+        # one layer: the free run is the teacher-forced run; hold it to the per-layer bar
+        dev = device_inputs(inp)
+        x0, _ = _oracle_inputs(wl, cfg, inp)
+        ref = O.forward(x0, inp["positions"], cfg, oracle_layer_getter(wl, cfg))
+        out = t2f(_run_gpu(enc, dev, inp, inp["seq_len"]))
+        assert rel_l2(out, ref) <= LAYER_TOL, f"rel {rel_l2(out, ref):.3g}"
+    finally:
+        enc.close()
+
+
+@pytest.mark.slow
+def test_image_layout_two_full_width_layers_with_deepstack():
+    wl = W.workload(2)
+    cfg = model_of(wl, 2)
+    inp = W.gen_inputs(wl)
+    enc = make_encoder(wl, cfg, max_tokens=inp["seq_len"])
+    try:
+        _check_layers_and_final(wl, cfg, enc, inp)
+    finally:
+        enc.close()
+
+
+@pytest.mark.slow
+def test_packed_prompts_two_full_width_layers():
+    wl = W.workload(4)
+    cfg = model_of(wl, 2)
+    inp = W.gen_inputs(wl)
+    S = inp["seq_len"]
+    enc = make_encoder(wl, cfg, max_tokens=S, max_seqs=32)
+    try:
+        _check_layers_and_final(wl, cfg, enc, inp, per_layer=False)
+        # packing is invisible: each prompt alone gives the same rows, bit for bit
+        dev = device_inputs(inp)
+        full = _run_gpu(enc, dev, inp, S)
+        cu = inp["cu_seqlens"]
+        for i in (0, 7, 15):
+            a, b = int(cu[i]), int(cu[i + 1])
+            one = {"positions": dev["positions"][:, a:b].contiguous(), "input_ids": dev["input_ids"][a:b],
+                   "visual_mask": None, "deepstack": None, "inputs_embeds": None}
+            sep = _run_gpu(enc, one, {"n_vis": 0, "cu_seqlens": np.array([0, b - a])}, b - a)
+            assert torch.equal(sep, full[a:b]), f"prompt {i}"
+    finally:
+        enc.close()
+
+
+@pytest.mark.slow
+def test_long_video_layout_one_full_width_layer():
+    wl = W.workload(3)
+    cfg = model_of(wl, 1)
+    inp = W.gen_inputs(wl)
+    enc = make_encoder(wl, cfg, max_tokens=inp["seq_len"])
+    try:
+        _check_layers_and_final(wl, cfg, enc, inp, per_layer=False)
+    finally:
+        enc.close()
+
+
+@pytest.mark.slow
+def test_full_depth_image_encode_prefix_rows():
+    """50 layers, seq 1024, in the launch configuration of the benchmark: the
+    oracle computes the first 192 rows (causal: they depend on the first 192
+    tokens only, 64 of them visual with DeepStack), compared element-wise with
+    the full encode's rows.  Then determinism and the causal-prefix property of
+    the GPU path itself, bit for bit."""
+    wl = W.workload(2)
+    cfg = wl.model
+    inp = W.gen_inputs(wl)
+    S = inp["seq_len"]
+    P = 192
+    enc = make_encoder(wl, cfg, max_tokens=S)
+    try:
+        dev = device_inputs(inp)
+        out = _run_gpu(enc, dev, inp, S)
+        assert torch.equal(_run_gpu(enc, dev, inp, S), out), "not deterministic"
+        n_vis_p = int(inp["visual_mask"][:P].sum())
+        pre_inp = {"n_vis": n_vis_p, "cu_seqlens": np.array([0, P])}
+        pre = {"positions": dev["positions"][:, :P].contiguous(), "input_ids": dev["input_ids"][:P],
+               "visual_mask": dev["visual_mask"][:P], "deepstack": dev["deepstack"][:, :n_vis_p].contiguous(),
+               "inputs_embeds": None}
+        assert torch.equal(_run_gpu(enc, pre, pre_inp, P), out[:P]), "causal prefix differs"
+        x0 = oracle_embed(wl, cfg, inp["input_ids"][:P])
+        ds = bits_to_f32(inp["deepstack"])[:, :n_vis_p]
+        ref = O.forward(x0, inp["positions"][:, :P], cfg, oracle_layer_getter(wl, cfg),
+                        inp["visual_mask"][:P], ds)
+        got = t2f(out[:P])
+        r, m = rel_l2(got, ref), max_abs_over_rms(got, ref)
+        assert r <= FINAL_TOL and m <= MAXABS_TOL, f"rel {r:.3g} max/rms {m:.3g}"
+    finally:
+        enc.close()
+
+
+def test_errors_are_reported_before_launch_and_from_the_device():
+    wl = W.workload(0)
+    cfg = wl.model
+    inp = W.gen_inputs(wl)
+    S = inp["seq_len"]
+    dev = device_inputs(inp)
+    enc = Q.Encoder(cfg, max_tokens=64, max_seqs=4, num_deepstack=1)
+    try:
+        out = torch.empty(S, cfg.hidden, dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(Q.H3encError) as e:
+            enc.encode(dev["input_ids"], dev["positions"], out)
+        assert e.value.code == 4  # NOT_LOADED
+        t = torch.zeros(cfg.hidden, dtype=torch.bfloat16, device="cuda")
+        assert enc.load("lm_head.weight", t) == 1
+        assert enc.load("model.language_model.norm.weight", t) == 1
+        assert enc.load("model.language_model.layers.7.input_layernorm.weight", t) == 1  # beyond kept layers
+        with pytest.raises(Q.H3encError) as e:
+            enc.load("model.language_model.layers.0.input_layernorm.weight",
+                     torch.zeros(cfg.hidden + 1, dtype=torch.bfloat16, device="cuda"))
+        assert e.value.code == 3
+        name = "model.language_model.layers.0.self_attn.q_proj.weight"
+        shp = (cfg.n_heads * cfg.head_dim, cfg.hidden)
+        fp8 = torch.zeros(shp, dtype=torch.uint8, device="cuda")
+        code = Q.lib.h3enc_load_weights(enc.handle, name.encode(), fp8.data_ptr(), 2, (Q._I64 * 2)(*shp), 2, 1)
+        assert code == 6 and "online FP8" in Q.h3enc_last_error(enc.handle)
+        enc.load(name, torch.zeros(shp, dtype=torch.bfloat16, device="cuda"))
+        with pytest.raises(Q.H3encError) as e:
+            enc.finalize()
+        assert e.value.code == 5
+        msg = Q.h3enc_last_error(enc.handle)
+        assert "embed_tokens" in msg and "qkv_proj: [k v]" in msg
+    finally:
+        enc.close()
+
+    enc = make_encoder(wl, cfg, max_tokens=64)
+    try:
+        out = torch.empty(S, cfg.hidden, dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(Q.H3encError) as e:   # S > max_tokens
+            Q.h3enc_encode(enc.handle, dev["input_ids"], dev["positions"], None, None, 0, 0, None, 65, out)
+        assert e.value.code == 2
+        with pytest.raises(Q.H3encError) as e:   # cu_seqlens not ending at S
+            Q.h3enc_encode(enc.handle, dev["input_ids"], dev["positions"], None, None, 0, 0, [0, 10, 40], S, out)
+        assert e.value.code == 2
+        with pytest.raises(Q.H3encError) as e:   # DeepStack without a mask
+            Q.h3enc_encode(enc.handle, dev["input_ids"], dev["positions"], None, dev["deepstack"], 1, 32, None, S,
+                           out)
+        assert e.value.code == 2
+        # device-side: visual count mismatch, then an out-of-range token id
+        Q.h3enc_encode(enc.handle, dev["input_ids"], dev["positions"], dev["visual_mask"], dev["deepstack"], 1, 31,
+                       None, S, out)
+        assert enc.status() == 3
+        bad = dev["input_ids"].clone()
+        bad[3] = cfg.vocab
+        Q.h3enc_encode(enc.handle, bad, dev["positions"], None, None, 0, 0, None, S, out)
+        assert enc.status() == 10
+        assert enc.status() == 0   # read-and-clear
+    finally:
+        enc.close()

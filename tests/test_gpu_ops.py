@@ -1,0 +1,237 @@
+"""Per-kernel parity: each CUDA kernel, called through the C ABI, against the
+CPU oracle's function on the same seeded bf16 inputs.
+
+Tolerances: a kernel computes in fp32 and rounds its output to bf16 once, so
+an element may differ from the fp32 oracle by half a bf16 ulp (2^-8 relative)
+plus fp32 reduction-order noise; checked as |gpu - ref| <= 2^-7 |ref| + 2^-9 rms(ref)
+per element.  Integer and copy kernels are bit-exact.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+from _harness import bits_to_f32, rel_l2, t2f
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import qwen3_vl_text_gb300 as Q  # noqa: E402  (raises if the library is missing)
+
+
+def _bf16(seed, name, shape, mean=0.0, sigma=1.0):
+    bits = W.normal_bf16(seed, name, shape, mean, sigma)
+    return W.bf16_bits_to_torch(bits).cuda(), bits_to_f32(bits)
+
+
+def _elementwise_ok(gpu, ref):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rms = np.sqrt(np.mean(ref * ref))
+    bad = np.abs(gpu - ref) > (2.0 ** -7) * np.abs(ref) + (2.0 ** -9) * rms
+    return int(bad.sum()), float(np.max(np.abs(gpu - ref)) / rms)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 64), (7, 256, 136), (129, 512, 256), (300, 768, 1024),
+                                   (512, 1024, 5120)])
+def test_gemm_store(M, N, K):
+    A, a = _bf16(1, "A", (M, K))
+    Wt, w = _bf16(2, "W", (N, K), sigma=0.05)
+    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    Q.h3enc_op_gemm(A, Wt, C, M, N, K, Q.EPI_STORE)
+    torch.cuda.synchronize()
+    bad, worst = _elementwise_ok(t2f(C), O.linear(a, w))
+    assert bad == 0, f"{bad} elements off, worst {worst}"
+
+
+def test_gemm_many_tiles_and_row_tail():
+    M, N, K = 1000, 2560, 512     # 8 x 10 tiles: more tiles than one wave needs on small parts, ragged M
+    A, a = _bf16(3, "A", (M, K))
+    Wt, w = _bf16(4, "W", (N, K), sigma=0.05)
+    C = torch.full((M + 3, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    Q.h3enc_op_gemm(A, Wt, C, M, N, K, Q.EPI_STORE)
+    torch.cuda.synchronize()
+    out = t2f(C)
+    bad, worst = _elementwise_ok(out[:M], O.linear(a, w))
+    assert bad == 0, f"{bad} elements off, worst {worst}"
+    assert (out[M:] == 7.0).all(), "rows past M were written"
+
+
+def test_gemm_residual_in_place():
+    M, N, K = 200, 512, 320
+    A, a = _bf16(5, "A", (M, K))
+    Wt, w = _bf16(6, "W", (N, K), sigma=0.05)
+    R, r = _bf16(7, "R", (M, N))
+    Q.h3enc_op_gemm(A, Wt, R, M, N, K, Q.EPI_RESIDUAL, R=R)
+    torch.cuda.synchronize()
+    bad, worst = _elementwise_ok(t2f(R), r + O.linear(a, w))
+    assert bad == 0, f"{bad} elements off, worst {worst}"
+
+
+def test_gemm_swiglu_packed_gate_up():
+    M, I, K = 150, 384, 256
+    A, a = _bf16(8, "A", (M, K))
+    G, g = _bf16(9, "G", (I, K), sigma=0.06)
+    U, u = _bf16(10, "U", (I, K), sigma=0.06)
+    Wp = torch.empty(2 * I, K, dtype=torch.bfloat16, device="cuda")
+    Q.h3enc_op_pack_gate_up(G, U, Wp, I, K)
+    C = torch.empty(M, I, dtype=torch.bfloat16, device="cuda")
+    Q.h3enc_op_gemm(A, Wp, C, M, 2 * I, K, Q.EPI_SWIGLU)
+    torch.cuda.synchronize()
+    ref = O.silu(O.linear(a, g)) * O.linear(a, u)
+    bad, worst = _elementwise_ok(t2f(C), ref)
+    assert bad == 0, f"{bad} elements off, worst {worst}"
+
+
+def test_deepstack_epilogue_is_bit_exact_scatter():
+    """down GEMM + residual + DeepStack equals the plain residual result with
+    bf16(h + ds[j]) at the j-th visual row, bit for bit; other rows untouched."""
+    M, N, K = 300, 512, 384
+    A, _ = _bf16(11, "A", (M, K))
+    Wt, _ = _bf16(12, "W", (N, K), sigma=0.05)
+    R, _ = _bf16(13, "R", (M, N))
+    mask = (W.uniform_ints(14, "mask", M, 0, 3) == 0).astype(np.uint8)
+    n_vis = int(mask.sum())
+    DS, ds = _bf16(15, "DS", (n_vis, N), sigma=0.5)
+    mk = torch.from_numpy(mask).cuda()
+    rank = torch.empty(M, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Q.h3enc_op_vis_rank(mk, M, n_vis, rank, status)
+    plain = R.clone()
+    Q.h3enc_op_gemm(A, Wt, plain, M, N, K, Q.EPI_RESIDUAL, R=plain)
+    withds = R.clone()
+    Q.h3enc_op_gemm(A, Wt, withds, M, N, K, Q.EPI_RESIDUAL_DS, R=withds, DS=DS, vis_rank=rank, n_vis=n_vis,
+                    status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    p = t2f(plain)
+    expect = p.copy()
+    rows = np.nonzero(mask)[0]
+    expect[rows] = (torch.from_numpy(p[rows] + ds).to(torch.bfloat16).float().numpy())
+    got = t2f(withds)
+    assert np.array_equal(got, expect)
+
+
+def test_packed_qkv_equals_separate_projections_bitwise():
+    M, K, nq, nkv, d = 77, 512, 4, 2, 128
+    A, _ = _bf16(16, "A", (M, K))
+    Wq, _ = _bf16(17, "Wq", (nq * d, K), sigma=0.05)
+    Wk, _ = _bf16(18, "Wk", (nkv * d, K), sigma=0.05)
+    Wv, _ = _bf16(19, "Wv", (nkv * d, K), sigma=0.05)
+    Wqkv = torch.cat([Wq, Wk, Wv])
+    N = Wqkv.shape[0]
+    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    Q.h3enc_op_gemm(A, Wqkv, C, M, N, K, Q.EPI_STORE)
+    parts = []
+    for w in (Wq, Wk, Wv):
+        c = torch.empty(M, w.shape[0], dtype=torch.bfloat16, device="cuda")
+        Q.h3enc_op_gemm(A, w, c, M, w.shape[0], K, Q.EPI_STORE)
+        parts.append(c)
+    torch.cuda.synchronize()
+    assert torch.equal(C, torch.cat(parts, dim=1))
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 256), (33, 5120), (513, 5120), (3, 8192)])
+def test_rmsnorm(rows, cols):
+    X, x = _bf16(20, "x", (rows, cols), sigma=3.0)
+    G, g = _bf16(21, "g", (cols,), 1.0, 0.1)
+    Y = torch.empty_like(X)
+    Q.h3enc_op_rmsnorm(X, G, Y, rows, cols, 1e-6)
+    torch.cuda.synchronize()
+    bad, worst = _elementwise_ok(t2f(Y), O.rms_norm(x, g, 1e-6))
+    assert bad == 0, f"{bad} elements off, worst {worst}"
+
+
+@pytest.mark.parametrize("wl_id", [0, 2, 3])
+def test_rope_table(wl_id):
+    wl = W.workload(wl_id)
+    m = wl.model
+    pos = W.gen_inputs(wl)["positions"]
+    S = pos.shape[1]
+    P = torch.from_numpy(pos).cuda()
+    c = torch.empty(S, m.head_dim // 2, device="cuda")
+    s = torch.empty_like(c)
+    Q.h3enc_op_rope_table(P, S, m.head_dim, m.rope_theta, m.mrope_section, c, s)
+    torch.cuda.synchronize()
+    rc, rs = O.rope_cos_sin(pos, m.head_dim, m.rope_theta, m.mrope_section, np.float64)
+    h = m.head_dim // 2
+    assert np.max(np.abs(c.cpu().numpy() - rc[:, :h])) < 2e-6
+    assert np.max(np.abs(s.cpu().numpy() - rs[:, :h])) < 2e-6
+
+
+@pytest.mark.parametrize("d,nq,nkv", [(64, 4, 2), (128, 64, 8)])
+def test_qk_norm_rope(d, nq, nkv):
+    S = 97
+    width = (nq + 2 * nkv) * d
+    X, x = _bf16(22, "qkv", (S, width), sigma=2.0)
+    Gq, gq = _bf16(23, "gq", (d,), 1.0, 0.1)
+    Gk, gk = _bf16(24, "gk", (d,), 1.0, 0.1)
+    pos = np.stack([np.arange(S) * 3, np.arange(S) * 5 + 1, np.arange(S) * 7 + 2]).astype(np.int32)
+    sec = (24, 20, 20) if d == 128 else (12, 10, 10)
+    c = torch.empty(S, d // 2, device="cuda")
+    s = torch.empty_like(c)
+    Q.h3enc_op_rope_table(torch.from_numpy(pos).cuda(), S, d, 5e6, sec, c, s)
+    Q.h3enc_op_qk_norm_rope(X, S, nq, nkv, d, Gq, Gk, 1e-6, c, s)
+    torch.cuda.synchronize()
+    cos, sin = O.rope_cos_sin(pos, d, 5e6, sec)
+    q = O.apply_rope(O.rms_norm(x[:, :nq * d].reshape(S, nq, d), gq, 1e-6), cos, sin).reshape(S, -1)
+    k = O.apply_rope(O.rms_norm(x[:, nq * d:(nq + nkv) * d].reshape(S, nkv, d), gk, 1e-6), cos, sin).reshape(S, -1)
+    ref = np.concatenate([q, k, x[:, (nq + nkv) * d:]], axis=1)
+    got = t2f(X)
+    bad, worst = _elementwise_ok(got, ref)
+    assert bad == 0, f"{bad} elements off, worst {worst}"
+    assert np.array_equal(got[:, (nq + nkv) * d:], x[:, (nq + nkv) * d:]), "v heads changed"
+
+
+@pytest.mark.parametrize("d,nq,nkv,cu", [
+    (64, 4, 2, [0, 48]),
+    (64, 4, 1, [0, 1, 130, 131, 300]),
+    (128, 16, 2, [0, 1024]),
+    (128, 8, 8, [0, 77, 77, 333, 600]),
+])
+def test_attention(d, nq, nkv, cu):
+    S = cu[-1]
+    width = (nq + 2 * nkv) * d
+    X, x = _bf16(25, "qkv", (S, width), sigma=1.0)
+    o = torch.empty(S, nq * d, dtype=torch.bfloat16, device="cuda")
+    Q.h3enc_op_attention(X, o, S, nq, nkv, d, cu if len(cu) > 2 else None)
+    torch.cuda.synchronize()
+    q = x[:, :nq * d].reshape(S, nq, d)
+    k = x[:, nq * d:(nq + nkv) * d].reshape(S, nkv, d)
+    v = x[:, (nq + nkv) * d:].reshape(S, nkv, d)
+    ref = O.causal_gqa_attention(q, k, v, cu)
+    got = t2f(o)
+    assert rel_l2(got, ref) < 6e-3
+    assert np.max(np.abs(got - ref)) < 0.05 * np.sqrt(np.mean(ref * ref))
+
+
+def test_embed_gather_bit_exact_and_bounds():
+    vocab, H, S = 1000, 256, 70
+    T, _ = _bf16(26, "table", (vocab, H), sigma=0.02)
+    ids = W.uniform_ints(27, "ids", S, 0, vocab).astype(np.int32)
+    out = torch.empty(S, H, dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Q.h3enc_op_embed(torch.from_numpy(ids).cuda(), T, vocab, H, out, S, status)
+    torch.cuda.synchronize()
+    assert torch.equal(out, T[torch.from_numpy(ids).long().cuda()]) and int(status.item()) == 0
+    ids[5] = vocab          # out of range -> zero row and the bounds bit
+    ids[9] = -1
+    Q.h3enc_op_embed(torch.from_numpy(ids).cuda(), T, vocab, H, out, S, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 2
+    assert (out[5] == 0).all() and (out[9] == 0).all()
+
+
+def test_vis_rank_scan():
+    for S, p in ((1, 1), (5000, 3), (2049, 2)):
+        mask = (W.uniform_ints(28 + S, "m", S, 0, p) == 0).astype(np.uint8)
+        n_vis = int(mask.sum())
+        rank = torch.empty(S, dtype=torch.int32, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        Q.h3enc_op_vis_rank(torch.from_numpy(mask).cuda(), S, n_vis, rank, status)
+        torch.cuda.synchronize()
+        expect = np.where(mask == 1, np.cumsum(mask) - 1, -1)
+        assert np.array_equal(rank.cpu().numpy(), expect) and int(status.item()) == 0
+        Q.h3enc_op_vis_rank(torch.from_numpy(mask).cuda(), S, n_vis + 1, rank, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 4
