@@ -20,8 +20,8 @@ def _declared():
 
 @pytest.fixture(scope="module")
 def Q():
-    from qwen3_vl_text_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__._build_module().build()
     import qwen3_vl_text_gb300
     return qwen3_vl_text_gb300
 
