@@ -202,7 +202,9 @@ def test_attention(d, nq, nkv, cu):
     ref = O.causal_gqa_attention(q, k, v, cu)
     got = t2f(o)
     assert rel_l2(got, ref) < 6e-3
-    assert np.max(np.abs(got - ref)) < 0.05 * np.sqrt(np.mean(ref * ref))
+    # rows differ in magnitude (early rows average few keys), so bound each row by its own norm
+    row_err = np.linalg.norm(got - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
+    assert row_err.max() < 1.5e-2, f"worst row rel {row_err.max():.3g}"
 
 
 def test_embed_gather_bit_exact_and_bounds():
