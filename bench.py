@@ -151,8 +151,87 @@ def run_reference(args):
     return 0
 
 
+def run_kernel(args):
+    """One kernel of the seq-1024 workload alone, device-timed (for ncu captures and tuning).
+    Prints one JSON line with the average launch time and the achieved rate."""
+    import torch
+
+    import qwen3_vl_text_gb300 as Q
+    import workloads as W
+    wl = W.workload(WORKLOAD_ID)
+    cfg = wl.model
+    S = args.seq
+    H, I, d, nq, nkv = cfg.hidden, cfg.intermediate, cfg.head_dim, cfg.n_heads, cfg.n_kv_heads
+    dev = "cuda"
+
+    def rnd(name, shape, sigma=0.02):
+        return W.normal_bf16(7, name, shape, 0.0, sigma, device=dev)
+
+    name = args.kernel
+    if name.startswith("gemm_"):
+        shapes = {"gemm_qkv": (cfg.qkv_out, H, Q.EPI_STORE), "gemm_o": (H, nq * d, Q.EPI_RESIDUAL),
+                  "gemm_gate_up": (2 * I, H, Q.EPI_SWIGLU), "gemm_down": (H, I, Q.EPI_RESIDUAL)}
+        N, K, epi = shapes[name]
+        A = rnd("A", (S, K), 1.0)
+        Wt = rnd("W", (N, K))
+        C = torch.empty(S, N // 2 if epi == Q.EPI_SWIGLU else N, dtype=torch.bfloat16, device=dev)
+        R = C if epi == Q.EPI_RESIDUAL else None
+        fn = lambda: Q.h3enc_op_gemm(A, Wt, C, S, N, K, epi, R=R)
+        work, unit = 2.0 * S * N * K / 1e12, "TFLOP/s"
+    elif name == "attention":
+        X = rnd("qkv", (S, cfg.qkv_out), 1.0)
+        O_ = torch.empty(S, nq * d, dtype=torch.bfloat16, device=dev)
+        fn = lambda: Q.h3enc_op_attention(X, O_, S, nq, nkv, d)
+        work, unit = 4.0 * nq * d * S * (S + 1) / 2 / 1e12, "TFLOP/s"
+    elif name == "rmsnorm":
+        X = rnd("x", (S, H), 1.0)
+        G = rnd("g", (H,), 1.0)
+        Y = torch.empty_like(X)
+        fn = lambda: Q.h3enc_op_rmsnorm(X, G, Y, S, H, 1e-6)
+        work, unit = 2.0 * S * H * 2 / 1e9, "GB/s"
+    elif name == "qk_rope":
+        X = rnd("qkv", (S, cfg.qkv_out), 1.0)
+        G = rnd("g", (d,), 1.0)
+        pos = torch.arange(S, dtype=torch.int32, device=dev).repeat(3, 1).contiguous()
+        c = torch.empty(S, d // 2, device=dev)
+        s_ = torch.empty_like(c)
+        Q.h3enc_op_rope_table(pos, S, d, cfg.rope_theta, cfg.mrope_section, c, s_)
+        fn = lambda: Q.h3enc_op_qk_norm_rope(X, S, nq, nkv, d, G, G, 1e-6, c, s_)
+        work, unit = (2.0 * S * (nq + nkv) * d * 2 + 2 * S * d * 4) / 1e9, "GB/s"
+    else:
+        raise SystemExit("unknown kernel " + name)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 256 MB > L2 between launches
+    for _ in range(args.steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ts.sort()
+    ms = ts[len(ts) // 2]
+    burst, sustained, hbm, src = _peaks()
+    peak = burst if unit == "TFLOP/s" else hbm
+    print(json.dumps({"kernel": name, "seq": S, "ms_median": ms, "ms_min": ts[0], "achieved": work / (ms / 1e3),
+                      "unit": unit, "peak": peak, "frac": work / (ms / 1e3) / peak,
+                      "peak_source": f"{src} {'bf16_tflops' if unit == 'TFLOP/s' else 'hbm_gbs'} (burst)"}),
+          flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--kernel", default=None,
+                    help="time one kernel alone: gemm_qkv, gemm_o, gemm_gate_up, gemm_down, attention, rmsnorm, "
+                         "qk_rope")
+    ap.add_argument("--seq", type=int, default=1024)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
@@ -161,6 +240,8 @@ def main():
     ap.add_argument("--cpu-layers", type=int, default=2)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.kernel:
+        return run_kernel(args)
     if args.impl == "reference":
         return run_reference(args)
 

@@ -232,7 +232,7 @@ def test_vis_rank_scan():
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
         Q.h3enc_op_vis_rank(torch.from_numpy(mask).cuda(), S, n_vis, rank, status)
         torch.cuda.synchronize()
-        expect = np.where(mask == 1, np.cumsum(mask) - 1, -1)
+        expect = np.where(mask == 1, np.cumsum(mask.astype(np.int64)) - 1, -1)
         assert np.array_equal(rank.cpu().numpy(), expect) and int(status.item()) == 0
         Q.h3enc_op_vis_rank(torch.from_numpy(mask).cuda(), S, n_vis + 1, rank, status)
         torch.cuda.synchronize()
