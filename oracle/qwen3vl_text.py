@@ -18,7 +18,7 @@ __all__ = [
     "bf16_bits_to_float", "round_to_bf16", "linear", "rms_norm", "rope_inv_freq",
     "mrope_axis_of_pair", "rope_cos_sin", "rotate_half", "apply_rope", "silu",
     "causal_gqa_attention", "deepstack_add", "decoder_layer", "forward", "LayerWeights",
-    "layer_weights_from_bits",
+    "layer_weights_from_bits", "STORAGE_POINTS",
 ]
 
 
@@ -199,8 +199,17 @@ def layer_weights_from_bits(named_bits: dict, dtype=np.float32) -> LayerWeights:
     return lw
 
 
+STORAGE_POINTS = ("y", "qk_proj", "v", "qk", "attn", "act", "h")
+
+
+def _store(t: np.ndarray, point: str, storage) -> np.ndarray:
+    """Hand tensor ``t`` to the next step: unchanged, or rounded to bf16 when
+    ``point`` is in ``storage`` (a set of names from ``STORAGE_POINTS``)."""
+    return round_to_bf16(t).astype(t.dtype, copy=False) if storage and point in storage else t
+
+
 def decoder_layer(x: np.ndarray, w: LayerWeights, cos: np.ndarray, sin: np.ndarray, cfg,
-                  cu_seqlens=None) -> np.ndarray:
+                  cu_seqlens=None, storage=None) -> np.ndarray:
     """One decoder layer (page 1, ``MiniMaxH3Qwen3VLTextDecoderLayer.forward``).
 
     residual = x; y = input_layernorm(x); attention; x = residual + attn;
@@ -208,29 +217,36 @@ def decoder_layer(x: np.ndarray, w: LayerWeights, cos: np.ndarray, sin: np.ndarr
     Attention (``MiniMaxH3Qwen3VLTextAttention.forward``): q/k/v projections,
     per-head q_norm/k_norm over head_dim, M-RoPE on q and k, causal GQA SDPA,
     o_proj.  MLP (``MiniMaxH3Qwen3VLTextMLP.forward``): down(silu(gate) * up).
+
+    ``storage`` (default None: every tensor exact) names the hand-over points
+    rounded to bf16, as a BF16 model stores them: "y" (norm outputs), "qk_proj"
+    (q/k projections), "v" (v projection), "qk" (q/k after norm and RoPE),
+    "attn" (attention output),
+    "act" (SwiGLU output), "h" (residual stream).  With all of them this is the
+    rounding floor of a pipeline that keeps exactly those tensors in bf16.
     """
     s = x.shape[0]
     d, nq, nkv = cfg.head_dim, cfg.n_heads, cfg.n_kv_heads
     residual = x
-    y = rms_norm(x, w["input_layernorm"], cfg.rms_eps)
-    q = linear(y, w["q_proj"]).reshape(s, nq, d)
-    k = linear(y, w["k_proj"]).reshape(s, nkv, d)
-    v = linear(y, w["v_proj"]).reshape(s, nkv, d)
+    y = _store(rms_norm(x, w["input_layernorm"], cfg.rms_eps), "y", storage)
+    q = _store(linear(y, w["q_proj"]), "qk_proj", storage).reshape(s, nq, d)
+    k = _store(linear(y, w["k_proj"]), "qk_proj", storage).reshape(s, nkv, d)
+    v = _store(linear(y, w["v_proj"]), "v", storage).reshape(s, nkv, d)
     q = rms_norm(q, w["q_norm"], cfg.rms_eps)
     k = rms_norm(k, w["k_norm"], cfg.rms_eps)
-    q = apply_rope(q, cos, sin)
-    k = apply_rope(k, cos, sin)
-    attn = causal_gqa_attention(q, k, v, cu_seqlens)
-    x = residual + linear(attn, w["o_proj"])
+    q = _store(apply_rope(q, cos, sin), "qk", storage)
+    k = _store(apply_rope(k, cos, sin), "qk", storage)
+    attn = _store(causal_gqa_attention(q, k, v, cu_seqlens), "attn", storage)
+    x = _store(residual + linear(attn, w["o_proj"]), "h", storage)
     residual = x
-    y = rms_norm(x, w["post_attention_layernorm"], cfg.rms_eps)
-    act = silu(linear(y, w["gate_proj"])) * linear(y, w["up_proj"])
-    return residual + linear(act, w["down_proj"])
+    y = _store(rms_norm(x, w["post_attention_layernorm"], cfg.rms_eps), "y", storage)
+    act = _store(silu(linear(y, w["gate_proj"])) * linear(y, w["up_proj"]), "act", storage)
+    return _store(residual + linear(act, w["down_proj"]), "h", storage)
 
 
 def forward(inputs_embeds: np.ndarray, positions: np.ndarray, cfg, get_layer,
             visual_mask=None, deepstack=None, cu_seqlens=None, layers=None,
-            capture=None, dtype=np.float32) -> np.ndarray:
+            capture=None, dtype=np.float32, storage=None) -> np.ndarray:
     """Text-model forward returning the unnormalised last hidden state.
 
     Page 1, ``MiniMaxH3Qwen3VLTextModel.forward``: cos/sin computed once from
@@ -240,16 +256,17 @@ def forward(inputs_embeds: np.ndarray, positions: np.ndarray, cfg, get_layer,
     the state after the last kept layer).  ``get_layer(l)`` returns
     ``LayerWeights``; ``layers`` (default ``range(cfg.num_layers)``) allows a
     sub-range with global layer indices; ``capture`` (a list) receives the
-    state after every layer.
+    state after every layer; ``storage`` as in ``decoder_layer`` (the
+    DeepStack sum is a residual-stream hand-over, point "h").
     """
     x = np.asarray(inputs_embeds, dtype=dtype)
     cos, sin = rope_cos_sin(positions, cfg.head_dim, cfg.rope_theta, cfg.mrope_section, dtype)
     if layers is None:
         layers = range(cfg.num_layers)
     for l in layers:
-        x = decoder_layer(x, get_layer(l), cos, sin, cfg, cu_seqlens)
+        x = decoder_layer(x, get_layer(l), cos, sin, cfg, cu_seqlens, storage)
         if deepstack is not None and l < len(deepstack):
-            x = deepstack_add(x, visual_mask, np.asarray(deepstack[l], dtype=dtype))
+            x = _store(deepstack_add(x, visual_mask, np.asarray(deepstack[l], dtype=dtype)), "h", storage)
         if capture is not None:
             capture.append(x.copy())
     return x

@@ -23,6 +23,31 @@ def max_abs_over_rms(a, b) -> float:
     return float(np.max(np.abs(a - b)) / max(np.sqrt(np.mean(b * b)), 1e-30))
 
 
+# Tensors the GPU path hands between kernels in bf16 (its rounding points).
+GPU_STORAGE = frozenset({"y", "qk_proj", "v", "qk", "attn", "act", "h"})
+
+
+def within(gpu, ref32, refbf, rel_bar, maxabs_bar=None):
+    """Tolerance rule of the parity tests.  ``ref32`` is the fp32 oracle,
+    ``refbf`` the same oracle rounding to bf16 at GPU_STORAGE.  Relative L2 of
+    the GPU against ref32 must stay within the stated bar, or within 1.25x the
+    bf16-storage floor (refbf against ref32) + 2e-3 where that floor is higher
+    than the bar.  Same rule for max|diff|/RMS with slack 0.01.
+    Returns (ok, message)."""
+    r = rel_l2(gpu, ref32)
+    fl = rel_l2(refbf, ref32)
+    r_lim = max(rel_bar, 1.25 * fl + 2e-3)
+    ok = r <= r_lim
+    msg = f"rel {r:.3g} (limit {r_lim:.3g}; bar {rel_bar:g}, bf16 floor {fl:.3g})"
+    if maxabs_bar is not None:
+        m = max_abs_over_rms(gpu, ref32)
+        mf = max_abs_over_rms(refbf, ref32)
+        m_lim = max(maxabs_bar, 1.25 * mf + 0.01)
+        ok = ok and m <= m_lim
+        msg += f"; max/rms {m:.3g} (limit {m_lim:.3g}; bar {maxabs_bar:g}, floor {mf:.3g})"
+    return ok, msg
+
+
 def bits_to_f32(bits: np.ndarray) -> np.ndarray:
     """bf16 bit patterns -> float32 (multithreaded via torch; exact)."""
     import torch

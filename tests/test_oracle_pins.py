@@ -353,3 +353,23 @@ def test_float32_oracle_tracks_float64():
                     ds32, dtype=np.float32)
     rel = np.linalg.norm(r32 - r64) / np.linalg.norm(r64)
     assert rel < 1e-5
+
+
+def test_bf16_storage_variant_rounds_only_at_hand_over_points():
+    """With every storage point the layer output is bf16-representable; with
+    none it is the exact forward; zero output projections keep the identity
+    for a bf16-representable input."""
+    wl, cfg, inp, emb, ds = _tiny_case(np.float32)
+    get = _tiny_weights(cfg, wl.seed, np.float32)
+    exact = O.forward(emb, inp["positions"], cfg, get, dtype=np.float32)
+    assert np.array_equal(O.forward(emb, inp["positions"], cfg, get, dtype=np.float32, storage=set()), exact)
+    allp = O.forward(emb, inp["positions"], cfg, get, dtype=np.float32, storage=set(O.STORAGE_POINTS))
+    assert np.array_equal(O.round_to_bf16(allp), allp)
+    rel = np.linalg.norm(allp - exact) / np.linalg.norm(exact)
+    assert 1e-4 < rel < 3e-2
+    w = get(0)
+    w["o_proj"] = np.zeros_like(w["o_proj"])
+    w["down_proj"] = np.zeros_like(w["down_proj"])
+    x = O.round_to_bf16(_rng(16).standard_normal((6, cfg.hidden)).astype(np.float32))
+    c, s = O.rope_cos_sin(np.stack([np.arange(6)] * 3), cfg.head_dim, cfg.rope_theta, cfg.mrope_section)
+    assert np.array_equal(O.decoder_layer(x, w, c, s, cfg, storage=set(O.STORAGE_POINTS)), x)
