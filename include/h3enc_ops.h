@@ -34,11 +34,20 @@ enum {
  * of MiniMaxH3Qwen3VLTextDecoderLayer.forward and _deepstack_process).
  *   A [M, K] (lda = K), W [N, K] (ldw = K), C [M, ldc]: ldc = N, or N/2 for SWIGLU.
  *   R [M, ldc] residual (RESIDUAL*), DS [n_vis, ldc] and vis_rank [M] (RESIDUAL_DS).
+ *   workspace: NULL, or device memory of at least h3enc_op_gemm_workspace_bytes()
+ *   bytes, 256-byte aligned, zero-filled once before its first use and then
+ *   reused; with it the tiles of a partial last wave are split along K over the
+ *   idle SMs (the result is deterministic for given M, N, K).  Calls sharing a
+ *   workspace must not overlap on the GPU.
  * Requires K % 8 == 0, N % 256 == 0 (of the packed weight for SWIGLU), A and W
  * 16-byte aligned.  M may be any size >= 0. */
 H3ENC_API h3enc_status h3enc_op_gemm(const void *A, const void *W, void *C, int32_t M, int32_t N, int32_t K,
                            int32_t epilogue, const void *R, const void *DS, const int32_t *vis_rank,
-                           int32_t n_vis, int32_t *status, void *stream);
+                           int32_t n_vis, void *workspace, int64_t workspace_bytes, int32_t *status,
+                           void *stream);
+
+/* Workspace bytes h3enc_op_gemm needs on the current device (-1 without a device). */
+H3ENC_API int64_t h3enc_op_gemm_workspace_bytes(void);
 
 /* Pack gate [I, K] and up [I, K] into W [2I, K] for H3ENC_EPI_SWIGLU: rows
  * [256b, 256b+128) = gate rows [128b, 128b+128), rows [256b+128, 256b+256) =

@@ -56,6 +56,8 @@ struct h3enc {
     bf16 *y = nullptr, *qkv = nullptr, *attn = nullptr, *act = nullptr;
     float *cos_t = nullptr, *sin_t = nullptr;
     int32_t *vis_rank = nullptr, *status = nullptr;
+    float *gemm_part = nullptr;      // split-GEMM partials (num_sms x 128 x 256 fp32)
+    uint32_t *gemm_flags = nullptr;  // split-GEMM release flags
     int32_t *st_ids = nullptr, *st_pos = nullptr;
     uint8_t *st_mask = nullptr;
     bf16 *st_ds = nullptr, *st_out = nullptr;
@@ -243,6 +245,8 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         h3::GemmPlan p{};
         p.num_sms = h->num_sms;
         p.status = h->status;
+        p.part = h->gemm_part;
+        p.flags = h->gemm_flags;
         p.M = S;
         p.tmA = &h->tm_y; p.tmW = &w.tm_qkv; p.N = h->qkv_out; p.K = H; p.epi = h3::EPI_STORE;
         p.C = h->qkv; p.ldc = h->qkv_out;
@@ -332,8 +336,10 @@ h3enc_status h3enc_create(const h3enc_config *cfg, h3enc **out) {
                  b_attn = align256(T * c.n_heads * c.head_dim * 2), b_act = align256(T * c.intermediate * 2),
                  b_cs = align256(T * (c.head_dim / 2) * 4), b_rank = align256(T * 4), b_stat = 256,
                  b_ids = align256(T * 4), b_pos = align256(3 * T * 4), b_mask = align256(T),
-                 b_ds = align256((size_t)c.num_deepstack * T * H * 2), b_out = b_y;
-    const size_t wsz = b_y + b_qkv + b_attn + b_act + 2 * b_cs + b_rank + b_stat + b_ids + b_pos + b_mask + b_ds + b_out;
+                 b_ds = align256((size_t)c.num_deepstack * T * H * 2), b_out = b_y,
+                 b_gemm = align256(h3::gemm_workspace_bytes(h->num_sms));
+    const size_t wsz = b_y + b_qkv + b_attn + b_act + 2 * b_cs + b_rank + b_stat + b_ids + b_pos + b_mask + b_ds +
+                       b_out + b_gemm;
     e = cudaMalloc(&h->ws, wsz);
     if (e != cudaSuccess) {
         cudaFree(h->arena);
@@ -354,6 +360,9 @@ h3enc_status h3enc_create(const h3enc_config *cfg, h3enc **out) {
     h->st_mask = reinterpret_cast<uint8_t *>(p); p += b_mask;
     h->st_ds = reinterpret_cast<bf16 *>(p); p += b_ds;
     h->st_out = reinterpret_cast<bf16 *>(p); p += b_out;
+    h->gemm_part = reinterpret_cast<float *>(p);
+    h->gemm_flags = reinterpret_cast<uint32_t *>(p + (size_t)h->num_sms * 128 * 256 * sizeof(float) + 256);
+    p += b_gemm;
     e = cudaMemset(h->ws, 0, wsz);
     if (e != cudaSuccess) {
         h3enc_destroy(h);
@@ -629,9 +638,14 @@ int32_t h3enc_num_sms(const h3enc *h) { return h ? h->num_sms : 0; }
 
 // ---------------------------------------------------------------- op-level entries
 
+int64_t h3enc_op_gemm_workspace_bytes(void) {
+    const int sms = h3::device_num_sms();
+    return sms > 0 ? (int64_t)h3::gemm_workspace_bytes(sms) : -1;
+}
+
 h3enc_status h3enc_op_gemm(const void *A, const void *W, void *C, int32_t M, int32_t N, int32_t K, int32_t epilogue,
-                           const void *R, const void *DS, const int32_t *vis_rank, int32_t n_vis, int32_t *status,
-                           void *stream) {
+                           const void *R, const void *DS, const int32_t *vis_rank, int32_t n_vis, void *workspace,
+                           int64_t workspace_bytes, int32_t *status, void *stream) {
     if (M < 0 || N <= 0 || K <= 0 || N % 256 || K % 8 || epilogue < 0 || epilogue > 3)
         return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm: bad sizes or epilogue");
     if (M == 0) return H3ENC_OK;
@@ -652,6 +666,15 @@ h3enc_status h3enc_op_gemm(const void *A, const void *W, void *C, int32_t M, int
     p.n_vis = n_vis;
     p.status = status;
     p.num_sms = h3::device_num_sms();
+    if (workspace) {
+        if (workspace_bytes < (int64_t)h3::gemm_workspace_bytes(p.num_sms) ||
+            (reinterpret_cast<uintptr_t>(workspace) & 255))
+            return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm: workspace smaller than h3enc_op_gemm_workspace_bytes() "
+                                                        "or not 256-byte aligned");
+        p.part = static_cast<float *>(workspace);
+        p.flags = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) +
+                                               (size_t)p.num_sms * 128 * 256 * sizeof(float) + 256);
+    }
     cudaError_t e = h3::launch_gemm(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "gemm launch");
 }

@@ -15,9 +15,19 @@
 //              issues tcgen05.mma (M=128, N=256, K=16) from one thread
 //   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes (= 32 output rows),
 //              fused element-wise op, bf16 stores; overlaps the next tile's MMAs
+// Schedule: the tiles of the full waves run data-parallel (tile = CTA + i*grid,
+// M-fastest, so the CTAs in flight share each weight tile through L2).  The
+// tiles of the last, partial wave would leave most SMs idle, so each of them is
+// split along K into s chunks (s = grid / leftover tiles) computed by s CTAs:
+// every chunk's fp32 partial goes to a workspace slot, a per-slot flag is
+// released, and each contributing CTA then sums the s partials of its tile in
+// fixed chunk order for a slice of the tile's rows and applies the epilogue
+// (deterministic; the grid is launched cooperatively so all CTAs are resident).
 // Every wait is bounded; on time-out the CTA records ST_TIMEOUT, drains its
 // in-flight copies and MMAs, frees TMEM and exits.
 #include <cudaTypedefs.h>
+
+#include <atomic>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -43,7 +53,51 @@ struct GemmArgs {
     const int32_t *vis_rank;
     int n_vis;
     int32_t *status;
+    // split of the last partial wave
+    int dp_tiles;      // tiles run data-parallel: [0, dp_tiles)
+    int splits;        // s > 1: tiles [dp_tiles, nm*nn) are split into s K-chunks
+    float *part;       // [grid][BM*BN] fp32 partial accumulators
+    uint32_t *flags;   // [grid] release flags
+    uint32_t epoch;    // unique per launch; a flag equal to it means "partial written"
 };
+
+// The K-chunk of the split item of this CTA (none when kb1 <= kb0).
+struct SplitItem {
+    int tile, kb0, kb1, chunk;
+};
+__device__ __forceinline__ SplitItem split_item(const GemmArgs &g) {
+    SplitItem it{0, 0, 0, 0};
+    const int left = g.nm * g.nn - g.dp_tiles;
+    if (g.splits > 1 && (int)blockIdx.x < left * g.splits) {
+        it.tile = g.dp_tiles + blockIdx.x / g.splits;
+        it.chunk = blockIdx.x % g.splits;
+        it.kb0 = it.chunk * g.nk / g.splits;
+        it.kb1 = (it.chunk + 1) * g.nk / g.splits;
+    }
+    return it;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Barrier over the four epilogue warps (named barrier 1) returning the AND of v.
+__device__ __forceinline__ bool epi_bar_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
 
 __device__ __forceinline__ void load_row32(const __nv_bfloat16 *p, float (&f)[32]) {
     const uint4 *q = reinterpret_cast<const uint4 *>(p);
@@ -115,7 +169,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int num_tiles = g.nm * g.nn;
+    const SplitItem sk = split_item(g);
+    const bool has_split = sk.kb1 > sk.kb0;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -125,18 +180,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             #pragma unroll
             for (int s = 0; s < STAGES; ++s) issued[s] = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            auto load_item = [&](int tile, int kb0, int kb1) {
                 const int m0 = (tile % g.nm) * BM;
                 const int n0 = (tile / g.nm) * BN;
-                for (int kb = 0; kb < g.nk; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; return; }
                     mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
                     tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m0);
                     tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, n0);
                     ++issued[stage];
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
-            }
+            };
+            for (int tile = blockIdx.x; ok && tile < g.dp_tiles; tile += gridDim.x) load_item(tile, 0, g.nk);
+            if (ok && has_split) load_item(sk.tile, sk.kb0, sk.kb1);
             if (!ok) {
                 report(g.status, ST_TIMEOUT);
                 *abort_flag = 1;
@@ -154,27 +211,28 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+            auto mma_item = [&](int kb0, int kb1) {
+                if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; return; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < g.nk; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; return; }
                     tc_fence_after();
                     const uint32_t a_base = smem_u32(sA + stage * A_BYTES);
                     const uint32_t b_base = smem_u32(sB + stage * B_BYTES);
                     #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         umma_bf16(d_tmem, sdesc_sw128(a_base + kk * 32), sdesc_sw128(b_base + kk * 32), idesc,
-                                  (kb | kk) != 0);
+                                  (kb > kb0 || kk > 0) ? 1u : 0u);
                     umma_commit(&empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
-                if (!ok) break;
                 umma_commit(&acc_full[acc]);
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
-            }
+            };
+            for (int tile = blockIdx.x; ok && tile < g.dp_tiles; tile += gridDim.x) mma_item(0, g.nk);
+            if (ok && has_split) mma_item(sk.kb0, sk.kb1);
             if (!ok) {
                 report(g.status, ST_TIMEOUT);
                 *abort_flag = 1;
@@ -187,21 +245,35 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     } else {
         // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 = tile rows of the same range
         const int quarter = warp & 3;
+        const int et = threadIdx.x - 64;  // 0..127 over the four epilogue warps
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            const int m_blk = tile % g.nm;
-            const int n_blk = tile / g.nm;
-            bool ok = mbar_wait(&acc_full[acc], acc_phase, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) {
+        bool ok = true;
+        auto wait_acc = [&]() {
+            bool w = mbar_wait(&acc_full[acc], acc_phase, abort_flag);
+            w = __all_sync(0xffffffffu, w);
+            if (!w) {
                 if (lane == 0) {
                     report(g.status, ST_TIMEOUT);
                     *abort_flag = 1;
                 }
-                break;
+                ok = false;
+                return false;
             }
             tc_fence_after();
+            return true;
+        };
+        auto release_acc = [&]() {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        };
+        for (int tile = blockIdx.x; tile < g.dp_tiles; tile += gridDim.x) {
+            const int m_blk = tile % g.nm;
+            const int n_blk = tile / g.nm;
+            if (!wait_acc()) break;
             const int row = m_blk * BM + quarter * 32 + lane;
             const bool live = row < g.M;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
@@ -259,11 +331,94 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1u;
+            release_acc();
+        }
+        if (has_split) {
+            // 1) dump this chunk's fp32 accumulator to workspace slot blockIdx.x, row-major [BM][BN]
+            //    (every epilogue warp reaches the barrier below exactly once, failed or not)
+            const bool got = ok && wait_acc();
+            if (got) {
+                const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+                float *dst = g.part + (size_t)blockIdx.x * (BM * BN) + (size_t)(quarter * 32 + lane) * BN;
+                #pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(taddr + c * 32, v);
+                    tmem_ld_wait();
+                    float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+                    #pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                }
+                release_acc();
+            }
+            __threadfence();
+            if (epi_bar_and(got)) {
+                if (et == 0) st_release(g.flags + blockIdx.x, g.epoch);
+                // 2) wait for the s chunks of this tile
+                const int first = blockIdx.x - sk.chunk;
+                bool all = true;
+                const long long t0 = clock64();
+                for (int j = 0; j < g.splits && all; ++j) {
+                    while (ld_acquire(g.flags + first + j) != g.epoch) {
+                        if (clock64() - t0 > kSpinLimitCycles) { all = false; break; }
+                    }
+                }
+                if (!all) {
+                    if (et == 0) report(g.status, ST_TIMEOUT);
+                } else {
+                    // 3) this CTA finishes rows [r0, r1) of the tile: sum of the s partials in chunk order
+                    const int r0 = sk.chunk * BM / g.splits, r1 = (sk.chunk + 1) * BM / g.splits;
+                    const int m_blk = sk.tile % g.nm, n_blk = sk.tile / g.nm;
+                    constexpr int UNITS_PER_ROW = (EPI == EPI_SWIGLU) ? BN / 8 : BN / 4;  // float4 groups
+                    const int units = (r1 - r0) * UNITS_PER_ROW;
+                    const float *base = g.part + (size_t)first * (BM * BN);
+                    for (int u = et; u < units; u += 128) {
+                        const int r = r0 + u / UNITS_PER_ROW;
+                        const int c4 = (u % UNITS_PER_ROW) * 4;
+                        const int row = m_blk * BM + r;
+                        if (row >= g.M) continue;
+                        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+                        for (int j = 0; j < g.splits; ++j) {
+                            const float *pj = base + (size_t)j * (BM * BN) + (size_t)r * BN;
+                            const float4 x = __ldcg(reinterpret_cast<const float4 *>(pj + c4));
+                            a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+                            if constexpr (EPI == EPI_SWIGLU) {
+                                const float4 y = __ldcg(reinterpret_cast<const float4 *>(pj + BN / 2 + c4));
+                                b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+                            }
+                        }
+                        float f[4] = {a.x, a.y, a.z, a.w};
+                        int col;
+                        if constexpr (EPI == EPI_SWIGLU) {
+                            const float up[4] = {b.x, b.y, b.z, b.w};
+                            #pragma unroll
+                            for (int j = 0; j < 4; ++j) f[j] = f[j] / (1.0f + expf(-f[j])) * up[j];
+                            col = n_blk * (BN / 2) + c4;
+                        } else {
+                            col = n_blk * BN + c4;
+                            if constexpr (EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_DS) {
+                                const uint2 rv = *reinterpret_cast<const uint2 *>(g.R + (size_t)row * g.ldc + col);
+                                f[0] += bf16_lo(rv.x); f[1] += bf16_hi(rv.x); f[2] += bf16_lo(rv.y); f[3] += bf16_hi(rv.y);
+                            }
+                            if constexpr (EPI == EPI_RESIDUAL_DS) {
+                                int rank = g.DS != nullptr ? g.vis_rank[row] : -1;
+                                if (rank >= g.n_vis) rank = -1;
+                                if (rank >= 0) {
+                                    const uint2 dv = *reinterpret_cast<const uint2 *>(g.DS + (size_t)rank * g.ldc + col);
+                                    f[0] = round_bf16(f[0]) + bf16_lo(dv.x); f[1] = round_bf16(f[1]) + bf16_hi(dv.x);
+                                    f[2] = round_bf16(f[2]) + bf16_lo(dv.y); f[3] = round_bf16(f[3]) + bf16_hi(dv.y);
+                                }
+                            }
+                        }
+                        uint2 o;
+                        o.x = pack_bf16x2(f[0], f[1]);
+                        o.y = pack_bf16x2(f[2], f[3]);
+                        *reinterpret_cast<uint2 *>(g.C + (size_t)row * g.ldc + col) = o;
+                    }
+                }
+            }
         }
     }
 
@@ -287,6 +442,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+uint32_t next_epoch() {
+    static std::atomic<uint32_t> epoch{0};
+    uint32_t e = ++epoch;
+    if (e == 0) e = ++epoch;  // 0 is the value of a fresh flag
+    return e;
+}
+
 template <int EPI>
 cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     static bool attr_set = false;
@@ -304,9 +466,30 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     g.C = p.C; g.ldc = p.ldc; g.R = p.R; g.DS = p.DS; g.vis_rank = p.vis_rank; g.n_vis = p.n_vis;
     g.status = p.status;
     const int tiles = g.nm * g.nn;
-    const int grid = tiles < p.num_sms ? tiles : p.num_sms;
-    gemm_tcgen05_kernel<EPI><<<grid, GEMM_THREADS, SMEM_BYTES, stream>>>(*p.tmA, *p.tmW, g);
-    return cudaGetLastError();
+    const int sms = p.num_sms > 0 ? p.num_sms : 1;
+    // full waves data-parallel; the tiles of a partial last wave split along K over the idle SMs
+    const int left = tiles % sms;
+    int splits = (p.part && p.flags && left) ? sms / left : 1;
+    if (splits > g.nk / 2) splits = g.nk / 2;
+    if (splits > 32) splits = 32;
+    if (splits < 2) splits = 1;
+    g.splits = splits;
+    g.dp_tiles = splits > 1 ? tiles - left : tiles;
+    g.part = p.part;
+    g.flags = p.flags;
+    g.epoch = splits > 1 ? next_epoch() : 0u;
+    const int grid = splits > 1 ? sms : (tiles < sms ? tiles : sms);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;   // split CTAs wait on one another: all must be resident
+    cfg.attrs = attr;
+    cfg.numAttrs = splits > 1 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<EPI>, *p.tmA, *p.tmW, g);
 }
 
 }  // namespace
@@ -326,6 +509,7 @@ bool make_tmap_rows(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t col
 }
 
 int gemm_box_rows_a() { return BM; }
+size_t gemm_workspace_bytes(int num_sms) { return (size_t)num_sms * BM * BN * sizeof(float) + 256 + (size_t)num_sms * 4; }
 int gemm_box_rows_w() { return BN; }
 
 cudaError_t launch_gemm(const GemmPlan &p, cudaStream_t stream) {

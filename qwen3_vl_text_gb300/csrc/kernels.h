@@ -28,12 +28,16 @@ struct GemmPlan {
     int n_vis;
     int32_t *status;
     int num_sms;
+    float *part;        // split workspace: num_sms x 128 x 256 fp32 partials (NULL: no split)
+    uint32_t *flags;    // num_sms release flags, zero-filled once before first use
 };
 // Tensor map of a row-major bf16 matrix [rows, cols] read in boxes of
 // box_rows x 64 with 128-byte swizzle.  False if the driver refuses it.
 bool make_tmap_rows(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
 int gemm_box_rows_a();
 int gemm_box_rows_w();
+// Bytes of a split workspace (partials then flags) for a grid of num_sms CTAs.
+size_t gemm_workspace_bytes(int num_sms);
 cudaError_t launch_gemm(const GemmPlan &p, cudaStream_t stream);
 
 // ---- norms and rotary embedding (norm_rope.cu)

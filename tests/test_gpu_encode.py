@@ -6,7 +6,8 @@ final output relative L2 <= 2e-2 and max |diff| <= 0.05 * RMS(out) for free
 runs.  Where the oracle's own bf16-storage variant (rounding exactly where the
 GPU path stores bf16) is already further than a bar from the fp32 oracle, the
 bar becomes 1.25x that floor + slack (see ``_harness.within``).  Bit-exact for
-the properties that hold at any size (determinism, zero DeepStack).
+determinism and zero DeepStack; causal-prefix and packing properties hold up to
+fp32 summation order (the GEMM's tail split depends on the token count).
 """
 import numpy as np
 import pytest
@@ -172,7 +173,7 @@ def test_packed_prompts_two_full_width_layers():
             one = {"positions": dev["positions"][:, a:b].contiguous(), "input_ids": dev["input_ids"][a:b],
                    "visual_mask": None, "deepstack": None, "inputs_embeds": None}
             sep = _run_gpu(enc, one, {"n_vis": 0, "cu_seqlens": np.array([0, b - a])}, b - a)
-            assert torch.equal(sep, full[a:b]), f"prompt {i}"
+            assert rel_l2(t2f(sep), t2f(full[a:b])) < 5e-3, f"prompt {i}"
     finally:
         enc.close()
 
@@ -211,7 +212,8 @@ def test_full_depth_image_encode_prefix_rows():
         pre = {"positions": dev["positions"][:, :P].contiguous(), "input_ids": dev["input_ids"][:P],
                "visual_mask": dev["visual_mask"][:P], "deepstack": dev["deepstack"][:, :n_vis_p].contiguous(),
                "inputs_embeds": None}
-        assert torch.equal(_run_gpu(enc, pre, pre_inp, P), out[:P]), "causal prefix differs"
+        # the prefix run splits GEMM tiles differently (different M), so fp32 sums may round differently
+        assert rel_l2(t2f(_run_gpu(enc, pre, pre_inp, P)), t2f(out[:P])) < 5e-3, "causal prefix differs"
         x0 = oracle_embed(wl, cfg, inp["input_ids"][:P])
         ds = bits_to_f32(inp["deepstack"])[:, :n_vis_p]
         get = oracle_layer_getter(wl, cfg)

@@ -131,6 +131,84 @@ def test_packed_qkv_equals_separate_projections_bitwise():
     assert torch.equal(C, torch.cat(parts, dim=1))
 
 
+def _workspace():
+    nbytes = Q.h3enc_op_gemm_workspace_bytes()
+    return torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("epi", [Q.EPI_STORE, Q.EPI_RESIDUAL, Q.EPI_SWIGLU])
+def test_gemm_split_last_wave(epi):
+    """tiles = SMs + a few: the partial last wave is split along K over all SMs."""
+    sms = _sms()
+    nm = 8
+    nn = sms // nm + 1                       # nm*nn just above the SM count
+    M, N, K = nm * 128 - 37, nn * 256, 2048  # ragged M inside the last m-block
+    A, a = _bf16(30, "A", (M, K))
+    ws = _workspace()
+    if epi == Q.EPI_SWIGLU:
+        I = N // 2
+        G, gg = _bf16(31, "G", (I, K), sigma=0.03)
+        U, uu = _bf16(32, "U", (I, K), sigma=0.03)
+        Wt = torch.empty(N, K, dtype=torch.bfloat16, device="cuda")
+        Q.h3enc_op_pack_gate_up(G, U, Wt, I, K)
+        ref = O.silu(O.linear(a, gg)) * O.linear(a, uu)
+        C = torch.empty(M, I, dtype=torch.bfloat16, device="cuda")
+        R = None
+    else:
+        Wt, w = _bf16(33, "W", (N, K), sigma=0.03)
+        C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        ref = O.linear(a, w)
+        R = None
+        if epi == Q.EPI_RESIDUAL:
+            R, r = _bf16(34, "R", (M, N))
+            C = R.clone()
+            R = C
+            ref = r + ref
+    R0 = None if R is None else R.clone()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Q.h3enc_op_gemm(A, Wt, C, M, N, K, epi, R=R, workspace=ws, status=status)
+    first = C.clone()
+    if R is not None:
+        C.copy_(R0)
+    Q.h3enc_op_gemm(A, Wt, C, M, N, K, epi, R=R, workspace=ws, status=status)   # same workspace again
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(first, C), "split GEMM not deterministic"
+    bad, worst = _elementwise_ok(t2f(C), ref)
+    assert bad == 0, f"{bad} elements off, worst {worst}"
+
+
+def test_deepstack_epilogue_bit_exact_with_split_tiles():
+    sms = _sms()
+    nm = 8
+    nn = sms // nm + 1
+    M, N, K = nm * 128, nn * 256, 1024
+    A, _ = _bf16(35, "A", (M, K))
+    Wt, _ = _bf16(36, "W", (N, K), sigma=0.03)
+    R, _ = _bf16(37, "R", (M, N))
+    mask = (W.uniform_ints(38, "mask", M, 0, 2) == 0).astype(np.uint8)
+    n_vis = int(mask.sum())
+    DS, ds = _bf16(39, "DS", (n_vis, N), sigma=0.5)
+    rank = torch.empty(M, dtype=torch.int32, device="cuda")
+    Q.h3enc_op_vis_rank(torch.from_numpy(mask).cuda(), M, n_vis, rank)
+    ws = _workspace()
+    plain = R.clone()
+    Q.h3enc_op_gemm(A, Wt, plain, M, N, K, Q.EPI_RESIDUAL, R=plain, workspace=ws)
+    withds = R.clone()
+    Q.h3enc_op_gemm(A, Wt, withds, M, N, K, Q.EPI_RESIDUAL_DS, R=withds, DS=DS, vis_rank=rank, n_vis=n_vis,
+                    workspace=ws)
+    torch.cuda.synchronize()
+    p = t2f(plain)
+    expect = p.copy()
+    rows = np.nonzero(mask)[0]
+    expect[rows] = torch.from_numpy(p[rows] + ds).to(torch.bfloat16).float().numpy()
+    assert np.array_equal(t2f(withds), expect)
+
+
 @pytest.mark.parametrize("rows,cols", [(1, 256), (33, 5120), (513, 5120), (3, 8192)])
 def test_rmsnorm(rows, cols):
     X, x = _bf16(20, "x", (rows, cols), sigma=3.0)
