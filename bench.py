@@ -176,7 +176,8 @@ def run_kernel(args):
         Wt = rnd("W", (N, K))
         C = torch.empty(S, N // 2 if epi == Q.EPI_SWIGLU else N, dtype=torch.bfloat16, device=dev)
         R = C if epi == Q.EPI_RESIDUAL else None
-        fn = lambda: Q.h3enc_op_gemm(A, Wt, C, S, N, K, epi, R=R)
+        ws = torch.zeros(Q.h3enc_op_gemm_workspace_bytes(), dtype=torch.uint8, device=dev)
+        fn = lambda: Q.h3enc_op_gemm(A, Wt, C, S, N, K, epi, R=R, workspace=ws)
         work, unit = 2.0 * S * N * K / 1e12, "TFLOP/s"
     elif name == "attention":
         X = rnd("qkv", (S, cfg.qkv_out), 1.0)

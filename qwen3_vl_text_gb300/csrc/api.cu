@@ -258,7 +258,7 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         });
         if (e != cudaSuccess) return cuda_fail(h, e, "q/k norm + rope");
         e = run(h, H3ENC_K_ATTN, st,
-                [&] { return h3::launch_attention(h->qkv, h->attn, S, nq, nkv, d, cu, n_seqs, st); });
+                [&] { return h3::launch_attention(h->qkv, h->attn, S, nq, nkv, d, cu, n_seqs, h->status, st); });
         if (e != cudaSuccess) return cuda_fail(h, e, "attention");
         p.tmA = &h->tm_attn; p.tmW = &w.tm_o; p.N = H; p.K = nq * d; p.epi = h3::EPI_RESIDUAL;
         p.C = out; p.ldc = H; p.R = out;
@@ -734,7 +734,8 @@ h3enc_status h3enc_op_attention(const void *qkv, void *o, int32_t S, int32_t n_h
             if (cu_seqlens[i + 1] < cu_seqlens[i]) return fail(nullptr, H3ENC_ERR_INVALID_ARG, "attention: bad cu_seqlens");
     }
     cudaError_t e = h3::launch_attention(static_cast<const bf16 *>(qkv), static_cast<bf16 *>(o), S, n_heads,
-                                         n_kv_heads, head_dim, cu_seqlens, n_seqs, static_cast<cudaStream_t>(stream));
+                                         n_kv_heads, head_dim, cu_seqlens, n_seqs, nullptr,
+                                         static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "attention launch");
 }
 

@@ -53,9 +53,9 @@ cudaError_t launch_rope_table(const int32_t *positions, int S, const RopeParams 
 cudaError_t launch_qk_norm_rope(bf16 *qkv, int S, int nq, int nkv, int d, const bf16 *wq, const bf16 *wk,
                                 float eps, const float *cos_t, const float *sin_t, cudaStream_t st);
 
-// ---- attention (attention.cu)
+// ---- attention on tcgen05 (attention_tc.cu)
 cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, int d, const int32_t *cu_host,
-                             int n_seqs, cudaStream_t st);
+                             int n_seqs, int32_t *status, cudaStream_t st);
 
 // ---- embedding gather, visual ranks, weight packing (embed.cu)
 cudaError_t launch_embed(const int32_t *ids, const bf16 *table, int vocab, int hidden, bf16 *out, int S,

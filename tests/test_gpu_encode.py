@@ -164,16 +164,23 @@ def test_packed_prompts_two_full_width_layers():
     enc = make_encoder(wl, cfg, max_tokens=S, max_seqs=32)
     try:
         _check_layers_and_final(wl, cfg, enc, inp, per_layer=False)
-        # packing is invisible: each prompt alone gives the same rows, bit for bit
+        # packing is invisible: each prompt encoded alone meets the same oracle bound as the packed rows
+        # (its GEMM tiles split differently, so equality holds up to fp32 summation order only)
         dev = device_inputs(inp)
-        full = _run_gpu(enc, dev, inp, S)
         cu = inp["cu_seqlens"]
+        get = oracle_layer_getter(wl, cfg)
+        ws = [get(l) for l in range(cfg.num_layers)]
         for i in (0, 7, 15):
             a, b = int(cu[i]), int(cu[i + 1])
             one = {"positions": dev["positions"][:, a:b].contiguous(), "input_ids": dev["input_ids"][a:b],
                    "visual_mask": None, "deepstack": None, "inputs_embeds": None}
-            sep = _run_gpu(enc, one, {"n_vis": 0, "cu_seqlens": np.array([0, b - a])}, b - a)
-            assert rel_l2(t2f(sep), t2f(full[a:b])) < 5e-3, f"prompt {i}"
+            sep = t2f(_run_gpu(enc, one, {"n_vis": 0, "cu_seqlens": np.array([0, b - a])}, b - a))
+            x0 = oracle_embed(wl, cfg, inp["input_ids"][a:b])
+            pos = inp["positions"][:, a:b]
+            ref = O.forward(x0, pos, cfg, ws.__getitem__)
+            refbf = O.forward(x0, pos, cfg, ws.__getitem__, storage=GPU_STORAGE)
+            ok, msg = within(sep, ref, refbf, FINAL_TOL, MAXABS_TOL)
+            assert ok, f"prompt {i} alone: " + msg
     finally:
         enc.close()
 
@@ -212,8 +219,10 @@ def test_full_depth_image_encode_prefix_rows():
         pre = {"positions": dev["positions"][:, :P].contiguous(), "input_ids": dev["input_ids"][:P],
                "visual_mask": dev["visual_mask"][:P], "deepstack": dev["deepstack"][:, :n_vis_p].contiguous(),
                "inputs_embeds": None}
-        # the prefix run splits GEMM tiles differently (different M), so fp32 sums may round differently
-        assert rel_l2(t2f(_run_gpu(enc, pre, pre_inp, P)), t2f(out[:P])) < 5e-3, "causal prefix differs"
+        # the prefix run splits GEMM tiles differently (different M): its fp32 sums round differently and
+        # this random-weight stack amplifies that to the size of the bf16 floor, so it is held to the
+        # same oracle bound below instead of bit equality with the full run
+        prefix_out = _run_gpu(enc, pre, pre_inp, P)
         x0 = oracle_embed(wl, cfg, inp["input_ids"][:P])
         ds = bits_to_f32(inp["deepstack"])[:, :n_vis_p]
         get = oracle_layer_getter(wl, cfg)
@@ -224,7 +233,9 @@ def test_full_depth_image_encode_prefix_rows():
             x32 = O.forward(x32, pos, cfg, lambda _: w, mk, ds, layers=[l])
             xbf = O.forward(xbf, pos, cfg, lambda _: w, mk, ds, layers=[l], storage=GPU_STORAGE)
         ok, msg = within(t2f(out[:P]), x32, xbf, FINAL_TOL, MAXABS_TOL)
-        assert ok, msg
+        assert ok, "full run: " + msg
+        ok, msg = within(t2f(prefix_out), x32, xbf, FINAL_TOL, MAXABS_TOL)
+        assert ok, "prefix run: " + msg
     finally:
         enc.close()
 
