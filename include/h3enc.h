@@ -179,6 +179,10 @@ enum {
  * launching stream) and accumulate per-class device time.  Resets totals. */
 H3ENC_API h3enc_status h3enc_set_profiling(h3enc *h, int32_t enable);
 
+/* As h3enc_set_profiling, timing only the classes whose bit (1 << class) is set
+ * in mask (0 = off); launches of the other classes are still counted. */
+H3ENC_API h3enc_status h3enc_set_profiling_classes(h3enc *h, uint32_t mask);
+
 /* Synchronise and return per-class totals since the last reset:
  * ms[k], launches[k] for k < n (n <= H3ENC_K_COUNT).  Resets totals. */
 H3ENC_API h3enc_status h3enc_get_profile(h3enc *h, double *ms, int64_t *launches, int32_t n);

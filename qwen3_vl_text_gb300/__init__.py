@@ -16,7 +16,7 @@ __all__ = [
     "lib", "H3encError", "Config", "STATUS", "EPI_STORE", "EPI_RESIDUAL", "EPI_SWIGLU", "EPI_RESIDUAL_DS",
     "h3enc_create", "h3enc_load_weights", "h3enc_finalize_weights", "h3enc_encode", "h3enc_encode_embeds",
     "h3enc_encode_host", "h3enc_set_layer_capture", "h3enc_get_status", "h3enc_last_error", "h3enc_destroy",
-    "h3enc_set_profiling", "h3enc_get_profile", "h3enc_launch_count", "h3enc_num_sms",
+    "h3enc_set_profiling", "h3enc_set_profiling_classes", "h3enc_get_profile", "h3enc_launch_count", "h3enc_num_sms",
     "h3enc_op_gemm", "h3enc_op_gemm_workspace_bytes", "h3enc_op_pack_gate_up", "h3enc_op_rmsnorm", "h3enc_op_rope_table",
     "h3enc_op_qk_norm_rope", "h3enc_op_attention", "h3enc_op_embed", "h3enc_op_vis_rank", "Encoder",
     "KERNEL_CLASSES",
@@ -67,6 +67,7 @@ _SIGS = {
     "h3enc_last_error": ([_P], ctypes.c_char_p),
     "h3enc_destroy": ([_P], None),
     "h3enc_set_profiling": ([_P, _I32], _I32),
+    "h3enc_set_profiling_classes": ([_P, ctypes.c_uint32], _I32),
     "h3enc_get_profile": ([_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I64), _I32], _I32),
     "h3enc_launch_count": ([_P], _I64),
     "h3enc_num_sms": ([_P], _I32),
@@ -182,6 +183,14 @@ def h3enc_destroy(h):
 
 def h3enc_set_profiling(h, enable: bool):
     return _check(lib.h3enc_set_profiling(h, 1 if enable else 0), h)
+
+
+def h3enc_set_profiling_classes(h, classes):
+    """Time only the named kernel classes (see KERNEL_CLASSES); [] turns profiling off."""
+    mask = 0
+    for c in classes:
+        mask |= 1 << KERNEL_CLASSES.index(c)
+    return _check(lib.h3enc_set_profiling_classes(h, mask), h)
 
 
 def h3enc_get_profile(h):

@@ -66,6 +66,7 @@ struct h3enc {
     std::string err;
     std::vector<void *> capture;
     bool prof = false;
+    uint32_t prof_mask = 0;
     std::vector<cudaEvent_t> ev_pool;
     std::vector<int> ev_class;
     size_t ev_used = 0;
@@ -94,8 +95,8 @@ h3enc_status cuda_fail(h3enc *h, cudaError_t e, const char *what) {
 // Run one kernel launch, timed per class when profiling is on.
 template <class F>
 cudaError_t run(h3enc *h, int cls, cudaStream_t st, F &&launch) {
-    size_t e0 = 0;
-    if (h->prof) {
+    size_t e0 = (size_t)-1;
+    if (h->prof && (h->prof_mask & (1u << cls))) {
         if (h->ev_used + 2 > h->ev_pool.size()) {
             for (int i = 0; i < 256; ++i) {
                 cudaEvent_t ev;
@@ -112,7 +113,7 @@ cudaError_t run(h3enc *h, int cls, cudaStream_t st, F &&launch) {
         }
     }
     cudaError_t e = launch();
-    if (h->prof && e0 != (size_t)-1) {
+    if (e0 != (size_t)-1) {
         cudaEventRecord(h->ev_pool[e0 + 1], st);
         h->ev_class[e0] = cls;
         h->ev_used += 2;
@@ -595,8 +596,13 @@ void h3enc_destroy(h3enc *h) {
 }
 
 h3enc_status h3enc_set_profiling(h3enc *h, int32_t enable) {
+    return h3enc_set_profiling_classes(h, enable ? 0xFFFFFFFFu : 0u);
+}
+
+h3enc_status h3enc_set_profiling_classes(h3enc *h, uint32_t mask) {
     if (!h) return fail(h, H3ENC_ERR_INVALID_ARG, "NULL handle");
-    h->prof = enable != 0;
+    h->prof = mask != 0;
+    h->prof_mask = mask;
     h->ev_used = 0;
     // reserve event pairs up front so a timed region never creates events
     while (h->prof && h->ev_pool.size() < 16384) {
