@@ -49,6 +49,38 @@ H3ENC_API h3enc_status h3enc_op_gemm(const void *A, const void *W, void *C, int3
 /* Workspace bytes h3enc_op_gemm needs on the current device (-1 without a device). */
 H3ENC_API int64_t h3enc_op_gemm_workspace_bytes(void);
 
+/* h3enc_op_gemm for callers that cannot allocate device memory (the pages have
+ * no counterpart: this is a library convenience).  Some callers have no way to
+ * hand over a workspace: code running inside another framework's allocator
+ * callback or after a memory pool has reserved the whole device, plugins that
+ * receive only their input and output buffers, hosts that forbid cudaMalloc
+ * after start-up.  This entry point computes exactly what h3enc_op_gemm
+ * computes with a workspace (same kernel, same split of the last wave), but its
+ * scratch is a fixed array inside the library's device image:
+ * h3enc_op_gemm_noalloc_scratch_bytes() bytes (20 MiB + 896 B, one 128 KiB
+ * fp32 slot and one flag per SM for up to 160 SMs), held by every GPU that
+ * loads the library until the process exits.  The caller passes inputs and
+ * outputs only; nothing is allocated or freed.
+ *   - The first call on a device looks up the array's device address and clears
+ *     its flags (a synchronous memset): make that first call before any stream
+ *     capture.  Later calls only launch the kernel.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents: calls that overlap on the GPU (other streams, other threads)
+ *     race and corrupt each other's results; serialise them.
+ *   - A device with more than 160 SMs would need more scratch than the array
+ *     holds: the call returns H3ENC_ERR_UNSUPPORTED (message from
+ *     h3enc_op_gemm_noalloc_last_error()).
+ * Arguments, requirements and other errors are those of h3enc_op_gemm. */
+H3ENC_API h3enc_status h3enc_op_gemm_noalloc(const void *A, const void *W, void *C, int32_t M, int32_t N, int32_t K,
+                                   int32_t epilogue, const void *R, const void *DS, const int32_t *vis_rank,
+                                   int32_t n_vis, int32_t *status, void *stream);
+
+/* Bytes of the fixed scratch array h3enc_op_gemm_noalloc uses. */
+H3ENC_API int64_t h3enc_op_gemm_noalloc_scratch_bytes(void);
+
+/* Message of the last h3enc_op_gemm_noalloc error on this thread ("" if none). */
+H3ENC_API const char *h3enc_op_gemm_noalloc_last_error(void);
+
 /* Pack gate [I, K] and up [I, K] into W [2I, K] for H3ENC_EPI_SWIGLU: rows
  * [256b, 256b+128) = gate rows [128b, 128b+128), rows [256b+128, 256b+256) =
  * up rows [128b, 128b+128).  Requires I % 128 == 0. */

@@ -17,7 +17,7 @@ __all__ = [
     "h3enc_create", "h3enc_load_weights", "h3enc_finalize_weights", "h3enc_encode", "h3enc_encode_embeds",
     "h3enc_encode_host", "h3enc_set_layer_capture", "h3enc_get_status", "h3enc_last_error", "h3enc_destroy",
     "h3enc_set_profiling", "h3enc_set_profiling_classes", "h3enc_get_profile", "h3enc_launch_count", "h3enc_num_sms",
-    "h3enc_op_gemm", "h3enc_op_gemm_workspace_bytes", "h3enc_op_pack_gate_up", "h3enc_op_rmsnorm", "h3enc_op_rope_table",
+    "h3enc_op_gemm", "h3enc_op_gemm_workspace_bytes", "h3enc_op_gemm_noalloc", "h3enc_op_gemm_noalloc_scratch_bytes", "h3enc_op_pack_gate_up", "h3enc_op_rmsnorm", "h3enc_op_rope_table",
     "h3enc_op_qk_norm_rope", "h3enc_op_attention", "h3enc_op_embed", "h3enc_op_vis_rank", "Encoder",
     "KERNEL_CLASSES",
 ]
@@ -73,6 +73,9 @@ _SIGS = {
     "h3enc_num_sms": ([_P], _I32),
     "h3enc_op_gemm": ([_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _I64, _P, _P], _I32),
     "h3enc_op_gemm_workspace_bytes": ([], _I64),
+    "h3enc_op_gemm_noalloc": ([_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _P], _I32),
+    "h3enc_op_gemm_noalloc_scratch_bytes": ([], _I64),
+    "h3enc_op_gemm_noalloc_last_error": ([], ctypes.c_char_p),
     "h3enc_op_pack_gate_up": ([_P, _P, _P, _I32, _I32, _P], _I32),
     "h3enc_op_rmsnorm": ([_P, _P, _P, _I32, _I32, _F, _P], _I32),
     "h3enc_op_rope_table": ([_P, _I32, _I32, _F, ctypes.POINTER(_I32), _P, _P, _P], _I32),
@@ -218,6 +221,22 @@ def h3enc_op_gemm(A, W, C, M, N, K, epilogue, R=None, DS=None, vis_rank=None, n_
 
 def h3enc_op_gemm_workspace_bytes() -> int:
     return lib.h3enc_op_gemm_workspace_bytes()
+
+
+def h3enc_op_gemm_noalloc(A, W, C, M, N, K, epilogue, R=None, DS=None, vis_rank=None, n_vis=0, status=None,
+                          stream=None):
+    """h3enc_op_gemm without a workspace argument, for callers that cannot allocate device
+    memory: the library's fixed device scratch array is used instead (shared by every call)."""
+    code = lib.h3enc_op_gemm_noalloc(_ptr(A), _ptr(W), _ptr(C), M, N, K, epilogue, _ptr(R), _ptr(DS),
+                                     _ptr(vis_rank), n_vis, _ptr(status), _stream(stream))
+    if code != 0:
+        msg = lib.h3enc_op_gemm_noalloc_last_error()
+        raise H3encError(code, msg.decode() if msg else "")
+    return code
+
+
+def h3enc_op_gemm_noalloc_scratch_bytes() -> int:
+    return lib.h3enc_op_gemm_noalloc_scratch_bytes()
 
 
 def h3enc_op_pack_gate_up(gate, up, W, I, K, stream=None):
