@@ -8,21 +8,26 @@
 // MiniMaxH3Qwen3VLTextDecoderLayer.forward, silu(gate) * up, and the DeepStack
 // add of MiniMaxH3Qwen3VLTextModel._deepstack_process.
 //
-// Design (one CTA per SM, persistent over 128 x 256 output tiles):
-//   warp 0     TMA producer: A tile 128 x 64 and W tile 256 x 64 (bf16, 128-byte
-//              swizzle) per k-block into a 4-stage shared-memory ring
-//   warp 1     allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and
-//              issues tcgen05.mma (M=128, N=256, K=16) from one thread
-//   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes (= 32 output rows),
+// Design: CTA pairs (clusters of 2, one CTA per SM), persistent over 256 x 256
+// output tiles.  CTA r of a pair owns output rows [128r, 128r+128) of the tile
+// and stages, per k-block of 64, its own 128 x 64 slice of A and its half (128
+// rows) of the 256 x 64 weight tile, so the pair reads each operand byte once.
+//   warp 0     TMA producer: both slices into a 6-stage ring; the copies of
+//              both CTAs complete on the leader CTA's stage barrier
+//   warp 1     allocates 512 TMEM columns in both CTAs (two 128-lane x 256-column
+//              fp32 accumulators); in the leader CTA one thread issues
+//              tcgen05.mma.cta_group::2 (M=256, N=256, K=16) and commits to the
+//              barriers of both CTAs
+//   warps 2-5  epilogue of each CTA: tcgen05.ld of their 32 TMEM lanes (= rows),
 //              fused element-wise op, bf16 stores; overlaps the next tile's MMAs
-// Schedule: the tiles of the full waves run data-parallel (tile = CTA + i*grid,
-// M-fastest, so the CTAs in flight share each weight tile through L2).  The
+// Schedule: the tiles of the full waves run data-parallel (tile = pair + i*pairs,
+// M-fastest, so the pairs in flight share each weight tile through L2).  The
 // tiles of the last, partial wave would leave most SMs idle, so each of them is
-// split along K into s chunks (s = grid / leftover tiles) computed by s CTAs:
-// every chunk's fp32 partial goes to a workspace slot, a per-slot flag is
-// released, and each contributing CTA then sums the s partials of its tile in
-// fixed chunk order for a slice of the tile's rows and applies the epilogue
-// (deterministic; the grid is launched cooperatively so all CTAs are resident).
+// split along K into s chunks (s = pairs / leftover tiles) computed by s pairs:
+// every CTA's fp32 partial goes to its workspace slot, a per-slot flag is
+// released, and each contributing CTA then sums the s partials of its half of
+// the tile in fixed chunk order for a slice of rows and applies the epilogue
+// (deterministic).  The grid never exceeds the number of co-resident pairs.
 // Every wait is bounded; on time-out the CTA records ST_TIMEOUT, drains its
 // in-flight copies and MMAs, frees TMEM and exits.
 #include <cudaTypedefs.h>
@@ -36,16 +41,19 @@ namespace h3 {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128;                          // output rows per CTA (a pair covers 256)
+constexpr int BN = 256;                          // output columns per tile
+constexpr int BK = 64;
+constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB
-constexpr int B_BYTES = BN * BK * 2;             // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
+constexpr int B_BYTES = (BN / 2) * BK * 2;       // 16 KB: this CTA's half of the weight tile
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB per CTA
 constexpr int GEMM_THREADS = 192;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
 
 struct GemmArgs {
     int M, N, K;
-    int nm, nn, nk;
+    int nm, nn, nk;        // nm: 256-row blocks
     __nv_bfloat16 *C;
     int ldc;
     const __nv_bfloat16 *R;
@@ -56,21 +64,21 @@ struct GemmArgs {
     // split of the last partial wave
     int dp_tiles;      // tiles run data-parallel: [0, dp_tiles)
     int splits;        // s > 1: tiles [dp_tiles, nm*nn) are split into s K-chunks
-    float *part;       // [grid][BM*BN] fp32 partial accumulators
+    float *part;       // [grid][BM*BN] fp32 partial accumulators (one slot per CTA)
     uint32_t *flags;   // [grid] release flags
     uint32_t epoch;    // unique per launch; a flag equal to it means "partial written"
 };
 
-// The K-chunk of the split item of this CTA (none when kb1 <= kb0).
+// The K-chunk of this pair's split item (none when kb1 <= kb0).
 struct SplitItem {
     int tile, kb0, kb1, chunk;
 };
-__device__ __forceinline__ SplitItem split_item(const GemmArgs &g) {
+__device__ __forceinline__ SplitItem split_item(const GemmArgs &g, int pair) {
     SplitItem it{0, 0, 0, 0};
     const int left = g.nm * g.nn - g.dp_tiles;
-    if (g.splits > 1 && (int)blockIdx.x < left * g.splits) {
-        it.tile = g.dp_tiles + blockIdx.x / g.splits;
-        it.chunk = blockIdx.x % g.splits;
+    if (g.splits > 1 && pair < left * g.splits) {
+        it.tile = g.dp_tiles + pair / g.splits;
+        it.chunk = pair % g.splits;
         it.kb0 = it.chunk * g.nk / g.splits;
         it.kb1 = (it.chunk + 1) * g.nk / g.splits;
     }
@@ -142,15 +150,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();       // 0: leader CTA of the pair
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&full[s], 1);      // leader's arrive.expect_tx; the copies of both CTAs complete on it
+            mbar_init(&empty[s], 1);     // leader's MMA commit, multicast to both CTAs
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], 4);
+            mbar_init(&acc_full[a], 1);  // leader's MMA commit, multicast to both CTAs
+            mbar_init(&acc_empty[a], 8); // the 4 epilogue warps of each CTA (the leader's barrier is used)
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -161,15 +172,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         prefetch_tmap(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, 512);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_slot, 512);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();   // barriers of both CTAs initialised before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const SplitItem sk = split_item(g);
+    const SplitItem sk = split_item(g, pair);
     const bool has_split = sk.kb1 > sk.kb0;
 
     if (warp == 0) {
@@ -181,31 +192,34 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int s = 0; s < STAGES; ++s) issued[s] = 0;
             bool ok = true;
             auto load_item = [&](int tile, int kb0, int kb1) {
-                const int m0 = (tile % g.nm) * BM;
-                const int n0 = (tile / g.nm) * BN;
+                const int m0 = (tile % g.nm) * (2 * BM) + (int)rank * BM;
+                const int n0 = (tile / g.nm) * BN + (int)rank * (BN / 2);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; return; }
-                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-                    tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m0);
-                    tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, n0);
+                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
+                    const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
+                    tma_load_2d_pair(sA + stage * A_BYTES, &tmA, bar, kb * BK, m0);
+                    tma_load_2d_pair(sB + stage * B_BYTES, &tmB, bar, kb * BK, n0);
                     ++issued[stage];
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             };
-            for (int tile = blockIdx.x; ok && tile < g.dp_tiles; tile += gridDim.x) load_item(tile, 0, g.nk);
+            for (int tile = pair; ok && tile < g.dp_tiles; tile += npairs) load_item(tile, 0, g.nk);
             if (ok && has_split) load_item(sk.tile, sk.kb0, sk.kb1);
             if (!ok) {
                 report(g.status, ST_TIMEOUT);
                 *abort_flag = 1;
-                // wait (bounded) for the copies still in flight into the ring
-                const int never = 0;
-                for (int s = 0; s < STAGES; ++s)
-                    if (issued[s]) mbar_wait(&full[s], (issued[s] - 1u) & 1u, &never);
+                // the leader waits (bounded) for the copies still in flight into the pair's rings
+                if (rank == 0) {
+                    const int never = 0;
+                    for (int s = 0; s < STAGES; ++s)
+                        if (issued[s]) mbar_wait(&full[s], (issued[s] - 1u) & 1u, &never);
+                }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = umma_idesc_bf16(BM, BN);
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = umma_idesc_bf16(2 * BM, BN);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -222,30 +236,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     const uint32_t b_base = smem_u32(sB + stage * B_BYTES);
                     #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_bf16(d_tmem, sdesc_sw128(a_base + kk * 32), sdesc_sw128(b_base + kk * 32), idesc,
-                                  (kb > kb0 || kk > 0) ? 1u : 0u);
-                    umma_commit(&empty[stage]);
+                        umma_bf16_pair(d_tmem, sdesc_sw128(a_base + kk * 32), sdesc_sw128(b_base + kk * 32), idesc,
+                                       (kb > kb0 || kk > 0) ? 1u : 0u);
+                    umma_commit_pair(&empty[stage], 0x3);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
-                umma_commit(&acc_full[acc]);
+                umma_commit_pair(&acc_full[acc], 0x3);
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             };
-            for (int tile = blockIdx.x; ok && tile < g.dp_tiles; tile += gridDim.x) mma_item(0, g.nk);
+            for (int tile = pair; ok && tile < g.dp_tiles; tile += npairs) mma_item(0, g.nk);
             if (ok && has_split) mma_item(sk.kb0, sk.kb1);
             if (!ok) {
                 report(g.status, ST_TIMEOUT);
                 *abort_flag = 1;
             }
             // every MMA issued by this thread has completed once `drain` flips
-            umma_commit(drain);
+            umma_commit_pair(drain, 0x1);
             const int never = 0;
             mbar_wait(drain, 0, &never);
         }
     } else {
-        // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 = tile rows of the same range
+        // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 = this CTA's tile rows of the same range
         const int quarter = warp & 3;
         const int et = threadIdx.x - 64;  // 0..127 over the four epilogue warps
+        const uint32_t acc_empty_lead[2] = {mapa_shared(smem_u32(&acc_empty[0]), 0),
+                                            mapa_shared(smem_u32(&acc_empty[1]), 0)};
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
@@ -266,15 +282,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         auto release_acc = [&]() {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            if (lane == 0) mbar_arrive_cluster(acc_empty_lead[acc]);
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         };
-        for (int tile = blockIdx.x; tile < g.dp_tiles; tile += gridDim.x) {
+        for (int tile = pair; tile < g.dp_tiles; tile += npairs) {
             const int m_blk = tile % g.nm;
             const int n_blk = tile / g.nm;
             if (!wait_acc()) break;
-            const int row = m_blk * BM + quarter * 32 + lane;
+            const int row = m_blk * (2 * BM) + (int)rank * BM + quarter * 32 + lane;
             const bool live = row < g.M;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
             if constexpr (EPI == EPI_SWIGLU) {
@@ -334,8 +350,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             release_acc();
         }
         if (has_split) {
-            // 1) dump this chunk's fp32 accumulator to workspace slot blockIdx.x, row-major [BM][BN]
-            //    (every epilogue warp reaches the barrier below exactly once, failed or not)
+            // 1) dump this CTA's fp32 accumulator (its 128 rows of the tile) to slot blockIdx.x, row-major
+            //    [BM][BN]; every epilogue warp reaches the barrier below exactly once, failed or not
             const bool got = ok && wait_acc();
             if (got) {
                 const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
@@ -356,32 +372,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             __threadfence();
             if (epi_bar_and(got)) {
                 if (et == 0) st_release(g.flags + blockIdx.x, g.epoch);
-                // 2) wait for the s chunks of this tile
-                const int first = blockIdx.x - sk.chunk;
+                // 2) wait for the same-rank CTAs of the s pairs that computed this tile
+                const int first_pair = pair - sk.chunk;
                 bool all = true;
                 const long long t0 = clock64();
                 for (int j = 0; j < g.splits && all; ++j) {
-                    while (ld_acquire(g.flags + first + j) != g.epoch) {
+                    while (ld_acquire(g.flags + 2 * (first_pair + j) + rank) != g.epoch) {
                         if (clock64() - t0 > kSpinLimitCycles) { all = false; break; }
                     }
                 }
                 if (!all) {
                     if (et == 0) report(g.status, ST_TIMEOUT);
                 } else {
-                    // 3) this CTA finishes rows [r0, r1) of the tile: sum of the s partials in chunk order
+                    // 3) rows [r0, r1) of this CTA's half: sum of the s partials in chunk order, then the epilogue
                     const int r0 = sk.chunk * BM / g.splits, r1 = (sk.chunk + 1) * BM / g.splits;
                     const int m_blk = sk.tile % g.nm, n_blk = sk.tile / g.nm;
                     constexpr int UNITS_PER_ROW = (EPI == EPI_SWIGLU) ? BN / 8 : BN / 4;  // float4 groups
                     const int units = (r1 - r0) * UNITS_PER_ROW;
-                    const float *base = g.part + (size_t)first * (BM * BN);
                     for (int u = et; u < units; u += 128) {
                         const int r = r0 + u / UNITS_PER_ROW;
                         const int c4 = (u % UNITS_PER_ROW) * 4;
-                        const int row = m_blk * BM + r;
+                        const int row = m_blk * (2 * BM) + (int)rank * BM + r;
                         if (row >= g.M) continue;
                         float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
                         for (int j = 0; j < g.splits; ++j) {
-                            const float *pj = base + (size_t)j * (BM * BN) + (size_t)r * BN;
+                            const float *pj = g.part + (size_t)(2 * (first_pair + j) + rank) * (BM * BN) +
+                                              (size_t)r * BN;
                             const float4 x = __ldcg(reinterpret_cast<const float4 *>(pj + c4));
                             a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
                             if constexpr (EPI == EPI_SWIGLU) {
@@ -422,10 +438,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
     }
 
-    __syncthreads();
+    tc_fence_before();
+    cluster_sync();   // the peer no longer reads this CTA's shared memory or signals its barriers
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, 512);
+        tmem_dealloc_pair(tmem_base, 512);
     }
 }
 
@@ -451,25 +468,41 @@ uint32_t next_epoch() {
 
 template <int EPI>
 cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
-    static bool attr_set = false;
-    if (!attr_set) {
+    static int max_pairs = 0;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    if (max_pairs == 0) {
         cudaError_t e = cudaFuncSetAttribute(gemm_tcgen05_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        cudaLaunchConfig_t q = {};
+        q.gridDim = dim3(2 * (p.num_sms / 2 > 0 ? p.num_sms / 2 : 1));
+        q.blockDim = dim3(GEMM_THREADS);
+        q.dynamicSmemBytes = SMEM_BYTES;
+        q.attrs = attr;
+        q.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_tcgen05_kernel<EPI>, &q);
+        if (e != cudaSuccess) return e;
+        if (n <= 0) return cudaErrorInvalidConfiguration;
+        max_pairs = n;
     }
     GemmArgs g;
     g.M = p.M; g.N = p.N; g.K = p.K;
-    g.nm = (p.M + BM - 1) / BM;
+    g.nm = (p.M + 2 * BM - 1) / (2 * BM);
     g.nn = p.N / BN;
     g.nk = (p.K + BK - 1) / BK;
     g.C = p.C; g.ldc = p.ldc; g.R = p.R; g.DS = p.DS; g.vis_rank = p.vis_rank; g.n_vis = p.n_vis;
     g.status = p.status;
     const int tiles = g.nm * g.nn;
-    const int sms = p.num_sms > 0 ? p.num_sms : 1;
-    // full waves data-parallel; the tiles of a partial last wave split along K over the idle SMs
-    const int left = tiles % sms;
-    int splits = (p.part && p.flags && left) ? sms / left : 1;
+    int pairs = p.num_sms / 2 < max_pairs ? p.num_sms / 2 : max_pairs;   // all pairs co-resident
+    if (pairs < 1) pairs = 1;
+    // full waves data-parallel; the tiles of a partial last wave split along K over the idle pairs
+    const int left = tiles % pairs;
+    int splits = (p.part && p.flags && left) ? pairs / left : 1;
     if (splits > g.nk / 2) splits = g.nk / 2;
     if (splits > 32) splits = 32;
     if (splits < 2) splits = 1;
@@ -478,17 +511,14 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     g.part = p.part;
     g.flags = p.flags;
     g.epoch = splits > 1 ? next_epoch() : 0u;
-    const int grid = splits > 1 ? sms : (tiles < sms ? tiles : sms);
+    const int grid_pairs = splits > 1 ? pairs : (tiles < pairs ? tiles : pairs);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
+    cfg.gridDim = dim3(2 * grid_pairs);
     cfg.blockDim = dim3(GEMM_THREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;   // split CTAs wait on one another: all must be resident
     cfg.attrs = attr;
-    cfg.numAttrs = splits > 1 ? 1 : 0;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<EPI>, *p.tmA, *p.tmW, g);
 }
 
@@ -510,7 +540,7 @@ bool make_tmap_rows(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t col
 
 int gemm_box_rows_a() { return BM; }
 size_t gemm_workspace_bytes(int num_sms) { return (size_t)num_sms * BM * BN * sizeof(float) + 256 + (size_t)num_sms * 4; }
-int gemm_box_rows_w() { return BN; }
+int gemm_box_rows_w() { return BN / 2; }
 
 cudaError_t launch_gemm(const GemmPlan &p, cudaStream_t stream) {
     if (p.M <= 0) return cudaSuccess;
