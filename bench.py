@@ -168,8 +168,20 @@ def run_kernel(args):
         return W.normal_bf16(7, name, shape, 0.0, sigma, device=dev)
 
     name = args.kernel
-    if name.startswith("gemm_"):
-        shapes = {"gemm_qkv": (cfg.qkv_out, H, Q.EPI_STORE), "gemm_o": (H, nq * d, Q.EPI_RESIDUAL),
+    if name == "gemm_qkv":
+        A = rnd("A", (S, H), 1.0)
+        Wt = rnd("W", (cfg.qkv_out, H))
+        G = rnd("g", (d,), 1.0)
+        pos = torch.arange(S, dtype=torch.int32, device=dev).repeat(3, 1).contiguous()
+        c = torch.empty(S, d // 2, device=dev)
+        s_ = torch.empty_like(c)
+        Q.h3enc_op_rope_table(pos, S, d, cfg.rope_theta, cfg.mrope_section, c, s_)
+        C = torch.empty(S, cfg.qkv_out, dtype=torch.bfloat16, device=dev)
+        ws = torch.zeros(Q.h3enc_op_gemm_workspace_bytes(), dtype=torch.uint8, device=dev)
+        fn = lambda: Q.h3enc_op_gemm_qkv_rope(A, Wt, C, S, H, nq, nkv, d, G, G, 1e-6, c, s_, workspace=ws)
+        work, unit = 2.0 * S * cfg.qkv_out * H / 1e12, "TFLOP/s"
+    elif name.startswith("gemm_"):
+        shapes = {"gemm_o": (H, nq * d, Q.EPI_RESIDUAL),
                   "gemm_gate_up": (2 * I, H, Q.EPI_SWIGLU), "gemm_down": (H, I, Q.EPI_RESIDUAL)}
         N, K, epi = shapes[name]
         A = rnd("A", (S, K), 1.0)
@@ -190,15 +202,6 @@ def run_kernel(args):
         Y = torch.empty_like(X)
         fn = lambda: Q.h3enc_op_rmsnorm(X, G, Y, S, H, 1e-6)
         work, unit = 2.0 * S * H * 2 / 1e9, "GB/s"
-    elif name == "qk_rope":
-        X = rnd("qkv", (S, cfg.qkv_out), 1.0)
-        G = rnd("g", (d,), 1.0)
-        pos = torch.arange(S, dtype=torch.int32, device=dev).repeat(3, 1).contiguous()
-        c = torch.empty(S, d // 2, device=dev)
-        s_ = torch.empty_like(c)
-        Q.h3enc_op_rope_table(pos, S, d, cfg.rope_theta, cfg.mrope_section, c, s_)
-        fn = lambda: Q.h3enc_op_qk_norm_rope(X, S, nq, nkv, d, G, G, 1e-6, c, s_)
-        work, unit = (2.0 * S * (nq + nkv) * d * 2 + 2 * S * d * 4) / 1e9, "GB/s"
     else:
         raise SystemExit("unknown kernel " + name)
     stream = torch.cuda.current_stream()
@@ -230,8 +233,8 @@ def run_kernel(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--kernel", default=None,
-                    help="time one kernel alone: gemm_qkv, gemm_o, gemm_gate_up, gemm_down, attention, rmsnorm, "
-                         "qk_rope")
+                    help="time one kernel alone: gemm_qkv (with the fused q/k norm + M-RoPE), gemm_o, "
+                         "gemm_gate_up, gemm_down, attention, rmsnorm")
     ap.add_argument("--seq", type=int, default=1024)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)

@@ -167,7 +167,7 @@ enum {
     H3ENC_K_PREP = 0,     /* embedding gather / input copy, M-RoPE tables, visual ranks */
     H3ENC_K_RMSNORM = 1,
     H3ENC_K_GEMM_QKV = 2,
-    H3ENC_K_QK_ROPE = 3,
+    H3ENC_K_QK_ROPE = 3,  /* unused: the q/k norm + RoPE runs inside the QKV projection */
     H3ENC_K_ATTN = 4,
     H3ENC_K_GEMM_O = 5,
     H3ENC_K_GEMM_GATE_UP = 6,

@@ -102,13 +102,20 @@ H3ENC_API h3enc_status h3enc_op_rope_table(const int32_t *positions, int32_t S, 
                                  const int32_t *section_host, float *cos_tab, float *sin_tab,
                                  void *stream);
 
-/* In place on qkv [S, (nq + 2*nkv)*head_dim]: every q head (columns h*d) and k
- * head (columns (nq + g)*d) becomes rope(rmsnorm(x, w_q or w_k)) with
- * rope(x)[j] = x[j]*cos[j] - x[j+d/2]*sin[j], rope(x)[j+d/2] = x[j+d/2]*cos[j] + x[j]*sin[j]
- * (page "... encoder.py", q_norm/k_norm then _apply_rotary_pos_emb).  v heads untouched. */
-H3ENC_API h3enc_status h3enc_op_qk_norm_rope(void *qkv, int32_t S, int32_t n_heads, int32_t n_kv_heads,
-                                   int32_t head_dim, const void *w_q, const void *w_k, float eps,
-                                   const float *cos_tab, const float *sin_tab, void *stream);
+/* QKV projection with the per-head q/k RMSNorm and M-RoPE fused into the GEMM
+ * epilogue (page "... encoder.py", MiniMaxH3Qwen3VLTextAttention.forward: the
+ * q/k/v projections, q_norm/k_norm over head_dim, then _apply_rotary_pos_emb):
+ *   qkv = A * W^T with W [(nq + 2*nkv)*d, K] (q rows, then k, then v);
+ *   every q head (columns h*d) and k head (columns (nq + g)*d) of qkv becomes
+ *   rope(rmsnorm(x, w_q or w_k, eps)) with, for j < d/2,
+ *     rope(x)[j] = x[j]*cos[j] - x[j+d/2]*sin[j],  rope(x)[j+d/2] = x[j+d/2]*cos[j] + x[j]*sin[j]
+ *   (cos/sin = the fp32 tables of h3enc_op_rope_table, [M, d/2]); v heads are the plain
+ *   projection.  C [M, (nq + 2*nkv)*d].  workspace as for h3enc_op_gemm.
+ * Requires head_dim in {64, 128} and (nq + 2*nkv)*d % 256 == 0. */
+H3ENC_API h3enc_status h3enc_op_gemm_qkv_rope(const void *A, const void *W, void *C, int32_t M, int32_t K,
+                                    int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, const void *w_q,
+                                    const void *w_k, float eps, const float *cos_tab, const float *sin_tab,
+                                    void *workspace, int64_t workspace_bytes, int32_t *status, void *stream);
 
 /* Causal GQA attention over packed sequences (page "... encoder.py",
  * MiniMaxH3Qwen3VLTextAttention.forward: repeat_interleave of K/V, SDPA with

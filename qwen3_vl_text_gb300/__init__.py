@@ -18,7 +18,7 @@ __all__ = [
     "h3enc_encode_host", "h3enc_set_layer_capture", "h3enc_get_status", "h3enc_last_error", "h3enc_destroy",
     "h3enc_set_profiling", "h3enc_set_profiling_classes", "h3enc_get_profile", "h3enc_launch_count", "h3enc_num_sms",
     "h3enc_op_gemm", "h3enc_op_gemm_workspace_bytes", "h3enc_op_gemm_noalloc", "h3enc_op_gemm_noalloc_scratch_bytes", "h3enc_op_pack_gate_up", "h3enc_op_rmsnorm", "h3enc_op_rope_table",
-    "h3enc_op_qk_norm_rope", "h3enc_op_attention", "h3enc_op_embed", "h3enc_op_vis_rank", "Encoder",
+    "h3enc_op_gemm_qkv_rope", "h3enc_op_attention", "h3enc_op_embed", "h3enc_op_vis_rank", "Encoder",
     "KERNEL_CLASSES",
 ]
 
@@ -79,7 +79,8 @@ _SIGS = {
     "h3enc_op_pack_gate_up": ([_P, _P, _P, _I32, _I32, _P], _I32),
     "h3enc_op_rmsnorm": ([_P, _P, _P, _I32, _I32, _F, _P], _I32),
     "h3enc_op_rope_table": ([_P, _I32, _I32, _F, ctypes.POINTER(_I32), _P, _P, _P], _I32),
-    "h3enc_op_qk_norm_rope": ([_P, _I32, _I32, _I32, _I32, _P, _P, _F, _P, _P, _P], _I32),
+    "h3enc_op_gemm_qkv_rope": ([_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _F, _P, _P, _P, _I64, _P, _P],
+                               _I32),
     "h3enc_op_attention": ([_P, _P, _I32, _I32, _I32, _I32, _P, _I32, _P], _I32),
     "h3enc_op_embed": ([_P, _P, _I32, _I32, _P, _I32, _P, _P], _I32),
     "h3enc_op_vis_rank": ([_P, _I32, _I32, _P, _P, _P], _I32),
@@ -252,9 +253,12 @@ def h3enc_op_rope_table(positions, S, head_dim, theta, section, cos_tab, sin_tab
                                           _ptr(sin_tab), _stream(stream)))
 
 
-def h3enc_op_qk_norm_rope(qkv, S, n_heads, n_kv_heads, head_dim, w_q, w_k, eps, cos_tab, sin_tab, stream=None):
-    return _check(lib.h3enc_op_qk_norm_rope(_ptr(qkv), S, n_heads, n_kv_heads, head_dim, _ptr(w_q), _ptr(w_k), eps,
-                                            _ptr(cos_tab), _ptr(sin_tab), _stream(stream)))
+def h3enc_op_gemm_qkv_rope(A, W, C, M, K, n_heads, n_kv_heads, head_dim, w_q, w_k, eps, cos_tab, sin_tab,
+                           workspace=None, status=None, stream=None):
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return _check(lib.h3enc_op_gemm_qkv_rope(_ptr(A), _ptr(W), _ptr(C), M, K, n_heads, n_kv_heads, head_dim,
+                                             _ptr(w_q), _ptr(w_k), eps, _ptr(cos_tab), _ptr(sin_tab),
+                                             _ptr(workspace), wbytes, _ptr(status), _stream(stream)))
 
 
 def h3enc_op_attention(qkv, o, S, n_heads, n_kv_heads, head_dim, cu_seqlens=None, stream=None):

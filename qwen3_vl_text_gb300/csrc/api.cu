@@ -249,18 +249,17 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         p.part = h->gemm_part;
         p.flags = h->gemm_flags;
         p.M = S;
-        p.tmA = &h->tm_y; p.tmW = &w.tm_qkv; p.N = h->qkv_out; p.K = H; p.epi = h3::EPI_STORE;
+        // QKV projection with q_norm/k_norm and M-RoPE fused into the epilogue
+        p.tmA = &h->tm_y; p.tmW = &w.tm_qkv; p.N = h->qkv_out; p.K = H; p.epi = h3::EPI_QKROPE;
         p.C = h->qkv; p.ldc = h->qkv_out;
+        p.wq = w.q_norm; p.wk = w.k_norm; p.cos_t = h->cos_t; p.sin_t = h->sin_t;
+        p.head_dim = d; p.nq = nq; p.nkv = nkv; p.eps = c.rms_eps;
         e = run(h, H3ENC_K_GEMM_QKV, st, [&] { return h3::launch_gemm(p, st); });
         if (e != cudaSuccess) return cuda_fail(h, e, "qkv gemm");
-        e = run(h, H3ENC_K_QK_ROPE, st, [&] {
-            return h3::launch_qk_norm_rope(h->qkv, S, nq, nkv, d, w.q_norm, w.k_norm, c.rms_eps, h->cos_t,
-                                           h->sin_t, st);
-        });
-        if (e != cudaSuccess) return cuda_fail(h, e, "q/k norm + rope");
         e = run(h, H3ENC_K_ATTN, st,
                 [&] { return h3::launch_attention(h->qkv, h->attn, S, nq, nkv, d, cu, n_seqs, h->status, st); });
         if (e != cudaSuccess) return cuda_fail(h, e, "attention");
+        p.wq = p.wk = nullptr; p.cos_t = p.sin_t = nullptr;
         p.tmA = &h->tm_attn; p.tmW = &w.tm_o; p.N = H; p.K = nq * d; p.epi = h3::EPI_RESIDUAL;
         p.C = out; p.ldc = H; p.R = out;
         e = run(h, H3ENC_K_GEMM_O, st, [&] { return h3::launch_gemm(p, st); });
@@ -716,16 +715,39 @@ h3enc_status h3enc_op_rope_table(const int32_t *positions, int32_t S, int32_t he
     return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "rope_table launch");
 }
 
-h3enc_status h3enc_op_qk_norm_rope(void *qkv, int32_t S, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
-                                   const void *w_q, const void *w_k, float eps, const float *cos_tab,
-                                   const float *sin_tab, void *stream) {
-    if (!qkv || !w_q || !w_k || !cos_tab || !sin_tab || S < 0 || n_heads < 1 || n_kv_heads < 1 ||
-        (head_dim != 64 && head_dim != 128))
-        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "qk_norm_rope: bad args");
-    cudaError_t e = h3::launch_qk_norm_rope(static_cast<bf16 *>(qkv), S, n_heads, n_kv_heads, head_dim,
-                                            static_cast<const bf16 *>(w_q), static_cast<const bf16 *>(w_k), eps,
-                                            cos_tab, sin_tab, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "qk_norm_rope launch");
+h3enc_status h3enc_op_gemm_qkv_rope(const void *A, const void *W, void *C, int32_t M, int32_t K, int32_t n_heads,
+                                    int32_t n_kv_heads, int32_t head_dim, const void *w_q, const void *w_k, float eps,
+                                    const float *cos_tab, const float *sin_tab, void *workspace,
+                                    int64_t workspace_bytes, int32_t *status, void *stream) {
+    const int64_t N = (int64_t)(n_heads + 2 * n_kv_heads) * head_dim;
+    if (M < 0 || K <= 0 || K % 8 || n_heads < 1 || n_kv_heads < 1 || (head_dim != 64 && head_dim != 128) ||
+        N % 256 || !w_q || !w_k || !cos_tab || !sin_tab)
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm_qkv_rope: bad sizes or NULL operand");
+    if (M == 0) return H3ENC_OK;
+    if (!A || !W || !C) return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm_qkv_rope: NULL operand");
+    CUtensorMap ta, tw;
+    if (!h3::make_tmap_rows(&ta, A, M, K, h3::gemm_box_rows_a()) ||
+        !h3::make_tmap_rows(&tw, W, N, K, h3::gemm_box_rows_w()))
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm_qkv_rope: operands not 16-byte aligned");
+    h3::GemmPlan p{};
+    p.tmA = &ta; p.tmW = &tw; p.M = M; p.N = (int)N; p.K = K; p.epi = h3::EPI_QKROPE;
+    p.C = static_cast<bf16 *>(C);
+    p.ldc = (int)N;
+    p.status = status;
+    p.num_sms = h3::device_num_sms();
+    p.wq = static_cast<const bf16 *>(w_q); p.wk = static_cast<const bf16 *>(w_k);
+    p.cos_t = cos_tab; p.sin_t = sin_tab;
+    p.head_dim = head_dim; p.nq = n_heads; p.nkv = n_kv_heads; p.eps = eps;
+    if (workspace) {
+        if (workspace_bytes < (int64_t)h3::gemm_workspace_bytes(p.num_sms) ||
+            (reinterpret_cast<uintptr_t>(workspace) & 255))
+            return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm_qkv_rope: workspace too small or misaligned");
+        p.part = static_cast<float *>(workspace);
+        p.flags = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) +
+                                               (size_t)p.num_sms * 128 * 256 * sizeof(float) + 256);
+    }
+    cudaError_t e = h3::launch_gemm(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "gemm_qkv_rope launch");
 }
 
 h3enc_status h3enc_op_attention(const void *qkv, void *o, int32_t S, int32_t n_heads, int32_t n_kv_heads,

@@ -67,6 +67,11 @@ struct GemmArgs {
     float *part;       // [grid][BM*BN] fp32 partial accumulators (one slot per CTA)
     uint32_t *flags;   // [grid] release flags
     uint32_t epoch;    // unique per launch; a flag equal to it means "partial written"
+    // EPI_QKROPE
+    const __nv_bfloat16 *wq, *wk;
+    const float *cos_t, *sin_t;
+    int head_dim, nq, nkv;
+    float eps;
 };
 
 // The K-chunk of this pair's split item (none when kb1 <= kb0).
@@ -311,12 +316,90 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         store_row32(g.C + (size_t)row * g.ldc + n_blk * (BN / 2) + c * 32, f);
                     }
                 }
+            } else if constexpr (EPI == EPI_QKROPE) {
+                // the tile holds BN/d whole heads: q and k heads get RMSNorm over d and M-RoPE
+                // (pairs j, j + d/2 both in this thread's row), v heads are stored as they are
+                const int d = g.head_dim, half = d >> 1;
+                #pragma unroll 1
+                for (int hh = 0; hh < BN / d; ++hh) {
+                    const int head = (n_blk * BN) / d + hh;
+                    const int cb = hh * d;
+                    __nv_bfloat16 *dst = g.C + (size_t)row * g.ldc + n_blk * BN + cb;
+                    const bool is_q = head < g.nq, is_k = !is_q && head < g.nq + g.nkv;
+                    if (!is_q && !is_k) {
+                        #pragma unroll 1
+                        for (int c = 0; c < d / 32; ++c) {
+                            uint32_t v[32];
+                            tmem_ld32(taddr + cb + c * 32, v);
+                            tmem_ld_wait();
+                            if (live) {
+                                float f[32];
+                                #pragma unroll
+                                for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+                                store_row32(dst + c * 32, f);
+                            }
+                        }
+                        continue;
+                    }
+                    float ss = 0.f;
+                    #pragma unroll 1
+                    for (int c = 0; c < d / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32(taddr + cb + c * 32, v);
+                        tmem_ld_wait();
+                        #pragma unroll
+                        for (int j = 0; j < 32; ++j) ss = fmaf(__uint_as_float(v[j]), __uint_as_float(v[j]), ss);
+                    }
+                    const float rstd = 1.0f / sqrtf(ss / (float)d + g.eps);
+                    const __nv_bfloat16 *w = is_q ? g.wq : g.wk;
+                    #pragma unroll 1
+                    for (int c = 0; c < half / 32; ++c) {
+                        uint32_t va[32], vb[32];
+                        tmem_ld32(taddr + cb + c * 32, va);
+                        tmem_ld32(taddr + cb + half + c * 32, vb);
+                        tmem_ld_wait();
+                        if (live) {
+                            const float *cs = g.cos_t + (size_t)row * half + c * 32;
+                            const float *sn = g.sin_t + (size_t)row * half + c * 32;
+                            uint32_t oa[16], ob[16];
+                            #pragma unroll
+                            for (int j = 0; j < 32; j += 4) {
+                                const float4 co = *reinterpret_cast<const float4 *>(cs + j);
+                                const float4 si = *reinterpret_cast<const float4 *>(sn + j);
+                                const uint2 wa = *reinterpret_cast<const uint2 *>(w + c * 32 + j);
+                                const uint2 wb = *reinterpret_cast<const uint2 *>(w + half + c * 32 + j);
+                                const float ga[4] = {bf16_lo(wa.x), bf16_hi(wa.x), bf16_lo(wa.y), bf16_hi(wa.y)};
+                                const float gb[4] = {bf16_lo(wb.x), bf16_hi(wb.x), bf16_lo(wb.y), bf16_hi(wb.y)};
+                                const float cv[4] = {co.x, co.y, co.z, co.w}, sv[4] = {si.x, si.y, si.z, si.w};
+                                float ra[4], rb[4];
+                                #pragma unroll
+                                for (int t = 0; t < 4; ++t) {
+                                    const float ya = __uint_as_float(va[j + t]) * rstd * ga[t];
+                                    const float yb = __uint_as_float(vb[j + t]) * rstd * gb[t];
+                                    ra[t] = ya * cv[t] - yb * sv[t];
+                                    rb[t] = yb * cv[t] + ya * sv[t];
+                                }
+                                oa[j / 2] = pack_bf16x2(ra[0], ra[1]);
+                                oa[j / 2 + 1] = pack_bf16x2(ra[2], ra[3]);
+                                ob[j / 2] = pack_bf16x2(rb[0], rb[1]);
+                                ob[j / 2 + 1] = pack_bf16x2(rb[2], rb[3]);
+                            }
+                            uint4 *pa = reinterpret_cast<uint4 *>(dst + c * 32);
+                            uint4 *pb = reinterpret_cast<uint4 *>(dst + half + c * 32);
+                            #pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                pa[q] = make_uint4(oa[4 * q], oa[4 * q + 1], oa[4 * q + 2], oa[4 * q + 3]);
+                                pb[q] = make_uint4(ob[4 * q], ob[4 * q + 1], ob[4 * q + 2], ob[4 * q + 3]);
+                            }
+                        }
+                    }
+                }
             } else {
-                int rank = -1;
+                int rank_ds = -1;
                 if constexpr (EPI == EPI_RESIDUAL_DS) {
                     if (live && g.DS != nullptr) {
-                        rank = g.vis_rank[row];
-                        if (rank >= g.n_vis) rank = -1;  // count mismatch is reported by the rank scan
+                        rank_ds = g.vis_rank[row];
+                        if (rank_ds >= g.n_vis) rank_ds = -1;  // count mismatch is reported by the rank scan
                     }
                 }
                 #pragma unroll 1
@@ -336,9 +419,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             for (int j = 0; j < 32; ++j) f[j] += r[j];
                         }
                         if constexpr (EPI == EPI_RESIDUAL_DS) {
-                            if (rank >= 0) {
+                            if (rank_ds >= 0) {
                                 float ds[32];
-                                load_row32(g.DS + (size_t)rank * g.ldc + col, ds);
+                                load_row32(g.DS + (size_t)rank_ds * g.ldc + col, ds);
                                 #pragma unroll
                                 for (int j = 0; j < 32; ++j) f[j] = round_bf16(f[j]) + ds[j];
                             }
@@ -387,6 +470,68 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     // 3) rows [r0, r1) of this CTA's half: sum of the s partials in chunk order, then the epilogue
                     const int r0 = sk.chunk * BM / g.splits, r1 = (sk.chunk + 1) * BM / g.splits;
                     const int m_blk = sk.tile % g.nm, n_blk = sk.tile / g.nm;
+                    if constexpr (EPI == EPI_QKROPE) {
+                        // four threads per (row, head): thread `sub` owns first-half columns
+                        // [sub*d/8, (sub+1)*d/8) and their RoPE partners d/2 further on
+                        const int d = g.head_dim, half = d >> 1, q4 = half >> 2, hpt = BN / d;
+                        const int sub = et & 3;
+                        const unsigned gmask = 0xFu << (lane & ~3);
+                        const int units = (r1 - r0) * hpt;
+                        for (int u = et >> 2; u < units; u += 32) {
+                            const int r = r0 + u / hpt, hh = u % hpt;
+                            const int row = m_blk * (2 * BM) + (int)rank * BM + r;
+                            if (row >= g.M) continue;   // same row for the four threads
+                            const int head = (n_blk * BN) / d + hh;
+                            const int ca = hh * d + sub * q4;      // first-half column inside the tile
+                            float a[16], b[16];
+                            #pragma unroll
+                            for (int i = 0; i < 16; ++i) a[i] = b[i] = 0.f;
+                            for (int j = 0; j < g.splits; ++j) {
+                                const float *pj = g.part + (size_t)(2 * (first_pair + j) + rank) * (BM * BN) +
+                                                  (size_t)r * BN;
+                                #pragma unroll
+                                for (int i = 0; i < 16; i += 4) {
+                                    if (i < q4) {
+                                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(pj + ca + i));
+                                        const float4 y = __ldcg(reinterpret_cast<const float4 *>(pj + ca + half + i));
+                                        a[i] += x.x; a[i + 1] += x.y; a[i + 2] += x.z; a[i + 3] += x.w;
+                                        b[i] += y.x; b[i + 1] += y.y; b[i + 2] += y.z; b[i + 3] += y.w;
+                                    }
+                                }
+                            }
+                            __nv_bfloat16 *dst = g.C + (size_t)row * g.ldc + n_blk * BN + ca;
+                            const bool is_q = head < g.nq, is_k = !is_q && head < g.nq + g.nkv;
+                            if (is_q || is_k) {
+                                float ss = 0.f;
+                                #pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    if (i < q4) ss = fmaf(a[i], a[i], fmaf(b[i], b[i], ss));
+                                ss += __shfl_xor_sync(gmask, ss, 1);
+                                ss += __shfl_xor_sync(gmask, ss, 2);
+                                const float rstd = 1.0f / sqrtf(ss / (float)d + g.eps);
+                                const __nv_bfloat16 *w = is_q ? g.wq : g.wk;
+                                const int jb = sub * q4;           // frequency index of a[0]
+                                #pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    if (i < q4) {
+                                        const float ya = a[i] * rstd * __bfloat162float(w[jb + i]);
+                                        const float yb = b[i] * rstd * __bfloat162float(w[half + jb + i]);
+                                        const float co = g.cos_t[(size_t)row * half + jb + i];
+                                        const float si = g.sin_t[(size_t)row * half + jb + i];
+                                        a[i] = ya * co - yb * si;
+                                        b[i] = yb * co + ya * si;
+                                    }
+                                }
+                            }
+                            #pragma unroll
+                            for (int i = 0; i < 16; i += 2) {
+                                if (i < q4) {
+                                    *reinterpret_cast<uint32_t *>(dst + i) = pack_bf16x2(a[i], a[i + 1]);
+                                    *reinterpret_cast<uint32_t *>(dst + half + i) = pack_bf16x2(b[i], b[i + 1]);
+                                }
+                            }
+                        }
+                    } else {
                     constexpr int UNITS_PER_ROW = (EPI == EPI_SWIGLU) ? BN / 8 : BN / 4;  // float4 groups
                     const int units = (r1 - r0) * UNITS_PER_ROW;
                     for (int u = et; u < units; u += 128) {
@@ -419,10 +564,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                 f[0] += bf16_lo(rv.x); f[1] += bf16_hi(rv.x); f[2] += bf16_lo(rv.y); f[3] += bf16_hi(rv.y);
                             }
                             if constexpr (EPI == EPI_RESIDUAL_DS) {
-                                int rank = g.DS != nullptr ? g.vis_rank[row] : -1;
-                                if (rank >= g.n_vis) rank = -1;
-                                if (rank >= 0) {
-                                    const uint2 dv = *reinterpret_cast<const uint2 *>(g.DS + (size_t)rank * g.ldc + col);
+                                int rank_ds = g.DS != nullptr ? g.vis_rank[row] : -1;
+                                if (rank_ds >= g.n_vis) rank_ds = -1;
+                                if (rank_ds >= 0) {
+                                    const uint2 dv = *reinterpret_cast<const uint2 *>(g.DS + (size_t)rank_ds * g.ldc + col);
                                     f[0] = round_bf16(f[0]) + bf16_lo(dv.x); f[1] = round_bf16(f[1]) + bf16_hi(dv.x);
                                     f[2] = round_bf16(f[2]) + bf16_lo(dv.y); f[3] = round_bf16(f[3]) + bf16_hi(dv.y);
                                 }
@@ -432,6 +577,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         o.x = pack_bf16x2(f[0], f[1]);
                         o.y = pack_bf16x2(f[2], f[3]);
                         *reinterpret_cast<uint2 *>(g.C + (size_t)row * g.ldc + col) = o;
+                    }
                     }
                 }
             }
@@ -497,6 +643,8 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     g.nk = (p.K + BK - 1) / BK;
     g.C = p.C; g.ldc = p.ldc; g.R = p.R; g.DS = p.DS; g.vis_rank = p.vis_rank; g.n_vis = p.n_vis;
     g.status = p.status;
+    g.wq = p.wq; g.wk = p.wk; g.cos_t = p.cos_t; g.sin_t = p.sin_t;
+    g.head_dim = p.head_dim; g.nq = p.nq; g.nkv = p.nkv; g.eps = p.eps;
     const int tiles = g.nm * g.nn;
     int pairs = p.num_sms / 2 < max_pairs ? p.num_sms / 2 : max_pairs;   // all pairs co-resident
     if (pairs < 1) pairs = 1;
@@ -549,6 +697,10 @@ cudaError_t launch_gemm(const GemmPlan &p, cudaStream_t stream) {
         case EPI_RESIDUAL: return launch_epi<EPI_RESIDUAL>(p, stream);
         case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(p, stream);
         case EPI_RESIDUAL_DS: return launch_epi<EPI_RESIDUAL_DS>(p, stream);
+        case EPI_QKROPE:
+            if ((p.head_dim != 64 && p.head_dim != 128) || !p.wq || !p.wk || !p.cos_t || !p.sin_t)
+                return cudaErrorInvalidValue;
+            return launch_epi<EPI_QKROPE>(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -10,7 +10,7 @@ namespace h3 {
 
 using bf16 = __nv_bfloat16;
 
-enum { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_RESIDUAL_DS = 3 };
+enum { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_RESIDUAL_DS = 3, EPI_QKROPE = 4 };
 
 constexpr int kMaxSeqs = 1024;
 constexpr int kMaxHalfDim = 64;
@@ -30,6 +30,11 @@ struct GemmPlan {
     int num_sms;
     float *part;        // split workspace: num_sms x 128 x 256 fp32 partials (NULL: no split)
     uint32_t *flags;    // num_sms release flags, zero-filled once before first use
+    // EPI_QKROPE: per-head RMSNorm of the q and k heads, then M-RoPE with the fp32 tables
+    const bf16 *wq = nullptr, *wk = nullptr;
+    const float *cos_t = nullptr, *sin_t = nullptr;   // [M, head_dim/2]
+    int head_dim = 0, nq = 0, nkv = 0;
+    float eps = 0.f;
 };
 // Tensor map of a row-major bf16 matrix [rows, cols] read in boxes of
 // box_rows x 64 with 128-byte swizzle.  False if the driver refuses it.
@@ -50,8 +55,7 @@ void make_rope_params(RopeParams *p, int head_dim, float theta, const int32_t se
 cudaError_t launch_rmsnorm(const bf16 *x, const bf16 *w, bf16 *y, int rows, int cols, float eps, cudaStream_t st);
 cudaError_t launch_rope_table(const int32_t *positions, int S, const RopeParams &rp, float *cos_t, float *sin_t,
                               cudaStream_t st);
-cudaError_t launch_qk_norm_rope(bf16 *qkv, int S, int nq, int nkv, int d, const bf16 *wq, const bf16 *wk,
-                                float eps, const float *cos_t, const float *sin_t, cudaStream_t st);
+
 
 // ---- attention on tcgen05 (attention_tc.cu)
 cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, int d, const int32_t *cu_host,

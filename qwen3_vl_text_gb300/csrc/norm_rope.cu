@@ -1,13 +1,12 @@
-// Memory-bound steps of the decoder layer: RMSNorm over the hidden size, the
-// M-RoPE cos/sin tables, and the fused per-head q/k RMSNorm + rotary embedding.
+// Memory-bound steps of the decoder layer: RMSNorm over the hidden size and the
+// M-RoPE cos/sin tables (the per-head q/k RMSNorm + rotary embedding runs in the
+// epilogue of the QKV projection, csrc/gemm.cu).
 //
 // Page "vllm-omni vllm_omni/diffusion/models/minimax_h3/encoder.py":
-// MiniMaxH3Qwen3VLRMSNorm (fp32 variance and scaling), the q_norm/k_norm calls
-// of MiniMaxH3Qwen3VLTextAttention.forward, _rotate_half /
-// _apply_rotary_pos_emb, and MiniMaxH3Qwen3VLTextRotaryEmbedding with
-// _apply_interleaved_mrope.  All arithmetic is fp32; each kernel rounds its
-// output to bf16 once (the pages' bf16 cast of cos/sin is not reproduced:
-// the tables stay fp32).
+// MiniMaxH3Qwen3VLRMSNorm (fp32 variance and scaling) and
+// MiniMaxH3Qwen3VLTextRotaryEmbedding with _apply_interleaved_mrope.  All
+// arithmetic is fp32; RMSNorm rounds its output to bf16 once; the pages' bf16
+// cast of cos/sin is not reproduced: the tables stay fp32.
 #include <cmath>
 
 #include "common.cuh"
@@ -90,65 +89,6 @@ __global__ void rope_table_kernel(const int32_t *__restrict__ pos, int S, const 
     sin_t[i] = sn;
 }
 
-// One warp per (token, q-or-k head).  Lane l holds elements [l*E, l*E+E) of
-// the head (E = D/32); lanes 0-15 hold the first half, lanes 16-31 the second,
-// so the rotate-half partner of a lane's element sits in lane l ^ 16.
-template <int D>
-__global__ void __launch_bounds__(256) qk_norm_rope_kernel(bf16 *qkv, int S, int nq, int nkv, int ld,
-                                                           const bf16 *__restrict__ wq,
-                                                           const bf16 *__restrict__ wk, float eps,
-                                                           const float *__restrict__ cos_t,
-                                                           const float *__restrict__ sin_t) {
-    constexpr int E = D / 32;
-    constexpr int HALF = D / 2;
-    const int lane = threadIdx.x & 31;
-    const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int nh = nq + nkv;
-    if (gw >= (long long)S * nh) return;
-    const int s = (int)(gw / nh);
-    const int h = (int)(gw - (long long)s * nh);
-    bf16 *p = qkv + (size_t)s * ld + (size_t)h * D + lane * E;
-    const bf16 *w = (h < nq ? wq : wk) + lane * E;
-    float f[E], g[E];
-    if constexpr (E == 4) {
-        const uint2 v = *reinterpret_cast<const uint2 *>(p);
-        const uint2 u = *reinterpret_cast<const uint2 *>(w);
-        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-        g[0] = bf16_lo(u.x); g[1] = bf16_hi(u.x); g[2] = bf16_lo(u.y); g[3] = bf16_hi(u.y);
-    } else {
-        const uint32_t v = *reinterpret_cast<const uint32_t *>(p);
-        const uint32_t u = *reinterpret_cast<const uint32_t *>(w);
-        f[0] = bf16_lo(v); f[1] = bf16_hi(v);
-        g[0] = bf16_lo(u); g[1] = bf16_hi(u);
-    }
-    float ss = 0.f;
-    #pragma unroll
-    for (int e = 0; e < E; ++e) ss = fmaf(f[e], f[e], ss);
-    ss = warp_sum(ss);
-    const float rstd = 1.0f / sqrtf(ss / (float)D + eps);
-    float y[E], o[E];
-    #pragma unroll
-    for (int e = 0; e < E; ++e) y[e] = f[e] * rstd * g[e];
-    const bool first = lane < 16;
-    const int j0 = (lane & 15) * E;  // frequency index of element 0 of this lane
-    const float *cr = cos_t + (size_t)s * HALF + j0;
-    const float *sr = sin_t + (size_t)s * HALF + j0;
-    #pragma unroll
-    for (int e = 0; e < E; ++e) {
-        const float partner = __shfl_xor_sync(0xffffffffu, y[e], 16);
-        const float c = cr[e], sn = sr[e];
-        o[e] = first ? (y[e] * c - partner * sn) : (y[e] * c + partner * sn);
-    }
-    if constexpr (E == 4) {
-        uint2 r;
-        r.x = pack_bf16x2(o[0], o[1]);
-        r.y = pack_bf16x2(o[2], o[3]);
-        *reinterpret_cast<uint2 *>(p) = r;
-    } else {
-        *reinterpret_cast<uint32_t *>(p) = pack_bf16x2(o[0], o[1]);
-    }
-}
-
 }  // namespace
 
 void make_rope_params(RopeParams *p, int head_dim, float theta, const int32_t section[3]) {
@@ -178,21 +118,6 @@ cudaError_t launch_rope_table(const int32_t *positions, int S, const RopeParams 
     if (S <= 0) return cudaSuccess;
     const int n = S * rp.half_dim;
     rope_table_kernel<<<(n + 255) / 256, 256, 0, st>>>(positions, S, rp, cos_t, sin_t);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_qk_norm_rope(bf16 *qkv, int S, int nq, int nkv, int d, const bf16 *wq, const bf16 *wk,
-                                float eps, const float *cos_t, const float *sin_t, cudaStream_t st) {
-    if (S <= 0) return cudaSuccess;
-    const long long warps = (long long)S * (nq + nkv);
-    const unsigned grid = (unsigned)((warps + 7) / 8);
-    const int ld = (nq + 2 * nkv) * d;
-    if (d == 128)
-        qk_norm_rope_kernel<128><<<grid, 256, 0, st>>>(qkv, S, nq, nkv, ld, wq, wk, eps, cos_t, sin_t);
-    else if (d == 64)
-        qk_norm_rope_kernel<64><<<grid, 256, 0, st>>>(qkv, S, nq, nkv, ld, wq, wk, eps, cos_t, sin_t);
-    else
-        return cudaErrorInvalidValue;
     return cudaGetLastError();
 }
 

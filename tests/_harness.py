@@ -24,7 +24,7 @@ def max_abs_over_rms(a, b) -> float:
 
 
 # Tensors the GPU path hands between kernels in bf16 (its rounding points).
-GPU_STORAGE = frozenset({"y", "qk_proj", "v", "qk", "attn", "act", "h"})
+GPU_STORAGE = frozenset({"y", "v", "qk", "attn", "act", "h"})
 
 
 def within(gpu, ref32, refbf, rel_bar, maxabs_bar=None):

@@ -237,28 +237,31 @@ def test_rope_table(wl_id):
     assert np.max(np.abs(s.cpu().numpy() - rs[:, :h])) < 2e-6
 
 
-@pytest.mark.parametrize("d,nq,nkv", [(64, 4, 2), (128, 64, 8)])
-def test_qk_norm_rope(d, nq, nkv):
-    S = 97
-    width = (nq + 2 * nkv) * d
-    X, x = _bf16(22, "qkv", (S, width), sigma=2.0)
-    Gq, gq = _bf16(23, "gq", (d,), 1.0, 0.1)
-    Gk, gk = _bf16(24, "gk", (d,), 1.0, 0.1)
-    pos = np.stack([np.arange(S) * 3, np.arange(S) * 5 + 1, np.arange(S) * 7 + 2]).astype(np.int32)
+@pytest.mark.parametrize("d,nq,nkv,M,split", [(64, 4, 2, 97, False), (128, 64, 8, 300, False),
+                                                (128, 64, 8, 1024, True), (64, 8, 4, 1000, True)])
+def test_qkv_projection_with_fused_norm_rope(d, nq, nkv, M, split):
+    K = 512
+    N = (nq + 2 * nkv) * d
+    A, a = _bf16(22, "A", (M, K))
+    Wt, w = _bf16(23, "Wqkv", (N, K), sigma=0.05)
+    Gq, gq = _bf16(24, "gq", (d,), 1.0, 0.1)
+    Gk, gk = _bf16(25, "gk", (d,), 1.0, 0.1)
+    pos = np.stack([np.arange(M) * 3, np.arange(M) * 5 + 1, np.arange(M) * 7 + 2]).astype(np.int32)
     sec = (24, 20, 20) if d == 128 else (12, 10, 10)
-    c = torch.empty(S, d // 2, device="cuda")
+    c = torch.empty(M, d // 2, device="cuda")
     s = torch.empty_like(c)
-    Q.h3enc_op_rope_table(torch.from_numpy(pos).cuda(), S, d, 5e6, sec, c, s)
-    Q.h3enc_op_qk_norm_rope(X, S, nq, nkv, d, Gq, Gk, 1e-6, c, s)
+    Q.h3enc_op_rope_table(torch.from_numpy(pos).cuda(), M, d, 5e6, sec, c, s)
+    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    ws = _workspace() if split else None
+    Q.h3enc_op_gemm_qkv_rope(A, Wt, C, M, K, nq, nkv, d, Gq, Gk, 1e-6, c, s, workspace=ws)
     torch.cuda.synchronize()
+    x = O.linear(a, w)
     cos, sin = O.rope_cos_sin(pos, d, 5e6, sec)
-    q = O.apply_rope(O.rms_norm(x[:, :nq * d].reshape(S, nq, d), gq, 1e-6), cos, sin).reshape(S, -1)
-    k = O.apply_rope(O.rms_norm(x[:, nq * d:(nq + nkv) * d].reshape(S, nkv, d), gk, 1e-6), cos, sin).reshape(S, -1)
+    q = O.apply_rope(O.rms_norm(x[:, :nq * d].reshape(M, nq, d), gq, 1e-6), cos, sin).reshape(M, -1)
+    k = O.apply_rope(O.rms_norm(x[:, nq * d:(nq + nkv) * d].reshape(M, nkv, d), gk, 1e-6), cos, sin).reshape(M, -1)
     ref = np.concatenate([q, k, x[:, (nq + nkv) * d:]], axis=1)
-    got = t2f(X)
-    bad, worst = _elementwise_ok(got, ref)
+    bad, worst = _elementwise_ok(t2f(C), ref)
     assert bad == 0, f"{bad} elements off, worst {worst}"
-    assert np.array_equal(got[:, (nq + nkv) * d:], x[:, (nq + nkv) * d:]), "v heads changed"
 
 
 @pytest.mark.parametrize("d,nq,nkv,cu", [
