@@ -102,6 +102,21 @@ class Clocks:
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def job_throughput(local_ms: float, units_per_rank: int, steps: int, dist=None, device=None):
+    """Whole-job rate of N independent replicas: every rank processed `units_per_rank`
+    units per step; the job took as long as its slowest rank (max over ranks).
+    Returns (units per second over all ranks, max milliseconds)."""
+    ms = float(local_ms)
+    world = 1
+    if dist is not None and dist.is_initialized():
+        import torch
+        world = dist.get_world_size()
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return world * units_per_rank * steps / (ms / 1e3), ms
+
+
 def cpu_oracle_layer_time(wl, inp, layers=1):
     """Seconds the CPU oracle takes for `layers` decoder layers of the workload."""
     import numpy as np
@@ -321,10 +336,7 @@ def main():
         step()
     prof = Q.h3enc_get_profile(enc.handle)
     Q.h3enc_set_profiling(enc.handle, False)
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    value, ms = job_throughput(ms, S, args.steps, dist, "cuda")
     if enc.status() != 0:
         raise RuntimeError("device status after the timed region: " + Q.h3enc_last_error(enc.handle))
 
@@ -346,17 +358,12 @@ def main():
     e2e_steps = max(3, args.steps // 2)
     for _ in range(e2e_steps):
         host_step()
-    e2e_s = time.perf_counter() - t0
-    if dist:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_value, e2e_ms = job_throughput((time.perf_counter() - t0) * 1e3, S, e2e_steps, dist, "cuda")
     h2d = (h_ids.numel() * 4 + h_pos.numel() * 4 + h_mask.numel() + h_ds.numel() * 2)
     d2h = h_out.numel() * 2
 
     burst, sustained, hbm, peak_src = _peaks()
     flops = encode_flops(cfg, inp["cu_seqlens"])
-    value = world * S * args.steps / (ms / 1e3)
     gu_ms, gu_n = prof_gu
     gu_flops = 2.0 * S * (2 * cfg.intermediate) * cfg.hidden
     gu_achieved = gu_flops / (gu_ms / gu_n / 1e3) / 1e12 if gu_n else 0.0
@@ -377,7 +384,7 @@ def main():
         "kernel_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
         "kernel_ms_note": "separate pass with an event pair around every launch",
         "gpu_launches": int(launches),
-        "e2e": {"value": world * S * e2e_steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "clocks": clk,
     }
