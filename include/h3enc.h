@@ -128,6 +128,18 @@ H3ENC_API h3enc_status h3enc_encode(h3enc *h, const int32_t *input_ids, const in
                           int32_t n_vis, const int32_t *cu_seqlens, int32_t n_seqs, int32_t seq_len,
                           void *out, void *stream);
 
+/* As h3enc_encode, with the visual rows' input embeddings replaced by the
+ * vision tower's merged features (page "... encoder.py", _encode:
+ * inputs_embeds.masked_scatter(mask, visual_embeds)): visual_embeds is device
+ * bf16 [n_vis, hidden], row j goes to the j-th visual row; NULL behaves as
+ * h3enc_encode.  A visual-mask count other than n_vis is reported by
+ * h3enc_get_status (H3ENC_ERR_SHAPE) and those rows keep their token embedding. */
+H3ENC_API h3enc_status h3enc_encode_multimodal(h3enc *h, const int32_t *input_ids, const int32_t *positions,
+                                     const uint8_t *visual_mask, const void *visual_embeds,
+                                     const void *deepstack, int32_t num_deepstack, int32_t n_vis,
+                                     const int32_t *cu_seqlens, int32_t n_seqs, int32_t seq_len, void *out,
+                                     void *stream);
+
 /* As h3enc_encode, from hidden states instead of token ids, over the layer
  * range [layer_begin, layer_end) (global layer indices: DeepStack level l still
  * follows layer l).  inputs_embeds: device bf16 [S, hidden]; it may equal out. */
@@ -161,6 +173,45 @@ H3ENC_API h3enc_status h3enc_get_status(h3enc *h);
 H3ENC_API const char *h3enc_last_error(const h3enc *h);
 
 H3ENC_API void h3enc_destroy(h3enc *h);
+
+/* ---- multimodal front end (ids -> positions, visual rows, DeepStack layout) ---- */
+
+/* M-RoPE positions [3, S] and the visual mask from token ids (page "vllm-omni
+ * ... encoder.py", _get_rope_index with _get_vision_position_ids, and
+ * _get_placeholder_mask).  HOST memory in and out.  Tokens equal to
+ * image_token_id / video_token_id are visual; consecutive tokens of one kind
+ * form a run.  A text run of n tokens at running start c gets (c+i, c+i, c+i)
+ * and c += n.  A visual run takes the next grid of its kind (image grids in
+ * order; a video of T frames counts as T grids of one frame), whose merged
+ * size t * (h/m) * (w/m) (m = spatial_merge_size) must equal the run length,
+ * gets (c+f, c+r, c+col) in (f, r, col) row-major order, and c += max(h, w)/m.
+ *   image_grid_thw [n_images, 3], video_grid_thw [n_videos, 3] (t, h, w before merging)
+ *   positions [3, S] out; visual_mask [S] out (1 = visual) or NULL;
+ *   visual_kind [S] out (0 text, 1 image, 2 video) or NULL;
+ *   n_image_tokens, n_video_tokens, mrope_delta (max position + 1 - S) out or NULL.
+ * H3ENC_ERR_SHAPE if a run does not match its grid or grids run out; the
+ * message is in h3enc_frontend_last_error(). */
+H3ENC_API h3enc_status h3enc_build_positions(const int32_t *input_ids, int32_t seq_len, int32_t image_token_id,
+                                   int32_t video_token_id, const int32_t *image_grid_thw, int32_t n_images,
+                                   const int32_t *video_grid_thw, int32_t n_videos,
+                                   int32_t spatial_merge_size, int32_t *positions, uint8_t *visual_mask,
+                                   uint8_t *visual_kind, int32_t *n_image_tokens, int32_t *n_video_tokens,
+                                   int32_t *mrope_delta);
+
+/* DeepStack features of images and videos interleaved in sequence order
+ * (page "... encoder.py", _aggregate_deepstack): for every level l,
+ * out[l][j] = the next image row if the j-th visual token is an image token,
+ * else the next video row.  visual_kind HOST [S] (from h3enc_build_positions);
+ * image_feats [levels, n_image_tokens, hidden], video_feats [levels,
+ * n_video_tokens, hidden], out [levels, n_image_tokens + n_video_tokens,
+ * hidden]: device bf16.  Asynchronous copies on `stream`. */
+H3ENC_API h3enc_status h3enc_aggregate_deepstack(const uint8_t *visual_kind, int32_t seq_len,
+                                       const void *image_feats, int32_t n_image_tokens, const void *video_feats,
+                                       int32_t n_video_tokens, int32_t levels, int32_t hidden, void *out,
+                                       void *stream);
+
+/* Message of the last front-end error on this thread. */
+H3ENC_API const char *h3enc_frontend_last_error(void);
 
 /* Kernel classes timed by the optional profiler. */
 enum {

@@ -14,9 +14,10 @@ import os
 
 __all__ = [
     "lib", "H3encError", "Config", "STATUS", "EPI_STORE", "EPI_RESIDUAL", "EPI_SWIGLU", "EPI_RESIDUAL_DS",
-    "h3enc_create", "h3enc_load_weights", "h3enc_finalize_weights", "h3enc_encode", "h3enc_encode_embeds",
+    "h3enc_create", "h3enc_load_weights", "h3enc_finalize_weights", "h3enc_encode", "h3enc_encode_embeds", "h3enc_encode_multimodal",
     "h3enc_encode_host", "h3enc_set_layer_capture", "h3enc_get_status", "h3enc_last_error", "h3enc_destroy",
     "h3enc_set_profiling", "h3enc_set_profiling_classes", "h3enc_get_profile", "h3enc_launch_count", "h3enc_num_sms",
+    "h3enc_build_positions", "h3enc_aggregate_deepstack",
     "h3enc_op_gemm", "h3enc_op_gemm_workspace_bytes", "h3enc_op_gemm_noalloc", "h3enc_op_gemm_noalloc_scratch_bytes", "h3enc_op_pack_gate_up", "h3enc_op_rmsnorm", "h3enc_op_rope_table",
     "h3enc_op_gemm_qkv_rope", "h3enc_op_attention", "h3enc_op_embed", "h3enc_op_vis_rank", "Encoder",
     "KERNEL_CLASSES",
@@ -61,6 +62,7 @@ _SIGS = {
     "h3enc_finalize_weights": ([_P], _I32),
     "h3enc_encode": ([_P, _P, _P, _P, _P, _I32, _I32, _P, _I32, _I32, _P, _P], _I32),
     "h3enc_encode_embeds": ([_P, _P, _I32, _I32, _P, _P, _P, _I32, _I32, _P, _I32, _I32, _P, _P], _I32),
+    "h3enc_encode_multimodal": ([_P, _P, _P, _P, _P, _P, _I32, _I32, _P, _I32, _I32, _P, _P], _I32),
     "h3enc_encode_host": ([_P, _P, _P, _P, _P, _I32, _I32, _P, _I32, _I32, _P, _P], _I32),
     "h3enc_set_layer_capture": ([_P, ctypes.POINTER(_P), _I32], _I32),
     "h3enc_get_status": ([_P], _I32),
@@ -73,6 +75,9 @@ _SIGS = {
     "h3enc_num_sms": ([_P], _I32),
     "h3enc_op_gemm": ([_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _I64, _P, _P], _I32),
     "h3enc_op_gemm_workspace_bytes": ([], _I64),
+    "h3enc_build_positions": ([_P, _I32, _I32, _I32, _P, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _P], _I32),
+    "h3enc_aggregate_deepstack": ([_P, _I32, _P, _I32, _P, _I32, _I32, _I32, _P, _P], _I32),
+    "h3enc_frontend_last_error": ([], ctypes.c_char_p),
     "h3enc_op_gemm_noalloc": ([_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _P], _I32),
     "h3enc_op_gemm_noalloc_scratch_bytes": ([], _I64),
     "h3enc_op_gemm_noalloc_last_error": ([], ctypes.c_char_p),
@@ -150,6 +155,15 @@ def h3enc_encode(h, input_ids, positions, visual_mask, deepstack, num_deepstack,
                                    num_deepstack, n_vis, cu, n_seqs, seq_len, _ptr(out), _stream(stream)), h)
 
 
+def h3enc_encode_multimodal(h, input_ids, positions, visual_mask, visual_embeds, deepstack, num_deepstack, n_vis,
+                            cu_seqlens, seq_len, out, stream=None):
+    cu = _host_i32(cu_seqlens)
+    n_seqs = len(cu) - 1 if cu is not None else 0
+    return _check(lib.h3enc_encode_multimodal(h, _ptr(input_ids), _ptr(positions), _ptr(visual_mask),
+                                              _ptr(visual_embeds), _ptr(deepstack), num_deepstack, n_vis, cu,
+                                              n_seqs, seq_len, _ptr(out), _stream(stream)), h)
+
+
 def h3enc_encode_embeds(h, inputs_embeds, layer_begin, layer_end, positions, visual_mask, deepstack,
                         num_deepstack, n_vis, cu_seqlens, seq_len, out, stream=None):
     cu = _host_i32(cu_seqlens)
@@ -165,6 +179,43 @@ def h3enc_encode_host(h, input_ids, positions, visual_mask, deepstack, num_deeps
     n_seqs = len(cu) - 1 if cu is not None else 0
     return _check(lib.h3enc_encode_host(h, _ptr(input_ids), _ptr(positions), _ptr(visual_mask), _ptr(deepstack),
                                         num_deepstack, n_vis, cu, n_seqs, seq_len, _ptr(out), _stream(stream)), h)
+
+
+def h3enc_build_positions(input_ids, image_token_id, video_token_id, image_grid_thw=None, video_grid_thw=None,
+                          spatial_merge_size=2):
+    """Host arrays in, (positions int32 [3,S], visual_mask uint8 [S], visual_kind uint8 [S],
+    n_image_tokens, n_video_tokens, mrope_delta) out."""
+    import numpy as np
+    ids = np.ascontiguousarray(input_ids, dtype=np.int32)
+    S = ids.shape[0]
+    img = None if image_grid_thw is None else np.ascontiguousarray(image_grid_thw, dtype=np.int32).reshape(-1, 3)
+    vid = None if video_grid_thw is None else np.ascontiguousarray(video_grid_thw, dtype=np.int32).reshape(-1, 3)
+    pos = np.zeros((3, S), dtype=np.int32)
+    mask = np.zeros(S, dtype=np.uint8)
+    kind = np.zeros(S, dtype=np.uint8)
+    ni, nv, delta = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    code = lib.h3enc_build_positions(ids.ctypes.data, S, image_token_id, video_token_id,
+                                     None if img is None else img.ctypes.data, 0 if img is None else len(img),
+                                     None if vid is None else vid.ctypes.data, 0 if vid is None else len(vid),
+                                     spatial_merge_size, pos.ctypes.data, mask.ctypes.data, kind.ctypes.data,
+                                     ctypes.byref(ni), ctypes.byref(nv), ctypes.byref(delta))
+    if code != 0:
+        raise H3encError(code, lib.h3enc_frontend_last_error().decode())
+    return pos, mask, kind, ni.value, nv.value, delta.value
+
+
+def h3enc_aggregate_deepstack(visual_kind, image_feats, video_feats, out, stream=None):
+    """visual_kind: host uint8 [S]; feats/out: device bf16 [levels, n, hidden] tensors (or None)."""
+    import numpy as np
+    kind = np.ascontiguousarray(visual_kind, dtype=np.uint8)
+    levels, _, hidden = out.shape
+    ni = 0 if image_feats is None else int(image_feats.shape[1])
+    nv = 0 if video_feats is None else int(video_feats.shape[1])
+    code = lib.h3enc_aggregate_deepstack(kind.ctypes.data, kind.shape[0], _ptr(image_feats), ni, _ptr(video_feats),
+                                         nv, levels, hidden, _ptr(out), _stream(stream))
+    if code != 0:
+        raise H3encError(code, lib.h3enc_frontend_last_error().decode())
+    return code
 
 
 def h3enc_set_layer_capture(h, tensors):

@@ -216,7 +216,7 @@ h3enc_status check_encode_args(h3enc *h, const void *positions, const uint8_t *m
 
 h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int lb, int le, const int32_t *pos,
                          const uint8_t *mask, const bf16 *ds, int nds, int n_vis, const int32_t *cu, int n_seqs,
-                         int S, bf16 *out, cudaStream_t st) {
+                         int S, bf16 *out, cudaStream_t st, const bf16 *visual_embeds = nullptr) {
     if (S == 0) return H3ENC_OK;
     const h3enc_config &c = h->cfg;
     const int H = c.hidden, d = c.head_dim, nq = c.n_heads, nkv = c.n_kv_heads, I = c.intermediate;
@@ -233,10 +233,18 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
     e = run(h, H3ENC_K_PREP, st, [&] { return h3::launch_rope_table(pos, S, h->rope, h->cos_t, h->sin_t, st); });
     if (e != cudaSuccess) return cuda_fail(h, e, "rope table");
     const bool use_ds = nds > 0 && n_vis > 0;
-    if (use_ds) {
+    const bool use_ve = visual_embeds != nullptr && n_vis > 0;
+    if (use_ds || use_ve) {
         e = run(h, H3ENC_K_PREP, st,
                 [&] { return h3::launch_vis_rank(mask, S, n_vis, h->vis_rank, h->status, st); });
         if (e != cudaSuccess) return cuda_fail(h, e, "visual ranks");
+    }
+    if (use_ve) {
+        // vision-merger rows replace the placeholder embeddings (masked_scatter in sequence order)
+        e = run(h, H3ENC_K_PREP, st, [&] {
+            return h3::launch_merge_visual_rows(h->vis_rank, visual_embeds, n_vis, H, out, S, st);
+        });
+        if (e != cudaSuccess) return cuda_fail(h, e, "visual embedding merge");
     }
     for (int l = lb; l < le; ++l) {
         LayerW &w = h->layers[l];
@@ -510,6 +518,24 @@ h3enc_status h3enc_encode(h3enc *h, const int32_t *input_ids, const int32_t *pos
     return encode_core(h, input_ids, nullptr, 0, h->cfg.num_layers, positions, visual_mask,
                        static_cast<const bf16 *>(deepstack), num_deepstack, n_vis, cu_seqlens, n_seqs, seq_len,
                        static_cast<bf16 *>(out), static_cast<cudaStream_t>(stream));
+}
+
+h3enc_status h3enc_encode_multimodal(h3enc *h, const int32_t *input_ids, const int32_t *positions,
+                                     const uint8_t *visual_mask, const void *visual_embeds, const void *deepstack,
+                                     int32_t num_deepstack, int32_t n_vis, const int32_t *cu_seqlens, int32_t n_seqs,
+                                     int32_t seq_len, void *out, void *stream) {
+    if (!h) return fail(h, H3ENC_ERR_INVALID_ARG, "NULL handle");
+    h3enc_status s = check_encode_args(h, positions, visual_mask, deepstack, num_deepstack, n_vis, cu_seqlens,
+                                       n_seqs, seq_len, out);
+    if (s != H3ENC_OK) return s;
+    if (h->cfg.vocab == 0) return fail(h, H3ENC_ERR_UNSUPPORTED, "model has no embedding table (vocab 0)");
+    if (seq_len > 0 && !input_ids) return fail(h, H3ENC_ERR_INVALID_ARG, "input_ids is NULL");
+    if (n_vis > 0 && visual_embeds && !visual_mask)
+        return fail(h, H3ENC_ERR_INVALID_ARG, "visual_embeds need a visual_mask");
+    return encode_core(h, input_ids, nullptr, 0, h->cfg.num_layers, positions, visual_mask,
+                       static_cast<const bf16 *>(deepstack), num_deepstack, n_vis, cu_seqlens, n_seqs, seq_len,
+                       static_cast<bf16 *>(out), static_cast<cudaStream_t>(stream),
+                       static_cast<const bf16 *>(visual_embeds));
 }
 
 h3enc_status h3enc_encode_embeds(h3enc *h, const void *inputs_embeds, int32_t layer_begin, int32_t layer_end,

@@ -455,15 +455,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             __threadfence();
             if (epi_bar_and(got)) {
                 if (et == 0) st_release(g.flags + blockIdx.x, g.epoch);
-                // 2) wait for the same-rank CTAs of the s pairs that computed this tile
+                // 2) wait for the same-rank CTAs of the s pairs that computed this tile: thread j polls
+                //    contributor j (all flags in flight at once), then the AND over the epilogue warps
                 const int first_pair = pair - sk.chunk;
-                bool all = true;
-                const long long t0 = clock64();
-                for (int j = 0; j < g.splits && all; ++j) {
-                    while (ld_acquire(g.flags + 2 * (first_pair + j) + rank) != g.epoch) {
-                        if (clock64() - t0 > kSpinLimitCycles) { all = false; break; }
+                bool seen = true;
+                if (et < g.splits) {
+                    const long long t0 = clock64();
+                    while (ld_acquire(g.flags + 2 * (first_pair + et) + rank) != g.epoch) {
+                        if (clock64() - t0 > kSpinLimitCycles) { seen = false; break; }
                     }
                 }
+                const bool all = epi_bar_and(seen);
                 if (!all) {
                     if (et == 0) report(g.status, ST_TIMEOUT);
                 } else {
@@ -540,14 +542,28 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         const int row = m_blk * (2 * BM) + (int)rank * BM + r;
                         if (row >= g.M) continue;
                         float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-                        for (int j = 0; j < g.splits; ++j) {
-                            const float *pj = g.part + (size_t)(2 * (first_pair + j) + rank) * (BM * BN) +
-                                              (size_t)r * BN;
-                            const float4 x = __ldcg(reinterpret_cast<const float4 *>(pj + c4));
-                            a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
-                            if constexpr (EPI == EPI_SWIGLU) {
-                                const float4 y = __ldcg(reinterpret_cast<const float4 *>(pj + BN / 2 + c4));
-                                b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+                        // partials in batches of 8 loads in flight, summed in chunk order
+                        const float *p0 = g.part + (size_t)(2 * first_pair + rank) * (BM * BN) + (size_t)r * BN + c4;
+                        constexpr size_t kPairStride = (size_t)2 * BM * BN;
+                        for (int j0 = 0; j0 < g.splits; j0 += 8) {
+                            float4 x[8], y[8];
+                            #pragma unroll
+                            for (int t = 0; t < 8; ++t) {
+                                if (j0 + t < g.splits) {
+                                    x[t] = __ldcg(reinterpret_cast<const float4 *>(p0 + (j0 + t) * kPairStride));
+                                    if constexpr (EPI == EPI_SWIGLU)
+                                        y[t] = __ldcg(reinterpret_cast<const float4 *>(p0 + (j0 + t) * kPairStride +
+                                                                                       BN / 2));
+                                }
+                            }
+                            #pragma unroll
+                            for (int t = 0; t < 8; ++t) {
+                                if (j0 + t < g.splits) {
+                                    a.x += x[t].x; a.y += x[t].y; a.z += x[t].z; a.w += x[t].w;
+                                    if constexpr (EPI == EPI_SWIGLU) {
+                                        b.x += y[t].x; b.y += y[t].y; b.z += y[t].z; b.w += y[t].w;
+                                    }
+                                }
                             }
                         }
                         float f[4] = {a.x, a.y, a.z, a.w};

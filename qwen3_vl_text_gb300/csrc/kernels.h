@@ -69,6 +69,9 @@ cudaError_t launch_vis_rank(const uint8_t *mask, int S, int n_vis, int32_t *rank
 cudaError_t pack_gate_up_rows(const bf16 *src, bf16 *W, int I, int K, int which, cudaMemcpyKind kind,
                               cudaStream_t st);
 
+cudaError_t launch_merge_visual_rows(const int32_t *vis_rank, const bf16 *src, int n_vis, int hidden, bf16 *out,
+                                     int S, cudaStream_t st);
+
 int device_num_sms();
 
 }  // namespace h3
