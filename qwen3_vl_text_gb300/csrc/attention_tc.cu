@@ -12,10 +12,14 @@
 //                S_j = Q K_j^T   (M=128, N=128, K=d)   into one of two TMEM S buffers
 //                O  += P_j V_j   (M=128, N=d,   K=128) into the TMEM O buffer; V is read
 //                                  as an MN-major operand straight from its TMA tile
-//   warps 2-5  one query row per thread: read S row from TMEM, causal mask, online
-//              softmax in fp32 with exp2 and a lazily updated running max (O is
-//              rescaled in TMEM only when the row max grows by more than 2^8), P as
-//              bf16 into swizzled shared memory; at the end O / l -> bf16 -> global
+//   warps 2+   NWG softmax warpgroups (4 for d = 128, 2 for d = 64); thread = one
+//              query row (its TMEM lane) x one NWG-th of the key columns: causal
+//              mask, online softmax in fp32 with exp2 and a lazily raised running
+//              max (row max combined across the warpgroups through shared memory
+//              once per tile; O rescaled in TMEM, each warpgroup its own columns,
+//              only when the max grows by more than 2^8), P as bf16 into swizzled
+//              shared memory; at the end the row sums are combined and O / l ->
+//              bf16 -> global
 // S_{j+1} is computed while the softmax warps work on S_j.  Every wait is bounded.
 #include <cmath>
 
@@ -28,7 +32,10 @@ namespace {
 
 constexpr int TQ = 128;
 constexpr int TK = 128;
-constexpr int ATC_THREADS = 192;
+template <int D>
+constexpr int kNWG = D == 128 ? 4 : 2;          // softmax warpgroups
+template <int D>
+constexpr int kThreads = 64 + 128 * kNWG<D>;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct AttnTcArgs {
@@ -53,12 +60,29 @@ struct TcLayout {
     static constexpr int OFF_K = OFF_Q + Q_BYTES;
     static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
     static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
-    static constexpr int OFF_BAR = OFF_P + P_BYTES;
+    static constexpr int OFF_RED = OFF_P + P_BYTES;                       // [2][NWG][128] maxima, [NWG][128] sums
+    static constexpr int RED_BYTES = 3 * kNWG<D> * TQ * 4;
+    static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
     static constexpr int SMEM = 1024 + OFF_BAR + 256;
 };
 
+// Barrier over the softmax warps (named barrier 1) returning the AND of v.
+template <int NT>
+__device__ __forceinline__ bool softmax_bar_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(NT)
+        : "memory");
+    return r != 0;
+}
+
 template <int D>
-__global__ void __launch_bounds__(ATC_THREADS, 1)
+__global__ void __launch_bounds__(kThreads<D>, 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ AttnTcArgs a) {
     using Lay = TcLayout<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -101,7 +125,7 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
     const int n_kt = (kend + TK - 1) / TK;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 12; ++i) mbar_init(bars + i, (bars + i == p_full) ? 4 : 1);
+        for (int i = 0; i < 12; ++i) mbar_init(bars + i, (bars + i == p_full) ? 4 * kNWG<D> : 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -190,34 +214,46 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
             mbar_wait(drain, 0, &never);
         }
     } else {
+        constexpr int NWG = kNWG<D>;
+        constexpr int KC = TK / NWG;                  // key columns of S per warpgroup
+        constexpr int OC = D / NWG;                   // columns of O per warpgroup (32)
+        const int wg = (warp - 2) >> 2;
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;            // row of the q tile = TMEM lane
         const int qpos = q0 + r;                      // position inside the sequence
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t p_row = smem_u32(sP) + r * 128;
+        float *red_max = reinterpret_cast<float *>(smem + Lay::OFF_RED);   // [2][NWG][TQ]
+        float *red_l = red_max + 2 * NWG * TQ;                             // [NWG][TQ]
         float m_use = -INFINITY, l = 0.f;
-        bool ok = true;
+        bool good = true;   // every exit is decided at a barrier so all softmax warps leave together
         for (int j = 0; j < n_kt; ++j) {
-            bool w = mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag);
-            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t sbuf = tS + lane_off + (j & 1) * TK;
-            const int key0 = j * TK;
-            const bool diag = key0 + TK - 1 > q0;
-            // pass 1: row max of the scaled, masked scores
+            good = __all_sync(0xffffffffu, good && mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag));
+            const uint32_t sbuf = tS + lane_off + (j & 1) * TK + wg * KC;
+            const int key0 = j * TK + wg * KC;
+            const bool diag = j * TK + TK - 1 > q0;
+            // pass 1: this warpgroup's part of the row max of the scaled, masked scores
             float mt = -INFINITY;
-            #pragma unroll 1
-            for (int c = 0; c < TK / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(sbuf + c * 32, v);
-                tmem_ld_wait();
-                #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float x = __uint_as_float(v[i]) * a.scale_log2;
-                    if (diag && key0 + c * 32 + i > qpos) x = -INFINITY;
-                    mt = fmaxf(mt, x);
+            if (good) {
+                tc_fence_after();
+                #pragma unroll 1
+                for (int c = 0; c < KC / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(sbuf + c * 32, v);
+                    tmem_ld_wait();
+                    #pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        float x = __uint_as_float(v[i]) * a.scale_log2;
+                        if (diag && key0 + c * 32 + i > qpos) x = -INFINITY;
+                        mt = fmaxf(mt, x);
+                    }
                 }
             }
+            red_max[((j & 1) * NWG + wg) * TQ + r] = mt;
+            if (!softmax_bar_and<128 * NWG>(good)) { good = false; break; }
+            mt = red_max[((j & 1) * NWG) * TQ + r];
+            #pragma unroll
+            for (int w2 = 1; w2 < NWG; ++w2) mt = fmaxf(mt, red_max[((j & 1) * NWG + w2) * TQ + r]);
             float alpha = 1.f;
             bool rescale = false;
             if (j == 0) {
@@ -229,85 +265,82 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
             }
             // P buffer and O are free once the previous P V product has completed
             if (j > 0) {
-                w = mbar_wait(pv_done, (j - 1) & 1, abort_flag);
-                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-                tc_fence_after();
+                good = __all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1, abort_flag));
+                if (good) tc_fence_after();
             }
-            if (__any_sync(0xffffffffu, rescale)) {
-                #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+            if (good) {
+                if (__any_sync(0xffffffffu, rescale)) {
                     uint32_t v[32];
-                    tmem_ld32(tO + lane_off + c * 32, v);
+                    tmem_ld32(tO + lane_off + wg * OC, v);
                     tmem_ld_wait();
                     #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                    tmem_st32(tO + lane_off + c * 32, v);
+                    tmem_st32(tO + lane_off + wg * OC, v);
+                    tmem_st_wait();
                 }
-                tmem_st_wait();
-            }
-            l *= alpha;
-            // pass 2: P = exp2(x - m_use) as bf16 into the K-major swizzled P tile
-            #pragma unroll 1
-            for (int c = 0; c < TK / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(sbuf + c * 32, v);
-                tmem_ld_wait();
-                uint32_t pk[16];
-                #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    float x0 = __uint_as_float(v[i]) * a.scale_log2;
-                    float x1 = __uint_as_float(v[i + 1]) * a.scale_log2;
-                    if (diag && key0 + c * 32 + i > qpos) x0 = -INFINITY;
-                    if (diag && key0 + c * 32 + i + 1 > qpos) x1 = -INFINITY;
-                    const float p0 = exp2f(x0 - m_use), p1 = exp2f(x1 - m_use);
-                    l += p0 + p1;
-                    pk[i >> 1] = pack_bf16x2(p0, p1);
-                }
-                #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int chunk = c * 4 + q;                      // 16-byte chunk = 8 keys
-                    const uint32_t addr = p_row + (chunk >> 3) * Lay::ATOM + (((chunk & 7) ^ (r & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(pk[4 * q]),
-                                 "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
-                                 : "memory");
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
-        }
-        // epilogue: O / l -> bf16 -> global rows of this sequence
-        if (ok) {
-            bool w = mbar_wait(pv_done, (n_kt - 1) & 1, abort_flag);
-            if (__all_sync(0xffffffffu, w)) {
-                tc_fence_after();
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                const bool live = qpos < L;
-                bf16 *dst = a.o + (size_t)(seg0 + qpos) * a.ld_o + (size_t)head * D;
+                l *= alpha;
+                // pass 2: P = exp2(x - m_use) as bf16 into the K-major swizzled P tile
                 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < KC / 32; ++c) {
                     uint32_t v[32];
-                    tmem_ld32(tO + lane_off + c * 32, v);
+                    tmem_ld32(sbuf + c * 32, v);
                     tmem_ld_wait();
-                    if (live) {
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
-                        #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 u;
-                            u.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
-                            u.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
-                            u.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
-                            u.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
-                            d4[q] = u;
-                        }
+                    uint32_t pk[16];
+                    #pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        float x0 = __uint_as_float(v[i]) * a.scale_log2;
+                        float x1 = __uint_as_float(v[i + 1]) * a.scale_log2;
+                        if (diag && key0 + c * 32 + i > qpos) x0 = -INFINITY;
+                        if (diag && key0 + c * 32 + i + 1 > qpos) x1 = -INFINITY;
+                        const float p0 = exp2f(x0 - m_use), p1 = exp2f(x1 - m_use);
+                        l += p0 + p1;
+                        pk[i >> 1] = pack_bf16x2(p0, p1);
+                    }
+                    #pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int chunk = (wg * KC + c * 32) / 8 + q;      // 16-byte chunk = 8 keys
+                        const uint32_t addr = p_row + (chunk >> 3) * Lay::ATOM + (((chunk & 7) ^ (r & 7)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(pk[4 * q]),
+                                     "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
+                                     : "memory");
                     }
                 }
-            } else {
-                ok = false;
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full);
             }
         }
-        if (!ok && lane == 0) {
+        // epilogue: row sums combined over the warpgroups, O / l -> bf16 -> global rows of this sequence
+        if (good) good = __all_sync(0xffffffffu, mbar_wait(pv_done, (n_kt - 1) & 1, abort_flag));
+        red_l[wg * TQ + r] = l;
+        if (softmax_bar_and<128 * NWG>(good)) {
+            tc_fence_after();
+            float lt = 0.f;
+            #pragma unroll
+            for (int w2 = 0; w2 < NWG; ++w2) lt += red_l[w2 * TQ + r];
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            const bool live = qpos < L;
+            bf16 *dst = a.o + (size_t)(seg0 + qpos) * a.ld_o + (size_t)head * D + wg * OC;
+            uint32_t v[32];
+            tmem_ld32(tO + lane_off + wg * OC, v);
+            tmem_ld_wait();
+            if (live) {
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+                #pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 u;
+                    u.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
+                    u.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
+                    u.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
+                    u.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
+                    d4[q] = u;
+                }
+            }
+        } else {
+            good = false;
+        }
+        if (!good && lane == 0) {
             report(a.status, ST_TIMEOUT);
             *abort_flag = 1;
         }
@@ -329,7 +362,7 @@ cudaError_t launch_tc(const CUtensorMap &tm, const AttnTcArgs &args, int grid, c
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    attention_tc_kernel<D><<<grid, ATC_THREADS, TcLayout<D>::SMEM, st>>>(tm, args);
+    attention_tc_kernel<D><<<grid, kThreads<D>, TcLayout<D>::SMEM, st>>>(tm, args);
     return cudaGetLastError();
 }
 

@@ -18,8 +18,9 @@
 //              fp32 accumulators); in the leader CTA one thread issues
 //              tcgen05.mma.cta_group::2 (M=256, N=256, K=16) and commits to the
 //              barriers of both CTAs
-//   warps 2-5  epilogue of each CTA: tcgen05.ld of their 32 TMEM lanes (= rows),
-//              fused element-wise op, bf16 stores; overlaps the next tile's MMAs
+//   warps 2-9  epilogue of each CTA, two warps per 32-lane TMEM quarter, each of
+//              the two taking half of the tile's columns: tcgen05.ld, fused
+//              element-wise op, bf16 stores; overlaps the next tile's MMAs
 // Schedule: the tiles of the full waves run data-parallel (tile = pair + i*pairs,
 // M-fastest, so the pairs in flight share each weight tile through L2).  The
 // tiles of the last, partial wave would leave most SMs idle, so each of them is
@@ -48,7 +49,9 @@ constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB
 constexpr int B_BYTES = (BN / 2) * BK * 2;       // 16 KB: this CTA's half of the weight tile
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB per CTA
-constexpr int GEMM_THREADS = 192;
+constexpr int EPI_WARPS = 8;
+constexpr int EPI_THREADS = EPI_WARPS * 32;
+constexpr int GEMM_THREADS = 64 + EPI_THREADS;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
 
 struct GemmArgs {
@@ -98,16 +101,16 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
 __device__ __forceinline__ void st_release(uint32_t *p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-// Barrier over the four epilogue warps (named barrier 1) returning the AND of v.
+// Barrier over the epilogue warps (named barrier 1) returning the AND of v.
 __device__ __forceinline__ bool epi_bar_and(bool v) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "bar.red.and.pred q, 1, %2, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)v)
+        : "r"((uint32_t)v), "n"(EPI_THREADS)
         : "memory");
     return r != 0;
 }
@@ -166,7 +169,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);  // leader's MMA commit, multicast to both CTAs
-            mbar_init(&acc_empty[a], 8); // the 4 epilogue warps of each CTA (the leader's barrier is used)
+            mbar_init(&acc_empty[a], 2 * EPI_WARPS); // the epilogue warps of both CTAs (leader's barrier used)
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -262,9 +265,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             mbar_wait(drain, 0, &never);
         }
     } else {
-        // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 = this CTA's tile rows of the same range
+        // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 = this CTA's tile rows of the same range;
+        // warps 2-5 take the first half of the tile's columns, warps 6-9 the second
         const int quarter = warp & 3;
-        const int et = threadIdx.x - 64;  // 0..127 over the four epilogue warps
+        const int ehalf = (warp - 2) >> 2;
+        const int et = threadIdx.x - 64;  // 0..255 over the epilogue warps
         const uint32_t acc_empty_lead[2] = {mapa_shared(smem_u32(&acc_empty[0]), 0),
                                             mapa_shared(smem_u32(&acc_empty[1]), 0)};
         int acc = 0;
@@ -300,7 +305,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
             if constexpr (EPI == EPI_SWIGLU) {
                 #pragma unroll 1
-                for (int c = 0; c < BN / 64; ++c) {
+                for (int c = ehalf * (BN / 128); c < (ehalf + 1) * (BN / 128); ++c) {
                     uint32_t vg[32], vu[32];
                     tmem_ld32(taddr + c * 32, vg);
                     tmem_ld32(taddr + BN / 2 + c * 32, vu);
@@ -320,8 +325,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 // the tile holds BN/d whole heads: q and k heads get RMSNorm over d and M-RoPE
                 // (pairs j, j + d/2 both in this thread's row), v heads are stored as they are
                 const int d = g.head_dim, half = d >> 1;
+                const int hpt = BN / d;
                 #pragma unroll 1
-                for (int hh = 0; hh < BN / d; ++hh) {
+                for (int hh = ehalf * (hpt >> 1); hh < (ehalf + 1) * (hpt >> 1); ++hh) {
                     const int head = (n_blk * BN) / d + hh;
                     const int cb = hh * d;
                     __nv_bfloat16 *dst = g.C + (size_t)row * g.ldc + n_blk * BN + cb;
@@ -403,18 +409,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     }
                 }
                 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = ehalf * (BN / 64); c < (ehalf + 1) * (BN / 64); ++c) {
+                    const int col = n_blk * BN + c * 32;
+                    float r[32];
+                    if constexpr (EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_DS) {
+                        if (live) load_row32(g.R + (size_t)row * g.ldc + col, r);   // in flight during the TMEM read
+                    }
                     uint32_t v[32];
                     tmem_ld32(taddr + c * 32, v);
                     tmem_ld_wait();
                     if (live) {
-                        const int col = n_blk * BN + c * 32;
                         float f[32];
                         #pragma unroll
                         for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
                         if constexpr (EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_DS) {
-                            float r[32];
-                            load_row32(g.R + (size_t)row * g.ldc + col, r);
                             #pragma unroll
                             for (int j = 0; j < 32; ++j) f[j] += r[j];
                         }
@@ -440,7 +448,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
                 float *dst = g.part + (size_t)blockIdx.x * (BM * BN) + (size_t)(quarter * 32 + lane) * BN;
                 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = ehalf * (BN / 64); c < (ehalf + 1) * (BN / 64); ++c) {
                     uint32_t v[32];
                     tmem_ld32(taddr + c * 32, v);
                     tmem_ld_wait();
@@ -479,7 +487,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         const int sub = et & 3;
                         const unsigned gmask = 0xFu << (lane & ~3);
                         const int units = (r1 - r0) * hpt;
-                        for (int u = et >> 2; u < units; u += 32) {
+                        for (int u = et >> 2; u < units; u += EPI_THREADS / 4) {
                             const int r = r0 + u / hpt, hh = u % hpt;
                             const int row = m_blk * (2 * BM) + (int)rank * BM + r;
                             if (row >= g.M) continue;   // same row for the four threads
@@ -536,7 +544,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     } else {
                     constexpr int UNITS_PER_ROW = (EPI == EPI_SWIGLU) ? BN / 8 : BN / 4;  // float4 groups
                     const int units = (r1 - r0) * UNITS_PER_ROW;
-                    for (int u = et; u < units; u += 128) {
+                    for (int u = et; u < units; u += EPI_THREADS) {
                         const int r = r0 + u / UNITS_PER_ROW;
                         const int c4 = (u % UNITS_PER_ROW) * 4;
                         const int row = m_blk * (2 * BM) + (int)rank * BM + r;
