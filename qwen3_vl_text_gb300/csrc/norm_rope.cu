@@ -16,8 +16,8 @@ namespace h3 {
 
 namespace {
 
-constexpr int NORM_ROWS = 8;    // one warp per row, 8 rows per CTA
-constexpr int NORM_VPL = 32;    // 16-byte vectors per lane -> cols <= 8192
+constexpr int NORM_THREADS = 128;
+constexpr int NORM_VPT = 8;  // 8 x 16-byte vectors per thread -> cols <= 8192
 
 __device__ __forceinline__ float warp_sum(float v) {
     #pragma unroll
@@ -25,28 +25,21 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// One warp per row: all of the row's 16-byte loads in flight at once, the sum
-// of squares reduced by shuffles, y = bf16(x * (1/sqrt(mean(x^2) + eps)) * w).
-__global__ void __launch_bounds__(NORM_ROWS * 32) rmsnorm_kernel(const bf16 *__restrict__ x,
-                                                                 const bf16 *__restrict__ w, bf16 *y, int rows,
-                                                                 int cols, float eps) {
-    const int lane = threadIdx.x & 31;
-    const int row = blockIdx.x * NORM_ROWS + (threadIdx.x >> 5);
-    if (row >= rows) return;
+// One CTA per row.  y = bf16(x * (1/sqrt(mean(x^2) + eps)) * w).
+__global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(const bf16 *__restrict__ x,
+                                                               const bf16 *__restrict__ w, bf16 *y, int cols,
+                                                               float eps) {
+    const int row = blockIdx.x;
     const int nvec = cols >> 3;
     const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)row * cols);
     const uint4 *wr = reinterpret_cast<const uint4 *>(w);
-    uint4 v[NORM_VPL];
+    uint4 v[NORM_VPT];
     float ss = 0.f;
     #pragma unroll
-    for (int i = 0; i < NORM_VPL; ++i) {
-        const int idx = lane + i * 32;
-        if (idx < nvec) v[i] = xr[idx];
-    }
-    #pragma unroll
-    for (int i = 0; i < NORM_VPL; ++i) {
-        const int idx = lane + i * 32;
+    for (int i = 0; i < NORM_VPT; ++i) {
+        const int idx = threadIdx.x + i * NORM_THREADS;
         if (idx < nvec) {
+            v[i] = xr[idx];
             const uint32_t u[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
             #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -56,12 +49,18 @@ __global__ void __launch_bounds__(NORM_ROWS * 32) rmsnorm_kernel(const bf16 *__r
             }
         }
     }
+    __shared__ float red[NORM_THREADS / 32];
     ss = warp_sum(ss);
-    const float rstd = 1.0f / sqrtf(ss / (float)cols + eps);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    #pragma unroll
+    for (int i = 0; i < NORM_THREADS / 32; ++i) tot += red[i];
+    const float rstd = 1.0f / sqrtf(tot / (float)cols + eps);
     uint4 *yr = reinterpret_cast<uint4 *>(y + (size_t)row * cols);
     #pragma unroll
-    for (int i = 0; i < NORM_VPL; ++i) {
-        const int idx = lane + i * 32;
+    for (int i = 0; i < NORM_VPT; ++i) {
+        const int idx = threadIdx.x + i * NORM_THREADS;
         if (idx < nvec) {
             const uint4 g = wr[idx];
             const uint32_t u[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
@@ -110,7 +109,7 @@ void make_rope_params(RopeParams *p, int head_dim, float theta, const int32_t se
 
 cudaError_t launch_rmsnorm(const bf16 *x, const bf16 *w, bf16 *y, int rows, int cols, float eps, cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
-    rmsnorm_kernel<<<(rows + NORM_ROWS - 1) / NORM_ROWS, NORM_ROWS * 32, 0, st>>>(x, w, y, rows, cols, eps);
+    rmsnorm_kernel<<<rows, NORM_THREADS, 0, st>>>(x, w, y, cols, eps);
     return cudaGetLastError();
 }
 
