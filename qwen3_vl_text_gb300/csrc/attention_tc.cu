@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(kThreads<D>, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
 
     // work item: heads fastest (the heads of one kv group are adjacent), heavy q tiles first
     const int head = blockIdx.x % a.nq;
@@ -137,6 +138,7 @@ __global__ void __launch_bounds__(kThreads<D>, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_wait();       // q/k/v are the previous kernel's output; o is read by the previous layer's o_proj
     const uint32_t tmem_base = *tmem_slot;
     const uint32_t tS = tmem_base;          // S buffers at columns 0 and 128
     const uint32_t tO = tmem_base + 256;    // O at columns 256 .. 256+D
@@ -362,8 +364,9 @@ cudaError_t launch_tc(const CUtensorMap &tm, const AttnTcArgs &args, int grid, c
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    attention_tc_kernel<D><<<grid, kThreads<D>, TcLayout<D>::SMEM, st>>>(tm, args);
-    return cudaGetLastError();
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(kThreads<D>), TcLayout<D>::SMEM, st, at);
+    return cudaLaunchKernelEx(&cfg, attention_tc_kernel<D>, tm, args);
 }
 
 }  // namespace

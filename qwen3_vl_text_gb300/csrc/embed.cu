@@ -15,6 +15,8 @@ namespace {
 __global__ void __launch_bounds__(256) embed_kernel(const int32_t *__restrict__ ids,
                                                     const bf16 *__restrict__ table, int vocab, int hidden,
                                                     bf16 *out, int S, int32_t *status) {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (row >= S) return;
@@ -33,6 +35,8 @@ __global__ void __launch_bounds__(SCAN_THREADS) vis_rank_kernel(const uint8_t *_
                                                                 int n_vis, int32_t *rank, int32_t *status) {
     __shared__ int warp_tot[SCAN_THREADS / 32];
     __shared__ int carry;
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) carry = 0;
@@ -72,15 +76,17 @@ __global__ void __launch_bounds__(SCAN_THREADS) vis_rank_kernel(const uint8_t *_
 cudaError_t launch_embed(const int32_t *ids, const bf16 *table, int vocab, int hidden, bf16 *out, int S,
                          int32_t *status, cudaStream_t st) {
     if (S <= 0) return cudaSuccess;
-    embed_kernel<<<(S + 7) / 8, 256, 0, st>>>(ids, table, vocab, hidden, out, S, status);
-    return cudaGetLastError();
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3((S + 7) / 8), dim3(256), 0, st, at);
+    return cudaLaunchKernelEx(&cfg, embed_kernel, ids, table, vocab, hidden, out, S, status);
 }
 
 cudaError_t launch_vis_rank(const uint8_t *mask, int S, int n_vis, int32_t *rank, int32_t *status,
                             cudaStream_t st) {
     if (S <= 0) return cudaSuccess;
-    vis_rank_kernel<<<1, SCAN_THREADS, 0, st>>>(mask, S, n_vis, rank, status);
-    return cudaGetLastError();
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3(1), dim3(SCAN_THREADS), 0, st, at);
+    return cudaLaunchKernelEx(&cfg, vis_rank_kernel, mask, S, n_vis, rank, status);
 }
 
 // which = 0: gate rows -> packed rows [256b, 256b+128); which = 1: up rows -> [256b+128, 256b+256).

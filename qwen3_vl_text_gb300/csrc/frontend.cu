@@ -29,6 +29,8 @@ h3enc_status ferr(h3enc_status s, const char *msg) {
 __global__ void __launch_bounds__(256) merge_visual_rows_kernel(const int32_t *__restrict__ vis_rank,
                                                                 const h3::bf16 *__restrict__ src, int n_vis,
                                                                 int hidden, h3::bf16 *out, int S) {
+    h3::pdl_trigger();
+    h3::pdl_wait();
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (row >= S) return;
@@ -45,8 +47,9 @@ namespace h3 {
 cudaError_t launch_merge_visual_rows(const int32_t *vis_rank, const bf16 *src, int n_vis, int hidden, bf16 *out,
                                      int S, cudaStream_t st) {
     if (S <= 0 || n_vis <= 0) return cudaSuccess;
-    merge_visual_rows_kernel<<<(S + 7) / 8, 256, 0, st>>>(vis_rank, src, n_vis, hidden, out, S);
-    return cudaGetLastError();
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3((S + 7) / 8), dim3(256), 0, st, at);
+    return cudaLaunchKernelEx(&cfg, merge_visual_rows_kernel, vis_rank, src, n_vis, hidden, out, S);
 }
 }  // namespace h3
 

@@ -161,6 +161,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t rank = cluster_ctarank();       // 0: leader CTA of the pair
     const int pair = blockIdx.x >> 1;
     const int npairs = gridDim.x >> 1;
+    pdl_trigger();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -187,6 +188,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     cluster_sync();   // barriers of both CTAs initialised before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();       // inputs of this GEMM are the previous kernel's outputs
 
     const SplitItem sk = split_item(g, pair);
     const bool has_split = sk.kb1 > sk.kb0;
@@ -639,7 +641,7 @@ uint32_t next_epoch() {
 template <int EPI>
 cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     static int max_pairs = 0;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
@@ -689,8 +691,10 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     cfg.blockDim = dim3(GEMM_THREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<EPI>, *p.tmA, *p.tmW, g);
 }
 

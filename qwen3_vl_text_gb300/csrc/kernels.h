@@ -74,4 +74,21 @@ cudaError_t launch_merge_visual_rows(const int32_t *vis_rank, const bf16 *src, i
 
 int device_num_sms();
 
+// Launch configuration with programmatic stream serialization (see pdl_wait in
+// common.cuh); attrs must hold room for the attribute and any extra ones the
+// caller appends after it.
+inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                     cudaLaunchAttribute *attrs) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
 }  // namespace h3

@@ -29,6 +29,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(const bf16 *__restrict__ x,
                                                                const bf16 *__restrict__ w, bf16 *y, int cols,
                                                                float eps) {
+    pdl_trigger();
+    pdl_wait();
     const int row = blockIdx.x;
     const int nvec = cols >> 3;
     const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)row * cols);
@@ -77,6 +79,8 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(const bf16 *__res
 // One thread per (token, frequency index j).
 __global__ void rope_table_kernel(const int32_t *__restrict__ pos, int S, const RopeParams rp, float *cos_t,
                                   float *sin_t) {
+    pdl_trigger();
+    pdl_wait();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= S * rp.half_dim) return;
     const int s = i / rp.half_dim;
@@ -109,16 +113,18 @@ void make_rope_params(RopeParams *p, int head_dim, float theta, const int32_t se
 
 cudaError_t launch_rmsnorm(const bf16 *x, const bf16 *w, bf16 *y, int rows, int cols, float eps, cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
-    rmsnorm_kernel<<<rows, NORM_THREADS, 0, st>>>(x, w, y, cols, eps);
-    return cudaGetLastError();
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3(rows), dim3(NORM_THREADS), 0, st, at);
+    return cudaLaunchKernelEx(&cfg, rmsnorm_kernel, x, w, y, cols, eps);
 }
 
 cudaError_t launch_rope_table(const int32_t *positions, int S, const RopeParams &rp, float *cos_t, float *sin_t,
                               cudaStream_t st) {
     if (S <= 0) return cudaSuccess;
     const int n = S * rp.half_dim;
-    rope_table_kernel<<<(n + 255) / 256, 256, 0, st>>>(positions, S, rp, cos_t, sin_t);
-    return cudaGetLastError();
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3((n + 255) / 256), dim3(256), 0, st, at);
+    return cudaLaunchKernelEx(&cfg, rope_table_kernel, positions, S, rp, cos_t, sin_t);
 }
 
 }  // namespace h3
