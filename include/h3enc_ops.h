@@ -36,15 +36,38 @@ enum {
  *   R [M, ldc] residual (RESIDUAL*), DS [n_vis, ldc] and vis_rank [M] (RESIDUAL_DS).
  *   workspace: NULL, or device memory of at least h3enc_op_gemm_workspace_bytes()
  *   bytes, 256-byte aligned, zero-filled once before its first use and then
- *   reused; with it the tiles of a partial last wave are split along K over the
- *   idle SMs (the result is deterministic for given M, N, K).  Calls sharing a
- *   workspace must not overlap on the GPU.
+ *   reused; with it the k-blocks of the tiles of a partial last wave are spread
+ *   evenly over all SMs (stream-K; the result is deterministic for given M, N,
+ *   K and SM count).  Calls sharing a workspace must not overlap on the GPU.
  * Requires K % 8 == 0, N % 256 == 0 (of the packed weight for SWIGLU), A and W
  * 16-byte aligned.  M may be any size >= 0. */
 H3ENC_API h3enc_status h3enc_op_gemm(const void *A, const void *W, void *C, int32_t M, int32_t N, int32_t K,
                            int32_t epilogue, const void *R, const void *DS, const int32_t *vis_rank,
                            int32_t n_vis, void *workspace, int64_t workspace_bytes, int32_t *status,
                            void *stream);
+
+/* Profiling aid: the next projection GEMM this host thread launches (through
+ * h3enc_op_gemm, h3enc_op_gemm_qkv_rope, h3enc_op_gemm_noalloc or inside an
+ * encode) records a timeline: CTA c writes 11 %globaltimer stamps (ns) to
+ * trace[c * 11 + k]: k = 0 start, 1 prologue done, 2 first load issued, 3 first
+ * MMA, 4 last data-parallel MMA issued, 5 data-parallel epilogues done, 6 first
+ * stream-K accumulator ready, 7 stream-K partials written, 8 first tile's
+ * contributor flags seen, 9 stream-K reduction done, 10 end.  The stream-K phase
+ * runs before the data-parallel tiles; stamps of phases a CTA does not run, and
+ * rows of CTAs beyond the grid, keep their contents.  trace: device uint64 of at
+ * least 11 * SM-count entries, alive until that GEMM has run. */
+H3ENC_API h3enc_status h3enc_op_gemm_trace_next(void *trace, int64_t trace_entries);
+
+/* Profiling aid: the next attention launch on this host thread (through
+ * h3enc_op_attention or inside an encode) records a timeline per persistent CTA
+ * (one per SM, at most one per work item; work items = heads * sum over
+ * sequences of ceil(len / 256)).  CTA c writes 9 entries at trace[c * 9]:
+ * 0 start and 6 end as %globaltimer ns; 1 set-up done, 2 first Q tiles landed,
+ * 3 first score tile ready, 4 last P written, 5 last P V product done as SM
+ * clock64 cycles; then 7 the SM id and 8 the number of key tiles processed.
+ * trace: device uint64 of at least 9 * ctas entries (ctas >= the SM count
+ * covers every launch), alive until that launch has run. */
+H3ENC_API h3enc_status h3enc_op_attention_trace_next(void *trace, int64_t trace_entries, int32_t ctas);
 
 /* Workspace bytes h3enc_op_gemm needs on the current device (-1 without a device). */
 H3ENC_API int64_t h3enc_op_gemm_workspace_bytes(void);
@@ -57,8 +80,8 @@ H3ENC_API int64_t h3enc_op_gemm_workspace_bytes(void);
  * after start-up.  This entry point computes exactly what h3enc_op_gemm
  * computes with a workspace (same kernel, same split of the last wave), but its
  * scratch is a fixed array inside the library's device image:
- * h3enc_op_gemm_noalloc_scratch_bytes() bytes (20 MiB + 896 B, one 128 KiB
- * fp32 slot and one flag per SM for up to 160 SMs), held by every GPU that
+ * h3enc_op_gemm_noalloc_scratch_bytes() bytes (40 MiB + 896 B, two 128 KiB
+ * fp32 slots and one flag per SM for up to 160 SMs), held by every GPU that
  * loads the library until the process exits.  The caller passes inputs and
  * outputs only; nothing is allocated or freed.
  *   - The first call on a device looks up the array's device address and clears

@@ -18,7 +18,7 @@ __all__ = [
     "h3enc_encode_host", "h3enc_set_layer_capture", "h3enc_get_status", "h3enc_last_error", "h3enc_destroy",
     "h3enc_set_profiling", "h3enc_set_profiling_classes", "h3enc_get_profile", "h3enc_launch_count", "h3enc_num_sms",
     "h3enc_build_positions", "h3enc_aggregate_deepstack",
-    "h3enc_op_gemm", "h3enc_op_gemm_workspace_bytes", "h3enc_op_gemm_noalloc", "h3enc_op_gemm_noalloc_scratch_bytes", "h3enc_op_pack_gate_up", "h3enc_op_rmsnorm", "h3enc_op_rope_table",
+    "h3enc_op_gemm", "h3enc_op_gemm_workspace_bytes", "h3enc_op_gemm_trace_next", "h3enc_op_attention_trace_next", "h3enc_op_gemm_noalloc", "h3enc_op_gemm_noalloc_scratch_bytes", "h3enc_op_pack_gate_up", "h3enc_op_rmsnorm", "h3enc_op_rope_table",
     "h3enc_op_gemm_qkv_rope", "h3enc_op_attention", "h3enc_op_embed", "h3enc_op_vis_rank", "Encoder",
     "KERNEL_CLASSES",
 ]
@@ -75,6 +75,8 @@ _SIGS = {
     "h3enc_num_sms": ([_P], _I32),
     "h3enc_op_gemm": ([_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _I64, _P, _P], _I32),
     "h3enc_op_gemm_workspace_bytes": ([], _I64),
+    "h3enc_op_gemm_trace_next": ([_P, _I64], _I32),
+    "h3enc_op_attention_trace_next": ([_P, _I64, _I32], _I32),
     "h3enc_build_positions": ([_P, _I32, _I32, _I32, _P, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _P], _I32),
     "h3enc_aggregate_deepstack": ([_P, _I32, _P, _I32, _P, _I32, _I32, _I32, _P, _P], _I32),
     "h3enc_frontend_last_error": ([], ctypes.c_char_p),
@@ -269,6 +271,18 @@ def h3enc_op_gemm(A, W, C, M, N, K, epilogue, R=None, DS=None, vis_rank=None, n_
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     return _check(lib.h3enc_op_gemm(_ptr(A), _ptr(W), _ptr(C), M, N, K, epilogue, _ptr(R), _ptr(DS),
                                     _ptr(vis_rank), n_vis, _ptr(workspace), wbytes, _ptr(status), _stream(stream)))
+
+
+def h3enc_op_gemm_trace_next(trace):
+    """Arm the phase timeline of the next GEMM this thread launches: `trace` is a device int64
+    tensor of >= 11 * SMs entries; CTA c writes its 11 stamps (ns) to trace[11c : 11c + 11]."""
+    _check(lib.h3enc_op_gemm_trace_next(_ptr(trace), trace.numel()))
+
+
+def h3enc_op_attention_trace_next(trace, ctas):
+    """Arm the per-CTA timeline of the next attention launch on this thread: `trace` is a device
+    int64 tensor of >= 9 * ctas entries (ctas = heads * query tiles of 128 rows)."""
+    _check(lib.h3enc_op_attention_trace_next(_ptr(trace), trace.numel(), ctas))
 
 
 def h3enc_op_gemm_workspace_bytes() -> int:

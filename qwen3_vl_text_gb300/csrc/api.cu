@@ -369,7 +369,7 @@ h3enc_status h3enc_create(const h3enc_config *cfg, h3enc **out) {
     h->st_ds = reinterpret_cast<bf16 *>(p); p += b_ds;
     h->st_out = reinterpret_cast<bf16 *>(p); p += b_out;
     h->gemm_part = reinterpret_cast<float *>(p);
-    h->gemm_flags = reinterpret_cast<uint32_t *>(p + (size_t)h->num_sms * 128 * 256 * sizeof(float) + 256);
+    h->gemm_flags = reinterpret_cast<uint32_t *>(p + h3::gemm_flags_offset(h->num_sms));
     p += b_gemm;
     e = cudaMemset(h->ws, 0, wsz);
     if (e != cudaSuccess) {
@@ -704,10 +704,25 @@ h3enc_status h3enc_op_gemm(const void *A, const void *W, void *C, int32_t M, int
                                                         "or not 256-byte aligned");
         p.part = static_cast<float *>(workspace);
         p.flags = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) +
-                                               (size_t)p.num_sms * 128 * 256 * sizeof(float) + 256);
+                                               h3::gemm_flags_offset(p.num_sms));
     }
     cudaError_t e = h3::launch_gemm(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "gemm launch");
+}
+
+h3enc_status h3enc_op_gemm_trace_next(void *trace, int64_t trace_entries) {
+    const int sms = h3::device_num_sms();
+    if (!trace || sms <= 0 || trace_entries < (int64_t)sms * 11)
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm_trace_next: trace needs 11 entries per SM");
+    h3::gemm_trace_next(static_cast<unsigned long long *>(trace));
+    return H3ENC_OK;
+}
+
+h3enc_status h3enc_op_attention_trace_next(void *trace, int64_t trace_entries, int32_t ctas) {
+    if (!trace || ctas <= 0 || trace_entries < (int64_t)ctas * h3::attention_trace_fields())
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "attention_trace_next: trace needs 9 entries per CTA");
+    h3::attention_trace_next(static_cast<unsigned long long *>(trace));
+    return H3ENC_OK;
 }
 
 h3enc_status h3enc_op_pack_gate_up(const void *gate, const void *up, void *W, int32_t I, int32_t K, void *stream) {
@@ -770,7 +785,7 @@ h3enc_status h3enc_op_gemm_qkv_rope(const void *A, const void *W, void *C, int32
             return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm_qkv_rope: workspace too small or misaligned");
         p.part = static_cast<float *>(workspace);
         p.flags = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) +
-                                               (size_t)p.num_sms * 128 * 256 * sizeof(float) + 256);
+                                               h3::gemm_flags_offset(p.num_sms));
     }
     cudaError_t e = h3::launch_gemm(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "gemm_qkv_rope launch");

@@ -6,21 +6,26 @@
 // 1/sqrt(d), output columns head-major.  Packed sequences (cu_seqlens) attend
 // only within themselves.
 //
-// One CTA = 128 query rows of one head; keys/values stream in tiles of 128.
-//   warp 0     TMA: Q once, K and V tiles into a 2-stage ring (128-byte swizzle)
-//   warp 1     TMEM allocation; tcgen05.mma from one thread:
-//                S_j = Q K_j^T   (M=128, N=128, K=d)   into one of two TMEM S buffers
-//                O  += P_j V_j   (M=128, N=d,   K=128) into the TMEM O buffer; V is read
-//                                  as an MN-major operand straight from its TMA tile
-//   warps 2+   NWG softmax warpgroups (4 for d = 128, 2 for d = 64); thread = one
-//              query row (its TMEM lane) x one NWG-th of the key columns: causal
-//              mask, online softmax in fp32 with exp2 and a lazily raised running
-//              max (row max combined across the warpgroups through shared memory
-//              once per tile; O rescaled in TMEM, each warpgroup its own columns,
-//              only when the max grows by more than 2^8), P as bf16 into swizzled
-//              shared memory; at the end the row sums are combined and O / l ->
-//              bf16 -> global
-// S_{j+1} is computed while the softmax warps work on S_j.  Every wait is bounded.
+// Work item = two query tiles of 128 rows (A = rows q0.., B = rows q0+128..) of one
+// head; both read the same key/value tiles of 128, so each K/V tile is staged once
+// for 256 query rows.  Persistent: one CTA per SM takes items heaviest first in
+// alternating-direction rounds; TMEM, barriers and the K/V ring carry over from
+// item to item, and an item's epilogue overlaps the next item's first products.
+//   warp 0     TMA: Q_A and Q_B once, K and V tiles into a 2-stage ring (128-byte swizzle)
+//   warp 1     TMEM allocation; tcgen05.mma from one thread, the two tiles interleaved
+//              so that the tensor core works on one tile while the other's softmax runs:
+//                S_t = Q_t K_j^T  (M=128, N=128, K=d)  into tile t's S columns
+//                O_t += P_t V_j   (M=128, N=d, K=128)  P_t read from TMEM (A operand),
+//                                  V as an MN-major operand straight from its TMA tile
+//              issue order per key tile j: P_A V_j, S_A(j+1), P_B V_j, S_B(j+1)
+//   warps 2-5  softmax of tile A, warps 6-9 of tile B: thread = one query row (its
+//              TMEM lane) holding the whole 128-key row of S in registers: causal
+//              mask, running max raised lazily (O rescaled in TMEM only when the max
+//              grows by more than 2^8), P = exp2(s - m) as packed bf16 written over
+//              the first 64 columns of its own S row; at the end O / l -> bf16 -> global
+// TMEM columns: S_A 0-127, S_B 128-255, O_A 256-(256+d), O_B 384-(384+d).
+// No softmax thread waits for another: the row max needs no exchange, and the
+// previous P V product is awaited only before a rescale.  Every wait is bounded.
 #include <cmath>
 
 #include "common.cuh"
@@ -32,10 +37,7 @@ namespace {
 
 constexpr int TQ = 128;
 constexpr int TK = 128;
-template <int D>
-constexpr int kNWG = D == 128 ? 4 : 2;          // softmax warpgroups
-template <int D>
-constexpr int kThreads = 64 + 128 * kNWG<D>;
+constexpr int kThreads = 64 + 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct AttnTcArgs {
@@ -44,45 +46,76 @@ struct AttnTcArgs {
     int nq, group;
     int k_col0, v_col0;
     float scale_log2;
-    int n_seqs, total_tiles;
+    int n_seqs, total_pairs, n_items;
     int32_t *status;
     int cu[kMaxSeqs + 1];
-    int tile_start[kMaxSeqs + 1];
+    int pair_start[kMaxSeqs + 1];   // first tile-pair index of each sequence
+    unsigned long long *trace;      // optional [grid][ATR_COUNT] timeline
 };
+
+// Timeline of one persistent CTA (h3enc_op_attention_trace_next): %globaltimer at
+// the start and the end, clock64 cycles for the phases in between (first item's Q,
+// first score tile, last item's last P and last P V product), the SM id and the
+// number of key tiles the CTA processed.
+enum { ATR_START = 0, ATR_READY, ATR_Q, ATR_S0, ATR_LAST_P, ATR_O, ATR_END, ATR_SMID, ATR_NKT, ATR_COUNT };
+__device__ __forceinline__ void astamp_ns(const AttnTcArgs &a, int what) {
+    if (a.trace) {
+        unsigned long long t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        a.trace[(size_t)blockIdx.x * ATR_COUNT + what] = t;
+    }
+}
+__device__ __forceinline__ void astamp_clk(const AttnTcArgs &a, int what) {
+    if (a.trace) a.trace[(size_t)blockIdx.x * ATR_COUNT + what] = (unsigned long long)clock64();
+}
 
 template <int D>
 struct TcLayout {
     static constexpr int ATOM = TQ * 128;          // one 64-column atom column of a 128-row tile: 16 KB
     static constexpr int Q_BYTES = TQ * D * 2;
     static constexpr int KV_BYTES = TK * D * 2;
-    static constexpr int P_BYTES = TQ * TK * 2;
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + Q_BYTES;
+    static constexpr int OFF_Q = 0;                             // Q_A, Q_B
+    static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
     static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
-    static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
-    static constexpr int OFF_RED = OFF_P + P_BYTES;                       // [2][NWG][128] maxima, [NWG][128] sums
-    static constexpr int RED_BYTES = 3 * kNWG<D> * TQ * 4;
-    static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
-    static constexpr int SMEM = 1024 + OFF_BAR + 256;
+    static constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
+    static constexpr int SMEM = 1024 + OFF_BAR + 256;   // 15 barriers, TMEM slot, abort flag
 };
 
-// Barrier over the softmax warps (named barrier 1) returning the AND of v.
-template <int NT>
-__device__ __forceinline__ bool softmax_bar_and(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, %2, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v), "n"(NT)
-        : "memory");
-    return r != 0;
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// One work item = (pair of query tiles, head); item k in heavy-first order.
+struct AttnItem {
+    int head, seg0, L, q0, nkt_a, nkt_b;
+};
+__device__ __forceinline__ AttnItem attn_item(const AttnTcArgs &a, int k) {
+    AttnItem it;
+    it.head = k % a.nq;                                   // heads fastest: one kv group's heads adjacent
+    const int pair_lin = a.total_pairs - 1 - k / a.nq;    // heavy tile pairs first
+    int lo = 0, hi = a.n_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.pair_start[mid] <= pair_lin) lo = mid; else hi = mid - 1;
+    }
+    it.seg0 = a.cu[lo];
+    it.L = a.cu[lo + 1] - it.seg0;
+    it.q0 = (pair_lin - a.pair_start[lo]) * (2 * TQ);
+    // key tiles of each query tile (tile B is empty when the sequence ends inside tile A)
+    it.nkt_a = (min(it.q0 + TQ, it.L) + TK - 1) / TK;
+    it.nkt_b = it.q0 + TQ < it.L ? (min(it.q0 + 2 * TQ, it.L) + TK - 1) / TK : 0;
+    return it;
+}
+// The r-th item of CTA b among G persistent CTAs: rounds of G items, alternate rounds
+// in reverse so the heavy items of one round pair with the light ones of the next.
+__device__ __forceinline__ int attn_item_index(int r, int b, int G) {
+    return r * G + ((r & 1) ? G - 1 - b : b);
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads<D>, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ AttnTcArgs a) {
     using Lay = TcLayout<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -90,43 +123,33 @@ __global__ void __launch_bounds__(kThreads<D>, 1)
     uint8_t *sQ = smem + Lay::OFF_Q;
     uint8_t *sK = smem + Lay::OFF_K;
     uint8_t *sV = smem + Lay::OFF_V;
-    uint8_t *sP = smem + Lay::OFF_P;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::OFF_BAR);
     uint64_t *q_full = bars + 0;
-    uint64_t *k_full = bars + 1;     // [2]
+    uint64_t *k_full = bars + 1;     // [2] ring stage
     uint64_t *v_full = bars + 3;     // [2]
     uint64_t *kv_empty = bars + 5;   // [2]
-    uint64_t *s_full = bars + 7;     // [2]
-    uint64_t *p_full = bars + 9;
-    uint64_t *pv_done = bars + 10;
-    uint64_t *drain = bars + 11;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 12);
+    uint64_t *s_full = bars + 7;     // [2] query tile
+    uint64_t *p_full = bars + 9;     // [2] query tile (4 softmax warps arrive)
+    uint64_t *pv_done = bars + 11;   // [2] query tile
+    uint64_t *drain = bars + 13;
+    uint64_t *q_empty = bars + 14;   // the item's score MMAs no longer read Q
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x, b = blockIdx.x;
     pdl_trigger();
-
-    // work item: heads fastest (the heads of one kv group are adjacent), heavy q tiles first
-    const int head = blockIdx.x % a.nq;
-    const int tile_lin = a.total_tiles - 1 - (int)(blockIdx.x / a.nq);
-    int seg = 0;
-    {
-        int lo = 0, hi = a.n_seqs - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (a.tile_start[mid] <= tile_lin) lo = mid; else hi = mid - 1;
+    if (threadIdx.x == 0) {
+        astamp_ns(a, ATR_START);
+        if (a.trace) {
+            uint32_t smid;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+            a.trace[(size_t)b * ATR_COUNT + ATR_SMID] = smid;
         }
-        seg = lo;
     }
-    const int seg0 = a.cu[seg];
-    const int L = a.cu[seg + 1] - seg0;
-    const int q0 = (tile_lin - a.tile_start[seg]) * TQ;
-    const int kvh = head / a.group;
-    const int kend = min(q0 + TQ, L);
-    const int n_kt = (kend + TK - 1) / TK;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 12; ++i) mbar_init(bars + i, (bars + i == p_full) ? 4 * kNWG<D> : 1);
+        for (int i = 0; i < 15; ++i) mbar_init(bars + i, (i == 9 || i == 10) ? 4 : 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -140,33 +163,49 @@ __global__ void __launch_bounds__(kThreads<D>, 1)
     tc_fence_after();
     pdl_wait();       // q/k/v are the previous kernel's output; o is read by the previous layer's o_proj
     const uint32_t tmem_base = *tmem_slot;
-    const uint32_t tS = tmem_base;          // S buffers at columns 0 and 128
-    const uint32_t tO = tmem_base + 256;    // O at columns 256 .. 256+D
+    if (threadIdx.x == 0) astamp_clk(a, ATR_READY);
 
     if (warp == 0) {
         if (lane == 0) {
             bool ok = true;
+            uint32_t g = 0;          // key/value tiles loaded so far (ring position)
             uint32_t issued[2] = {0, 0};
-            mbar_arrive_expect_tx(q_full, Lay::Q_BYTES);
-            for (int c = 0; c < D / 64; ++c)
-                tma_load_2d(sQ + c * Lay::ATOM, &tm, q_full, head * D + c * 64, seg0 + q0);
-            for (int j = 0; j < n_kt && ok; ++j) {
-                const int s = j & 1;
-                if (j >= 2 && !mbar_wait(&kv_empty[s], ((j >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
-                const int y = seg0 + j * TK;
-                mbar_arrive_expect_tx(&k_full[s], Lay::KV_BYTES);
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_2d(sK + s * Lay::KV_BYTES + c * Lay::ATOM, &tm, &k_full[s], a.k_col0 + kvh * D + c * 64, y);
-                mbar_arrive_expect_tx(&v_full[s], Lay::KV_BYTES);
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_2d(sV + s * Lay::KV_BYTES + c * Lay::ATOM, &tm, &v_full[s], a.v_col0 + kvh * D + c * 64, y);
-                ++issued[s];
+            int steps = 0;
+            for (int r = 0, it = 0; ok; ++r, ++it) {
+                const int k = attn_item_index(r, b, G);
+                if (k >= a.n_items) break;
+                const AttnItem w = attn_item(a, k);
+                const int kvh = w.head / a.group;
+                const int n_kt = w.nkt_b > w.nkt_a ? w.nkt_b : w.nkt_a;
+                steps += n_kt;
+                if (it > 0 && !mbar_wait(q_empty, (it - 1) & 1, abort_flag)) { ok = false; break; }
+                const int nq_tiles = w.nkt_b > 0 ? 2 : 1;
+                mbar_arrive_expect_tx(q_full, nq_tiles * Lay::Q_BYTES);
+                for (int t = 0; t < nq_tiles; ++t)
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_2d(sQ + t * Lay::Q_BYTES + c * Lay::ATOM, &tm, q_full, w.head * D + c * 64,
+                                    w.seg0 + w.q0 + t * TQ);
+                for (int j = 0; j < n_kt; ++j, ++g) {
+                    const int s = g & 1;
+                    if (g >= 2 && !mbar_wait(&kv_empty[s], ((g >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+                    const int y = w.seg0 + j * TK;
+                    mbar_arrive_expect_tx(&k_full[s], Lay::KV_BYTES);
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_2d(sK + s * Lay::KV_BYTES + c * Lay::ATOM, &tm, &k_full[s],
+                                    a.k_col0 + kvh * D + c * 64, y);
+                    mbar_arrive_expect_tx(&v_full[s], Lay::KV_BYTES);
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_2d(sV + s * Lay::KV_BYTES + c * Lay::ATOM, &tm, &v_full[s],
+                                    a.v_col0 + kvh * D + c * 64, y);
+                    ++issued[s];
+                }
             }
+            if (a.trace) a.trace[(size_t)b * ATR_COUNT + ATR_NKT] = (unsigned long long)steps;
             if (!ok) {
                 report(a.status, ST_TIMEOUT);
                 *abort_flag = 1;
+                // the copies still in flight land before the CTA may exit
                 const int never = 0;
-                mbar_wait(q_full, 0, &never);
                 for (int s = 0; s < 2; ++s)
                     if (issued[s]) {
                         mbar_wait(&k_full[s], (issued[s] - 1) & 1, &never);
@@ -178,34 +217,63 @@ __global__ void __launch_bounds__(kThreads<D>, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_s = umma_idesc_bf16(TQ, TK);
             constexpr uint32_t idesc_o = umma_idesc_bf16(TQ, D) | (1u << 16);   // B (V) is MN-major
-            bool ok = mbar_wait(q_full, 0, abort_flag);
-            auto issue_s = [&](int j) {
-                const int s = j & 1;
-                if (!mbar_wait(&k_full[s], (j >> 1) & 1, abort_flag)) return false;
+            bool ok = true;
+            uint32_t g = 0;               // ring position of the item's first key tile
+            uint32_t np[2] = {0, 0};      // P V products issued per query tile (p_full phases)
+            // S_t = Q_t K^T for ring position gj into tile t's S columns
+            auto issue_s = [&](int t, uint32_t gj) {
+                const int s = gj & 1;
+                if (!mbar_wait(&k_full[s], (gj >> 1) & 1, abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t qa = smem_u32(sQ), kb = smem_u32(sK + s * Lay::KV_BYTES);
+                const uint32_t qa = smem_u32(sQ + t * Lay::Q_BYTES), kb = smem_u32(sK + s * Lay::KV_BYTES);
                 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * Lay::ATOM + (kk & 3) * 32;
-                    umma_bf16(tS + s * TK, sdesc_sw128(qa + off), sdesc_sw128(kb + off), idesc_s, kk > 0);
+                    umma_bf16(tmem_base + t * TQ, sdesc_sw128(qa + off), sdesc_sw128(kb + off), idesc_s, kk > 0);
                 }
-                umma_commit(&s_full[s]);
+                umma_commit(&s_full[t]);
                 return true;
             };
-            if (ok) ok = issue_s(0);
-            for (int j = 0; j < n_kt && ok; ++j) {
-                if (j + 1 < n_kt && !issue_s(j + 1)) { ok = false; break; }
-                if (!mbar_wait(p_full, j & 1, abort_flag)) { ok = false; break; }
-                const int s = j & 1;
-                if (!mbar_wait(&v_full[s], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+            // O_t (+)= P_t V with P_t packed in the first 64 columns of tile t's S
+            auto issue_pv = [&](int t, uint32_t gj, bool first) {
+                const int s = gj & 1;
+                if (!mbar_wait(&p_full[t], np[t] & 1, abort_flag)) return false;
+                if (!mbar_wait(&v_full[s], (gj >> 1) & 1, abort_flag)) return false;
+                ++np[t];
                 tc_fence_after();
-                const uint32_t pa = smem_u32(sP), vb = smem_u32(sV + s * Lay::KV_BYTES);
+                const uint32_t vb = smem_u32(sV + s * Lay::KV_BYTES);
+                const uint32_t pt = tmem_base + (uint32_t)(t * TQ);
                 #pragma unroll
                 for (int kk = 0; kk < TK / 16; ++kk)
-                    umma_bf16(tO, sdesc_sw128(pa + (kk >> 2) * Lay::ATOM + (kk & 3) * 32),
-                              sdesc_sw128_mn(vb + kk * 2048, Lay::ATOM, 1024), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&kv_empty[s]);
-                umma_commit(pv_done);
+                    umma_bf16_ts(tmem_base + 256 + t * 128, pt + kk * 8,
+                                 sdesc_sw128_mn(vb + kk * 2048, Lay::ATOM, 1024), idesc_o,
+                                 (!first || kk > 0) ? 1u : 0u);
+                umma_commit(&pv_done[t]);
+                return true;
+            };
+            for (int r = 0, it = 0; ok; ++r, ++it) {
+                const int k = attn_item_index(r, b, G);
+                if (k >= a.n_items) break;
+                const AttnItem w = attn_item(a, k);
+                const int n_kt = w.nkt_b > w.nkt_a ? w.nkt_b : w.nkt_a;
+                if (!mbar_wait(q_full, it & 1, abort_flag)) { ok = false; break; }
+                if (it == 0) astamp_clk(a, ATR_Q);
+                ok = issue_s(0, g);
+                if (ok && w.nkt_b > 0) ok = issue_s(1, g);
+                if (ok && n_kt == 1) umma_commit(q_empty);
+                for (int j = 0; j < n_kt && ok; ++j) {
+                    if (j < w.nkt_a) {
+                        if (!issue_pv(0, g + j, j == 0)) { ok = false; break; }
+                        if (j + 1 < w.nkt_a && !issue_s(0, g + j + 1)) { ok = false; break; }
+                    }
+                    if (j < w.nkt_b) {
+                        if (!issue_pv(1, g + j, j == 0)) { ok = false; break; }
+                        if (j + 1 < w.nkt_b && !issue_s(1, g + j + 1)) { ok = false; break; }
+                    }
+                    if (j == n_kt - 2) umma_commit(q_empty);   // the item's last score MMAs are issued
+                    umma_commit(&kv_empty[(g + j) & 1]);
+                }
+                g += n_kt;
             }
             if (!ok) {
                 report(a.status, ST_TIMEOUT);
@@ -216,131 +284,130 @@ __global__ void __launch_bounds__(kThreads<D>, 1)
             mbar_wait(drain, 0, &never);
         }
     } else {
-        constexpr int NWG = kNWG<D>;
-        constexpr int KC = TK / NWG;                  // key columns of S per warpgroup
-        constexpr int OC = D / NWG;                   // columns of O per warpgroup (32)
-        const int wg = (warp - 2) >> 2;
+        const int t = (warp - 2) >> 2;                // query tile of this warpgroup
         const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;            // row of the q tile = TMEM lane
-        const int qpos = q0 + r;                      // position inside the sequence
+        const int r_row = quarter * 32 + lane;        // row of the query tile = TMEM lane
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t p_row = smem_u32(sP) + r * 128;
-        float *red_max = reinterpret_cast<float *>(smem + Lay::OFF_RED);   // [2][NWG][TQ]
-        float *red_l = red_max + 2 * NWG * TQ;                             // [NWG][TQ]
-        float m_use = -INFINITY, l = 0.f;
-        bool good = true;   // every exit is decided at a barrier so all softmax warps leave together
-        for (int j = 0; j < n_kt; ++j) {
-            good = __all_sync(0xffffffffu, good && mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag));
-            const uint32_t sbuf = tS + lane_off + (j & 1) * TK + wg * KC;
-            const int key0 = j * TK + wg * KC;
-            const bool diag = j * TK + TK - 1 > q0;
-            // pass 1: this warpgroup's part of the row max of the scaled, masked scores
-            float mt = -INFINITY;
-            if (good) {
+        const uint32_t tS = tmem_base + lane_off + (uint32_t)(t * TQ);
+        const uint32_t tO = tmem_base + lane_off + (uint32_t)(256 + t * 128);
+        uint32_t c = 0;                               // steps of this query tile so far (barrier phases)
+        bool good = true;
+        for (int r = 0; good; ++r) {
+            const int k = attn_item_index(r, b, G);
+            if (k >= a.n_items) break;
+            const AttnItem w = attn_item(a, k);
+            const int nkt = t == 0 ? w.nkt_a : w.nkt_b;
+            if (nkt == 0) continue;
+            const int qtile0 = w.q0 + t * TQ;
+            const int qpos = qtile0 + r_row;          // position inside the sequence
+            float m_use = -INFINITY, l = 0.f;
+            for (int j = 0; j < nkt; ++j, ++c) {
+                good = __all_sync(0xffffffffu, mbar_wait(&s_full[t], c & 1, abort_flag));
+                if (!good) break;
+                if (c == 0 && threadIdx.x == 64) astamp_clk(a, ATR_S0);
                 tc_fence_after();
-                #pragma unroll 1
-                for (int c = 0; c < KC / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(sbuf + c * 32, v);
+                uint32_t v[TK];
+                {
+                    uint32_t (&v0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[0]);
+                    uint32_t (&v1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[32]);
+                    uint32_t (&v2)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[64]);
+                    uint32_t (&v3)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[96]);
+                    tmem_ld32(tS, v0);
+                    tmem_ld32(tS + 32, v1);
+                    tmem_ld32(tS + 64, v2);
+                    tmem_ld32(tS + 96, v3);
                     tmem_ld_wait();
+                }
+                // keys after the query masked (the diagonal tile only); row max of the raw scores
+                // (the scale is positive) as 8 independent chains
+                const int key0 = j * TK;
+                if (key0 + TK - 1 > qtile0) {
+                    #pragma unroll
+                    for (int i = 0; i < TK; ++i)
+                        if (key0 + i > qpos) v[i] = __float_as_uint(-INFINITY);
+                }
+                float mx[8];
+                #pragma unroll
+                for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(v[u]);
+                #pragma unroll
+                for (int i = 8; i < TK; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(v[i]));
+                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * a.scale_log2;
+                float alpha = 1.f;
+                bool rescale = false;
+                if (j == 0) {
+                    m_use = mt;
+                } else if (mt > m_use + kRescaleThreshold) {
+                    alpha = ex2(m_use - mt);
+                    m_use = mt;
+                    rescale = true;
+                }
+                // P = exp2(s * scale - m) packed as bf16 pairs over the first 64 columns of this
+                // row of S; the row sum in 4 independent chains
+                const float neg_m = -m_use;
+                float rs[4] = {0.f, 0.f, 0.f, 0.f};
+                #pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[32];
                     #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        float x = __uint_as_float(v[i]) * a.scale_log2;
-                        if (diag && key0 + c * 32 + i > qpos) x = -INFINITY;
-                        mt = fmaxf(mt, x);
+                        const float p0 = ex2(fmaf(__uint_as_float(v[64 * h + 2 * i]), a.scale_log2, neg_m));
+                        const float p1 = ex2(fmaf(__uint_as_float(v[64 * h + 2 * i + 1]), a.scale_log2, neg_m));
+                        rs[i & 3] += p0 + p1;
+                        pk[i] = pack_bf16x2(p0, p1);
                     }
+                    tmem_st32(tS + 32 * h, pk);
                 }
-            }
-            red_max[((j & 1) * NWG + wg) * TQ + r] = mt;
-            if (!softmax_bar_and<128 * NWG>(good)) { good = false; break; }
-            mt = red_max[((j & 1) * NWG) * TQ + r];
-            #pragma unroll
-            for (int w2 = 1; w2 < NWG; ++w2) mt = fmaxf(mt, red_max[((j & 1) * NWG + w2) * TQ + r]);
-            float alpha = 1.f;
-            bool rescale = false;
-            if (j == 0) {
-                m_use = mt;
-            } else if (mt > m_use + kRescaleThreshold) {
-                alpha = exp2f(m_use - mt);
-                m_use = mt;
-                rescale = true;
-            }
-            // P buffer and O are free once the previous P V product has completed
-            if (j > 0) {
-                good = __all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1, abort_flag));
-                if (good) tc_fence_after();
-            }
-            if (good) {
+                l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+                // O is rescaled after the previous P V product of this tile has completed
                 if (__any_sync(0xffffffffu, rescale)) {
-                    uint32_t v[32];
-                    tmem_ld32(tO + lane_off + wg * OC, v);
-                    tmem_ld_wait();
-                    #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                    tmem_st32(tO + lane_off + wg * OC, v);
-                    tmem_st_wait();
-                }
-                l *= alpha;
-                // pass 2: P = exp2(x - m_use) as bf16 into the K-major swizzled P tile
-                #pragma unroll 1
-                for (int c = 0; c < KC / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(sbuf + c * 32, v);
-                    tmem_ld_wait();
-                    uint32_t pk[16];
-                    #pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float x0 = __uint_as_float(v[i]) * a.scale_log2;
-                        float x1 = __uint_as_float(v[i + 1]) * a.scale_log2;
-                        if (diag && key0 + c * 32 + i > qpos) x0 = -INFINITY;
-                        if (diag && key0 + c * 32 + i + 1 > qpos) x1 = -INFINITY;
-                        const float p0 = exp2f(x0 - m_use), p1 = exp2f(x1 - m_use);
-                        l += p0 + p1;
-                        pk[i >> 1] = pack_bf16x2(p0, p1);
-                    }
-                    #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int chunk = (wg * KC + c * 32) / 8 + q;      // 16-byte chunk = 8 keys
-                        const uint32_t addr = p_row + (chunk >> 3) * Lay::ATOM + (((chunk & 7) ^ (r & 7)) << 4);
-                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(pk[4 * q]),
-                                     "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
-                                     : "memory");
+                    good = __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (c - 1) & 1, abort_flag));
+                    if (!good) break;
+                    tc_fence_after();
+                    #pragma unroll 1
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + cc * 32, o);
+                        tmem_ld_wait();
+                        #pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(tO + cc * 32, o);
                     }
                 }
-                fence_proxy_async_smem();
+                tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(p_full);
+                if (lane == 0) mbar_arrive(&p_full[t]);
             }
-        }
-        // epilogue: row sums combined over the warpgroups, O / l -> bf16 -> global rows of this sequence
-        if (good) good = __all_sync(0xffffffffu, mbar_wait(pv_done, (n_kt - 1) & 1, abort_flag));
-        red_l[wg * TQ + r] = l;
-        if (softmax_bar_and<128 * NWG>(good)) {
+            if (!good) break;
+            if (threadIdx.x == 64) astamp_clk(a, ATR_LAST_P);
+            // epilogue: O / l -> bf16 -> global rows of this sequence; the next item's first P V
+            // product (which overwrites O) waits for this warp's next P, issued after these reads
+            good = __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (c - 1) & 1, abort_flag));
+            if (!good) break;
+            if (threadIdx.x == 64) astamp_clk(a, ATR_O);
             tc_fence_after();
-            float lt = 0.f;
-            #pragma unroll
-            for (int w2 = 0; w2 < NWG; ++w2) lt += red_l[w2 * TQ + r];
-            const float inv = lt > 0.f ? 1.f / lt : 0.f;
-            const bool live = qpos < L;
-            bf16 *dst = a.o + (size_t)(seg0 + qpos) * a.ld_o + (size_t)head * D + wg * OC;
-            uint32_t v[32];
-            tmem_ld32(tO + lane_off + wg * OC, v);
-            tmem_ld_wait();
-            if (live) {
-                uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-                #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint4 u;
-                    u.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
-                    u.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
-                    u.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
-                    u.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
-                    d4[q] = u;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const bool live = qpos < w.L;
+            bf16 *dst = a.o + (size_t)(w.seg0 + qpos) * a.ld_o + (size_t)w.head * D;
+            #pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t v[32];
+                tmem_ld32(tO + cc * 32, v);
+                tmem_ld_wait();
+                if (live) {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + cc * 32);
+                    #pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 u;
+                        u.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
+                        u.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
+                        u.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
+                        u.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
+                        d4[q] = u;
+                    }
                 }
             }
-        } else {
-            good = false;
         }
         if (!good && lane == 0) {
             report(a.status, ST_TIMEOUT);
@@ -348,7 +415,10 @@ __global__ void __launch_bounds__(kThreads<D>, 1)
         }
     }
 
+    __syncwarp();
+    tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) astamp_ns(a, ATR_END);
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, 512);
@@ -365,12 +435,16 @@ cudaError_t launch_tc(const CUtensorMap &tm, const AttnTcArgs &args, int grid, c
         attr = true;
     }
     cudaLaunchAttribute at[1];
-    cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(kThreads<D>), TcLayout<D>::SMEM, st, at);
+    cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(kThreads), TcLayout<D>::SMEM, st, at);
     return cudaLaunchKernelEx(&cfg, attention_tc_kernel<D>, tm, args);
 }
 
+thread_local unsigned long long *t_attn_trace = nullptr;
+
 }  // namespace
 
+void attention_trace_next(unsigned long long *trace) { t_attn_trace = trace; }
+int attention_trace_fields() { return ATR_COUNT; }
 cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, int d, const int32_t *cu_host,
                              int n_seqs, int32_t *status, cudaStream_t st) {
     if (S <= 0) return cudaSuccess;
@@ -387,12 +461,14 @@ cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, i
     args.v_col0 = (nq + nkv) * d;
     args.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
     args.status = status;
-    int n = 0, tiles = 0;
+    args.trace = t_attn_trace;
+    t_attn_trace = nullptr;
+    int n = 0, pairs = 0;
     if (!cu_host) {
         args.cu[0] = 0;
         args.cu[1] = S;
-        args.tile_start[0] = 0;
-        tiles = (S + TQ - 1) / TQ;
+        args.pair_start[0] = 0;
+        pairs = (S + 2 * TQ - 1) / (2 * TQ);
         n = 1;
     } else {
         args.cu[0] = 0;
@@ -400,16 +476,19 @@ cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, i
             const int len = cu_host[i + 1] - cu_host[i];
             if (len <= 0) continue;
             args.cu[n] = cu_host[i];
-            args.tile_start[n] = tiles;
-            tiles += (len + TQ - 1) / TQ;
+            args.pair_start[n] = pairs;
+            pairs += (len + 2 * TQ - 1) / (2 * TQ);
             ++n;
             args.cu[n] = cu_host[i + 1];
         }
     }
     if (n == 0) return cudaSuccess;
     args.n_seqs = n;
-    args.total_tiles = tiles;
-    const int grid = tiles * nq;
+    args.total_pairs = pairs;
+    args.n_items = pairs * nq;
+    int sms = device_num_sms();
+    if (sms <= 0) sms = 1;
+    const int grid = args.n_items < sms ? args.n_items : sms;   // persistent: one CTA per SM
     return d == 128 ? launch_tc<128>(tm, args, grid, st) : launch_tc<64>(tm, args, grid, st);
 }
 

@@ -23,12 +23,14 @@
 //              element-wise op, bf16 stores; overlaps the next tile's MMAs
 // Schedule: the tiles of the full waves run data-parallel (tile = pair + i*pairs,
 // M-fastest, so the pairs in flight share each weight tile through L2).  The
-// tiles of the last, partial wave would leave most SMs idle, so each of them is
-// split along K into s chunks (s = pairs / leftover tiles) computed by s pairs:
-// every CTA's fp32 partial goes to its workspace slot, a per-slot flag is
-// released, and each contributing CTA then sums the s partials of its half of
-// the tile in fixed chunk order for a slice of rows and applies the epilogue
-// (deterministic).  The grid never exceeds the number of co-resident pairs.
+// tiles of the last, partial wave would leave SMs idle, so their k-blocks are laid
+// end to end and cut into equal contiguous ranges, one per pair (stream-K); a range
+// covers parts of at most two tiles.  Every pair runs its range FIRST: each CTA
+// writes the fp32 partial of each part to a workspace slot, releases its flag,
+// waits for the other contributors of those tiles, and sums the partials of a
+// slice of rows in range order (deterministic) with the epilogue applied - all
+// while the tensor cores already work on the pair's data-parallel tiles.  The grid
+// never exceeds the number of co-resident pairs, so every wait ends.
 // Every wait is bounded; on time-out the CTA records ST_TIMEOUT, drains its
 // in-flight copies and MMAs, frees TMEM and exits.
 #include <cudaTypedefs.h>
@@ -53,6 +55,8 @@ constexpr int EPI_WARPS = 8;
 constexpr int EPI_THREADS = EPI_WARPS * 32;
 constexpr int GEMM_THREADS = 64 + EPI_THREADS;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+constexpr int kMinStreamKBlocks = 4;             // smallest k-range a stream-K pair takes
+static_assert(BM * BN % 4 == 0, "partials are written as float4");
 
 struct GemmArgs {
     int M, N, K;
@@ -64,10 +68,11 @@ struct GemmArgs {
     const int32_t *vis_rank;
     int n_vis;
     int32_t *status;
-    // split of the last partial wave
+    // stream-K over the last partial wave
     int dp_tiles;      // tiles run data-parallel: [0, dp_tiles)
-    int splits;        // s > 1: tiles [dp_tiles, nm*nn) are split into s K-chunks
-    float *part;       // [grid][BM*BN] fp32 partial accumulators (one slot per CTA)
+    int sk_pairs;      // pairs [0, sk_pairs) share the k-blocks of tiles [dp_tiles, nm*nn); 0: none
+    long long sk_work; // (nm*nn - dp_tiles) * nk
+    float *part;       // [2*grid][BM*BN] fp32 partials: slot 4*pair + 2*part + rank
     uint32_t *flags;   // [grid] release flags
     uint32_t epoch;    // unique per launch; a flag equal to it means "partial written"
     // EPI_QKROPE
@@ -75,22 +80,63 @@ struct GemmArgs {
     const float *cos_t, *sin_t;
     int head_dim, nq, nkv;
     float eps;
+    unsigned long long *trace;   // optional [grid][TR_COUNT] %globaltimer stamps
 };
 
-// The K-chunk of this pair's split item (none when kb1 <= kb0).
-struct SplitItem {
-    int tile, kb0, kb1, chunk;
-};
-__device__ __forceinline__ SplitItem split_item(const GemmArgs &g, int pair) {
-    SplitItem it{0, 0, 0, 0};
-    const int left = g.nm * g.nn - g.dp_tiles;
-    if (g.splits > 1 && pair < left * g.splits) {
-        it.tile = g.dp_tiles + pair / g.splits;
-        it.chunk = pair % g.splits;
-        it.kb0 = it.chunk * g.nk / g.splits;
-        it.kb1 = (it.chunk + 1) * g.nk / g.splits;
+// Phase stamps of the optional timeline (h3enc_op_gemm_traced).
+enum { TR_START = 0, TR_READY, TR_FIRST_LOAD, TR_FIRST_MMA, TR_LAST_DP_MMA, TR_DP_EPI_DONE, TR_SPLIT_MMA_DONE,
+       TR_DUMP_DONE, TR_FLAGS_SEEN, TR_REDUCE_DONE, TR_END, TR_COUNT };
+__device__ __forceinline__ void stamp(const GemmArgs &g, int what) {
+    if (g.trace) {
+        unsigned long long t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        g.trace[(size_t)blockIdx.x * TR_COUNT + what] = t;
     }
-    return it;
+}
+
+// Stream-K ranges: pair p owns k-iterations [start(p), start(p+1)) of the tail laid
+// end to end (tail tile t holds iterations [t*nk, (t+1)*nk)).
+__device__ __forceinline__ long long sk_start(const GemmArgs &g, int p) {
+    return (long long)p * g.sk_work / g.sk_pairs;
+}
+// The pair whose range holds iteration x.
+__device__ __forceinline__ int sk_pair_of(const GemmArgs &g, long long x) {
+    return (int)(((x + 1) * g.sk_pairs - 1) / g.sk_work);
+}
+// The (at most two) parts of this pair's range, each inside one tile.
+struct StreamK {
+    int n;
+    int tile[2], kb0[2], kb1[2];
+};
+__device__ __forceinline__ StreamK stream_k(const GemmArgs &g, int pair) {
+    StreamK sk{};
+    if (pair >= g.sk_pairs) return sk;
+    long long x = sk_start(g, pair);
+    const long long e = sk_start(g, pair + 1);
+    while (x < e && sk.n < 2) {
+        const int t = (int)(x / g.nk);
+        const long long te = (long long)(t + 1) * g.nk;
+        const long long pe = e < te ? e : te;
+        sk.tile[sk.n] = t;
+        sk.kb0[sk.n] = (int)(x - (long long)t * g.nk);
+        sk.kb1[sk.n] = (int)(pe - (long long)t * g.nk);
+        ++sk.n;
+        x = pe;
+    }
+    return sk;
+}
+// Contributors [pa, pb] of tail tile t, and the part index of t within pair q's range.
+__device__ __forceinline__ void sk_contributors(const GemmArgs &g, int t, int &pa, int &pb) {
+    pa = sk_pair_of(g, (long long)t * g.nk);
+    pb = sk_pair_of(g, (long long)(t + 1) * g.nk - 1);
+}
+__device__ __forceinline__ int sk_part_index(const GemmArgs &g, int q, int t) {
+    return sk_start(g, q) < (long long)t * g.nk ? 1 : 0;
+}
+// Partial slots are written coalesced: float4 (row r, columns col..col+3) of the
+// 128 x 256 partial sits at float4 index ((col/32)*8 + (col%32)/4)*128 + r.
+__device__ __forceinline__ size_t part_f4(int r, int col) {
+    return ((size_t)((col >> 5) * 8 + ((col & 31) >> 2)) << 7) + (size_t)r;
 }
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
@@ -162,6 +208,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int pair = blockIdx.x >> 1;
     const int npairs = gridDim.x >> 1;
     pdl_trigger();
+    if (threadIdx.x == 0) stamp(g, TR_START);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -189,9 +236,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     pdl_wait();       // inputs of this GEMM are the previous kernel's outputs
+    if (threadIdx.x == 0) stamp(g, TR_READY);
 
-    const SplitItem sk = split_item(g, pair);
-    const bool has_split = sk.kb1 > sk.kb0;
+    const StreamK sk = stream_k(g, pair);
 
     if (warp == 0) {
         if (lane == 0) {
@@ -210,12 +257,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
                     tma_load_2d_pair(sA + stage * A_BYTES, &tmA, bar, kb * BK, m0);
                     tma_load_2d_pair(sB + stage * B_BYTES, &tmB, bar, kb * BK, n0);
+                    if (issued[0] + issued[1] == 0 && stage == 0) stamp(g, TR_FIRST_LOAD);
                     ++issued[stage];
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             };
+            for (int j = 0; ok && j < sk.n; ++j) load_item(g.dp_tiles + sk.tile[j], sk.kb0[j], sk.kb1[j]);
             for (int tile = pair; ok && tile < g.dp_tiles; tile += npairs) load_item(tile, 0, g.nk);
-            if (ok && has_split) load_item(sk.tile, sk.kb0, sk.kb1);
             if (!ok) {
                 report(g.status, ST_TIMEOUT);
                 *abort_flag = 1;
@@ -235,8 +283,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
+            bool first_mma = true;
             auto mma_item = [&](int kb0, int kb1) {
                 if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; return; }
+                if (first_mma) { stamp(g, TR_FIRST_MMA); first_mma = false; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -255,8 +305,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             };
+            for (int j = 0; ok && j < sk.n; ++j) mma_item(sk.kb0[j], sk.kb1[j]);
             for (int tile = pair; ok && tile < g.dp_tiles; tile += npairs) mma_item(0, g.nk);
-            if (ok && has_split) mma_item(sk.kb0, sk.kb1);
+            stamp(g, TR_LAST_DP_MMA);
             if (!ok) {
                 report(g.status, ST_TIMEOUT);
                 *abort_flag = 1;
@@ -298,12 +349,213 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         };
+        // ---- stream-K parts first: their partials, flags and reduction overlap the MMAs of the
+        //      data-parallel tiles ----
+        if (sk.n > 0) {
+            // 1) the fp32 accumulator of part j (this CTA's 128 rows) goes to slot 4*pair + 2*j + rank;
+            //    every epilogue warp reaches each barrier below, failed or not
+            bool dumped = true;
+            for (int j = 0; j < sk.n; ++j) {
+                const bool got = ok && wait_acc();
+                if (et == 0 && j == 0) stamp(g, TR_SPLIT_MMA_DONE);
+                if (got) {
+                    const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+                    float4 *slot = reinterpret_cast<float4 *>(g.part) + (size_t)(4 * pair + 2 * j + (int)rank) * (BM * BN / 4);
+                    const int r = quarter * 32 + lane;
+                    #pragma unroll 1
+                    for (int c = ehalf * (BN / 64); c < (ehalf + 1) * (BN / 64); ++c) {
+                        uint32_t v[32];
+                        tmem_ld32(taddr + c * 32, v);
+                        tmem_ld_wait();
+                        #pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            slot[part_f4(r, c * 32 + 4 * q)] =
+                                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                    }
+                    release_acc();
+                }
+                dumped = dumped && got;
+            }
+            __threadfence();
+            if (epi_bar_and(dumped)) {
+                if (et == 0) {
+                    stamp(g, TR_DUMP_DONE);
+                    st_release(g.flags + blockIdx.x, g.epoch);
+                }
+                for (int j = 0; j < sk.n; ++j) {
+                    // 2) wait for the same-rank CTAs of the tile's contributors: thread i polls contributor
+                    //    pa + i (all flags in flight at once), then the AND over the epilogue warps
+                    const int t = sk.tile[j];
+                    int pa, pb;
+                    sk_contributors(g, t, pa, pb);
+                    const int nc = pb - pa + 1;
+                    bool seen = true;
+                    if (et < nc) {
+                        const long long t0 = clock64();
+                        while (ld_acquire(g.flags + 2 * (pa + et) + rank) != g.epoch) {
+                            if (clock64() - t0 > kSpinLimitCycles) { seen = false; break; }
+                        }
+                    }
+                    const bool all = epi_bar_and(seen);
+                    if (et == 0 && j == 0) stamp(g, TR_FLAGS_SEEN);
+                    if (!all) {
+                        if (et == 0) report(g.status, ST_TIMEOUT);
+                        break;
+                    }
+                    // 3) rows [r0, r1) of this CTA's half: the contributors' partials summed in range order,
+                    //    then the epilogue
+                    const int ci = pair - pa;
+                    const int r0 = ci * BM / nc, r1 = (ci + 1) * BM / nc;
+                    const int tile = g.dp_tiles + t;
+                    const int m_blk = tile % g.nm, n_blk = tile / g.nm;
+                    const int slot_pa = 4 * pa + 2 * sk_part_index(g, pa, t) + (int)rank;
+                    auto slot_of = [&](int k) {   // contributor pa + k
+                        return reinterpret_cast<const float4 *>(g.part) +
+                               (size_t)(k == 0 ? slot_pa : 4 * (pa + k) + (int)rank) * (BM * BN / 4);
+                    };
+                    if constexpr (EPI == EPI_QKROPE) {
+                        // four threads per (row, head): thread `sub` owns first-half columns
+                        // [sub*d/8, (sub+1)*d/8) and their RoPE partners d/2 further on
+                        const int d = g.head_dim, half = d >> 1, q4 = half >> 2, hpt = BN / d;
+                        const int sub = et & 3;
+                        const unsigned gmask = 0xFu << (lane & ~3);
+                        const int units = (r1 - r0) * hpt;
+                        for (int u = et >> 2; u < units; u += EPI_THREADS / 4) {
+                            const int r = r0 + u / hpt, hh = u % hpt;
+                            const int row = m_blk * (2 * BM) + (int)rank * BM + r;
+                            if (row >= g.M) continue;   // same row for the four threads
+                            const int head = (n_blk * BN) / d + hh;
+                            const int ca = hh * d + sub * q4;      // first-half column inside the tile
+                            float a[16], b[16];
+                            #pragma unroll
+                            for (int i = 0; i < 16; ++i) a[i] = b[i] = 0.f;
+                            for (int k = 0; k < nc; ++k) {
+                                const float4 *pk = slot_of(k);
+                                #pragma unroll
+                                for (int i = 0; i < 16; i += 4) {
+                                    if (i < q4) {
+                                        const float4 x = __ldcg(pk + part_f4(r, ca + i));
+                                        const float4 y = __ldcg(pk + part_f4(r, ca + half + i));
+                                        a[i] += x.x; a[i + 1] += x.y; a[i + 2] += x.z; a[i + 3] += x.w;
+                                        b[i] += y.x; b[i + 1] += y.y; b[i + 2] += y.z; b[i + 3] += y.w;
+                                    }
+                                }
+                            }
+                            __nv_bfloat16 *dst = g.C + (size_t)row * g.ldc + n_blk * BN + ca;
+                            const bool is_q = head < g.nq, is_k = !is_q && head < g.nq + g.nkv;
+                            if (is_q || is_k) {
+                                float ss = 0.f;
+                                #pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    if (i < q4) ss = fmaf(a[i], a[i], fmaf(b[i], b[i], ss));
+                                ss += __shfl_xor_sync(gmask, ss, 1);
+                                ss += __shfl_xor_sync(gmask, ss, 2);
+                                const float rstd = 1.0f / sqrtf(ss / (float)d + g.eps);
+                                const __nv_bfloat16 *w = is_q ? g.wq : g.wk;
+                                const int jb = sub * q4;           // frequency index of a[0]
+                                #pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    if (i < q4) {
+                                        const float ya = a[i] * rstd * __bfloat162float(w[jb + i]);
+                                        const float yb = b[i] * rstd * __bfloat162float(w[half + jb + i]);
+                                        const float co = g.cos_t[(size_t)row * half + jb + i];
+                                        const float si = g.sin_t[(size_t)row * half + jb + i];
+                                        a[i] = ya * co - yb * si;
+                                        b[i] = yb * co + ya * si;
+                                    }
+                                }
+                            }
+                            #pragma unroll
+                            for (int i = 0; i < 16; i += 2) {
+                                if (i < q4) {
+                                    *reinterpret_cast<uint32_t *>(dst + i) = pack_bf16x2(a[i], a[i + 1]);
+                                    *reinterpret_cast<uint32_t *>(dst + half + i) = pack_bf16x2(b[i], b[i + 1]);
+                                }
+                            }
+                        }
+                    } else {
+                        // consecutive threads take consecutive rows of one float4 column group
+                        constexpr int GROUPS = (EPI == EPI_SWIGLU) ? BN / 8 : BN / 4;
+                        const int nr = r1 - r0;
+                        const int units = nr * GROUPS;
+                        for (int u = et; u < units; u += EPI_THREADS) {
+                            const int r = r0 + u % nr;
+                            const int c4 = (u / nr) * 4;
+                            const int row = m_blk * (2 * BM) + (int)rank * BM + r;
+                            if (row >= g.M) continue;
+                            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+                            const size_t ia = part_f4(r, c4), ib = part_f4(r, c4 + BN / 2);
+                            // partials in batches of 8 loads in flight, summed in range order
+                            for (int k0 = 0; k0 < nc; k0 += 8) {
+                                float4 x[8], y[8];
+                                #pragma unroll
+                                for (int k = 0; k < 8; ++k) {
+                                    if (k0 + k < nc) {
+                                        const float4 *pk = slot_of(k0 + k);
+                                        x[k] = __ldcg(pk + ia);
+                                        if constexpr (EPI == EPI_SWIGLU) y[k] = __ldcg(pk + ib);
+                                    }
+                                }
+                                #pragma unroll
+                                for (int k = 0; k < 8; ++k) {
+                                    if (k0 + k < nc) {
+                                        a.x += x[k].x; a.y += x[k].y; a.z += x[k].z; a.w += x[k].w;
+                                        if constexpr (EPI == EPI_SWIGLU) {
+                                            b.x += y[k].x; b.y += y[k].y; b.z += y[k].z; b.w += y[k].w;
+                                        }
+                                    }
+                                }
+                            }
+                            float f[4] = {a.x, a.y, a.z, a.w};
+                            int col;
+                            if constexpr (EPI == EPI_SWIGLU) {
+                                const float up[4] = {b.x, b.y, b.z, b.w};
+                                #pragma unroll
+                                for (int i = 0; i < 4; ++i) f[i] = f[i] / (1.0f + expf(-f[i])) * up[i];
+                                col = n_blk * (BN / 2) + c4;
+                            } else {
+                                col = n_blk * BN + c4;
+                                if constexpr (EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_DS) {
+                                    const uint2 rv = *reinterpret_cast<const uint2 *>(g.R + (size_t)row * g.ldc + col);
+                                    f[0] += bf16_lo(rv.x); f[1] += bf16_hi(rv.x); f[2] += bf16_lo(rv.y); f[3] += bf16_hi(rv.y);
+                                }
+                                if constexpr (EPI == EPI_RESIDUAL_DS) {
+                                    int rank_ds = g.DS != nullptr ? g.vis_rank[row] : -1;
+                                    if (rank_ds >= g.n_vis) rank_ds = -1;
+                                    if (rank_ds >= 0) {
+                                        const uint2 dv = *reinterpret_cast<const uint2 *>(g.DS + (size_t)rank_ds * g.ldc + col);
+                                        f[0] = round_bf16(f[0]) + bf16_lo(dv.x); f[1] = round_bf16(f[1]) + bf16_hi(dv.x);
+                                        f[2] = round_bf16(f[2]) + bf16_lo(dv.y); f[3] = round_bf16(f[3]) + bf16_hi(dv.y);
+                                    }
+                                }
+                            }
+                            uint2 o;
+                            o.x = pack_bf16x2(f[0], f[1]);
+                            o.y = pack_bf16x2(f[2], f[3]);
+                            *reinterpret_cast<uint2 *>(g.C + (size_t)row * g.ldc + col) = o;
+                        }
+                    }
+                }
+            }
+            if (et == 0) stamp(g, TR_REDUCE_DONE);
+        }
         for (int tile = pair; tile < g.dp_tiles; tile += npairs) {
             const int m_blk = tile % g.nm;
             const int n_blk = tile / g.nm;
-            if (!wait_acc()) break;
             const int row = m_blk * (2 * BM) + (int)rank * BM + quarter * 32 + lane;
             const bool live = row < g.M;
+            uint4 rpre[BN / 16];   // this thread's BN/2 residual columns
+            if constexpr (EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_DS) {
+                // the residual does not depend on the accumulator: its loads fly while the MMAs finish
+                if (live) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(g.R + (size_t)row * g.ldc + n_blk * BN +
+                                                                       ehalf * (BN / 2));
+                    #pragma unroll
+                    for (int i = 0; i < BN / 16; ++i) rpre[i] = src[i];
+                }
+            }
+            if (!wait_acc()) break;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
             if constexpr (EPI == EPI_SWIGLU) {
                 #pragma unroll 1
@@ -410,13 +662,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         if (rank_ds >= g.n_vis) rank_ds = -1;  // count mismatch is reported by the rank scan
                     }
                 }
-                #pragma unroll 1
-                for (int c = ehalf * (BN / 64); c < (ehalf + 1) * (BN / 64); ++c) {
+                #pragma unroll
+                for (int cc = 0; cc < BN / 64; ++cc) {
+                    const int c = ehalf * (BN / 64) + cc;
                     const int col = n_blk * BN + c * 32;
-                    float r[32];
-                    if constexpr (EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_DS) {
-                        if (live) load_row32(g.R + (size_t)row * g.ldc + col, r);   // in flight during the TMEM read
-                    }
                     uint32_t v[32];
                     tmem_ld32(taddr + c * 32, v);
                     tmem_ld_wait();
@@ -426,7 +675,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
                         if constexpr (EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_DS) {
                             #pragma unroll
-                            for (int j = 0; j < 32; ++j) f[j] += r[j];
+                            for (int i = 0; i < 4; ++i) {
+                                const uint4 rv = rpre[cc * 4 + i];
+                                f[8 * i + 0] += bf16_lo(rv.x); f[8 * i + 1] += bf16_hi(rv.x);
+                                f[8 * i + 2] += bf16_lo(rv.y); f[8 * i + 3] += bf16_hi(rv.y);
+                                f[8 * i + 4] += bf16_lo(rv.z); f[8 * i + 5] += bf16_hi(rv.z);
+                                f[8 * i + 6] += bf16_lo(rv.w); f[8 * i + 7] += bf16_hi(rv.w);
+                            }
                         }
                         if constexpr (EPI == EPI_RESIDUAL_DS) {
                             if (rank_ds >= 0) {
@@ -442,176 +697,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             release_acc();
         }
-        if (has_split) {
-            // 1) dump this CTA's fp32 accumulator (its 128 rows of the tile) to slot blockIdx.x, row-major
-            //    [BM][BN]; every epilogue warp reaches the barrier below exactly once, failed or not
-            const bool got = ok && wait_acc();
-            if (got) {
-                const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-                float *dst = g.part + (size_t)blockIdx.x * (BM * BN) + (size_t)(quarter * 32 + lane) * BN;
-                #pragma unroll 1
-                for (int c = ehalf * (BN / 64); c < (ehalf + 1) * (BN / 64); ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(taddr + c * 32, v);
-                    tmem_ld_wait();
-                    float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
-                    #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-                }
-                release_acc();
-            }
-            __threadfence();
-            if (epi_bar_and(got)) {
-                if (et == 0) st_release(g.flags + blockIdx.x, g.epoch);
-                // 2) wait for the same-rank CTAs of the s pairs that computed this tile: thread j polls
-                //    contributor j (all flags in flight at once), then the AND over the epilogue warps
-                const int first_pair = pair - sk.chunk;
-                bool seen = true;
-                if (et < g.splits) {
-                    const long long t0 = clock64();
-                    while (ld_acquire(g.flags + 2 * (first_pair + et) + rank) != g.epoch) {
-                        if (clock64() - t0 > kSpinLimitCycles) { seen = false; break; }
-                    }
-                }
-                const bool all = epi_bar_and(seen);
-                if (!all) {
-                    if (et == 0) report(g.status, ST_TIMEOUT);
-                } else {
-                    // 3) rows [r0, r1) of this CTA's half: sum of the s partials in chunk order, then the epilogue
-                    const int r0 = sk.chunk * BM / g.splits, r1 = (sk.chunk + 1) * BM / g.splits;
-                    const int m_blk = sk.tile % g.nm, n_blk = sk.tile / g.nm;
-                    if constexpr (EPI == EPI_QKROPE) {
-                        // four threads per (row, head): thread `sub` owns first-half columns
-                        // [sub*d/8, (sub+1)*d/8) and their RoPE partners d/2 further on
-                        const int d = g.head_dim, half = d >> 1, q4 = half >> 2, hpt = BN / d;
-                        const int sub = et & 3;
-                        const unsigned gmask = 0xFu << (lane & ~3);
-                        const int units = (r1 - r0) * hpt;
-                        for (int u = et >> 2; u < units; u += EPI_THREADS / 4) {
-                            const int r = r0 + u / hpt, hh = u % hpt;
-                            const int row = m_blk * (2 * BM) + (int)rank * BM + r;
-                            if (row >= g.M) continue;   // same row for the four threads
-                            const int head = (n_blk * BN) / d + hh;
-                            const int ca = hh * d + sub * q4;      // first-half column inside the tile
-                            float a[16], b[16];
-                            #pragma unroll
-                            for (int i = 0; i < 16; ++i) a[i] = b[i] = 0.f;
-                            for (int j = 0; j < g.splits; ++j) {
-                                const float *pj = g.part + (size_t)(2 * (first_pair + j) + rank) * (BM * BN) +
-                                                  (size_t)r * BN;
-                                #pragma unroll
-                                for (int i = 0; i < 16; i += 4) {
-                                    if (i < q4) {
-                                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(pj + ca + i));
-                                        const float4 y = __ldcg(reinterpret_cast<const float4 *>(pj + ca + half + i));
-                                        a[i] += x.x; a[i + 1] += x.y; a[i + 2] += x.z; a[i + 3] += x.w;
-                                        b[i] += y.x; b[i + 1] += y.y; b[i + 2] += y.z; b[i + 3] += y.w;
-                                    }
-                                }
-                            }
-                            __nv_bfloat16 *dst = g.C + (size_t)row * g.ldc + n_blk * BN + ca;
-                            const bool is_q = head < g.nq, is_k = !is_q && head < g.nq + g.nkv;
-                            if (is_q || is_k) {
-                                float ss = 0.f;
-                                #pragma unroll
-                                for (int i = 0; i < 16; ++i)
-                                    if (i < q4) ss = fmaf(a[i], a[i], fmaf(b[i], b[i], ss));
-                                ss += __shfl_xor_sync(gmask, ss, 1);
-                                ss += __shfl_xor_sync(gmask, ss, 2);
-                                const float rstd = 1.0f / sqrtf(ss / (float)d + g.eps);
-                                const __nv_bfloat16 *w = is_q ? g.wq : g.wk;
-                                const int jb = sub * q4;           // frequency index of a[0]
-                                #pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    if (i < q4) {
-                                        const float ya = a[i] * rstd * __bfloat162float(w[jb + i]);
-                                        const float yb = b[i] * rstd * __bfloat162float(w[half + jb + i]);
-                                        const float co = g.cos_t[(size_t)row * half + jb + i];
-                                        const float si = g.sin_t[(size_t)row * half + jb + i];
-                                        a[i] = ya * co - yb * si;
-                                        b[i] = yb * co + ya * si;
-                                    }
-                                }
-                            }
-                            #pragma unroll
-                            for (int i = 0; i < 16; i += 2) {
-                                if (i < q4) {
-                                    *reinterpret_cast<uint32_t *>(dst + i) = pack_bf16x2(a[i], a[i + 1]);
-                                    *reinterpret_cast<uint32_t *>(dst + half + i) = pack_bf16x2(b[i], b[i + 1]);
-                                }
-                            }
-                        }
-                    } else {
-                    constexpr int UNITS_PER_ROW = (EPI == EPI_SWIGLU) ? BN / 8 : BN / 4;  // float4 groups
-                    const int units = (r1 - r0) * UNITS_PER_ROW;
-                    for (int u = et; u < units; u += EPI_THREADS) {
-                        const int r = r0 + u / UNITS_PER_ROW;
-                        const int c4 = (u % UNITS_PER_ROW) * 4;
-                        const int row = m_blk * (2 * BM) + (int)rank * BM + r;
-                        if (row >= g.M) continue;
-                        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-                        // partials in batches of 8 loads in flight, summed in chunk order
-                        const float *p0 = g.part + (size_t)(2 * first_pair + rank) * (BM * BN) + (size_t)r * BN + c4;
-                        constexpr size_t kPairStride = (size_t)2 * BM * BN;
-                        for (int j0 = 0; j0 < g.splits; j0 += 8) {
-                            float4 x[8], y[8];
-                            #pragma unroll
-                            for (int t = 0; t < 8; ++t) {
-                                if (j0 + t < g.splits) {
-                                    x[t] = __ldcg(reinterpret_cast<const float4 *>(p0 + (j0 + t) * kPairStride));
-                                    if constexpr (EPI == EPI_SWIGLU)
-                                        y[t] = __ldcg(reinterpret_cast<const float4 *>(p0 + (j0 + t) * kPairStride +
-                                                                                       BN / 2));
-                                }
-                            }
-                            #pragma unroll
-                            for (int t = 0; t < 8; ++t) {
-                                if (j0 + t < g.splits) {
-                                    a.x += x[t].x; a.y += x[t].y; a.z += x[t].z; a.w += x[t].w;
-                                    if constexpr (EPI == EPI_SWIGLU) {
-                                        b.x += y[t].x; b.y += y[t].y; b.z += y[t].z; b.w += y[t].w;
-                                    }
-                                }
-                            }
-                        }
-                        float f[4] = {a.x, a.y, a.z, a.w};
-                        int col;
-                        if constexpr (EPI == EPI_SWIGLU) {
-                            const float up[4] = {b.x, b.y, b.z, b.w};
-                            #pragma unroll
-                            for (int j = 0; j < 4; ++j) f[j] = f[j] / (1.0f + expf(-f[j])) * up[j];
-                            col = n_blk * (BN / 2) + c4;
-                        } else {
-                            col = n_blk * BN + c4;
-                            if constexpr (EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_DS) {
-                                const uint2 rv = *reinterpret_cast<const uint2 *>(g.R + (size_t)row * g.ldc + col);
-                                f[0] += bf16_lo(rv.x); f[1] += bf16_hi(rv.x); f[2] += bf16_lo(rv.y); f[3] += bf16_hi(rv.y);
-                            }
-                            if constexpr (EPI == EPI_RESIDUAL_DS) {
-                                int rank_ds = g.DS != nullptr ? g.vis_rank[row] : -1;
-                                if (rank_ds >= g.n_vis) rank_ds = -1;
-                                if (rank_ds >= 0) {
-                                    const uint2 dv = *reinterpret_cast<const uint2 *>(g.DS + (size_t)rank_ds * g.ldc + col);
-                                    f[0] = round_bf16(f[0]) + bf16_lo(dv.x); f[1] = round_bf16(f[1]) + bf16_hi(dv.x);
-                                    f[2] = round_bf16(f[2]) + bf16_lo(dv.y); f[3] = round_bf16(f[3]) + bf16_hi(dv.y);
-                                }
-                            }
-                        }
-                        uint2 o;
-                        o.x = pack_bf16x2(f[0], f[1]);
-                        o.y = pack_bf16x2(f[2], f[3]);
-                        *reinterpret_cast<uint2 *>(g.C + (size_t)row * g.ldc + col) = o;
-                    }
-                    }
-                }
-            }
-        }
+        if (et == 0) stamp(g, TR_DP_EPI_DONE);
     }
 
     tc_fence_before();
     cluster_sync();   // the peer no longer reads this CTA's shared memory or signals its barriers
+    if (threadIdx.x == 0) stamp(g, TR_END);
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, 512);
@@ -671,21 +762,28 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     g.status = p.status;
     g.wq = p.wq; g.wk = p.wk; g.cos_t = p.cos_t; g.sin_t = p.sin_t;
     g.head_dim = p.head_dim; g.nq = p.nq; g.nkv = p.nkv; g.eps = p.eps;
+    g.trace = p.trace;
     const int tiles = g.nm * g.nn;
     int pairs = p.num_sms / 2 < max_pairs ? p.num_sms / 2 : max_pairs;   // all pairs co-resident
     if (pairs < 1) pairs = 1;
-    // full waves data-parallel; the tiles of a partial last wave split along K over the idle pairs
+    // full waves data-parallel; the k-blocks of a partial last wave spread over all pairs (stream-K),
+    // at least kMinStreamKBlocks per pair; when that leaves one tile per pair it stays data-parallel
     const int left = tiles % pairs;
-    int splits = (p.part && p.flags && left) ? pairs / left : 1;
-    if (splits > g.nk / 2) splits = g.nk / 2;
-    if (splits > 32) splits = 32;
-    if (splits < 2) splits = 1;
-    g.splits = splits;
-    g.dp_tiles = splits > 1 ? tiles - left : tiles;
+    int sk_pairs = 0;
+    if (p.part && p.flags && left) {
+        const long long work = (long long)left * g.nk;
+        long long ps = work / kMinStreamKBlocks;
+        if (ps > pairs) ps = pairs;
+        if (ps > EPI_THREADS) ps = EPI_THREADS;   // one polling thread per contributor
+        if (ps > left) sk_pairs = (int)ps;
+    }
+    g.sk_pairs = sk_pairs;
+    g.sk_work = (long long)left * g.nk;
+    g.dp_tiles = sk_pairs ? tiles - left : tiles;
     g.part = p.part;
     g.flags = p.flags;
-    g.epoch = splits > 1 ? next_epoch() : 0u;
-    const int grid_pairs = splits > 1 ? pairs : (tiles < pairs ? tiles : pairs);
+    g.epoch = sk_pairs ? next_epoch() : 0u;
+    const int grid_pairs = g.dp_tiles >= pairs ? pairs : (sk_pairs > g.dp_tiles ? sk_pairs : g.dp_tiles);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * grid_pairs);
     cfg.blockDim = dim3(GEMM_THREADS);
@@ -715,11 +813,24 @@ bool make_tmap_rows(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t col
 }
 
 int gemm_box_rows_a() { return BM; }
-size_t gemm_workspace_bytes(int num_sms) { return (size_t)num_sms * BM * BN * sizeof(float) + 256 + (size_t)num_sms * 4; }
+// Stream-K partials: two 128 x 256 fp32 slots per CTA (a range covers parts of at most two tiles),
+// then one release flag per CTA.
+size_t gemm_flags_offset(int num_sms) { return (size_t)2 * num_sms * BM * BN * sizeof(float) + 256; }
+size_t gemm_workspace_bytes(int num_sms) { return gemm_flags_offset(num_sms) + (size_t)num_sms * 4; }
 int gemm_box_rows_w() { return BN / 2; }
 
-cudaError_t launch_gemm(const GemmPlan &p, cudaStream_t stream) {
-    if (p.M <= 0) return cudaSuccess;
+namespace {
+thread_local unsigned long long *t_trace_next = nullptr;
+}
+void gemm_trace_next(unsigned long long *trace) { t_trace_next = trace; }
+
+cudaError_t launch_gemm(const GemmPlan &p_in, cudaStream_t stream) {
+    if (p_in.M <= 0) return cudaSuccess;
+    GemmPlan p = p_in;
+    if (t_trace_next) {
+        p.trace = t_trace_next;
+        t_trace_next = nullptr;
+    }
     switch (p.epi) {
         case EPI_STORE: return launch_epi<EPI_STORE>(p, stream);
         case EPI_RESIDUAL: return launch_epi<EPI_RESIDUAL>(p, stream);

@@ -1,7 +1,7 @@
 // Projection GEMM for callers that cannot allocate device memory.
 //
-// h3enc_op_gemm needs a caller-allocated workspace for the K-split of its last
-// partial wave.  Some callers have no way to provide one: code that runs inside
+// h3enc_op_gemm needs a caller-allocated workspace for the stream-K split of its
+// last partial wave.  Some callers have no way to provide one: code that runs inside
 // another framework's allocator callback or after a memory pool has reserved the
 // whole device, plugins that are handed only input and output buffers, and hosts
 // that forbid cudaMalloc after start-up.  h3enc_op_gemm_noalloc runs the same
@@ -16,11 +16,11 @@
 
 namespace {
 
-// Partials of the split phase: one 128 x 256 fp32 slot per SM, then one flag per SM.
+// Partials of the stream-K phase: two 128 x 256 fp32 slots per SM, then one flag per SM.
 constexpr int kMaxSlots = 160;                                      // SMs the array is sized for
 constexpr size_t kSlotBytes = 128 * 256 * sizeof(float);            // 128 KiB
-constexpr size_t kFlagOffset = (size_t)kMaxSlots * kSlotBytes + 256;
-constexpr size_t kScratchBytes = kFlagOffset + (size_t)kMaxSlots * sizeof(uint32_t);  // 20 MiB + 896 B
+constexpr size_t kFlagOffset = (size_t)2 * kMaxSlots * kSlotBytes + 256;
+constexpr size_t kScratchBytes = kFlagOffset + (size_t)kMaxSlots * sizeof(uint32_t);  // 40 MiB + 896 B
 
 static __device__ __align__(256) unsigned char g_gemm_scratch[kScratchBytes];
 
@@ -93,13 +93,13 @@ H3ENC_API h3enc_status h3enc_op_gemm_noalloc(const void *A, const void *W, void 
         snprintf(g_error, sizeof g_error, "gemm_noalloc: cannot query the SM count");
         return H3ENC_ERR_CUDA;
     }
-    // the split needs one 128 KiB slot and one flag per SM: a device with more SMs than the array
-    // has slots needs more scratch than the array holds and is refused
+    // the split needs two 128 KiB slots and one flag per SM: a device with more SMs than the array
+    // is sized for needs more scratch than the array holds and is refused
     if (sms > kMaxSlots) {
         snprintf(g_error, sizeof g_error,
                  "gemm_noalloc: this device has %d SMs and needs %zu scratch bytes; the static scratch holds %zu "
                  "(%d SMs) - use h3enc_op_gemm with a workspace",
-                 sms, (size_t)sms * (kSlotBytes + sizeof(uint32_t)) + 256, kScratchBytes, kMaxSlots);
+                 sms, h3::gemm_workspace_bytes(sms), kScratchBytes, kMaxSlots);
         return H3ENC_ERR_UNSUPPORTED;
     }
     unsigned char *scratch = nullptr;

@@ -35,6 +35,7 @@ struct GemmPlan {
     const float *cos_t = nullptr, *sin_t = nullptr;   // [M, head_dim/2]
     int head_dim = 0, nq = 0, nkv = 0;
     float eps = 0.f;
+    unsigned long long *trace = nullptr;   // optional per-CTA phase timeline (11 stamps per CTA)
 };
 // Tensor map of a row-major bf16 matrix [rows, cols] read in boxes of
 // box_rows x 64 with 128-byte swizzle.  False if the driver refuses it.
@@ -43,7 +44,14 @@ int gemm_box_rows_a();
 int gemm_box_rows_w();
 // Bytes of a split workspace (partials then flags) for a grid of num_sms CTAs.
 size_t gemm_workspace_bytes(int num_sms);
+size_t gemm_flags_offset(int num_sms);   // byte offset of the release flags inside the workspace
 cudaError_t launch_gemm(const GemmPlan &p, cudaStream_t stream);
+// The next launch_gemm on this thread records its phase timeline into trace ([grid][11] %globaltimer ns).
+void gemm_trace_next(unsigned long long *trace);
+// The next launch_attention on this thread records a per-CTA timeline into trace
+// ([grid][attention_trace_fields()] entries).
+void attention_trace_next(unsigned long long *trace);
+int attention_trace_fields();
 
 // ---- norms and rotary embedding (norm_rope.cu)
 struct RopeParams {

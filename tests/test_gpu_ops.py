@@ -140,13 +140,26 @@ def _sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
+def _stream_k_shape(case, pairs):
+    """(M, N, K) of 256 x 256 tiles against `pairs` SM pairs:
+    tail4  one full wave + 4 tiles, each tile's k-blocks shared by whole pairs
+    span   one full wave + 40 tiles: pair ranges straddle two tiles
+    nodp   16 tiles, fewer than pairs: no data-parallel wave, ranges straddle tiles
+    few    16 tiles of 4 k-blocks: too little work to share, plain data-parallel"""
+    if case == "tail4":
+        return 4 * 256 - 37, (pairs // 4 + 1) * 256, 2048
+    if case == "span":
+        return 4 * 256 - 37, ((pairs + 40) // 4) * 256, 1280
+    if case == "nodp":
+        return 2 * 256 - 100, 8 * 256, 4096
+    return 2 * 256 - 100, 8 * 256, 256
+
+
+@pytest.mark.parametrize("case", ["tail4", "span", "nodp", "few"])
 @pytest.mark.parametrize("epi", [Q.EPI_STORE, Q.EPI_RESIDUAL, Q.EPI_SWIGLU])
-def test_gemm_split_last_wave(epi):
-    """tiles = SMs + a few: the partial last wave is split along K over all SMs."""
-    sms = _sms()
-    nm = 8
-    nn = sms // nm + 1                       # nm*nn just above the SM count
-    M, N, K = nm * 128 - 37, nn * 256, 2048  # ragged M inside the last m-block
+def test_gemm_split_last_wave(epi, case):
+    """Tiles of a partial last wave spread over all SM pairs (stream-K), M ragged inside the last m-block."""
+    M, N, K = _stream_k_shape(case, _sms() // 2)
     A, a = _bf16(30, "A", (M, K))
     ws = _workspace()
     if epi == Q.EPI_SWIGLU:
@@ -237,10 +250,10 @@ def test_rope_table(wl_id):
     assert np.max(np.abs(s.cpu().numpy() - rs[:, :h])) < 2e-6
 
 
-@pytest.mark.parametrize("d,nq,nkv,M,split", [(64, 4, 2, 97, False), (128, 64, 8, 300, False),
-                                                (128, 64, 8, 1024, True), (64, 8, 4, 1000, True)])
-def test_qkv_projection_with_fused_norm_rope(d, nq, nkv, M, split):
-    K = 512
+@pytest.mark.parametrize("d,nq,nkv,M,K,split", [(64, 4, 2, 97, 512, False), (128, 64, 8, 300, 512, False),
+                                                  (128, 64, 8, 1024, 512, True), (64, 8, 4, 1000, 512, True),
+                                                  (128, 64, 8, 1024, 5120, True), (64, 8, 4, 1000, 1344, True)])
+def test_qkv_projection_with_fused_norm_rope(d, nq, nkv, M, K, split):
     N = (nq + 2 * nkv) * d
     A, a = _bf16(22, "A", (M, K))
     Wt, w = _bf16(23, "Wqkv", (N, K), sigma=0.05)
