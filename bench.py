@@ -26,6 +26,9 @@ sys.path.insert(0, ROOT)
 
 WORKLOAD_ID = 2
 GEMM_GU_CLASS = "gemm_gate_up"
+# DRAM bytes (read + write) of one gate/up launch at seq 1024, from the ncu capture in
+# profiles/gemm_gate_up_seq1024_ncu.md (same kernel source as this build).
+GATE_UP_TRAFFIC_BYTES = 650.6e6
 
 
 def _peaks():
@@ -380,7 +383,7 @@ def main():
         "tflops": flops * args.steps / (ms / 1e3) / 1e12,
         "roofline": {"kernel": "gemm_tcgen05 gate/up + SwiGLU", "bound": "tensor", "achieved": gu_achieved,
                      "peak": sustained, "unit": "TFLOP/s", "frac": gu_achieved / sustained,
-                     "peak_source": f"{peak_src} bf16_tflops_sustained", "traffic": None},
+                     "peak_source": f"{peak_src} bf16_tflops_sustained", "traffic": GATE_UP_TRAFFIC_BYTES},
         "kernel_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
         "kernel_ms_note": "separate pass with an event pair around every launch",
         "gpu_launches": int(launches),
