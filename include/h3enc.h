@@ -80,6 +80,12 @@ typedef struct {
     int32_t max_tokens;     /* largest S of one encode (workspace sizing) */
     int32_t max_seqs;       /* largest number of packed sequences, <= 1024 */
     int32_t num_deepstack;  /* largest number of DeepStack levels accepted */
+    int32_t linear_fp8;     /* 1: online FP8 linears (page "vllm-omni ... encoder.py",
+                               _validate_encoder_quant_config: the bf16 checkpoint is
+                               quantised at h3enc_finalize_weights to e4m3 with one fp32
+                               scale per output channel, activations to e4m3 with one
+                               scale per token on every encode; attention stays bf16).
+                               0: plain bf16.  The bf16 weights stay loaded. */
 } h3enc_config;
 
 typedef struct h3enc h3enc;
@@ -218,7 +224,7 @@ enum {
     H3ENC_K_PREP = 0,     /* embedding gather / input copy, M-RoPE tables, visual ranks */
     H3ENC_K_RMSNORM = 1,
     H3ENC_K_GEMM_QKV = 2,
-    H3ENC_K_QK_ROPE = 3,  /* unused: the q/k norm + RoPE runs inside the QKV projection */
+    H3ENC_K_QUANT = 3,    /* FP8 mode: e4m3 quantisation of the attention and SwiGLU outputs */
     H3ENC_K_ATTN = 4,
     H3ENC_K_GEMM_O = 5,
     H3ENC_K_GEMM_GATE_UP = 6,

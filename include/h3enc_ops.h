@@ -110,6 +110,30 @@ H3ENC_API const char *h3enc_op_gemm_noalloc_last_error(void);
 H3ENC_API h3enc_status h3enc_op_pack_gate_up(const void *gate, const void *up, void *W, int32_t I, int32_t K,
                                    void *stream);
 
+/* Online-FP8 projection (page "vllm-omni ... encoder.py",
+ * _validate_encoder_quant_config and the _is_quantized_linear branches): as
+ * h3enc_op_gemm with e4m3 operands A [M, K] and W [N, K] (one byte per element,
+ * row-major, 16-byte aligned, K % 16 == 0), their fp32 scales sa [M] (per row of
+ * A) and sw [N] (per row of W, 16-byte aligned): the product is
+ * (A * sa) (W * sw)^T accumulated in fp32 on the tensor cores, then the same
+ * epilogues (STORE, RESIDUAL, SWIGLU, RESIDUAL_DS) and the same workspace rules. */
+H3ENC_API h3enc_status h3enc_op_gemm_fp8(const void *A, const void *W, const float *sa, const float *sw, void *C,
+                               int32_t M, int32_t N, int32_t K, int32_t epilogue, const void *R, const void *DS,
+                               const int32_t *vis_rank, int32_t n_vis, void *workspace, int64_t workspace_bytes,
+                               int32_t *status, void *stream);
+
+/* Per-row e4m3 quantisation of a bf16 matrix x [rows, cols] (cols % 8 == 0):
+ * scale[r] = amax(row r) / 448 in fp32 (1 for an all-zero row), q = e4m3(x / scale)
+ * with the division in fp32, rounded to nearest even, saturating at +-448
+ * (the "fn" variant).  q [rows, cols] bytes; x 16-byte aligned. */
+H3ENC_API h3enc_status h3enc_op_quant_rows(const void *x, int32_t rows, int32_t cols, void *q, float *scale,
+                                 void *stream);
+
+/* RMSNorm of x [rows, cols] (as h3enc_op_rmsnorm, output rounded to bf16) followed
+ * by h3enc_op_quant_rows of that bf16 output: q [rows, cols] e4m3, scale [rows]. */
+H3ENC_API h3enc_status h3enc_op_rmsnorm_q8(const void *x, const void *w, void *q, float *scale, int32_t rows,
+                                 int32_t cols, float eps, void *stream);
+
 /* y = bf16(w * x / sqrt(mean(x^2) + eps)) per row, fp32 math (page "...
  * encoder.py", MiniMaxH3Qwen3VLRMSNorm).  x, y [rows, cols]; cols % 8 == 0,
  * cols <= 8192; y may equal x. */

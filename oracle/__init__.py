@@ -16,3 +16,4 @@ on random weights, whose output has no independent value to compare with
 ("parity unpinned" beyond the per-step pins and the structural invariants).
 """
 from .qwen3vl_text import *  # noqa: F401,F403
+from . import fp8  # noqa: F401  (online-FP8 linears)

@@ -209,7 +209,7 @@ def _store(t: np.ndarray, point: str, storage) -> np.ndarray:
 
 
 def decoder_layer(x: np.ndarray, w: LayerWeights, cos: np.ndarray, sin: np.ndarray, cfg,
-                  cu_seqlens=None, storage=None) -> np.ndarray:
+                  cu_seqlens=None, storage=None, fp8=False) -> np.ndarray:
     """One decoder layer (page 1, ``MiniMaxH3Qwen3VLTextDecoderLayer.forward``).
 
     residual = x; y = input_layernorm(x); attention; x = residual + attn;
@@ -224,29 +224,37 @@ def decoder_layer(x: np.ndarray, w: LayerWeights, cos: np.ndarray, sin: np.ndarr
     "attn" (attention output),
     "act" (SwiGLU output), "h" (residual stream).  With all of them this is the
     rounding floor of a pipeline that keeps exactly those tensors in bf16.
+
+    ``fp8`` runs the four projections as online-FP8 linears (``oracle.fp8``):
+    the packed QKV and gate/up projections of the quantised branch are, per output
+    channel, the same as the separate q/k/v and gate/up products computed here.
     """
+    if fp8:
+        from .fp8 import fp8_linear as lin
+    else:
+        lin = linear
     s = x.shape[0]
     d, nq, nkv = cfg.head_dim, cfg.n_heads, cfg.n_kv_heads
     residual = x
     y = _store(rms_norm(x, w["input_layernorm"], cfg.rms_eps), "y", storage)
-    q = _store(linear(y, w["q_proj"]), "qk_proj", storage).reshape(s, nq, d)
-    k = _store(linear(y, w["k_proj"]), "qk_proj", storage).reshape(s, nkv, d)
-    v = _store(linear(y, w["v_proj"]), "v", storage).reshape(s, nkv, d)
+    q = _store(lin(y, w["q_proj"]), "qk_proj", storage).reshape(s, nq, d)
+    k = _store(lin(y, w["k_proj"]), "qk_proj", storage).reshape(s, nkv, d)
+    v = _store(lin(y, w["v_proj"]), "v", storage).reshape(s, nkv, d)
     q = rms_norm(q, w["q_norm"], cfg.rms_eps)
     k = rms_norm(k, w["k_norm"], cfg.rms_eps)
     q = _store(apply_rope(q, cos, sin), "qk", storage)
     k = _store(apply_rope(k, cos, sin), "qk", storage)
     attn = _store(causal_gqa_attention(q, k, v, cu_seqlens), "attn", storage)
-    x = _store(residual + linear(attn, w["o_proj"]), "h", storage)
+    x = _store(residual + lin(attn, w["o_proj"]), "h", storage)
     residual = x
     y = _store(rms_norm(x, w["post_attention_layernorm"], cfg.rms_eps), "y", storage)
-    act = _store(silu(linear(y, w["gate_proj"])) * linear(y, w["up_proj"]), "act", storage)
-    return _store(residual + linear(act, w["down_proj"]), "h", storage)
+    act = _store(silu(lin(y, w["gate_proj"])) * lin(y, w["up_proj"]), "act", storage)
+    return _store(residual + lin(act, w["down_proj"]), "h", storage)
 
 
 def forward(inputs_embeds: np.ndarray, positions: np.ndarray, cfg, get_layer,
             visual_mask=None, deepstack=None, cu_seqlens=None, layers=None,
-            capture=None, dtype=np.float32, storage=None) -> np.ndarray:
+            capture=None, dtype=np.float32, storage=None, fp8=False) -> np.ndarray:
     """Text-model forward returning the unnormalised last hidden state.
 
     Page 1, ``MiniMaxH3Qwen3VLTextModel.forward``: cos/sin computed once from
@@ -257,14 +265,15 @@ def forward(inputs_embeds: np.ndarray, positions: np.ndarray, cfg, get_layer,
     ``LayerWeights``; ``layers`` (default ``range(cfg.num_layers)``) allows a
     sub-range with global layer indices; ``capture`` (a list) receives the
     state after every layer; ``storage`` as in ``decoder_layer`` (the
-    DeepStack sum is a residual-stream hand-over, point "h").
+    DeepStack sum is a residual-stream hand-over, point "h"); ``fp8`` as in
+    ``decoder_layer``.
     """
     x = np.asarray(inputs_embeds, dtype=dtype)
     cos, sin = rope_cos_sin(positions, cfg.head_dim, cfg.rope_theta, cfg.mrope_section, dtype)
     if layers is None:
         layers = range(cfg.num_layers)
     for l in layers:
-        x = decoder_layer(x, get_layer(l), cos, sin, cfg, cu_seqlens, storage)
+        x = decoder_layer(x, get_layer(l), cos, sin, cfg, cu_seqlens, storage, fp8)
         if deepstack is not None and l < len(deepstack):
             x = _store(deepstack_add(x, visual_mask, np.asarray(deepstack[l], dtype=dtype)), "h", storage)
         if capture is not None:

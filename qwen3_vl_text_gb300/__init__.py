@@ -18,7 +18,8 @@ __all__ = [
     "h3enc_encode_host", "h3enc_set_layer_capture", "h3enc_get_status", "h3enc_last_error", "h3enc_destroy",
     "h3enc_set_profiling", "h3enc_set_profiling_classes", "h3enc_get_profile", "h3enc_launch_count", "h3enc_num_sms",
     "h3enc_build_positions", "h3enc_aggregate_deepstack",
-    "h3enc_op_gemm", "h3enc_op_gemm_workspace_bytes", "h3enc_op_gemm_trace_next", "h3enc_op_attention_trace_next", "h3enc_op_gemm_noalloc", "h3enc_op_gemm_noalloc_scratch_bytes", "h3enc_op_pack_gate_up", "h3enc_op_rmsnorm", "h3enc_op_rope_table",
+    "h3enc_op_gemm", "h3enc_op_gemm_workspace_bytes", "h3enc_op_gemm_trace_next", "h3enc_op_attention_trace_next", "h3enc_op_gemm_noalloc", "h3enc_op_gemm_noalloc_scratch_bytes", "h3enc_op_pack_gate_up", "h3enc_op_rmsnorm", "h3enc_op_gemm_fp8", "h3enc_op_quant_rows",
+    "h3enc_op_rmsnorm_q8", "h3enc_op_rope_table",
     "h3enc_op_gemm_qkv_rope", "h3enc_op_attention", "h3enc_op_embed", "h3enc_op_vis_rank", "Encoder",
     "KERNEL_CLASSES",
 ]
@@ -30,7 +31,7 @@ STATUS = {0: "OK", 1: "WARN_IGNORED", 2: "ERR_INVALID_ARG", 3: "ERR_SHAPE", 4: "
           5: "ERR_MISSING_WEIGHTS", 6: "ERR_UNSUPPORTED", 7: "ERR_CUDA", 8: "ERR_OOM",
           9: "ERR_DEVICE_TIMEOUT", 10: "ERR_DEVICE_BOUNDS"}
 EPI_STORE, EPI_RESIDUAL, EPI_SWIGLU, EPI_RESIDUAL_DS = 0, 1, 2, 3
-KERNEL_CLASSES = ["prep", "rmsnorm", "gemm_qkv", "qk_rope", "attention", "gemm_o", "gemm_gate_up", "gemm_down"]
+KERNEL_CLASSES = ["prep", "rmsnorm", "gemm_qkv", "quant", "attention", "gemm_o", "gemm_gate_up", "gemm_down"]
 
 
 class H3encError(RuntimeError):
@@ -44,7 +45,7 @@ class Config(ctypes.Structure):
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("intermediate", ctypes.c_int32),
                 ("vocab", ctypes.c_int32), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
                 ("mrope_section", ctypes.c_int32 * 3), ("max_tokens", ctypes.c_int32),
-                ("max_seqs", ctypes.c_int32), ("num_deepstack", ctypes.c_int32)]
+                ("max_seqs", ctypes.c_int32), ("num_deepstack", ctypes.c_int32), ("linear_fp8", ctypes.c_int32)]
 
 
 def _load():
@@ -85,6 +86,9 @@ _SIGS = {
     "h3enc_op_gemm_noalloc_last_error": ([], ctypes.c_char_p),
     "h3enc_op_pack_gate_up": ([_P, _P, _P, _I32, _I32, _P], _I32),
     "h3enc_op_rmsnorm": ([_P, _P, _P, _I32, _I32, _F, _P], _I32),
+    "h3enc_op_gemm_fp8": ([_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _I64, _P, _P], _I32),
+    "h3enc_op_quant_rows": ([_P, _I32, _I32, _P, _P, _P], _I32),
+    "h3enc_op_rmsnorm_q8": ([_P, _P, _P, _P, _I32, _I32, _F, _P], _I32),
     "h3enc_op_rope_table": ([_P, _I32, _I32, _F, ctypes.POINTER(_I32), _P, _P, _P], _I32),
     "h3enc_op_gemm_qkv_rope": ([_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _F, _P, _P, _P, _I64, _P, _P],
                                _I32),
@@ -309,6 +313,24 @@ def h3enc_op_pack_gate_up(gate, up, W, I, K, stream=None):
     return _check(lib.h3enc_op_pack_gate_up(_ptr(gate), _ptr(up), _ptr(W), I, K, _stream(stream)))
 
 
+def h3enc_op_gemm_fp8(A, W, sa, sw, C, M, N, K, epilogue, R=None, DS=None, vis_rank=None, n_vis=0, workspace=None,
+                      status=None, stream=None):
+    """e4m3 projection: C = epilogue((A * sa) (W * sw)^T); A [M,K] and W [N,K] uint8 e4m3 bytes,
+    sa [M] and sw [N] float32."""
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return _check(lib.h3enc_op_gemm_fp8(_ptr(A), _ptr(W), _ptr(sa), _ptr(sw), _ptr(C), M, N, K, epilogue, _ptr(R),
+                                        _ptr(DS), _ptr(vis_rank), n_vis, _ptr(workspace), wbytes, _ptr(status),
+                                        _stream(stream)))
+
+
+def h3enc_op_quant_rows(x, rows, cols, q, scale, stream=None):
+    return _check(lib.h3enc_op_quant_rows(_ptr(x), rows, cols, _ptr(q), _ptr(scale), _stream(stream)))
+
+
+def h3enc_op_rmsnorm_q8(x, w, q, scale, rows, cols, eps, stream=None):
+    return _check(lib.h3enc_op_rmsnorm_q8(_ptr(x), _ptr(w), _ptr(q), _ptr(scale), rows, cols, eps, _stream(stream)))
+
+
 def h3enc_op_rmsnorm(x, w, y, rows, cols, eps, stream=None):
     return _check(lib.h3enc_op_rmsnorm(_ptr(x), _ptr(w), _ptr(y), rows, cols, eps, _stream(stream)))
 
@@ -349,13 +371,14 @@ class Encoder:
     config attributes (num_layers, hidden, n_heads, n_kv_heads, head_dim,
     intermediate, vocab, rms_eps, rope_theta, mrope_section)."""
 
-    def __init__(self, model, max_tokens: int, max_seqs: int = 64, num_deepstack: int = 3):
+    def __init__(self, model, max_tokens: int, max_seqs: int = 64, num_deepstack: int = 3, fp8: bool = False):
         c = Config()
         c.num_layers, c.hidden, c.n_heads = model.num_layers, model.hidden, model.n_heads
         c.n_kv_heads, c.head_dim, c.intermediate = model.n_kv_heads, model.head_dim, model.intermediate
         c.vocab, c.rms_eps, c.rope_theta = model.vocab, model.rms_eps, model.rope_theta
         c.mrope_section = (ctypes.c_int32 * 3)(*model.mrope_section)
         c.max_tokens, c.max_seqs, c.num_deepstack = max_tokens, max_seqs, num_deepstack
+        c.linear_fp8 = 1 if fp8 else 0
         self.model = model
         self.handle = h3enc_create(c)
 

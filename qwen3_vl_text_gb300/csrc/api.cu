@@ -62,6 +62,18 @@ struct h3enc {
     uint8_t *st_mask = nullptr;
     bf16 *st_ds = nullptr, *st_out = nullptr;
     CUtensorMap tm_y, tm_attn, tm_act;
+    // online FP8 (linear_fp8): e4m3 copies of the four projections with per-row scales, e4m3
+    // activations with per-token scales
+    struct Layer8 {
+        uint8_t *qkv, *o, *gu, *down;
+        float *s_qkv, *s_o, *s_gu, *s_down;
+        CUtensorMap tm_qkv, tm_o, tm_gu, tm_down;
+    };
+    char *arena8 = nullptr, *ws8 = nullptr;
+    std::vector<Layer8> layers8;
+    uint8_t *y8 = nullptr, *attn8 = nullptr, *act8 = nullptr;
+    float *sy = nullptr, *sattn = nullptr, *sact = nullptr;
+    CUtensorMap tm_y8, tm_attn8, tm_act8;
     bool finalized = false;
     std::string err;
     std::vector<void *> capture;
@@ -133,6 +145,8 @@ h3enc_status validate_config(const h3enc_config *c) {
         return fail(nullptr, H3ENC_ERR_INVALID_ARG, "config: rms_eps and rope_theta must be > 0");
     if (c->mrope_section[0] < 0 || c->mrope_section[1] < 0 || c->mrope_section[2] < 0)
         return fail(nullptr, H3ENC_ERR_INVALID_ARG, "config: negative mrope_section");
+    if (c->linear_fp8 != 0 && c->linear_fp8 != 1)
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "config: linear_fp8 must be 0 or 1");
     if (c->head_dim != 64 && c->head_dim != 128)
         return fail(nullptr, H3ENC_ERR_UNSUPPORTED, "config: head_dim %d not in {64, 128}", c->head_dim);
     if (c->n_heads % c->n_kv_heads)
@@ -214,6 +228,86 @@ h3enc_status check_encode_args(h3enc *h, const void *positions, const uint8_t *m
     return check_seqs(h, cu, n_seqs, S);
 }
 
+// Online FP8: the e4m3 weight arena (four projections per layer + per-row scales) and
+// the e4m3 activation workspace with per-token scales.
+h3enc_status create_fp8(h3enc *h) {
+    const h3enc_config &c = h->cfg;
+    const size_t H = c.hidden, QO = h->qkv_out, AO = (size_t)c.n_heads * c.head_dim, I = c.intermediate;
+    const size_t b_qkv = align256(QO * H), b_o = align256(H * AO), b_gu = align256(2 * I * H),
+                 b_down = align256(H * I), s_qkv = align256(QO * 4), s_o = align256(H * 4),
+                 s_gu = align256(2 * I * 4), s_down = align256(H * 4);
+    const size_t per = b_qkv + b_o + b_gu + b_down + s_qkv + s_o + s_gu + s_down;
+    cudaError_t e = cudaMalloc(&h->arena8, per * (size_t)c.num_layers);
+    if (e != cudaSuccess)
+        return fail(h, H3ENC_ERR_OOM, "FP8 weight arena of %zu bytes: %s", per * (size_t)c.num_layers,
+                    cudaGetErrorString(e));
+    h->layers8.resize(c.num_layers);
+    char *p = h->arena8;
+    for (auto &w : h->layers8) {
+        w.qkv = reinterpret_cast<uint8_t *>(p); p += b_qkv;
+        w.o = reinterpret_cast<uint8_t *>(p); p += b_o;
+        w.gu = reinterpret_cast<uint8_t *>(p); p += b_gu;
+        w.down = reinterpret_cast<uint8_t *>(p); p += b_down;
+        w.s_qkv = reinterpret_cast<float *>(p); p += s_qkv;
+        w.s_o = reinterpret_cast<float *>(p); p += s_o;
+        w.s_gu = reinterpret_cast<float *>(p); p += s_gu;
+        w.s_down = reinterpret_cast<float *>(p); p += s_down;
+    }
+    const size_t T = c.max_tokens;
+    const size_t b_y = align256(T * H), b_a = align256(T * AO), b_act = align256(T * I), b_s = align256(T * 4);
+    const size_t wsz = b_y + b_a + b_act + 3 * b_s;
+    e = cudaMalloc(&h->ws8, wsz);
+    if (e != cudaSuccess) return fail(h, H3ENC_ERR_OOM, "FP8 workspace of %zu bytes: %s", wsz, cudaGetErrorString(e));
+    p = h->ws8;
+    h->y8 = reinterpret_cast<uint8_t *>(p); p += b_y;
+    h->attn8 = reinterpret_cast<uint8_t *>(p); p += b_a;
+    h->act8 = reinterpret_cast<uint8_t *>(p); p += b_act;
+    h->sy = reinterpret_cast<float *>(p); p += b_s;
+    h->sattn = reinterpret_cast<float *>(p); p += b_s;
+    h->sact = reinterpret_cast<float *>(p);
+    e = cudaMemset(h->ws8, 0, wsz);
+    if (e != cudaSuccess) return fail(h, H3ENC_ERR_CUDA, "FP8 workspace clear: %s", cudaGetErrorString(e));
+    const uint32_t ba = (uint32_t)h3::gemm_box_rows_a();
+    if (!h3::make_tmap_rows_e4m3(&h->tm_y8, h->y8, T, H, ba) ||
+        !h3::make_tmap_rows_e4m3(&h->tm_attn8, h->attn8, T, AO, ba) ||
+        !h3::make_tmap_rows_e4m3(&h->tm_act8, h->act8, T, I, ba))
+        return fail(h, H3ENC_ERR_CUDA, "cuTensorMapEncodeTiled refused an FP8 workspace operand");
+    return H3ENC_OK;
+}
+
+// Quantise the loaded bf16 projections of every layer (one scale per output row).
+h3enc_status finalize_fp8(h3enc *h) {
+    const h3enc_config &c = h->cfg;
+    const int H = c.hidden, QO = h->qkv_out, AO = c.n_heads * c.head_dim, I = c.intermediate;
+    cudaError_t e = cudaDeviceSynchronize();   // weight uploads issued on other streams have landed
+    if (e != cudaSuccess) return cuda_fail(h, e, "FP8 weight quantisation (sync)");
+    cudaStream_t st;
+    e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cuda_fail(h, e, "FP8 weight quantisation (stream)");
+    const uint32_t bw = (uint32_t)h3::gemm_box_rows_w();
+    for (int l = 0; l < c.num_layers && e == cudaSuccess; ++l) {
+        LayerW &w = h->layers[l];
+        h3enc::Layer8 &q = h->layers8[l];
+        e = h3::launch_quant_rows(w.qkv, H, QO, H, q.qkv, H, q.s_qkv, st);
+        if (e == cudaSuccess) e = h3::launch_quant_rows(w.o, AO, H, AO, q.o, AO, q.s_o, st);
+        if (e == cudaSuccess) e = h3::launch_quant_rows(w.gu, H, 2 * I, H, q.gu, H, q.s_gu, st);
+        if (e == cudaSuccess) e = h3::launch_quant_rows(w.down, I, H, I, q.down, I, q.s_down, st);
+        if (e == cudaSuccess &&
+            (!h3::make_tmap_rows_e4m3(&q.tm_qkv, q.qkv, QO, H, bw) || !h3::make_tmap_rows_e4m3(&q.tm_o, q.o, H, AO, bw) ||
+             !h3::make_tmap_rows_e4m3(&q.tm_gu, q.gu, 2 * (size_t)I, H, bw) ||
+             !h3::make_tmap_rows_e4m3(&q.tm_down, q.down, H, I, bw))) {
+            cudaStreamDestroy(st);
+            return fail(h, H3ENC_ERR_CUDA, "cuTensorMapEncodeTiled refused an FP8 weight operand");
+        }
+    }
+    const cudaError_t e2 = cudaStreamSynchronize(st);
+    cudaStreamDestroy(st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "FP8 weight quantisation");
+    if (e2 != cudaSuccess) return cuda_fail(h, e2, "FP8 weight quantisation");
+    return H3ENC_OK;
+}
+
+
 h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int lb, int le, const int32_t *pos,
                          const uint8_t *mask, const bf16 *ds, int nds, int n_vis, const int32_t *cu, int n_seqs,
                          int S, bf16 *out, cudaStream_t st, const bf16 *visual_embeds = nullptr) {
@@ -246,10 +340,16 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         });
         if (e != cudaSuccess) return cuda_fail(h, e, "visual embedding merge");
     }
+    const bool f8 = c.linear_fp8 != 0;
+    const int AO = nq * d;
     for (int l = lb; l < le; ++l) {
         LayerW &w = h->layers[l];
-        e = run(h, H3ENC_K_RMSNORM, st,
-                [&] { return h3::launch_rmsnorm(out, w.in_norm, h->y, S, H, c.rms_eps, st); });
+        h3enc::Layer8 *w8 = f8 ? &h->layers8[l] : nullptr;
+        // input_layernorm (FP8: its bf16 output quantised per token in the same kernel)
+        e = run(h, H3ENC_K_RMSNORM, st, [&] {
+            return f8 ? h3::launch_rmsnorm_q8(out, w.in_norm, h->y8, h->sy, S, H, c.rms_eps, st)
+                      : h3::launch_rmsnorm(out, w.in_norm, h->y, S, H, c.rms_eps, st);
+        });
         if (e != cudaSuccess) return cuda_fail(h, e, "input_layernorm");
         h3::GemmPlan p{};
         p.num_sms = h->num_sms;
@@ -257,8 +357,13 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         p.part = h->gemm_part;
         p.flags = h->gemm_flags;
         p.M = S;
+        p.fp8 = f8;
         // QKV projection with q_norm/k_norm and M-RoPE fused into the epilogue
-        p.tmA = &h->tm_y; p.tmW = &w.tm_qkv; p.N = h->qkv_out; p.K = H; p.epi = h3::EPI_QKROPE;
+        p.tmA = f8 ? &h->tm_y8 : &h->tm_y;
+        p.tmW = f8 ? &w8->tm_qkv : &w.tm_qkv;
+        p.sa = f8 ? h->sy : nullptr;
+        p.sw = f8 ? w8->s_qkv : nullptr;
+        p.N = h->qkv_out; p.K = H; p.epi = h3::EPI_QKROPE;
         p.C = h->qkv; p.ldc = h->qkv_out;
         p.wq = w.q_norm; p.wk = w.k_norm; p.cos_t = h->cos_t; p.sin_t = h->sin_t;
         p.head_dim = d; p.nq = nq; p.nkv = nkv; p.eps = c.rms_eps;
@@ -267,19 +372,44 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         e = run(h, H3ENC_K_ATTN, st,
                 [&] { return h3::launch_attention(h->qkv, h->attn, S, nq, nkv, d, cu, n_seqs, h->status, st); });
         if (e != cudaSuccess) return cuda_fail(h, e, "attention");
+        if (f8) {
+            e = run(h, H3ENC_K_QUANT, st, [&] {
+                return h3::launch_quant_rows(h->attn, AO, S, AO, h->attn8, AO, h->sattn, st);
+            });
+            if (e != cudaSuccess) return cuda_fail(h, e, "attention output quantisation");
+        }
         p.wq = p.wk = nullptr; p.cos_t = p.sin_t = nullptr;
-        p.tmA = &h->tm_attn; p.tmW = &w.tm_o; p.N = H; p.K = nq * d; p.epi = h3::EPI_RESIDUAL;
+        p.tmA = f8 ? &h->tm_attn8 : &h->tm_attn;
+        p.tmW = f8 ? &w8->tm_o : &w.tm_o;
+        p.sa = f8 ? h->sattn : nullptr;
+        p.sw = f8 ? w8->s_o : nullptr;
+        p.N = H; p.K = AO; p.epi = h3::EPI_RESIDUAL;
         p.C = out; p.ldc = H; p.R = out;
         e = run(h, H3ENC_K_GEMM_O, st, [&] { return h3::launch_gemm(p, st); });
         if (e != cudaSuccess) return cuda_fail(h, e, "o_proj gemm");
-        e = run(h, H3ENC_K_RMSNORM, st,
-                [&] { return h3::launch_rmsnorm(out, w.post_norm, h->y, S, H, c.rms_eps, st); });
+        e = run(h, H3ENC_K_RMSNORM, st, [&] {
+            return f8 ? h3::launch_rmsnorm_q8(out, w.post_norm, h->y8, h->sy, S, H, c.rms_eps, st)
+                      : h3::launch_rmsnorm(out, w.post_norm, h->y, S, H, c.rms_eps, st);
+        });
         if (e != cudaSuccess) return cuda_fail(h, e, "post_attention_layernorm");
-        p.tmA = &h->tm_y; p.tmW = &w.tm_gu; p.N = 2 * I; p.K = H; p.epi = h3::EPI_SWIGLU;
+        p.tmA = f8 ? &h->tm_y8 : &h->tm_y;
+        p.tmW = f8 ? &w8->tm_gu : &w.tm_gu;
+        p.sa = f8 ? h->sy : nullptr;
+        p.sw = f8 ? w8->s_gu : nullptr;
+        p.N = 2 * I; p.K = H; p.epi = h3::EPI_SWIGLU;
         p.C = h->act; p.ldc = I; p.R = nullptr;
         e = run(h, H3ENC_K_GEMM_GATE_UP, st, [&] { return h3::launch_gemm(p, st); });
         if (e != cudaSuccess) return cuda_fail(h, e, "gate/up gemm");
-        p.tmA = &h->tm_act; p.tmW = &w.tm_down; p.N = H; p.K = I; p.C = out; p.ldc = H; p.R = out;
+        if (f8) {
+            e = run(h, H3ENC_K_QUANT, st,
+                    [&] { return h3::launch_quant_rows(h->act, I, S, I, h->act8, I, h->sact, st); });
+            if (e != cudaSuccess) return cuda_fail(h, e, "SwiGLU output quantisation");
+        }
+        p.tmA = f8 ? &h->tm_act8 : &h->tm_act;
+        p.tmW = f8 ? &w8->tm_down : &w.tm_down;
+        p.sa = f8 ? h->sact : nullptr;
+        p.sw = f8 ? w8->s_down : nullptr;
+        p.N = H; p.K = I; p.C = out; p.ldc = H; p.R = out;
         if (use_ds && l < nds) {
             p.epi = h3::EPI_RESIDUAL_DS;
             p.DS = ds + (size_t)l * n_vis * H;
@@ -375,6 +505,14 @@ h3enc_status h3enc_create(const h3enc_config *cfg, h3enc **out) {
     if (e != cudaSuccess) {
         h3enc_destroy(h);
         return fail(nullptr, H3ENC_ERR_CUDA, "workspace clear: %s", cudaGetErrorString(e));
+    }
+    if (c.linear_fp8) {
+        h3enc_status s8 = create_fp8(h);
+        if (s8 != H3ENC_OK) {
+            const std::string msg = h->err;
+            h3enc_destroy(h);
+            return fail(nullptr, s8, "%s", msg.c_str());
+        }
     }
     const uint32_t ba = (uint32_t)h3::gemm_box_rows_a();
     if (!h3::make_tmap_rows(&h->tm_y, h->y, T, H, ba) ||
@@ -502,6 +640,10 @@ h3enc_status h3enc_finalize_weights(h3enc *h) {
             !h3::make_tmap_rows(&w.tm_down, w.down, H, c.intermediate, bw))
             return fail(h, H3ENC_ERR_CUDA, "cuTensorMapEncodeTiled refused a weight operand");
     }
+    if (c.linear_fp8) {
+        h3enc_status s8 = finalize_fp8(h);
+        if (s8 != H3ENC_OK) return s8;
+    }
     h->finalized = true;
     return H3ENC_OK;
 }
@@ -615,6 +757,8 @@ const char *h3enc_last_error(const h3enc *h) { return h ? h->err.c_str() : g_cre
 void h3enc_destroy(h3enc *h) {
     if (!h) return;
     for (cudaEvent_t ev : h->ev_pool) cudaEventDestroy(ev);
+    if (h->ws8) cudaFree(h->ws8);
+    if (h->arena8) cudaFree(h->arena8);
     if (h->ws) cudaFree(h->ws);
     if (h->arena) cudaFree(h->arena);
     delete h;
@@ -734,6 +878,62 @@ h3enc_status h3enc_op_pack_gate_up(const void *gate, const void *up, void *W, in
         e = h3::pack_gate_up_rows(static_cast<const bf16 *>(up), static_cast<bf16 *>(W), I, K, 1,
                                   cudaMemcpyDeviceToDevice, st);
     return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "pack gate/up");
+}
+
+h3enc_status h3enc_op_gemm_fp8(const void *A, const void *W, const float *sa, const float *sw, void *C, int32_t M,
+                               int32_t N, int32_t K, int32_t epilogue, const void *R, const void *DS,
+                               const int32_t *vis_rank, int32_t n_vis, void *workspace, int64_t workspace_bytes,
+                               int32_t *status, void *stream) {
+    if (M < 0 || N <= 0 || K <= 0 || N % 256 || K % 16 || epilogue < 0 || epilogue > 3)
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm_fp8: bad sizes or epilogue");
+    if (M == 0) return H3ENC_OK;
+    if (!A || !W || !sa || !sw || !C || ((epilogue == H3ENC_EPI_RESIDUAL || epilogue == H3ENC_EPI_RESIDUAL_DS) && !R) ||
+        (epilogue == H3ENC_EPI_RESIDUAL_DS && DS && !vis_rank) || (reinterpret_cast<uintptr_t>(sw) & 15))
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm_fp8: NULL operand or sw not 16-byte aligned");
+    CUtensorMap ta, tw;
+    if (!h3::make_tmap_rows_e4m3(&ta, A, M, K, h3::gemm_box_rows_a()) ||
+        !h3::make_tmap_rows_e4m3(&tw, W, N, K, h3::gemm_box_rows_w()))
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm_fp8: operands not 16-byte aligned or driver refused the map");
+    h3::GemmPlan p{};
+    p.tmA = &ta; p.tmW = &tw; p.M = M; p.N = N; p.K = K; p.epi = epilogue;
+    p.fp8 = true; p.sa = sa; p.sw = sw;
+    p.C = static_cast<bf16 *>(C);
+    p.ldc = epilogue == H3ENC_EPI_SWIGLU ? N / 2 : N;
+    p.R = static_cast<const bf16 *>(R);
+    p.DS = static_cast<const bf16 *>(DS);
+    p.vis_rank = vis_rank;
+    p.n_vis = n_vis;
+    p.status = status;
+    p.num_sms = h3::device_num_sms();
+    if (workspace) {
+        if (workspace_bytes < (int64_t)h3::gemm_workspace_bytes(p.num_sms) ||
+            (reinterpret_cast<uintptr_t>(workspace) & 255))
+            return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm_fp8: workspace smaller than "
+                                                        "h3enc_op_gemm_workspace_bytes() or not 256-byte aligned");
+        p.part = static_cast<float *>(workspace);
+        p.flags = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + h3::gemm_flags_offset(p.num_sms));
+    }
+    cudaError_t e = h3::launch_gemm(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "gemm_fp8 launch");
+}
+
+h3enc_status h3enc_op_quant_rows(const void *x, int32_t rows, int32_t cols, void *q, float *scale, void *stream) {
+    if (!x || !q || !scale || rows < 0 || cols <= 0 || cols % 8 || (reinterpret_cast<uintptr_t>(x) & 15) ||
+        (reinterpret_cast<uintptr_t>(q) & 7))
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "quant_rows: bad args");
+    cudaError_t e = h3::launch_quant_rows(static_cast<const bf16 *>(x), cols, rows, cols, static_cast<uint8_t *>(q),
+                                          cols, scale, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "quant_rows launch");
+}
+
+h3enc_status h3enc_op_rmsnorm_q8(const void *x, const void *w, void *q, float *scale, int32_t rows, int32_t cols,
+                                 float eps, void *stream) {
+    if (!x || !w || !q || !scale || rows < 0 || cols <= 0 || cols % 8 || cols > 8192)
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "rmsnorm_q8: bad args");
+    cudaError_t e = h3::launch_rmsnorm_q8(static_cast<const bf16 *>(x), static_cast<const bf16 *>(w),
+                                          static_cast<uint8_t *>(q), scale, rows, cols, eps,
+                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "rmsnorm_q8 launch");
 }
 
 h3enc_status h3enc_op_rmsnorm(const void *x, const void *w, void *y, int32_t rows, int32_t cols, float eps,

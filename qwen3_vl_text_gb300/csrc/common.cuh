@@ -149,6 +149,11 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
 __host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
+// Instruction descriptor, kind::f8f6f4: D fp32 (bits 4-5 = 1), A and B e4m3 (format
+// code 0 in bits 7-9 and 10-12), both K-major, N>>3 at bits 17-22, M>>4 at bits 24-28.
+__host__ __device__ constexpr uint32_t umma_idesc_e4m3(int m, int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
 
 // Shared-memory matrix descriptor for a K-major operand staged by TMA with
 // 128-byte swizzle: rows of 128 B (64 bf16), 8-row swizzle atoms 1024 B apart.
@@ -275,6 +280,22 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc,
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+// kind::f8f6f4 pair MMA: A and B e4m3, fp32 accumulate, K = 32 per instruction.
+__device__ __forceinline__ void umma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+template <bool F8>
+__device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    if constexpr (F8) umma_e4m3_pair(d_tmem, a_desc, b_desc, idesc, accumulate);
+    else umma_bf16_pair(d_tmem, a_desc, b_desc, idesc, accumulate);
 }
 // Arrive once on the mbarrier at this shared offset in every CTA of cta_mask when
 // all pair MMAs issued so far by this thread have completed.

@@ -1,0 +1,157 @@
+// Online-FP8 operands of the projections: per-row e4m3 quantisation of bf16
+// tensors (weights once at finalize, activations on every encode) and the
+// RMSNorm that emits its output already quantised.
+//
+// Page "vllm-omni vllm_omni/diffusion/models/minimax_h3/encoder.py":
+// _validate_encoder_quant_config (online FP8 only) and the _is_quantized_linear
+// branches (packed QKV / gate-up as one quantised linear).  Scaling: one fp32
+// scale per row, amax / 448; q = e4m3(x / scale) with the division in fp32,
+// rounded to nearest even and saturating (the e4m3 "fn" variant, largest 448).
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace h3 {
+
+namespace {
+
+constexpr int QT = 256;   // threads per row
+
+__device__ __forceinline__ float block_max(float v, float *red) {
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float m = red[0];
+    #pragma unroll
+    for (int i = 1; i < QT / 32; ++i) m = fmaxf(m, red[i]);
+    return m;
+}
+
+// Eight values -> eight e4m3 bytes (x / scale in fp32, then the hardware conversion).
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float scale) {
+    uint32_t w[2];
+    #pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const __nv_fp8x2_storage_t lo =
+            __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(f[4 * h], scale), __fdiv_rn(f[4 * h + 1], scale)),
+                                     __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t hi =
+            __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(f[4 * h + 2], scale), __fdiv_rn(f[4 * h + 3], scale)),
+                                     __NV_SATFINITE, __NV_E4M3);
+        w[h] = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+    return make_uint2(w[0], w[1]);
+}
+
+__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+// One CTA per row: amax pass, then the quantising pass (the row is re-read from L1/L2).
+__global__ void __launch_bounds__(QT) quant_rows_kernel(const bf16 *__restrict__ x, int ldx, int cols,
+                                                        uint8_t *__restrict__ q, int ldq, float *scale) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ float red[QT / 32];
+    const int row = blockIdx.x;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)row * ldx);
+    const int nvec = cols >> 3;
+    float amax = 0.f;
+    for (int i = threadIdx.x; i < nvec; i += QT) {
+        float f[8];
+        unpack8(xr[i], f);
+        #pragma unroll
+        for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
+    }
+    amax = block_max(amax, red);
+    const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    if (threadIdx.x == 0) scale[row] = s;
+    uint2 *qr = reinterpret_cast<uint2 *>(q + (size_t)row * ldq);
+    for (int i = threadIdx.x; i < nvec; i += QT) {
+        float f[8];
+        unpack8(xr[i], f);
+        qr[i] = quant8(f, s);
+    }
+}
+
+// RMSNorm of one row kept in registers (cols <= 8192), rounded to bf16, then quantised.
+constexpr int NQ_VPT = 4;   // 4 x 8 elements per thread -> cols <= 8192
+__global__ void __launch_bounds__(QT) rmsnorm_q8_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
+                                                        uint8_t *__restrict__ q, float *scale, int cols,
+                                                        float eps) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ float red[QT / 32];
+    const int row = blockIdx.x;
+    const int nvec = cols >> 3;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)row * cols);
+    const uint4 *wr = reinterpret_cast<const uint4 *>(w);
+    float f[NQ_VPT][8];
+    float ss = 0.f;
+    #pragma unroll
+    for (int i = 0; i < NQ_VPT; ++i) {
+        const int idx = threadIdx.x + i * QT;
+        if (idx < nvec) {
+            unpack8(xr[idx], f[i]);
+            #pragma unroll
+            for (int k = 0; k < 8; ++k) ss = fmaf(f[i][k], f[i][k], ss);
+        }
+    }
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    #pragma unroll
+    for (int i = 0; i < QT / 32; ++i) tot += red[i];
+    const float rstd = 1.0f / sqrtf(tot / (float)cols + eps);
+    __syncthreads();   // red is reused by the max below
+    float amax = 0.f;
+    #pragma unroll
+    for (int i = 0; i < NQ_VPT; ++i) {
+        const int idx = threadIdx.x + i * QT;
+        if (idx < nvec) {
+            float g[8];
+            unpack8(wr[idx], g);
+            #pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                f[i][k] = round_bf16(f[i][k] * rstd * g[k]);   // the norm's bf16 output
+                amax = fmaxf(amax, fabsf(f[i][k]));
+            }
+        }
+    }
+    amax = block_max(amax, red);
+    const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    if (threadIdx.x == 0) scale[row] = s;
+    uint2 *qr = reinterpret_cast<uint2 *>(q + (size_t)row * cols);
+    #pragma unroll
+    for (int i = 0; i < NQ_VPT; ++i) {
+        const int idx = threadIdx.x + i * QT;
+        if (idx < nvec) qr[idx] = quant8(f[i], s);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quant_rows(const bf16 *x, int ldx, int rows, int cols, uint8_t *q, int ldq, float *scale,
+                              cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    if (cols % 8 || ldx % 8 || ldq % 8) return cudaErrorInvalidValue;
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3(rows), dim3(QT), 0, st, at);
+    return cudaLaunchKernelEx(&cfg, quant_rows_kernel, x, ldx, cols, q, ldq, scale);
+}
+
+cudaError_t launch_rmsnorm_q8(const bf16 *x, const bf16 *w, uint8_t *q, float *scale, int rows, int cols, float eps,
+                              cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    if (cols % 8 || cols > QT * NQ_VPT * 8) return cudaErrorInvalidValue;
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3(rows), dim3(QT), 0, st, at);
+    return cudaLaunchKernelEx(&cfg, rmsnorm_q8_kernel, x, w, q, scale, cols, eps);
+}
+
+}  // namespace h3

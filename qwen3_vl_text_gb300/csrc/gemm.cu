@@ -46,7 +46,8 @@ namespace {
 
 constexpr int BM = 128;                          // output rows per CTA (a pair covers 256)
 constexpr int BN = 256;                          // output columns per tile
-constexpr int BK = 64;
+constexpr int BK = 64;                           // bf16 elements per k-block (128 bytes per row)
+constexpr int BK8 = 128;                         // e4m3 elements per k-block (the same 128 bytes)
 constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB
 constexpr int B_BYTES = (BN / 2) * BK * 2;       // 16 KB: this CTA's half of the weight tile
@@ -81,6 +82,8 @@ struct GemmArgs {
     int head_dim, nq, nkv;
     float eps;
     unsigned long long *trace;   // optional [grid][TR_COUNT] %globaltimer stamps
+    // e4m3 operands: C = (A8 * sa[row]) (W8 * sw[col])^T
+    const float *sa, *sw;
 };
 
 // Phase stamps of the optional timeline (h3enc_op_gemm_traced).
@@ -186,7 +189,7 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16 *p, const float (&f)[3
     }
 }
 
-template <int EPI>
+template <int EPI, bool F8>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs g) {
@@ -255,8 +258,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; return; }
                     if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
                     const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
-                    tma_load_2d_pair(sA + stage * A_BYTES, &tmA, bar, kb * BK, m0);
-                    tma_load_2d_pair(sB + stage * B_BYTES, &tmB, bar, kb * BK, n0);
+                    constexpr int kbe = F8 ? BK8 : BK;   // elements of one 128-byte k-block row
+                    tma_load_2d_pair(sA + stage * A_BYTES, &tmA, bar, kb * kbe, m0);
+                    tma_load_2d_pair(sB + stage * B_BYTES, &tmB, bar, kb * kbe, n0);
                     if (issued[0] + issued[1] == 0 && stage == 0) stamp(g, TR_FIRST_LOAD);
                     ++issued[stage];
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -277,7 +281,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
-            constexpr uint32_t idesc = umma_idesc_bf16(2 * BM, BN);
+            constexpr uint32_t idesc = F8 ? umma_idesc_e4m3(2 * BM, BN) : umma_idesc_bf16(2 * BM, BN);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -295,8 +299,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     const uint32_t a_base = smem_u32(sA + stage * A_BYTES);
                     const uint32_t b_base = smem_u32(sB + stage * B_BYTES);
                     #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_bf16_pair(d_tmem, sdesc_sw128(a_base + kk * 32), sdesc_sw128(b_base + kk * 32), idesc,
+                    for (int kk = 0; kk < 4; ++kk)   // 32-byte steps: K = 16 bf16 or K = 32 e4m3 per MMA
+                        umma_pair<F8>(d_tmem, sdesc_sw128(a_base + kk * 32), sdesc_sw128(b_base + kk * 32), idesc,
                                        (kb > kb0 || kk > 0) ? 1u : 0u);
                     umma_commit_pair(&empty[stage], 0x3);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -323,6 +327,28 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int quarter = warp & 3;
         const int ehalf = (warp - 2) >> 2;
         const int et = threadIdx.x - 64;  // 0..255 over the epilogue warps
+        // e4m3 operands: accumulator column n of row m times sa[m] * sw[n] (32 columns from n0; the
+        // sw loads are the same address across the warp)
+        auto dq32 = [&](uint32_t (&v)[32], int m, bool live_row, int n0) {
+            if constexpr (F8) {
+                const float sr = live_row ? g.sa[m] : 0.f;
+                const float4 *w4 = reinterpret_cast<const float4 *>(g.sw + n0);
+                #pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 sw = w4[q];
+                    v[4 * q + 0] = __float_as_uint(__uint_as_float(v[4 * q + 0]) * (sr * sw.x));
+                    v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) * (sr * sw.y));
+                    v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) * (sr * sw.z));
+                    v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) * (sr * sw.w));
+                }
+            }
+        };
+        auto dq4 = [&](float *f, float sr, int n0) {
+            if constexpr (F8) {
+                const float4 sw = *reinterpret_cast<const float4 *>(g.sw + n0);
+                f[0] *= sr * sw.x; f[1] *= sr * sw.y; f[2] *= sr * sw.z; f[3] *= sr * sw.w;
+            }
+        };
         const uint32_t acc_empty_lead[2] = {mapa_shared(smem_u32(&acc_empty[0]), 0),
                                             mapa_shared(smem_u32(&acc_empty[1]), 0)};
         int acc = 0;
@@ -442,6 +468,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                     }
                                 }
                             }
+                            if constexpr (F8) {
+                                const float sr = g.sa[row];
+                                #pragma unroll
+                                for (int i = 0; i < 16; i += 4) {
+                                    if (i < q4) {
+                                        dq4(a + i, sr, n_blk * BN + ca + i);
+                                        dq4(b + i, sr, n_blk * BN + ca + half + i);
+                                    }
+                                }
+                            }
                             __nv_bfloat16 *dst = g.C + (size_t)row * g.ldc + n_blk * BN + ca;
                             const bool is_q = head < g.nq, is_k = !is_q && head < g.nq + g.nkv;
                             if (is_q || is_k) {
@@ -508,9 +544,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                 }
                             }
                             float f[4] = {a.x, a.y, a.z, a.w};
+                            float up[4] = {b.x, b.y, b.z, b.w};
+                            if constexpr (F8) {
+                                const float sr = g.sa[row];
+                                dq4(f, sr, n_blk * BN + c4);
+                                if constexpr (EPI == EPI_SWIGLU) dq4(up, sr, n_blk * BN + BN / 2 + c4);
+                            }
                             int col;
                             if constexpr (EPI == EPI_SWIGLU) {
-                                const float up[4] = {b.x, b.y, b.z, b.w};
                                 #pragma unroll
                                 for (int i = 0; i < 4; ++i) f[i] = f[i] / (1.0f + expf(-f[i])) * up[i];
                                 col = n_blk * (BN / 2) + c4;
@@ -564,6 +605,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     tmem_ld32(taddr + c * 32, vg);
                     tmem_ld32(taddr + BN / 2 + c * 32, vu);
                     tmem_ld_wait();
+                    dq32(vg, row, live, n_blk * BN + c * 32);
+                    dq32(vu, row, live, n_blk * BN + BN / 2 + c * 32);
                     if (live) {
                         float f[32];
                         #pragma unroll
@@ -592,6 +635,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             uint32_t v[32];
                             tmem_ld32(taddr + cb + c * 32, v);
                             tmem_ld_wait();
+                            dq32(v, row, live, n_blk * BN + cb + c * 32);
                             if (live) {
                                 float f[32];
                                 #pragma unroll
@@ -607,6 +651,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         uint32_t v[32];
                         tmem_ld32(taddr + cb + c * 32, v);
                         tmem_ld_wait();
+                        dq32(v, row, live, n_blk * BN + cb + c * 32);
                         #pragma unroll
                         for (int j = 0; j < 32; ++j) ss = fmaf(__uint_as_float(v[j]), __uint_as_float(v[j]), ss);
                     }
@@ -618,6 +663,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         tmem_ld32(taddr + cb + c * 32, va);
                         tmem_ld32(taddr + cb + half + c * 32, vb);
                         tmem_ld_wait();
+                        dq32(va, row, live, n_blk * BN + cb + c * 32);
+                        dq32(vb, row, live, n_blk * BN + cb + half + c * 32);
                         if (live) {
                             const float *cs = g.cos_t + (size_t)row * half + c * 32;
                             const float *sn = g.sin_t + (size_t)row * half + c * 32;
@@ -669,6 +716,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     uint32_t v[32];
                     tmem_ld32(taddr + c * 32, v);
                     tmem_ld_wait();
+                    dq32(v, row, live, col);
                     if (live) {
                         float f[32];
                         #pragma unroll
@@ -729,7 +777,7 @@ uint32_t next_epoch() {
     return e;
 }
 
-template <int EPI>
+template <int EPI, bool F8>
 cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     static int max_pairs = 0;
     cudaLaunchAttribute attr[2];
@@ -738,7 +786,7 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     if (max_pairs == 0) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tcgen05_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(gemm_tcgen05_kernel<EPI, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              SMEM_BYTES);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t q = {};
@@ -748,7 +796,7 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
         q.attrs = attr;
         q.numAttrs = 1;
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, gemm_tcgen05_kernel<EPI>, &q);
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_tcgen05_kernel<EPI, F8>, &q);
         if (e != cudaSuccess) return e;
         if (n <= 0) return cudaErrorInvalidConfiguration;
         max_pairs = n;
@@ -757,7 +805,8 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     g.M = p.M; g.N = p.N; g.K = p.K;
     g.nm = (p.M + 2 * BM - 1) / (2 * BM);
     g.nn = p.N / BN;
-    g.nk = (p.K + BK - 1) / BK;
+    g.nk = F8 ? (p.K + BK8 - 1) / BK8 : (p.K + BK - 1) / BK;
+    g.sa = p.sa; g.sw = p.sw;
     g.C = p.C; g.ldc = p.ldc; g.R = p.R; g.DS = p.DS; g.vis_rank = p.vis_rank; g.n_vis = p.n_vis;
     g.status = p.status;
     g.wq = p.wq; g.wk = p.wk; g.cos_t = p.cos_t; g.sin_t = p.sin_t;
@@ -793,7 +842,7 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<EPI>, *p.tmA, *p.tmW, g);
+    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<EPI, F8>, *p.tmA, *p.tmW, g);
 }
 
 }  // namespace
@@ -807,6 +856,19 @@ bool make_tmap_rows(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t col
     cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_rows_e4m3(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn || rows == 0 || cols == 0 || cols % 16 != 0 || (reinterpret_cast<uintptr_t>(ptr) & 15)) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {(cuuint32_t)BK8, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -831,15 +893,27 @@ cudaError_t launch_gemm(const GemmPlan &p_in, cudaStream_t stream) {
         p.trace = t_trace_next;
         t_trace_next = nullptr;
     }
+    if (p.epi == EPI_QKROPE &&
+        ((p.head_dim != 64 && p.head_dim != 128) || !p.wq || !p.wk || !p.cos_t || !p.sin_t))
+        return cudaErrorInvalidValue;
+    if (p.fp8) {
+        // the scales are read as float4 groups of 4 columns
+        if (!p.sa || !p.sw || (reinterpret_cast<uintptr_t>(p.sw) & 15)) return cudaErrorInvalidValue;
+        switch (p.epi) {
+            case EPI_STORE: return launch_epi<EPI_STORE, true>(p, stream);
+            case EPI_RESIDUAL: return launch_epi<EPI_RESIDUAL, true>(p, stream);
+            case EPI_SWIGLU: return launch_epi<EPI_SWIGLU, true>(p, stream);
+            case EPI_RESIDUAL_DS: return launch_epi<EPI_RESIDUAL_DS, true>(p, stream);
+            case EPI_QKROPE: return launch_epi<EPI_QKROPE, true>(p, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (p.epi) {
-        case EPI_STORE: return launch_epi<EPI_STORE>(p, stream);
-        case EPI_RESIDUAL: return launch_epi<EPI_RESIDUAL>(p, stream);
-        case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(p, stream);
-        case EPI_RESIDUAL_DS: return launch_epi<EPI_RESIDUAL_DS>(p, stream);
-        case EPI_QKROPE:
-            if ((p.head_dim != 64 && p.head_dim != 128) || !p.wq || !p.wk || !p.cos_t || !p.sin_t)
-                return cudaErrorInvalidValue;
-            return launch_epi<EPI_QKROPE>(p, stream);
+        case EPI_STORE: return launch_epi<EPI_STORE, false>(p, stream);
+        case EPI_RESIDUAL: return launch_epi<EPI_RESIDUAL, false>(p, stream);
+        case EPI_SWIGLU: return launch_epi<EPI_SWIGLU, false>(p, stream);
+        case EPI_RESIDUAL_DS: return launch_epi<EPI_RESIDUAL_DS, false>(p, stream);
+        case EPI_QKROPE: return launch_epi<EPI_QKROPE, false>(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

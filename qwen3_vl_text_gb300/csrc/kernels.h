@@ -28,7 +28,7 @@ struct GemmPlan {
     int n_vis;
     int32_t *status;
     int num_sms;
-    float *part;        // split workspace: num_sms x 128 x 256 fp32 partials (NULL: no split)
+    float *part;        // stream-K workspace: 2 x num_sms x 128 x 256 fp32 partials (NULL: no split)
     uint32_t *flags;    // num_sms release flags, zero-filled once before first use
     // EPI_QKROPE: per-head RMSNorm of the q and k heads, then M-RoPE with the fp32 tables
     const bf16 *wq = nullptr, *wk = nullptr;
@@ -36,10 +36,25 @@ struct GemmPlan {
     int head_dim = 0, nq = 0, nkv = 0;
     float eps = 0.f;
     unsigned long long *trace = nullptr;   // optional per-CTA phase timeline (11 stamps per CTA)
+    // e4m3 operands (tensor maps from make_tmap_rows_e4m3): C = (A * sa[row]) (W * sw[col])^T,
+    // sa [M] and sw [N] fp32 (sw 16-byte aligned)
+    bool fp8 = false;
+    const float *sa = nullptr, *sw = nullptr;
 };
 // Tensor map of a row-major bf16 matrix [rows, cols] read in boxes of
 // box_rows x 64 with 128-byte swizzle.  False if the driver refuses it.
 bool make_tmap_rows(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// The same for an e4m3 matrix (one byte per element): boxes of box_rows x 128.
+bool make_tmap_rows_e4m3(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// Per-row e4m3 quantisation: scale[r] = amax(row r) / 448 (1 for a zero row),
+// q = e4m3(x / scale) rounded to nearest even, saturating; x and q row-major with
+// leading dimensions ldx / ldq (elements).  cols % 8 == 0.
+cudaError_t launch_quant_rows(const bf16 *x, int ldx, int rows, int cols, uint8_t *q, int ldq, float *scale,
+                              cudaStream_t st);
+// RMSNorm (as launch_rmsnorm, output rounded to bf16) followed by the per-row
+// e4m3 quantisation of that bf16 output.
+cudaError_t launch_rmsnorm_q8(const bf16 *x, const bf16 *w, uint8_t *q, float *scale, int rows, int cols, float eps,
+                              cudaStream_t st);
 int gemm_box_rows_a();
 int gemm_box_rows_w();
 // Bytes of a split workspace (partials then flags) for a grid of num_sms CTAs.

@@ -373,3 +373,100 @@ def test_bf16_storage_variant_rounds_only_at_hand_over_points():
     x = O.round_to_bf16(_rng(16).standard_normal((6, cfg.hidden)).astype(np.float32))
     c, s = O.rope_cos_sin(np.stack([np.arange(6)] * 3), cfg.head_dim, cfg.rope_theta, cfg.mrope_section)
     assert np.array_equal(O.decoder_layer(x, w, c, s, cfg, storage=set(O.STORAGE_POINTS)), x)
+
+
+# ---------------------------------------------------------------------------
+# online-FP8 linears (oracle.fp8)
+# ---------------------------------------------------------------------------
+
+def test_e4m3_round_matches_torch_converter():
+    """Against torch's independent float8_e4m3fn conversion (round to nearest even) on
+    random values across the whole finite range, subnormals and exact ties."""
+    torch = pytest.importorskip("torch")
+    rng = _rng(40)
+    x = np.concatenate([
+        rng.standard_normal(20000) * 100.0,
+        rng.standard_normal(20000) * 2.0 ** -7,                  # subnormal range
+        (np.arange(-4000, 4000) + 0.5) * 2.0 ** -9,              # ties between subnormals
+        np.ldexp(1.0 + (np.arange(16) + 0.5) / 8.0, 3),          # ties between normals in [8, 16)
+    ]).astype(np.float32)
+    x = np.clip(x, -448.0, 448.0)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(O.fp8.e4m3_round(x), ref)
+
+
+def test_e4m3_grid_facts():
+    r = O.fp8.e4m3_round
+    assert r(np.array([448.0]))[0] == 448.0                   # largest finite
+    assert r(np.array([600.0, -1e6]))[0] == 448.0 and r(np.array([-1e6]))[0] == -448.0   # saturating
+    assert r(np.array([2.0 ** -9]))[0] == 2.0 ** -9           # smallest subnormal
+    assert r(np.array([2.0 ** -10]))[0] == 0.0                # tie with 0 -> even (0)
+    assert r(np.array([3 * 2.0 ** -10]))[0] == 2.0 ** -8      # tie 1.5 ulp -> even (2 ulp)
+    assert r(np.array([1.0 + 2.0 ** -4]))[0] == 1.0           # tie -> even mantissa 000
+    assert r(np.array([1.0 + 3 * 2.0 ** -4]))[0] == 1.25      # tie -> even mantissa 010
+    assert r(np.array([15.5]))[0] == 16.0                     # rounds up into the next binade
+    # the positive finite values from the bit layout: 7 subnormals m/8 * 2^-6, normals (1 + m/8) * 2^(E-7)
+    # for E = 1..15 except E = 15, m = 7 (the NaN code of the fn variant): 126 values
+    grid = [m / 8 * 2.0 ** -6 for m in range(1, 8)]
+    grid += [(1 + m / 8) * 2.0 ** (E - 7) for E in range(1, 16) for m in range(8) if not (E == 15 and m == 7)]
+    grid = np.array(sorted(grid))
+    assert len(grid) == 126 and grid[-1] == 448.0
+    assert np.array_equal(r(grid), grid) and np.array_equal(r(-grid), -grid)
+    mid = (grid[:-1] + grid[1:]) / 2                          # every midpoint goes to a neighbour
+    got = r(mid)
+    assert np.all((got == grid[:-1]) | (got == grid[1:]))
+    assert np.all(np.diff(r(np.linspace(-500, 500, 100001))) >= 0)   # monotone
+
+
+def test_quantize_rows_scales_and_error_bound():
+    rng = _rng(41)
+    x = O.round_to_bf16(rng.standard_normal((5, 300)).astype(np.float32) * np.array([1e-3, 1, 7, 300, 0])[:, None])
+    q, s = O.fp8.quantize_rows(x)
+    assert s[4] == 1.0 and np.all(q[4] == 0)                  # zero row
+    for i in range(4):
+        amax = np.max(np.abs(x[i]))
+        assert s[i] == np.float32(amax) / np.float32(448.0)
+        assert np.max(np.abs(q[i])) == 448.0                  # the largest element lands on +-448
+        deq = q[i] * s[i]
+        big = np.abs(x[i]) >= 2.0 ** -6 * s[i]                # normal range of e4m3 after scaling
+        assert np.all(np.abs(deq - x[i])[big] <= 2.0 ** -4 * np.abs(x[i])[big] * (1 + 1e-6))
+        assert np.all(np.abs(deq - x[i])[~big] <= 2.0 ** -10 * s[i] * (1 + 1e-6))
+
+
+def test_fp8_linear_is_exact_on_the_grid_and_scales_back():
+    """Rows already on the e4m3 grid with amax 448 have scale 1 and quantise to
+    themselves: the FP8 linear is then the plain product.  Scaling a row of x or
+    of w by a power of two scales the output row / column by it (scales act per row)."""
+    rng = _rng(42)
+    g = O.fp8.e4m3_round(rng.uniform(-448, 448, (6, 64)))
+    g[:, 0] = 448.0
+    h = O.fp8.e4m3_round(rng.uniform(-448, 448, (5, 64)))
+    h[:, 3] = -448.0
+    assert np.array_equal(O.fp8.fp8_linear(g, h), O.linear(g.astype(np.float64), h.astype(np.float64)))
+    x = O.round_to_bf16(rng.standard_normal((4, 64)).astype(np.float32))
+    w = O.round_to_bf16(rng.standard_normal((3, 64)).astype(np.float32))
+    base = O.fp8.fp8_linear(x, w)
+    x2 = x.copy(); x2[1] *= 8.0
+    w2 = w.copy(); w2[2] *= 0.25
+    out = O.fp8.fp8_linear(x2, w2)
+    expect = base.copy(); expect[1] *= 8.0; expect[:, 2] *= 0.25
+    assert np.array_equal(out, expect)
+
+
+def test_fp8_layer_tracks_the_bf16_layer():
+    """The FP8 tiny model stays within the quantisation error of the exact one
+    (e4m3 keeps 3 fraction bits: a few % relative per projection, compounding over
+    the 8 projections of the two layers) and does differ from it."""
+    wl, cfg, inp, emb, ds = _tiny_case(np.float32)
+    get = _tiny_weights(cfg, wl.seed, np.float32)
+    exact = O.forward(emb, inp["positions"], cfg, get, inp["visual_mask"], ds, dtype=np.float32)
+    q8 = O.forward(emb, inp["positions"], cfg, get, inp["visual_mask"], ds, dtype=np.float32, fp8=True)
+    rel = np.linalg.norm(q8 - exact) / np.linalg.norm(exact)
+    assert 1e-3 < rel < 1e-1
+    # one projection alone: the relative error of a K = 256 product is a few %
+    rng = _rng(43)
+    x = O.round_to_bf16(rng.standard_normal((32, 256)).astype(np.float32))
+    w = O.round_to_bf16(rng.standard_normal((48, 256)).astype(np.float32) * 0.02)
+    ref = O.linear(x.astype(np.float64), w.astype(np.float64))
+    e1 = np.linalg.norm(O.fp8.fp8_linear(x, w) - ref) / np.linalg.norm(ref)
+    assert 5e-3 < e1 < 4e-2
