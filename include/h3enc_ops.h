@@ -123,9 +123,10 @@ H3ENC_API h3enc_status h3enc_op_gemm_fp8(const void *A, const void *W, const flo
                                int32_t *status, void *stream);
 
 /* Per-row e4m3 quantisation of a bf16 matrix x [rows, cols] (cols % 8 == 0):
- * scale[r] = amax(row r) / 448 in fp32 (1 for an all-zero row), q = e4m3(x / scale)
- * with the division in fp32, rounded to nearest even, saturating at +-448
- * (the "fn" variant).  q [rows, cols] bytes; x 16-byte aligned. */
+ * scale[r] = amax(row r) / 448 in fp32 (1 for an all-zero row), q = e4m3(x * inv)
+ * with inv = 448 / amax and the product each rounded once in fp32, then rounded
+ * to nearest even, saturating at +-448 (the "fn" variant).  q [rows, cols]
+ * bytes; x 16-byte aligned. */
 H3ENC_API h3enc_status h3enc_op_quant_rows(const void *x, int32_t rows, int32_t cols, void *q, float *scale,
                                  void *stream);
 

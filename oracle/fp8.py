@@ -16,7 +16,9 @@ not spell out the scaling; the reading taken here (and by the CUDA path) is:
   matrix), ``scale = amax(row) / 448``;
 * activations: one fp32 scale per token (row), computed at run time from the
   bf16 activation the projection receives, same rule;
-* ``q = e4m3(x / scale)`` with the division in fp32; a row of zeros gets scale 1;
+* ``q = e4m3(x * (448 / amax))``, the reciprocal and the product each rounded
+  once in fp32 (a multiply per element instead of a divide); a row of zeros
+  gets scale 1 and quantises to zeros;
 * ``y = (q_a * s_a) @ (q_w * s_w)^T`` accumulated exactly (float64 here).
 """
 from __future__ import annotations
@@ -49,12 +51,16 @@ def e4m3_round(x: np.ndarray) -> np.ndarray:
 
 
 def quantize_rows(x: np.ndarray):
-    """Per-row quantisation: ``scale = amax / 448`` (fp32), ``q = e4m3(x / scale)``
-    with the division in fp32.  Returns (q as float64 grid values, scale float32[rows])."""
+    """Per-row quantisation: ``scale = amax / 448`` and ``inv = 448 / amax`` (each one
+    fp32 division), ``q = e4m3(x * inv)`` with the product in fp32.
+    Returns (q as float64 grid values, scale float32[rows])."""
     x32 = np.asarray(x, dtype=np.float32)
     amax = np.max(np.abs(x32), axis=1)
-    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
-    q = e4m3_round((x32 / scale[:, None]).astype(np.float32))
+    pos = amax > 0
+    safe = np.where(pos, amax, np.float32(1.0)).astype(np.float32)
+    scale = np.where(pos, safe / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    inv = np.where(pos, np.float32(E4M3_MAX) / safe, np.float32(1.0)).astype(np.float32)
+    q = e4m3_round((x32 * inv[:, None]).astype(np.float32))
     return q, scale
 
 

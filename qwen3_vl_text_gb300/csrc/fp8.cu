@@ -5,8 +5,9 @@
 // Page "vllm-omni vllm_omni/diffusion/models/minimax_h3/encoder.py":
 // _validate_encoder_quant_config (online FP8 only) and the _is_quantized_linear
 // branches (packed QKV / gate-up as one quantised linear).  Scaling: one fp32
-// scale per row, amax / 448; q = e4m3(x / scale) with the division in fp32,
-// rounded to nearest even and saturating (the e4m3 "fn" variant, largest 448).
+// scale per row, amax / 448; q = e4m3(x * (448 / amax)) with the reciprocal and
+// the product each rounded once in fp32, then rounded to nearest even and
+// saturating (the e4m3 "fn" variant, largest 448).
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -29,16 +30,16 @@ __device__ __forceinline__ float block_max(float v, float *red) {
     return m;
 }
 
-// Eight values -> eight e4m3 bytes (x / scale in fp32, then the hardware conversion).
-__device__ __forceinline__ uint2 quant8(const float (&f)[8], float scale) {
+// Eight values -> eight e4m3 bytes (x * inv in fp32, then the hardware conversion).
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float inv) {
     uint32_t w[2];
     #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const __nv_fp8x2_storage_t lo =
-            __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(f[4 * h], scale), __fdiv_rn(f[4 * h + 1], scale)),
+            __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(f[4 * h], inv), __fmul_rn(f[4 * h + 1], inv)),
                                      __NV_SATFINITE, __NV_E4M3);
         const __nv_fp8x2_storage_t hi =
-            __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(f[4 * h + 2], scale), __fdiv_rn(f[4 * h + 3], scale)),
+            __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(f[4 * h + 2], inv), __fmul_rn(f[4 * h + 3], inv)),
                                      __NV_SATFINITE, __NV_E4M3);
         w[h] = (uint32_t)lo | ((uint32_t)hi << 16);
     }
@@ -67,13 +68,13 @@ __global__ void __launch_bounds__(QT) quant_rows_kernel(const bf16 *__restrict__
         for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
     }
     amax = block_max(amax, red);
-    const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-    if (threadIdx.x == 0) scale[row] = s;
+    const float inv = amax > 0.f ? __fdiv_rn(448.0f, amax) : 1.0f;
+    if (threadIdx.x == 0) scale[row] = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
     uint2 *qr = reinterpret_cast<uint2 *>(q + (size_t)row * ldq);
     for (int i = threadIdx.x; i < nvec; i += QT) {
         float f[8];
         unpack8(xr[i], f);
-        qr[i] = quant8(f, s);
+        qr[i] = quant8(f, inv);
     }
 }
 
@@ -124,13 +125,13 @@ __global__ void __launch_bounds__(QT) rmsnorm_q8_kernel(const bf16 *__restrict__
         }
     }
     amax = block_max(amax, red);
-    const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-    if (threadIdx.x == 0) scale[row] = s;
+    const float inv = amax > 0.f ? __fdiv_rn(448.0f, amax) : 1.0f;
+    if (threadIdx.x == 0) scale[row] = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
     uint2 *qr = reinterpret_cast<uint2 *>(q + (size_t)row * cols);
     #pragma unroll
     for (int i = 0; i < NQ_VPT; ++i) {
         const int idx = threadIdx.x + i * QT;
-        if (idx < nvec) qr[idx] = quant8(f[i], s);
+        if (idx < nvec) qr[idx] = quant8(f[i], inv);
     }
 }
 

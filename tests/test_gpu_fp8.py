@@ -174,3 +174,29 @@ def test_fp8_encode_tiny_model_against_fp8_oracle():
     e_orc = rel_l2(ref8, ref)
     assert e_gpu < 1.5 * e_orc + 1e-2, (e_gpu, e_orc)
     assert rel_l2(t2f(out16), ref) < e_gpu                 # the bf16 path is the more accurate one
+
+
+def test_fp8_one_full_width_layer_against_fp8_oracle():
+    """One 5120-wide layer (64 q / 8 kv heads, intermediate 25600) at 512 tokens in FP8
+    mode: every projection runs the e4m3 GEMM at full size (stream-K tails included)."""
+    wl = W.workload(1)
+    cfg = wl.model
+    inp = W.gen_inputs(wl)
+    S = inp["seq_len"]
+    enc = make_encoder(wl, cfg, max_tokens=S, fp8=True)
+    try:
+        x = W.bf16_bits_to_torch(inp["inputs_embeds"]).cuda()
+        pos = torch.from_numpy(inp["positions"]).cuda()
+        out = torch.empty(S, cfg.hidden, dtype=torch.bfloat16, device="cuda")
+        Q.h3enc_encode_embeds(enc.handle, x, 0, cfg.num_layers, pos, None, None, 0, 0, None, S, out)
+        torch.cuda.synchronize()
+        assert enc.status() == 0, Q.h3enc_last_error(enc.handle)
+        got = t2f(out)
+    finally:
+        enc.close()
+    x0 = bits_to_f32(inp["inputs_embeds"])
+    w = oracle_layer_getter(wl, cfg)(0)
+    ref8 = O.forward(x0, inp["positions"], cfg, lambda _: w, fp8=True)
+    ref8bf = O.forward(x0, inp["positions"], cfg, lambda _: w, fp8=True, storage=GPU_STORAGE)
+    ok, msg = within(got, ref8, ref8bf, 5e-3)
+    assert ok, "fp8 layer vs fp8 oracle: " + msg
