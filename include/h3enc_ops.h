@@ -80,7 +80,7 @@ H3ENC_API int64_t h3enc_op_gemm_workspace_bytes(void);
  * after start-up.  This entry point computes exactly what h3enc_op_gemm
  * computes with a workspace (same kernel, same split of the last wave), but its
  * scratch is a fixed array inside the library's device image:
- * h3enc_op_gemm_noalloc_scratch_bytes() bytes (40 MiB + 896 B, two 128 KiB
+ * h3enc_op_gemm_noalloc_scratch_bytes() bytes (40 MiB + 904 B, two 128 KiB
  * fp32 slots and one flag per SM for up to 160 SMs), held by every GPU that
  * loads the library until the process exits.  The caller passes inputs and
  * outputs only; nothing is allocated or freed.

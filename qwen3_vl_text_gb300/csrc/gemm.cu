@@ -35,8 +35,6 @@
 // in-flight copies and MMAs, frees TMEM and exits.
 #include <cudaTypedefs.h>
 
-#include <atomic>
-
 #include "common.cuh"
 #include "kernels.h"
 
@@ -74,8 +72,9 @@ struct GemmArgs {
     int sk_pairs;      // pairs [0, sk_pairs) share the k-blocks of tiles [dp_tiles, nm*nn); 0: none
     long long sk_work; // (nm*nn - dp_tiles) * nk
     float *part;       // [2*grid][BM*BN] fp32 partials: slot 4*pair + 2*part + rank
-    uint32_t *flags;   // [grid] release flags
-    uint32_t epoch;    // unique per launch; a flag equal to it means "partial written"
+    uint32_t *flags;   // [grid] release flags: equal to this launch's epoch = "partial written"
+    uint32_t *ctrl;    // [2] in device memory: the epoch of the last stream-K launch on this
+                       // workspace, and the count of this launch's finished CTAs
     // EPI_QKROPE
     const __nv_bfloat16 *wq, *wk;
     const float *cos_t, *sin_t;
@@ -95,6 +94,14 @@ __device__ __forceinline__ void stamp(const GemmArgs &g, int what) {
         asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
         g.trace[(size_t)blockIdx.x * TR_COUNT + what] = t;
     }
+}
+
+// Epoch of a stream-K launch: one more than the workspace's last one (0 is skipped: it is the
+// value of a fresh flag).  Read after the dependency wait; the last CTA to finish stores it, so a
+// launch replayed from a CUDA graph gets a new epoch too.
+__device__ __forceinline__ uint32_t sk_epoch(const GemmArgs &g) {
+    const uint32_t e = __ldcg(g.ctrl) + 1u;
+    return e == 0u ? 1u : e;
 }
 
 // Stream-K ranges: pair p owns k-iterations [start(p), start(p+1)) of the tail laid
@@ -407,7 +414,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (epi_bar_and(dumped)) {
                 if (et == 0) {
                     stamp(g, TR_DUMP_DONE);
-                    st_release(g.flags + blockIdx.x, g.epoch);
+                    st_release(g.flags + blockIdx.x, sk_epoch(g));
                 }
                 for (int j = 0; j < sk.n; ++j) {
                     // 2) wait for the same-rank CTAs of the tile's contributors: thread i polls contributor
@@ -419,7 +426,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     bool seen = true;
                     if (et < nc) {
                         const long long t0 = clock64();
-                        while (ld_acquire(g.flags + 2 * (pa + et) + rank) != g.epoch) {
+                        const uint32_t epoch = sk_epoch(g);
+                        while (ld_acquire(g.flags + 2 * (pa + et) + rank) != epoch) {
                             if (clock64() - t0 > kSpinLimitCycles) { seen = false; break; }
                         }
                     }
@@ -750,7 +758,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
     tc_fence_before();
     cluster_sync();   // the peer no longer reads this CTA's shared memory or signals its barriers
-    if (threadIdx.x == 0) stamp(g, TR_END);
+    if (threadIdx.x == 0) {
+        stamp(g, TR_END);
+        if (g.sk_pairs) {
+            // the last CTA of the launch records its epoch; every CTA has read it long before
+            const uint32_t epoch = sk_epoch(g);
+            __threadfence();
+            if (atomicAdd(g.ctrl + 1, 1u) == gridDim.x - 1) {
+                g.ctrl[1] = 0u;
+                __threadfence();
+                st_release(g.ctrl, epoch);
+            }
+        }
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, 512);
@@ -768,13 +788,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
     }
     return fn;
-}
-
-uint32_t next_epoch() {
-    static std::atomic<uint32_t> epoch{0};
-    uint32_t e = ++epoch;
-    if (e == 0) e = ++epoch;  // 0 is the value of a fresh flag
-    return e;
 }
 
 template <int EPI, bool F8>
@@ -831,7 +844,7 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     g.dp_tiles = sk_pairs ? tiles - left : tiles;
     g.part = p.part;
     g.flags = p.flags;
-    g.epoch = sk_pairs ? next_epoch() : 0u;
+    g.ctrl = p.flags ? p.flags + p.num_sms : nullptr;
     const int grid_pairs = g.dp_tiles >= pairs ? pairs : (sk_pairs > g.dp_tiles ? sk_pairs : g.dp_tiles);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * grid_pairs);
@@ -878,7 +891,8 @@ int gemm_box_rows_a() { return BM; }
 // Stream-K partials: two 128 x 256 fp32 slots per CTA (a range covers parts of at most two tiles),
 // then one release flag per CTA.
 size_t gemm_flags_offset(int num_sms) { return (size_t)2 * num_sms * BM * BN * sizeof(float) + 256; }
-size_t gemm_workspace_bytes(int num_sms) { return gemm_flags_offset(num_sms) + (size_t)num_sms * 4; }
+// then the launch epoch and a finished-CTA counter
+size_t gemm_workspace_bytes(int num_sms) { return gemm_flags_offset(num_sms) + (size_t)num_sms * 4 + 8; }
 int gemm_box_rows_w() { return BN / 2; }
 
 namespace {

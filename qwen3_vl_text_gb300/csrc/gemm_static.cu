@@ -16,11 +16,13 @@
 
 namespace {
 
-// Partials of the stream-K phase: two 128 x 256 fp32 slots per SM, then one flag per SM.
+// Partials of the stream-K phase: two 128 x 256 fp32 slots per SM, then one flag per SM, then
+// the launch epoch and the finished-CTA counter (found right after the flags of the SMs in use).
 constexpr int kMaxSlots = 160;                                      // SMs the array is sized for
 constexpr size_t kSlotBytes = 128 * 256 * sizeof(float);            // 128 KiB
 constexpr size_t kFlagOffset = (size_t)2 * kMaxSlots * kSlotBytes + 256;
-constexpr size_t kScratchBytes = kFlagOffset + (size_t)kMaxSlots * sizeof(uint32_t);  // 40 MiB + 896 B
+constexpr size_t kFlagWords = kMaxSlots + 2;
+constexpr size_t kScratchBytes = kFlagOffset + kFlagWords * sizeof(uint32_t);  // 40 MiB + 904 B
 
 static __device__ __align__(256) unsigned char g_gemm_scratch[kScratchBytes];
 
@@ -52,8 +54,9 @@ h3enc_status scratch_for_current_device(unsigned char **out) {
             snprintf(g_error, sizeof g_error, "gemm_noalloc: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
             return H3ENC_ERR_CUDA;
         }
-        // a flag equal to the epoch of a launch means "partial written": start from zero
-        e = cudaMemset(static_cast<unsigned char *>(p) + kFlagOffset, 0, (size_t)kMaxSlots * sizeof(uint32_t));
+        // a flag equal to the epoch of a launch means "partial written": flags, epoch and counter
+        // start from zero
+        e = cudaMemset(static_cast<unsigned char *>(p) + kFlagOffset, 0, kFlagWords * sizeof(uint32_t));
         if (e == cudaSuccess) e = cudaDeviceSynchronize();
         if (e != cudaSuccess) {
             snprintf(g_error, sizeof g_error, "gemm_noalloc: clearing the flags failed: %s", cudaGetErrorString(e));
