@@ -73,6 +73,7 @@ struct h3enc {
     std::vector<Layer8> layers8;
     uint8_t *y8 = nullptr, *attn8 = nullptr, *act8 = nullptr;
     float *sy = nullptr, *sattn = nullptr, *sact = nullptr;
+    float *amax_attn = nullptr, *amax_act = nullptr;   // per-row |max| published by the producers
     CUtensorMap tm_y8, tm_attn8, tm_act8;
     bool finalized = false;
     std::string err;
@@ -255,7 +256,7 @@ h3enc_status create_fp8(h3enc *h) {
     }
     const size_t T = c.max_tokens;
     const size_t b_y = align256(T * H), b_a = align256(T * AO), b_act = align256(T * I), b_s = align256(T * 4);
-    const size_t wsz = b_y + b_a + b_act + 3 * b_s;
+    const size_t wsz = b_y + b_a + b_act + 5 * b_s;
     e = cudaMalloc(&h->ws8, wsz);
     if (e != cudaSuccess) return fail(h, H3ENC_ERR_OOM, "FP8 workspace of %zu bytes: %s", wsz, cudaGetErrorString(e));
     p = h->ws8;
@@ -264,7 +265,9 @@ h3enc_status create_fp8(h3enc *h) {
     h->act8 = reinterpret_cast<uint8_t *>(p); p += b_act;
     h->sy = reinterpret_cast<float *>(p); p += b_s;
     h->sattn = reinterpret_cast<float *>(p); p += b_s;
-    h->sact = reinterpret_cast<float *>(p);
+    h->sact = reinterpret_cast<float *>(p); p += b_s;
+    h->amax_attn = reinterpret_cast<float *>(p); p += b_s;
+    h->amax_act = reinterpret_cast<float *>(p);
     e = cudaMemset(h->ws8, 0, wsz);
     if (e != cudaSuccess) return fail(h, H3ENC_ERR_CUDA, "FP8 workspace clear: %s", cudaGetErrorString(e));
     const uint32_t ba = (uint32_t)h3::gemm_box_rows_a();
@@ -342,6 +345,11 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
     }
     const bool f8 = c.linear_fp8 != 0;
     const int AO = nq * d;
+    if (f8 && le > lb) {
+        // the quantising passes clear the row maxima after use; start every encode from zeros
+        e = cudaMemsetAsync(h->amax_attn, 0, 2 * align256((size_t)c.max_tokens * 4), st);
+        if (e != cudaSuccess) return cuda_fail(h, e, "FP8 row maxima clear");
+    }
     for (int l = lb; l < le; ++l) {
         LayerW &w = h->layers[l];
         h3enc::Layer8 *w8 = f8 ? &h->layers8[l] : nullptr;
@@ -370,11 +378,14 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         e = run(h, H3ENC_K_GEMM_QKV, st, [&] { return h3::launch_gemm(p, st); });
         if (e != cudaSuccess) return cuda_fail(h, e, "qkv gemm");
         e = run(h, H3ENC_K_ATTN, st,
-                [&] { return h3::launch_attention(h->qkv, h->attn, S, nq, nkv, d, cu, n_seqs, h->status, st); });
+                [&] {
+                    return h3::launch_attention(h->qkv, h->attn, S, nq, nkv, d, cu, n_seqs, h->status, st,
+                                                f8 ? h->amax_attn : nullptr);
+                });
         if (e != cudaSuccess) return cuda_fail(h, e, "attention");
         if (f8) {
             e = run(h, H3ENC_K_QUANT, st, [&] {
-                return h3::launch_quant_rows(h->attn, AO, S, AO, h->attn8, AO, h->sattn, st);
+                return h3::launch_quant_rows_amax(h->attn, AO, S, AO, h->attn8, AO, h->sattn, h->amax_attn, st);
             });
             if (e != cudaSuccess) return cuda_fail(h, e, "attention output quantisation");
         }
@@ -398,11 +409,12 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         p.sw = f8 ? w8->s_gu : nullptr;
         p.N = 2 * I; p.K = H; p.epi = h3::EPI_SWIGLU;
         p.C = h->act; p.ldc = I; p.R = nullptr;
+        p.row_amax = f8 ? h->amax_act : nullptr;
         e = run(h, H3ENC_K_GEMM_GATE_UP, st, [&] { return h3::launch_gemm(p, st); });
         if (e != cudaSuccess) return cuda_fail(h, e, "gate/up gemm");
         if (f8) {
             e = run(h, H3ENC_K_QUANT, st,
-                    [&] { return h3::launch_quant_rows(h->act, I, S, I, h->act8, I, h->sact, st); });
+                    [&] { return h3::launch_quant_rows_amax(h->act, I, S, I, h->act8, I, h->sact, h->amax_act, st); });
             if (e != cudaSuccess) return cuda_fail(h, e, "SwiGLU output quantisation");
         }
         p.tmA = f8 ? &h->tm_act8 : &h->tm_act;

@@ -51,6 +51,7 @@ struct AttnTcArgs {
     int cu[kMaxSeqs + 1];
     int pair_start[kMaxSeqs + 1];   // first tile-pair index of each sequence
     unsigned long long *trace;      // optional [grid][ATR_COUNT] timeline
+    float *row_amax;                // optional [S]: atomic max of |output| per row (bf16 values, >= 0)
 };
 
 // Timeline of one persistent CTA (h3enc_op_attention_trace_next): %globaltimer at
@@ -390,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const bool live = qpos < w.L;
             bf16 *dst = a.o + (size_t)(w.seg0 + qpos) * a.ld_o + (size_t)w.head * D;
+            float rmax = 0.f;   // largest |bf16 output| of this row's head
             #pragma unroll 1
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t v[32];
@@ -405,9 +407,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         u.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
                         u.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
                         d4[q] = u;
+                        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+                        #pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            rmax = fmaxf(rmax, fmaxf(fabsf(bf16_lo(uw[k])), fabsf(bf16_hi(uw[k]))));
                     }
                 }
             }
+            // non-negative floats order like their bit patterns: an integer max is exact
+            if (live && a.row_amax)
+                atomicMax(reinterpret_cast<int *>(a.row_amax + w.seg0 + qpos), __float_as_int(rmax));
         }
         if (!good && lane == 0) {
             report(a.status, ST_TIMEOUT);
@@ -446,7 +455,7 @@ thread_local unsigned long long *t_attn_trace = nullptr;
 void attention_trace_next(unsigned long long *trace) { t_attn_trace = trace; }
 int attention_trace_fields() { return ATR_COUNT; }
 cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, int d, const int32_t *cu_host,
-                             int n_seqs, int32_t *status, cudaStream_t st) {
+                             int n_seqs, int32_t *status, cudaStream_t st, float *row_amax) {
     if (S <= 0) return cudaSuccess;
     if (d != 64 && d != 128) return cudaErrorInvalidValue;
     static AttnTcArgs args;
@@ -462,6 +471,7 @@ cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, i
     args.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
     args.status = status;
     args.trace = t_attn_trace;
+    args.row_amax = row_amax;
     t_attn_trace = nullptr;
     int n = 0, pairs = 0;
     if (!cu_host) {

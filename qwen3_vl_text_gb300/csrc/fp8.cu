@@ -78,6 +78,41 @@ __global__ void __launch_bounds__(QT) quant_rows_kernel(const bf16 *__restrict__
     }
 }
 
+// One CTA per row with the row's amax already known: a single quantising pass; the amax
+// slot is cleared for the next producer once every thread has read it.
+__global__ void __launch_bounds__(QT) quant_rows_amax_kernel(const bf16 *__restrict__ x, int ldx, int cols,
+                                                             uint8_t *__restrict__ q, int ldq, float *scale,
+                                                             float *row_amax) {
+    pdl_trigger();
+    pdl_wait();
+    const int row = blockIdx.x;
+    const float amax = row_amax[row];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        row_amax[row] = 0.f;
+        scale[row] = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    }
+    const float inv = amax > 0.f ? __fdiv_rn(448.0f, amax) : 1.0f;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)row * ldx);
+    uint2 *qr = reinterpret_cast<uint2 *>(q + (size_t)row * ldq);
+    const int nvec = cols >> 3;
+    // four 16-byte loads in flight per thread before the first conversion
+    for (int i0 = threadIdx.x; i0 < nvec; i0 += 4 * QT) {
+        uint4 v[4];
+        #pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (i0 + u * QT < nvec) v[u] = xr[i0 + u * QT];
+        #pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (i0 + u * QT < nvec) {
+                float f[8];
+                unpack8(v[u], f);
+                qr[i0 + u * QT] = quant8(f, inv);
+            }
+        }
+    }
+}
+
 // RMSNorm of one row kept in registers (cols <= 8192), rounded to bf16, then quantised.
 constexpr int NQ_VPT = 4;   // 4 x 8 elements per thread -> cols <= 8192
 __global__ void __launch_bounds__(QT) rmsnorm_q8_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
@@ -144,6 +179,15 @@ cudaError_t launch_quant_rows(const bf16 *x, int ldx, int rows, int cols, uint8_
     cudaLaunchAttribute at[1];
     cudaLaunchConfig_t cfg = pdl_config(dim3(rows), dim3(QT), 0, st, at);
     return cudaLaunchKernelEx(&cfg, quant_rows_kernel, x, ldx, cols, q, ldq, scale);
+}
+
+cudaError_t launch_quant_rows_amax(const bf16 *x, int ldx, int rows, int cols, uint8_t *q, int ldq, float *scale,
+                                   float *row_amax, cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    if (cols % 8 || ldx % 8 || ldq % 8 || !row_amax) return cudaErrorInvalidValue;
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3(rows), dim3(QT), 0, st, at);
+    return cudaLaunchKernelEx(&cfg, quant_rows_amax_kernel, x, ldx, cols, q, ldq, scale, row_amax);
 }
 
 cudaError_t launch_rmsnorm_q8(const bf16 *x, const bf16 *w, uint8_t *q, float *scale, int rows, int cols, float eps,

@@ -83,6 +83,7 @@ struct GemmArgs {
     unsigned long long *trace;   // optional [grid][TR_COUNT] %globaltimer stamps
     // e4m3 operands: C = (A8 * sa[row]) (W8 * sw[col])^T
     const float *sa, *sw;
+    float *row_amax;   // EPI_SWIGLU, optional: per-row max |bf16 output| (integer atomic max)
 };
 
 // Phase stamps of the optional timeline (h3enc_op_gemm_traced).
@@ -583,6 +584,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             o.x = pack_bf16x2(f[0], f[1]);
                             o.y = pack_bf16x2(f[2], f[3]);
                             *reinterpret_cast<uint2 *>(g.C + (size_t)row * g.ldc + col) = o;
+                            if constexpr (EPI == EPI_SWIGLU) {
+                                if (g.row_amax) {
+                                    const float m = fmaxf(fmaxf(fabsf(bf16_lo(o.x)), fabsf(bf16_hi(o.x))),
+                                                          fmaxf(fabsf(bf16_lo(o.y)), fabsf(bf16_hi(o.y))));
+                                    atomicMax(reinterpret_cast<int *>(g.row_amax + row), __float_as_int(m));
+                                }
+                            }
                         }
                     }
                 }
@@ -607,6 +615,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (!wait_acc()) break;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
             if constexpr (EPI == EPI_SWIGLU) {
+                float rmax = 0.f;   // largest |bf16 output| of this thread's row in the tile
                 #pragma unroll 1
                 for (int c = ehalf * (BN / 128); c < (ehalf + 1) * (BN / 128); ++c) {
                     uint32_t vg[32], vu[32];
@@ -622,10 +631,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             const float gt = __uint_as_float(vg[j]);
                             const float up = __uint_as_float(vu[j]);
                             f[j] = gt / (1.0f + expf(-gt)) * up;
+                            rmax = fmaxf(rmax, fabsf(round_bf16(f[j])));
                         }
                         store_row32(g.C + (size_t)row * g.ldc + n_blk * (BN / 2) + c * 32, f);
                     }
                 }
+                // non-negative floats order like their bit patterns: an integer max is exact
+                if (live && g.row_amax) atomicMax(reinterpret_cast<int *>(g.row_amax + row), __float_as_int(rmax));
             } else if constexpr (EPI == EPI_QKROPE) {
                 // the tile holds BN/d whole heads: q and k heads get RMSNorm over d and M-RoPE
                 // (pairs j, j + d/2 both in this thread's row), v heads are stored as they are
@@ -820,6 +832,7 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     g.nn = p.N / BN;
     g.nk = F8 ? (p.K + BK8 - 1) / BK8 : (p.K + BK - 1) / BK;
     g.sa = p.sa; g.sw = p.sw;
+    g.row_amax = p.row_amax;
     g.C = p.C; g.ldc = p.ldc; g.R = p.R; g.DS = p.DS; g.vis_rank = p.vis_rank; g.n_vis = p.n_vis;
     g.status = p.status;
     g.wq = p.wq; g.wk = p.wk; g.cos_t = p.cos_t; g.sin_t = p.sin_t;

@@ -40,6 +40,8 @@ struct GemmPlan {
     // sa [M] and sw [N] fp32 (sw 16-byte aligned)
     bool fp8 = false;
     const float *sa = nullptr, *sw = nullptr;
+    // EPI_SWIGLU (optional): each row's largest |bf16 output| merged with an integer atomic max
+    float *row_amax = nullptr;
 };
 // Tensor map of a row-major bf16 matrix [rows, cols] read in boxes of
 // box_rows x 64 with 128-byte swizzle.  False if the driver refuses it.
@@ -51,6 +53,10 @@ bool make_tmap_rows_e4m3(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_
 // leading dimensions ldx / ldq (elements).  cols % 8 == 0.
 cudaError_t launch_quant_rows(const bf16 *x, int ldx, int rows, int cols, uint8_t *q, int ldq, float *scale,
                               cudaStream_t st);
+// The same quantisation with each row's amax given (row_amax, as produced by the attention or
+// SwiGLU epilogue): one pass over x; row_amax is reset to zero for its next producer.
+cudaError_t launch_quant_rows_amax(const bf16 *x, int ldx, int rows, int cols, uint8_t *q, int ldq, float *scale,
+                                   float *row_amax, cudaStream_t st);
 // RMSNorm (as launch_rmsnorm, output rounded to bf16) followed by the per-row
 // e4m3 quantisation of that bf16 output.
 cudaError_t launch_rmsnorm_q8(const bf16 *x, const bf16 *w, uint8_t *q, float *scale, int rows, int cols, float eps,
@@ -81,8 +87,10 @@ cudaError_t launch_rope_table(const int32_t *positions, int S, const RopeParams 
 
 
 // ---- attention on tcgen05 (attention_tc.cu)
+// row_amax (optional, [S] floats): each row's largest |bf16 output| is merged in with an
+// integer atomic max (the buffer must hold zeros or smaller values beforehand).
 cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, int d, const int32_t *cu_host,
-                             int n_seqs, int32_t *status, cudaStream_t st);
+                             int n_seqs, int32_t *status, cudaStream_t st, float *row_amax = nullptr);
 
 // ---- embedding gather, visual ranks, weight packing (embed.cu)
 cudaError_t launch_embed(const int32_t *ids, const bf16 *table, int vocab, int hidden, bf16 *out, int S,
