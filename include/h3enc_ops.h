@@ -49,7 +49,8 @@ H3ENC_API h3enc_status h3enc_op_gemm(const void *A, const void *W, void *C, int3
 /* Profiling aid: the next projection GEMM this host thread launches (through
  * h3enc_op_gemm, h3enc_op_gemm_qkv_rope, h3enc_op_gemm_noalloc or inside an
  * encode) records a timeline: CTA c writes 11 %globaltimer stamps (ns) to
- * trace[c * 11 + k]: k = 0 start, 1 prologue done, 2 first load issued, 3 first
+ * trace[c * 11 + k]: k = 0 start, 1 prologue done, 2 last data-parallel accumulator
+ * ready (epilogue start of the last tile), 3 first
  * MMA, 4 last data-parallel MMA issued, 5 data-parallel epilogues done, 6 first
  * stream-K accumulator ready, 7 stream-K partials written, 8 first tile's
  * contributor flags seen, 9 stream-K reduction done, 10 end.  The stream-K phase

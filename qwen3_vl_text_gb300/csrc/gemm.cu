@@ -53,7 +53,11 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB per CTA
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_THREADS = EPI_WARPS * 32;
 constexpr int GEMM_THREADS = 64 + EPI_THREADS;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+// per epilogue warp two 32 x 32 bf16 staging slots for the TMA tile stores
+constexpr int C_SLOT_BYTES = 32 * 32 * 2;
+constexpr int C_STAGE_BYTES = EPI_WARPS * 2 * C_SLOT_BYTES;   // 32 KB
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + C_STAGE_BYTES + 256;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
 constexpr int kMinStreamKBlocks = 4;             // smallest k-range a stream-K pair takes
 static_assert(BM * BN % 4 == 0, "partials are written as float4");
 
@@ -87,7 +91,7 @@ struct GemmArgs {
 };
 
 // Phase stamps of the optional timeline (h3enc_op_gemm_traced).
-enum { TR_START = 0, TR_READY, TR_FIRST_LOAD, TR_FIRST_MMA, TR_LAST_DP_MMA, TR_DP_EPI_DONE, TR_SPLIT_MMA_DONE,
+enum { TR_START = 0, TR_READY, TR_LAST_ACC, TR_FIRST_MMA, TR_LAST_DP_MMA, TR_DP_EPI_DONE, TR_SPLIT_MMA_DONE,
        TR_DUMP_DONE, TR_FLAGS_SEEN, TR_REDUCE_DONE, TR_END, TR_COUNT };
 __device__ __forceinline__ void stamp(const GemmArgs &g, int what) {
     if (g.trace) {
@@ -184,28 +188,16 @@ __device__ __forceinline__ void load_row32(const __nv_bfloat16 *p, float (&f)[32
     }
 }
 
-__device__ __forceinline__ void store_row32(__nv_bfloat16 *p, const float (&f)[32]) {
-    uint4 *q = reinterpret_cast<uint4 *>(p);
-    #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint4 v;
-        v.x = pack_bf16x2(f[8 * i + 0], f[8 * i + 1]);
-        v.y = pack_bf16x2(f[8 * i + 2], f[8 * i + 3]);
-        v.z = pack_bf16x2(f[8 * i + 4], f[8 * i + 5]);
-        v.w = pack_bf16x2(f[8 * i + 6], f[8 * i + 7]);
-        q[i] = v;
-    }
-}
-
 template <int EPI, bool F8>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const GemmArgs g) {
+                        const __grid_constant__ CUtensorMap tmC, const GemmArgs g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * A_BYTES;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
+    uint8_t *sC = sB + STAGES * B_BYTES;   // epilogue staging (1024-byte aligned)
+    uint64_t *full = reinterpret_cast<uint64_t *>(sC + C_STAGE_BYTES);
     uint64_t *empty = full + STAGES;
     uint64_t *acc_full = empty + STAGES;
     uint64_t *acc_empty = acc_full + 2;
@@ -269,7 +261,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     constexpr int kbe = F8 ? BK8 : BK;   // elements of one 128-byte k-block row
                     tma_load_2d_pair(sA + stage * A_BYTES, &tmA, bar, kb * kbe, m0);
                     tma_load_2d_pair(sB + stage * B_BYTES, &tmB, bar, kb * kbe, n0);
-                    if (issued[0] + issued[1] == 0 && stage == 0) stamp(g, TR_FIRST_LOAD);
                     ++issued[stage];
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -356,6 +347,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const float4 sw = *reinterpret_cast<const float4 *>(g.sw + n0);
                 f[0] *= sr * sw.x; f[1] *= sr * sw.y; f[2] *= sr * sw.z; f[3] *= sr * sw.w;
             }
+        };
+        // data-parallel outputs leave through shared memory: the warp's 32 rows x 32 columns are
+        // written to one of its two slots (row = lane, 64 bytes each) and stored by one TMA tile
+        // store (rows past M are clipped); a slot is refilled once its store has read it
+        uint8_t *cslots = sC + (warp - 2) * 2 * C_SLOT_BYTES;
+        uint32_t cstores = 0;
+        auto store_chunk = [&](const uint32_t (&pk)[16], int col, int row0) {
+            uint8_t *slot = cslots + (cstores & 1) * C_SLOT_BYTES;
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+            uint4 *dst = reinterpret_cast<uint4 *>(slot + lane * 64);
+            #pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && row0 < g.M) {   // a box wholly past the last row is not issued
+                tma_store_2d(&tmC, slot, col, row0);
+                bulk_commit();
+            }
+            ++cstores;
+        };
+        auto store_chunk_f = [&](const float (&f)[32], int col, int row0) {
+            uint32_t pk[16];
+            #pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+            store_chunk(pk, col, row0);
         };
         const uint32_t acc_empty_lead[2] = {mapa_shared(smem_u32(&acc_empty[0]), 0),
                                             mapa_shared(smem_u32(&acc_empty[1]), 0)};
@@ -600,7 +617,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int tile = pair; tile < g.dp_tiles; tile += npairs) {
             const int m_blk = tile % g.nm;
             const int n_blk = tile / g.nm;
-            const int row = m_blk * (2 * BM) + (int)rank * BM + quarter * 32 + lane;
+            const int row0 = m_blk * (2 * BM) + (int)rank * BM + quarter * 32;   // the warp's first row
+            const int row = row0 + lane;
             const bool live = row < g.M;
             uint4 rpre[BN / 16];   // this thread's BN/2 residual columns
             if constexpr (EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_DS) {
@@ -613,6 +631,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
             }
             if (!wait_acc()) break;
+            if (et == 0) stamp(g, TR_LAST_ACC);   // overwritten per tile: the last one stays
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
             if constexpr (EPI == EPI_SWIGLU) {
                 float rmax = 0.f;   // largest |bf16 output| of this thread's row in the tile
@@ -624,17 +643,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     tmem_ld_wait();
                     dq32(vg, row, live, n_blk * BN + c * 32);
                     dq32(vu, row, live, n_blk * BN + BN / 2 + c * 32);
-                    if (live) {
-                        float f[32];
-                        #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float gt = __uint_as_float(vg[j]);
-                            const float up = __uint_as_float(vu[j]);
-                            f[j] = gt / (1.0f + expf(-gt)) * up;
-                            rmax = fmaxf(rmax, fabsf(round_bf16(f[j])));
-                        }
-                        store_row32(g.C + (size_t)row * g.ldc + n_blk * (BN / 2) + c * 32, f);
+                    float f[32];
+                    #pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float gt = __uint_as_float(vg[j]);
+                        const float up = __uint_as_float(vu[j]);
+                        f[j] = gt / (1.0f + expf(-gt)) * up;
+                        rmax = fmaxf(rmax, fabsf(round_bf16(f[j])));
                     }
+                    store_chunk_f(f, n_blk * (BN / 2) + c * 32, row0);
                 }
                 // non-negative floats order like their bit patterns: an integer max is exact
                 if (live && g.row_amax) atomicMax(reinterpret_cast<int *>(g.row_amax + row), __float_as_int(rmax));
@@ -647,7 +664,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 for (int hh = ehalf * (hpt >> 1); hh < (ehalf + 1) * (hpt >> 1); ++hh) {
                     const int head = (n_blk * BN) / d + hh;
                     const int cb = hh * d;
-                    __nv_bfloat16 *dst = g.C + (size_t)row * g.ldc + n_blk * BN + cb;
                     const bool is_q = head < g.nq, is_k = !is_q && head < g.nq + g.nkv;
                     if (!is_q && !is_k) {
                         #pragma unroll 1
@@ -656,12 +672,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             tmem_ld32(taddr + cb + c * 32, v);
                             tmem_ld_wait();
                             dq32(v, row, live, n_blk * BN + cb + c * 32);
-                            if (live) {
-                                float f[32];
-                                #pragma unroll
-                                for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
-                                store_row32(dst + c * 32, f);
-                            }
+                            float f[32];
+                            #pragma unroll
+                            for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+                            store_chunk_f(f, n_blk * BN + cb + c * 32, row0);
                         }
                         continue;
                     }
@@ -685,10 +699,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         tmem_ld_wait();
                         dq32(va, row, live, n_blk * BN + cb + c * 32);
                         dq32(vb, row, live, n_blk * BN + cb + half + c * 32);
+                        uint32_t oa[16], ob[16];
+                        #pragma unroll
+                        for (int i = 0; i < 16; ++i) oa[i] = ob[i] = 0u;   // rows past M: clipped by the store
                         if (live) {
                             const float *cs = g.cos_t + (size_t)row * half + c * 32;
                             const float *sn = g.sin_t + (size_t)row * half + c * 32;
-                            uint32_t oa[16], ob[16];
                             #pragma unroll
                             for (int j = 0; j < 32; j += 4) {
                                 const float4 co = *reinterpret_cast<const float4 *>(cs + j);
@@ -711,14 +727,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                 ob[j / 2] = pack_bf16x2(rb[0], rb[1]);
                                 ob[j / 2 + 1] = pack_bf16x2(rb[2], rb[3]);
                             }
-                            uint4 *pa = reinterpret_cast<uint4 *>(dst + c * 32);
-                            uint4 *pb = reinterpret_cast<uint4 *>(dst + half + c * 32);
-                            #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                pa[q] = make_uint4(oa[4 * q], oa[4 * q + 1], oa[4 * q + 2], oa[4 * q + 3]);
-                                pb[q] = make_uint4(ob[4 * q], ob[4 * q + 1], ob[4 * q + 2], ob[4 * q + 3]);
-                            }
                         }
+                        store_chunk(oa, n_blk * BN + cb + c * 32, row0);
+                        store_chunk(ob, n_blk * BN + cb + half + c * 32, row0);
                     }
                 }
             } else {
@@ -737,10 +748,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     tmem_ld32(taddr + c * 32, v);
                     tmem_ld_wait();
                     dq32(v, row, live, col);
+                    float f[32];
+                    #pragma unroll
+                    for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
                     if (live) {
-                        float f[32];
-                        #pragma unroll
-                        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
                         if constexpr (EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_DS) {
                             #pragma unroll
                             for (int i = 0; i < 4; ++i) {
@@ -759,12 +770,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                 for (int j = 0; j < 32; ++j) f[j] = round_bf16(f[j]) + ds[j];
                             }
                         }
-                        store_row32(g.C + (size_t)row * g.ldc + col, f);
                     }
+                    store_chunk_f(f, col, row0);
                 }
             }
             release_acc();
         }
+        if (lane == 0) bulk_wait_all();   // this warp's tile stores have landed
         if (et == 0) stamp(g, TR_DP_EPI_DONE);
     }
 
@@ -800,6 +812,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
     }
     return fn;
+}
+
+// Output map for the epilogue's tile stores: bf16 [rows, ld] row-major, boxes of 32 x 32, no swizzle.
+bool make_tmap_c(CUtensorMap *m, void *ptr, uint64_t rows, uint64_t ld) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn || rows == 0 || ld == 0 || (ld * 2) % 16 != 0 || (reinterpret_cast<uintptr_t>(ptr) & 15)) return false;
+    cuuint64_t dims[2] = {ld, rows};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 template <int EPI, bool F8>
@@ -868,7 +893,9 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<EPI, F8>, *p.tmA, *p.tmW, g);
+    CUtensorMap tmC;
+    if (!make_tmap_c(&tmC, p.C, (uint64_t)p.M, (uint64_t)p.ldc)) return cudaErrorInvalidValue;
+    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<EPI, F8>, *p.tmA, *p.tmW, tmC, g);
 }
 
 }  // namespace
