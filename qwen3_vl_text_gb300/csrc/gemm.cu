@@ -176,6 +176,10 @@ __device__ __forceinline__ bool epi_bar_and(bool v) {
     return r != 0;
 }
 
+// silu(g) * u = g * u / (1 + e^-g), with the fast exponential and division intrinsics (a few
+// ulps of fp32, far below the bf16 rounding of the result); a very negative g gives 0.
+__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g * u, 1.0f + __expf(-g)); }
+
 __device__ __forceinline__ void load_row32(const __nv_bfloat16 *p, float (&f)[32]) {
     const uint4 *q = reinterpret_cast<const uint4 *>(p);
     #pragma unroll
@@ -579,7 +583,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             int col;
                             if constexpr (EPI == EPI_SWIGLU) {
                                 #pragma unroll
-                                for (int i = 0; i < 4; ++i) f[i] = f[i] / (1.0f + expf(-f[i])) * up[i];
+                                for (int i = 0; i < 4; ++i) f[i] = silu_mul(f[i], up[i]);
                                 col = n_blk * (BN / 2) + c4;
                             } else {
                                 col = n_blk * BN + c4;
@@ -648,7 +652,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     for (int j = 0; j < 32; ++j) {
                         const float gt = __uint_as_float(vg[j]);
                         const float up = __uint_as_float(vu[j]);
-                        f[j] = gt / (1.0f + expf(-gt)) * up;
+                        f[j] = silu_mul(gt, up);
                         rmax = fmaxf(rmax, fabsf(round_bf16(f[j])));
                     }
                     store_chunk_f(f, n_blk * (BN / 2) + c * 32, row0);
