@@ -26,6 +26,7 @@
 // TMEM columns: S_A 0-127, S_B 128-255, O_A 256-(256+d), O_B 384-(384+d).
 // No softmax thread waits for another: the row max needs no exchange, and the
 // previous P V product is awaited only before a rescale.  Every wait is bounded.
+#include <atomic>
 #include <cmath>
 
 #include "common.cuh"
@@ -436,12 +437,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 cudaError_t launch_tc(const CUtensorMap &tm, const AttnTcArgs &args, int grid, cudaStream_t st) {
-    static bool attr = false;
-    if (!attr) {
+    static std::atomic<bool> attr_of[kMaxDevices];   // per device: the shared-memory opt-in
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!attr_of[dev].load()) {
         cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              TcLayout<D>::SMEM);
         if (e != cudaSuccess) return e;
-        attr = true;
+        attr_of[dev].store(true);
     }
     cudaLaunchAttribute at[1];
     cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(kThreads), TcLayout<D>::SMEM, st, at);
@@ -458,7 +461,7 @@ cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, i
                              int n_seqs, int32_t *status, cudaStream_t st, float *row_amax) {
     if (S <= 0) return cudaSuccess;
     if (d != 64 && d != 128) return cudaErrorInvalidValue;
-    static AttnTcArgs args;
+    AttnTcArgs args;   // per call: launches from several host threads do not share it
     const int ld = (nq + 2 * nkv) * d;
     CUtensorMap tm;
     if (!make_tmap_rows(&tm, qkv, (uint64_t)S, (uint64_t)ld, TQ)) return cudaErrorInvalidValue;

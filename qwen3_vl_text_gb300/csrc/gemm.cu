@@ -35,6 +35,8 @@
 // in-flight copies and MMAs, frees TMEM and exits.
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -833,7 +835,11 @@ bool make_tmap_c(CUtensorMap *m, void *ptr, uint64_t rows, uint64_t ld) {
 
 template <int EPI, bool F8>
 cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
-    static int max_pairs = 0;
+    // per device: the shared-memory opt-in and the number of co-resident pairs
+    static std::atomic<int> max_pairs_of[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    int max_pairs = max_pairs_of[dev].load();
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -854,6 +860,7 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         if (n <= 0) return cudaErrorInvalidConfiguration;
         max_pairs = n;
+        max_pairs_of[dev].store(n);
     }
     GemmArgs g;
     g.M = p.M; g.N = p.N; g.K = p.K;

@@ -26,7 +26,7 @@ constexpr size_t kScratchBytes = kFlagOffset + kFlagWords * sizeof(uint32_t);  /
 
 static __device__ __align__(256) unsigned char g_gemm_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
+using h3::kMaxDevices;
 std::mutex g_setup_mutex;
 unsigned char *g_scratch_addr[kMaxDevices] = {nullptr};
 

@@ -13,6 +13,7 @@ using bf16 = __nv_bfloat16;
 enum { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_RESIDUAL_DS = 3, EPI_QKROPE = 4 };
 
 constexpr int kMaxSeqs = 1024;
+constexpr int kMaxDevices = 64;   // per-device launch caches
 constexpr int kMaxHalfDim = 64;
 
 // ---- projection GEMM (gemm.cu)
