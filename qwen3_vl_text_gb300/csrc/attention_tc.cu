@@ -83,6 +83,31 @@ struct TcLayout {
     static constexpr int SMEM = 1024 + OFF_BAR + 256;   // 15 barriers, TMEM slot, abort flag
 };
 
+// Paired fp32 arithmetic (two lanes per instruction) and the three-input maximum.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t r, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -328,13 +353,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < TK; ++i)
                         if (key0 + i > qpos) v[i] = __float_as_uint(-INFINITY);
                 }
+                // (three-input maxima: chain u takes scores u, u + 8, ..., u + 120)
                 float mx[8];
                 #pragma unroll
-                for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(v[u]);
-                #pragma unroll
-                for (int i = 8; i < TK; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(v[i]));
-                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * a.scale_log2;
+                for (int u = 0; u < 8; ++u) {
+                    float m = __uint_as_float(v[u]);
+                    #pragma unroll
+                    for (int k = 1; k < 15; k += 2)
+                        m = fmax3(m, __uint_as_float(v[u + 8 * k]), __uint_as_float(v[u + 8 * k + 8]));
+                    mx[u] = fmaxf(m, __uint_as_float(v[u + 120]));
+                }
+                const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7])) *
+                                 a.scale_log2;
                 float alpha = 1.f;
                 bool rescale = false;
                 if (j == 0) {
@@ -345,22 +375,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rescale = true;
                 }
                 // P = exp2(s * scale - m) packed as bf16 pairs over the first 64 columns of this
-                // row of S; the row sum in 4 independent chains
-                const float neg_m = -m_use;
-                float rs[4] = {0.f, 0.f, 0.f, 0.f};
+                // row of S; scale-and-subtract and the row sum on fp32 pairs, the sum in 4 chains
+                const uint64_t scale2 = f32x2(a.scale_log2, a.scale_log2);
+                const uint64_t neg_m2 = f32x2(-m_use, -m_use);
+                uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
                 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t pk[32];
                     #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float p0 = ex2(fmaf(__uint_as_float(v[64 * h + 2 * i]), a.scale_log2, neg_m));
-                        const float p1 = ex2(fmaf(__uint_as_float(v[64 * h + 2 * i + 1]), a.scale_log2, neg_m));
-                        rs[i & 3] += p0 + p1;
+                        const uint64_t x2 = ffma2(f32x2(__uint_as_float(v[64 * h + 2 * i]),
+                                                        __uint_as_float(v[64 * h + 2 * i + 1])),
+                                                  scale2, neg_m2);
+                        float x0, x1;
+                        f32x2_split(x2, x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        rs2[i & 3] = fadd2(rs2[i & 3], f32x2(p0, p1));
                         pk[i] = pack_bf16x2(p0, p1);
                     }
                     tmem_st32(tS + 32 * h, pk);
                 }
-                l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+                float rs = 0.f;
+                #pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float r0, r1;
+                    f32x2_split(rs2[q], r0, r1);
+                    rs += r0 + r1;
+                }
+                l = l * alpha + rs;
                 // O is rescaled after the previous P V product of this tile has completed
                 if (__any_sync(0xffffffffu, rescale)) {
                     good = __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (c - 1) & 1, abort_flag));
