@@ -200,3 +200,34 @@ def test_fp8_one_full_width_layer_against_fp8_oracle():
     ref8bf = O.forward(x0, inp["positions"], cfg, lambda _: w, fp8=True, storage=GPU_STORAGE)
     ok, msg = within(got, ref8, ref8bf, 5e-3)
     assert ok, "fp8 layer vs fp8 oracle: " + msg
+
+
+@pytest.mark.slow
+def test_fp8_packed_prompts_two_full_width_layers():
+    """16 packed prompts of 77-512 tokens through two full-width layers in FP8 mode: per-token
+    activation scales and block-diagonal attention over cu_seqlens, against the oracle's FP8
+    forward on the same packing."""
+    import dataclasses
+    wl = W.workload(4)
+    cfg = dataclasses.replace(wl.model, num_layers=2)
+    inp = W.gen_inputs(wl)
+    S = inp["seq_len"]
+    cu = [int(c) for c in inp["cu_seqlens"]]
+    enc = make_encoder(wl, cfg, max_tokens=S, max_seqs=32, fp8=True)
+    try:
+        ids = torch.from_numpy(inp["input_ids"]).cuda()
+        pos = torch.from_numpy(inp["positions"]).cuda()
+        out = torch.empty(S, cfg.hidden, dtype=torch.bfloat16, device="cuda")
+        Q.h3enc_encode(enc.handle, ids, pos, None, None, 0, 0, cu, S, out)
+        torch.cuda.synchronize()
+        assert enc.status() == 0, Q.h3enc_last_error(enc.handle)
+        got = t2f(out)
+    finally:
+        enc.close()
+    x0 = oracle_embed(wl, cfg, inp["input_ids"])
+    get = oracle_layer_getter(wl, cfg)
+    ws = [get(l) for l in range(cfg.num_layers)]
+    ref8 = O.forward(x0, inp["positions"], cfg, ws.__getitem__, cu_seqlens=cu, fp8=True)
+    ref8bf = O.forward(x0, inp["positions"], cfg, ws.__getitem__, cu_seqlens=cu, fp8=True, storage=GPU_STORAGE)
+    ok, msg = within(got, ref8, ref8bf, 2e-2, 0.05)
+    assert ok, "fp8 packed prompts vs fp8 oracle: " + msg
