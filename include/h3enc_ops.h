@@ -70,6 +70,16 @@ H3ENC_API h3enc_status h3enc_op_gemm_trace_next(void *trace, int64_t trace_entri
  * covers every launch), alive until that launch has run. */
 H3ENC_API h3enc_status h3enc_op_attention_trace_next(void *trace, int64_t trace_entries, int32_t ctas);
 
+/* Failure-detection self-test (no counterpart on the pages).  Launches one
+ * thread on `stream` that waits, through the library's bounded-wait helpers,
+ * either until the device word *flag equals `expect` (use_mbarrier = 0) or on a
+ * shared-memory mbarrier that nothing arrives on (use_mbarrier = 1).  A wait that
+ * is not satisfied within the wait limit (about 2 s of SM clock) ORs ST_TIMEOUT
+ * (1) into the device int32 *status and returns; the context stays usable.
+ * flag: device memory (ignored when use_mbarrier = 1). */
+H3ENC_API h3enc_status h3enc_op_wait_probe(const uint32_t *flag, uint32_t expect, int32_t use_mbarrier,
+                                 int32_t *status, void *stream);
+
 /* Workspace bytes h3enc_op_gemm needs on the current device (-1 without a device). */
 H3ENC_API int64_t h3enc_op_gemm_workspace_bytes(void);
 

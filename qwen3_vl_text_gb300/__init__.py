@@ -19,7 +19,7 @@ __all__ = [
     "h3enc_set_profiling", "h3enc_set_profiling_classes", "h3enc_get_profile", "h3enc_launch_count", "h3enc_num_sms",
     "h3enc_build_positions", "h3enc_aggregate_deepstack",
     "h3enc_op_gemm", "h3enc_op_gemm_workspace_bytes", "h3enc_op_gemm_trace_next", "h3enc_op_attention_trace_next", "h3enc_op_gemm_noalloc", "h3enc_op_gemm_noalloc_scratch_bytes", "h3enc_op_pack_gate_up", "h3enc_op_rmsnorm", "h3enc_op_gemm_fp8", "h3enc_op_quant_rows",
-    "h3enc_op_rmsnorm_q8", "h3enc_op_rope_table",
+    "h3enc_op_rmsnorm_q8", "h3enc_op_wait_probe", "h3enc_op_rope_table",
     "h3enc_op_gemm_qkv_rope", "h3enc_op_attention", "h3enc_op_embed", "h3enc_op_vis_rank", "Encoder",
     "KERNEL_CLASSES",
 ]
@@ -88,6 +88,7 @@ _SIGS = {
     "h3enc_op_rmsnorm": ([_P, _P, _P, _I32, _I32, _F, _P], _I32),
     "h3enc_op_gemm_fp8": ([_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _I64, _P, _P], _I32),
     "h3enc_op_quant_rows": ([_P, _I32, _I32, _P, _P, _P], _I32),
+    "h3enc_op_wait_probe": ([_P, ctypes.c_uint32, _I32, _P, _P], _I32),
     "h3enc_op_rmsnorm_q8": ([_P, _P, _P, _P, _I32, _I32, _F, _P], _I32),
     "h3enc_op_rope_table": ([_P, _I32, _I32, _F, ctypes.POINTER(_I32), _P, _P, _P], _I32),
     "h3enc_op_gemm_qkv_rope": ([_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _F, _P, _P, _P, _I64, _P, _P],
@@ -329,6 +330,13 @@ def h3enc_op_quant_rows(x, rows, cols, q, scale, stream=None):
 
 def h3enc_op_rmsnorm_q8(x, w, q, scale, rows, cols, eps, stream=None):
     return _check(lib.h3enc_op_rmsnorm_q8(_ptr(x), _ptr(w), _ptr(q), _ptr(scale), rows, cols, eps, _stream(stream)))
+
+
+def h3enc_op_wait_probe(flag, expect, use_mbarrier, status, stream=None):
+    """Bounded-wait self-test: waits for *flag == expect (or on an mbarrier nobody completes);
+    a timeout ORs 1 into the device int32 `status`."""
+    return _check(lib.h3enc_op_wait_probe(_ptr(flag), expect, 1 if use_mbarrier else 0, _ptr(status),
+                                          _stream(stream)))
 
 
 def h3enc_op_rmsnorm(x, w, y, rows, cols, eps, stream=None):

@@ -298,3 +298,28 @@ def test_errors_are_reported_before_launch_and_from_the_device():
         assert enc.status() == 0   # read-and-clear
     finally:
         enc.close()
+
+
+def test_bounded_wait_times_out_into_the_status_and_the_context_survives():
+    """Failure detection without a fault: a wait on a flag nothing sets, and one on an
+    mbarrier nothing completes, give up after the wait limit and report ST_TIMEOUT;
+    a satisfied wait reports nothing; kernels still run afterwards."""
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for use_mbar in (False, True):
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        Q.h3enc_op_wait_probe(flag, 1, use_mbar, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) & 1, "the wait did not report its timeout"
+    flag.fill_(7)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Q.h3enc_op_wait_probe(flag, 7, False, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    # the context is intact: a GEMM still matches its oracle
+    A = W.bf16_bits_to_torch(W.normal_bf16(95, "A", (64, 256))).cuda()
+    Wt = W.bf16_bits_to_torch(W.normal_bf16(96, "W", (256, 256), 0.0, 0.05)).cuda()
+    C = torch.empty(64, 256, dtype=torch.bfloat16, device="cuda")
+    Q.h3enc_op_gemm(A, Wt, C, 64, 256, 256, Q.EPI_STORE)
+    torch.cuda.synchronize()
+    ref = O.linear(t2f(A).astype(np.float64), t2f(Wt).astype(np.float64))
+    assert rel_l2(t2f(C), ref) < 5e-3
