@@ -366,6 +366,7 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         p.flags = h->gemm_flags;
         p.M = S;
         p.fp8 = f8;
+        p.w_static = true;   // weights change only at load/finalize, never inside an encode
         // QKV projection with q_norm/k_norm and M-RoPE fused into the epilogue
         p.tmA = f8 ? &h->tm_y8 : &h->tm_y;
         p.tmW = f8 ? &w8->tm_qkv : &w.tm_qkv;

@@ -90,6 +90,8 @@ struct GemmArgs {
     // e4m3 operands: C = (A8 * sa[row]) (W8 * sw[col])^T
     const float *sa, *sw;
     float *row_amax;   // EPI_SWIGLU, optional: per-row max |bf16 output| (integer atomic max)
+    int w_static;      // W is not written by earlier kernels of the stream: its first stages are
+                       // fetched before the dependency wait
 };
 
 // Phase stamps of the optional timeline (h3enc_op_gemm_traced).
@@ -244,9 +246,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     cluster_sync();   // barriers of both CTAs initialised before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    pdl_wait();       // inputs of this GEMM are the previous kernel's outputs
-    if (threadIdx.x == 0) stamp(g, TR_READY);
-
+    // the previous kernel's outputs (A, the residual, the workspace) are touched only after the
+    // dependency wait, which each role takes itself
     const StreamK sk = stream_k(g, pair);
 
     if (warp == 0) {
@@ -271,8 +272,45 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             };
-            for (int j = 0; ok && j < sk.n; ++j) load_item(g.dp_tiles + sk.tile[j], sk.kb0[j], sk.kb1[j]);
-            for (int tile = pair; ok && tile < g.dp_tiles; tile += npairs) load_item(tile, 0, g.nk);
+            // weights that no earlier kernel writes: the first ring stages of the first item get
+            // their weight half while the previous kernel is still finishing
+            constexpr int kbe0 = F8 ? BK8 : BK;
+            int pre = 0;
+            {
+                const bool has = sk.n > 0 || pair < g.dp_tiles;
+                const int ft = sk.n > 0 ? g.dp_tiles + sk.tile[0] : pair;
+                const int fk0 = sk.n > 0 ? sk.kb0[0] : 0, fk1 = sk.n > 0 ? sk.kb1[0] : g.nk;
+                if (g.w_static && has) {
+                    pre = fk1 - fk0 < STAGES ? fk1 - fk0 : STAGES;
+                    const int n0 = (ft / g.nm) * BN + (int)rank * (BN / 2);
+                    for (int i = 0; i < pre; ++i) {   // a fresh ring: every stage is free
+                        if (rank == 0) mbar_arrive_expect_tx(&full[i], 2 * STAGE_BYTES);
+                        tma_load_2d_pair(sB + i * B_BYTES, &tmB, mapa_shared(smem_u32(&full[i]), 0),
+                                         (fk0 + i) * kbe0, n0);
+                    }
+                }
+                pdl_wait();
+                stamp(g, TR_READY);
+                if (pre) {
+                    const int m0 = (ft % g.nm) * (2 * BM) + (int)rank * BM;
+                    for (int i = 0; i < pre; ++i) {
+                        tma_load_2d_pair(sA + i * A_BYTES, &tmA, mapa_shared(smem_u32(&full[i]), 0),
+                                         (fk0 + i) * kbe0, m0);
+                        ++issued[i];
+                    }
+                    stage = pre % STAGES;
+                    if (pre == STAGES) phase ^= 1u;
+                }
+            }
+            int skip = pre;   // k-blocks of the first item already issued
+            for (int j = 0; ok && j < sk.n; ++j) {
+                load_item(g.dp_tiles + sk.tile[j], sk.kb0[j] + skip, sk.kb1[j]);
+                skip = 0;
+            }
+            for (int tile = pair; ok && tile < g.dp_tiles; tile += npairs) {
+                load_item(tile, skip, g.nk);
+                skip = 0;
+            }
             if (!ok) {
                 report(g.status, ST_TIMEOUT);
                 *abort_flag = 1;
@@ -285,6 +323,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
         }
     } else if (warp == 1) {
+        pdl_wait();
         if (lane == 0 && rank == 0) {
             constexpr uint32_t idesc = F8 ? umma_idesc_e4m3(2 * BM, BN) : umma_idesc_bf16(2 * BM, BN);
             int stage = 0;
@@ -327,6 +366,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             mbar_wait(drain, 0, &never);
         }
     } else {
+        pdl_wait();   // the residual, DeepStack rows, scales and the workspace come from earlier kernels
         // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 = this CTA's tile rows of the same range;
         // warps 2-5 take the first half of the tile's columns, warps 6-9 the second
         const int quarter = warp & 3;
@@ -869,6 +909,7 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     g.nk = F8 ? (p.K + BK8 - 1) / BK8 : (p.K + BK - 1) / BK;
     g.sa = p.sa; g.sw = p.sw;
     g.row_amax = p.row_amax;
+    g.w_static = p.w_static ? 1 : 0;
     g.C = p.C; g.ldc = p.ldc; g.R = p.R; g.DS = p.DS; g.vis_rank = p.vis_rank; g.n_vis = p.n_vis;
     g.status = p.status;
     g.wq = p.wq; g.wk = p.wk; g.cos_t = p.cos_t; g.sin_t = p.sin_t;

@@ -43,6 +43,9 @@ struct GemmPlan {
     const float *sa = nullptr, *sw = nullptr;
     // EPI_SWIGLU (optional): each row's largest |bf16 output| merged with an integer atomic max
     float *row_amax = nullptr;
+    // true when no kernel earlier in the stream writes W (model weights): the weight half of the
+    // first ring stages is fetched before waiting for the previous kernel
+    bool w_static = false;
 };
 // Tensor map of a row-major bf16 matrix [rows, cols] read in boxes of
 // box_rows x 64 with 128-byte swizzle.  False if the driver refuses it.
