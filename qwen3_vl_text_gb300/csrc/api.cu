@@ -19,6 +19,8 @@
 #include "../../include/h3enc_ops.h"
 #include "kernels.h"
 
+#include <nvtx3/nvToolsExt.h>
+
 using h3::bf16;
 
 namespace {
@@ -106,8 +108,20 @@ h3enc_status cuda_fail(h3enc *h, cudaError_t e, const char *what) {
 }
 
 // Run one kernel launch, timed per class when profiling is on.
+// NVTX ranges (encode, layer, launch) for timeline tools; without an attached tool each
+// push/pop is a few nanoseconds.  Popped on scope exit, error returns included.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+const char *const kClassName[H3ENC_K_COUNT] = {"prep",      "rmsnorm", "gemm_qkv",     "quant",
+                                               "attention", "gemm_o",  "gemm_gate_up", "gemm_down"};
+
 template <class F>
 cudaError_t run(h3enc *h, int cls, cudaStream_t st, F &&launch) {
+    NvtxRange range(kClassName[cls]);
     size_t e0 = (size_t)-1;
     if (h->prof && (h->prof_mask & (1u << cls))) {
         if (h->ev_used + 2 > h->ev_pool.size()) {
@@ -315,6 +329,7 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
                          const uint8_t *mask, const bf16 *ds, int nds, int n_vis, const int32_t *cu, int n_seqs,
                          int S, bf16 *out, cudaStream_t st, const bf16 *visual_embeds = nullptr) {
     if (S == 0) return H3ENC_OK;
+    NvtxRange encode_range(h->cfg.linear_fp8 ? "h3enc encode (fp8)" : "h3enc encode");
     const h3enc_config &c = h->cfg;
     const int H = c.hidden, d = c.head_dim, nq = c.n_heads, nkv = c.n_kv_heads, I = c.intermediate;
     cudaError_t e;
@@ -351,6 +366,9 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         if (e != cudaSuccess) return cuda_fail(h, e, "FP8 row maxima clear");
     }
     for (int l = lb; l < le; ++l) {
+        char layer_name[32];
+        snprintf(layer_name, sizeof layer_name, "layer %d", l);
+        NvtxRange layer_range(layer_name);
         LayerW &w = h->layers[l];
         h3enc::Layer8 *w8 = f8 ? &h->layers8[l] : nullptr;
         // input_layernorm (FP8: its bf16 output quantised per token in the same kernel)
