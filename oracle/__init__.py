@@ -11,9 +11,11 @@ float32 (or float64) from bf16-rounded weights and inputs.  It shares no code
 with the CUDA path.
 
 Parity status of each function is listed in its docstring; every function is
-pinned by ``tests/test_oracle_pins.py`` except the end-to-end 50-layer forward
+pinned by ``tests/test_oracle_pins.py`` (the front end by the hand-derived
+fixtures under ``tests/golden/``) except the end-to-end 50-layer forward
 on random weights, whose output has no independent value to compare with
 ("parity unpinned" beyond the per-step pins and the structural invariants).
 """
 from .qwen3vl_text import *  # noqa: F401,F403
 from . import fp8  # noqa: F401  (online-FP8 linears)
+from . import frontend  # noqa: F401  (token ids -> positions, visual rows, DeepStack order)

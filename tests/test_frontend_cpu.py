@@ -1,9 +1,10 @@
 """Positions and visual rows from token ids (host code, no GPU).
 
-Pinned to a worked example done by hand from the pages' rule (text runs count
-up on all three axes; a visual grid counts (frame, row, column) from the
-running start, which then advances by max(h, w)/merge), and to the layouts of
-the benchmark workloads, which were written from their own description."""
+The host helper against the oracle's restatement of the pages' rule on seeded
+random layouts (element by element, integers bit-exact), on the empty sequence
+and on the malformed layouts both reject, and against the layouts of the
+benchmark workloads, which were written from their own description.  The
+hand-derived examples live in tests/golden/positions.txt (test_golden.py)."""
 import numpy as np
 import pytest
 
@@ -19,27 +20,6 @@ def Q():
 
 
 IMG, VID = 151655, 151656
-
-
-def test_hand_worked_image_example(Q):
-    # 2 text, an image of grid (1, 4, 8) before a 2x2 merge = 2 x 4 tokens, 2 text
-    ids = [5, 6] + [IMG] * 8 + [7, 8]
-    pos, mask, kind, ni, nv, delta = Q.h3enc_build_positions(ids, IMG, VID, image_grid_thw=[[1, 4, 8]])
-    assert pos[0].tolist() == [0, 1] + [2] * 8 + [6, 7]
-    assert pos[1].tolist() == [0, 1] + [2, 2, 2, 2, 3, 3, 3, 3] + [6, 7]
-    assert pos[2].tolist() == [0, 1] + [2, 3, 4, 5, 2, 3, 4, 5] + [6, 7]
-    assert mask.tolist() == [0, 0] + [1] * 8 + [0, 0]
-    assert kind.tolist() == [0, 0] + [1] * 8 + [0, 0]
-    assert (ni, nv, delta) == (8, 0, 8 - 12)
-
-
-def test_hand_worked_video_frames_example(Q):
-    # a video of 2 frames (grid (2, 2, 4) -> 2 frames of 1 x 2 tokens), frames separated by a text token
-    ids = [1] + [VID] * 2 + [2] + [VID] * 2
-    pos, mask, kind, ni, nv, delta = Q.h3enc_build_positions(ids, IMG, VID, video_grid_thw=[[2, 2, 4]])
-    # frame 1 at start 1: t 1, h 1, w 1..2; start -> 1 + max(2,4)/2 = 3; text 3; frame 2 at 4
-    assert pos.tolist() == [[0, 1, 1, 3, 4, 4], [0, 1, 1, 3, 4, 4], [0, 1, 2, 3, 4, 5]]
-    assert kind.tolist() == [0, 2, 2, 0, 2, 2] and (ni, nv) == (0, 4)
 
 
 def test_benchmark_image_layout_from_ids(Q):
@@ -60,3 +40,57 @@ def test_run_length_must_match_grid(Q):
         Q.h3enc_build_positions([1] + [IMG] * 4 + [2] + [IMG] * 4, IMG, VID, image_grid_thw=[[1, 4, 4]])
     with pytest.raises(Q.H3encError):
         Q.h3enc_build_positions([IMG] * 4, IMG, VID, image_grid_thw=[[1, 3, 4]])   # 3 not divisible by 2
+
+
+def _random_layout(rng, merge):
+    """Seeded sequence of text runs, images and multi-frame videos (frames split by text)."""
+    ids, img, vid = [], [], []
+    text = lambda n: ids.extend(int(x) for x in rng.integers(0, 100000, n))
+    text(int(rng.integers(0, 4)))
+    for _ in range(int(rng.integers(0, 5))):
+        gh, gw = merge * int(rng.integers(1, 5)), merge * int(rng.integers(1, 5))
+        n = (gh // merge) * (gw // merge)
+        if rng.random() < 0.5:
+            img.append([1, gh, gw])
+            ids.extend([IMG] * n)
+        else:
+            t = int(rng.integers(1, 4))
+            vid.append([t, gh, gw])
+            for f in range(t):
+                ids.extend([VID] * n)
+                if f + 1 < t:
+                    text(int(rng.integers(1, 3)))
+        text(int(rng.integers(1, 4)))
+    return np.array(ids, dtype=np.int64), (img or None), (vid or None)
+
+
+@pytest.mark.parametrize("merge", [1, 2])
+def test_positions_match_the_oracle_on_random_layouts(Q, merge):
+    import oracle as O
+    rng = np.random.default_rng(4242 + merge)
+    for _ in range(300):
+        ids, img, vid = _random_layout(rng, merge)
+        pos, mask, kind, ni, nv, delta = Q.h3enc_build_positions(ids, IMG, VID, img, vid, spatial_merge_size=merge)
+        opos, odelta = O.frontend.rope_index(ids, IMG, VID, img, vid, spatial_merge_size=merge)
+        types = O.frontend.token_types(ids, IMG, VID)
+        assert np.array_equal(pos, opos) and delta == odelta
+        assert np.array_equal(kind, types) and np.array_equal(mask, types != 0)
+        assert (ni, nv) == (int((types == 1).sum()), int((types == 2).sum()))
+
+
+def test_empty_sequence_and_mismatches_agree_with_the_oracle(Q):
+    import oracle as O
+    pos, mask, kind, ni, nv, delta = Q.h3enc_build_positions(np.zeros(0, dtype=np.int64), IMG, VID)
+    opos, odelta = O.frontend.rope_index(np.zeros(0, dtype=np.int64), IMG, VID)
+    assert pos.shape == opos.shape == (3, 0) and delta == odelta == 0 and (ni, nv) == (0, 0)
+    bad = [
+        ([1] + [IMG] * 3 + [2], [[1, 4, 4]], None),            # 3 tokens for a 2 x 2 grid
+        ([1] + [VID] * 8, None, [[2, 4, 4]]),                   # two frames with no text between
+        ([1] + [IMG] * 4 + [2] + [IMG] * 4, [[1, 4, 4]], None), # a second image with no grid
+    ]
+    for ids, img, vid in bad:
+        with pytest.raises(ValueError):
+            O.frontend.rope_index(ids, IMG, VID, img, vid)
+        with pytest.raises(Q.H3encError) as e:
+            Q.h3enc_build_positions(ids, IMG, VID, img, vid)
+        assert e.value.code == 3

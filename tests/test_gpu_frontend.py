@@ -22,16 +22,15 @@ def test_aggregate_deepstack_interleaves_images_and_videos():
     H, levels = 256, 3
     kind = np.array([0] * 3 + [1] * 5 + [0] * 2 + [2] * 4 + [1] * 3 + [2] * 2 + [0], dtype=np.uint8)
     ni, nv = int((kind == 1).sum()), int((kind == 2).sum())
-    img = W.bf16_bits_to_torch(W.normal_bf16(60, "img", (levels, ni, H))).cuda()
-    vid = W.bf16_bits_to_torch(W.normal_bf16(61, "vid", (levels, nv, H))).cuda()
+    img_bits = W.normal_bf16(60, "img", (levels, ni, H))
+    vid_bits = W.normal_bf16(61, "vid", (levels, nv, H))
     out = torch.empty(levels, ni + nv, H, dtype=torch.bfloat16, device="cuda")
-    Q.h3enc_aggregate_deepstack(kind, img, vid, out)
+    Q.h3enc_aggregate_deepstack(kind, W.bf16_bits_to_torch(img_bits).cuda(), W.bf16_bits_to_torch(vid_bits).cuda(),
+                                out)
     torch.cuda.synchronize()
-    vis = kind[kind != 0]
-    expect = torch.empty_like(out)
-    expect[:, torch.from_numpy(np.nonzero(vis == 1)[0]).cuda()] = img
-    expect[:, torch.from_numpy(np.nonzero(vis == 2)[0]).cuda()] = vid
-    assert torch.equal(out, expect)
+    mask, expect = O.frontend.aggregate_deepstack(kind, bits_to_f32(img_bits), bits_to_f32(vid_bits))
+    assert np.array_equal(mask, kind != 0)
+    assert np.array_equal(t2f(out), expect)          # a copy: bit-exact
 
 
 def _tiny_ids_with_placeholders():
@@ -74,7 +73,7 @@ def test_multimodal_encode_from_ids_against_oracle():
     finally:
         enc.close()
     x0 = bits_to_f32(W.gen_weight(wl.seed, W.embed_name(), (cfg.vocab, H), 0.0, 0.02, rows=ids))
-    x0[mask == 1] = bits_to_f32(vis_bits)           # masked_scatter: row j to the j-th visual position
+    x0 = O.frontend.masked_scatter_rows(x0, O.frontend.placeholder_rows(ids, IMG), bits_to_f32(vis_bits))
     get = oracle_layer_getter(wl, cfg)
     ws = [get(l) for l in range(cfg.num_layers)]
     dsf = bits_to_f32(ds_bits)
