@@ -233,7 +233,11 @@ enum {
 };
 
 /* enable != 0: record a CUDA event pair around every kernel launch (on the
- * launching stream) and accumulate per-class device time.  Resets totals. */
+ * launching stream) and accumulate per-class device time.  Resets totals.
+ * An encode captured into a CUDA graph while profiling is on carries the event
+ * pairs as event-record nodes: each replay records them again, and the next
+ * h3enc_get_profile returns the durations of the latest replay (launch counts
+ * are those of the capture; the reset then detaches the pairs). */
 H3ENC_API h3enc_status h3enc_set_profiling(h3enc *h, int32_t enable);
 
 /* As h3enc_set_profiling, timing only the classes whose bit (1 << class) is set

@@ -119,6 +119,14 @@ struct NvtxRange {
 const char *const kClassName[H3ENC_K_COUNT] = {"prep",      "rmsnorm", "gemm_qkv",     "quant",
                                                "attention", "gemm_o",  "gemm_gate_up", "gemm_down"};
 
+// Under stream capture the timing events become event-record nodes of the graph, so every
+// replay records them again and the host reads the latest replay's durations.
+inline void record_timing_event(cudaEvent_t ev, cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) cs = cudaStreamCaptureStatusNone;
+    cudaEventRecordWithFlags(ev, st, cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0u);
+}
+
 template <class F>
 cudaError_t run(h3enc *h, int cls, cudaStream_t st, F &&launch) {
     NvtxRange range(kClassName[cls]);
@@ -134,14 +142,14 @@ cudaError_t run(h3enc *h, int cls, cudaStream_t st, F &&launch) {
         }
         if (h->ev_used + 2 <= h->ev_pool.size()) {
             e0 = h->ev_used;
-            cudaEventRecord(h->ev_pool[e0], st);
+            record_timing_event(h->ev_pool[e0], st);
         } else {
             e0 = (size_t)-1;
         }
     }
     cudaError_t e = launch();
     if (e0 != (size_t)-1) {
-        cudaEventRecord(h->ev_pool[e0 + 1], st);
+        record_timing_event(h->ev_pool[e0 + 1], st);
         h->ev_class[e0] = cls;
         h->ev_used += 2;
     }

@@ -56,3 +56,45 @@ def test_encode_replayed_from_a_cuda_graph_matches_eager(fp8):
         assert enc.status() == 0, Q.h3enc_last_error(enc.handle)
     finally:
         enc.close()
+
+
+def test_profiled_graph_replays_time_the_gate_up_launches():
+    """Profiling events captured with the encode are graph nodes: after the replays the
+    gate/up class reports one duration per layer (the latest replay), the output stays
+    the eager one, and the classes not profiled report nothing."""
+    wl = W.workload(0)
+    cfg = wl.model
+    inp = W.gen_inputs(wl)
+    S, H = inp["seq_len"], cfg.hidden
+    enc = make_encoder(wl, cfg, max_tokens=S)
+    try:
+        pos = torch.from_numpy(inp["positions"]).cuda()
+        x = W.bf16_bits_to_torch(W.normal_bf16(90, "graph_x", (S, H))).cuda()
+        want = torch.empty(S, H, dtype=torch.bfloat16, device="cuda")
+        got = torch.empty_like(want)
+        side = torch.cuda.Stream()
+
+        def encode(out, stream):
+            Q.h3enc_encode_embeds(enc.handle, x, 0, cfg.num_layers, pos, None, None, 0, 0, None, S, out,
+                                  stream=stream)
+
+        encode(want, torch.cuda.current_stream())
+        side.wait_stream(torch.cuda.current_stream())
+        encode(got, side)
+        torch.cuda.synchronize()
+        Q.h3enc_set_profiling_classes(enc.handle, ["gemm_gate_up"])
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            encode(got, side)
+        got.zero_()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        prof = Q.h3enc_get_profile(enc.handle)
+        assert torch.equal(got, want)
+        ms, n = prof["gemm_gate_up"]
+        assert n == cfg.num_layers and ms > 0.0
+        assert all(v[0] == 0.0 for k, v in prof.items() if k != "gemm_gate_up")
+        assert enc.status() == 0, Q.h3enc_last_error(enc.handle)
+    finally:
+        enc.close()
