@@ -28,7 +28,7 @@ WORKLOAD_ID = 2
 GEMM_GU_CLASS = "gemm_gate_up"
 # DRAM bytes (read + write) of one gate/up launch at seq 1024, from the ncu capture in
 # profiles/gemm_gate_up_seq1024_ncu.md (same kernel source as this build).
-GATE_UP_TRAFFIC_BYTES = 645.0e6
+GATE_UP_TRAFFIC_BYTES = 646.9e6
 
 
 def _peaks():
@@ -203,7 +203,13 @@ def run_kernel(args):
         Q.h3enc_op_rope_table(pos, S, d, cfg.rope_theta, cfg.mrope_section, c, s_)
         C = torch.empty(S, cfg.qkv_out, dtype=torch.bfloat16, device=dev)
         ws = torch.zeros(Q.h3enc_op_gemm_workspace_bytes(), dtype=torch.uint8, device=dev)
-        fn = lambda: Q.h3enc_op_gemm_qkv_rope(A, Wt, C, S, H, nq, nkv, d, G, G, 1e-6, c, s_, workspace=ws)
+        if args.fold:   # the input RMSNorm folded in: rows scaled by the statistics of A
+            ss = torch.empty(H // 128, S, dtype=torch.float32, device=dev)
+            Q.h3enc_op_row_sumsq(A, S, H, ss)
+            fn = lambda: Q.h3enc_op_gemm_qkv_rope_rms(A, Wt, C, S, H, nq, nkv, d, G, G, 1e-6, c, s_, ss, 1e-6,
+                                                      workspace=ws)
+        else:
+            fn = lambda: Q.h3enc_op_gemm_qkv_rope(A, Wt, C, S, H, nq, nkv, d, G, G, 1e-6, c, s_, workspace=ws)
         work, unit = 2.0 * S * cfg.qkv_out * H / 1e12, "TFLOP/s"
     elif name.startswith("gemm_"):
         shapes = {"gemm_o": (H, nq * d, Q.EPI_RESIDUAL),
@@ -223,6 +229,13 @@ def run_kernel(args):
             Q.h3enc_op_quant_rows(A, S, K, A8, sa)
             Q.h3enc_op_quant_rows(Wt, N, K, W8, sw)
             fn = lambda: Q.h3enc_op_gemm_fp8(A8, W8, sa, sw, C, S, N, K, epi, R=R, workspace=ws)
+        elif args.fold and epi == Q.EPI_SWIGLU:   # consumer of the post-attention statistics
+            ss = torch.empty(K // 128, S, dtype=torch.float32, device=dev)
+            Q.h3enc_op_row_sumsq(A, S, K, ss)
+            fn = lambda: Q.h3enc_op_gemm_rms(A, Wt, C, S, N, K, epi, ss_in=ss, eps=1e-6, workspace=ws)
+        elif args.fold:   # producer of the next norm's statistics
+            ss = torch.empty(N // 128, S, dtype=torch.float32, device=dev)
+            fn = lambda: Q.h3enc_op_gemm_rms(A, Wt, C, S, N, K, epi, R=R, ss_out=ss, workspace=ws)
         else:
             fn = lambda: Q.h3enc_op_gemm(A, Wt, C, S, N, K, epi, R=R, workspace=ws)
         work, unit = 2.0 * S * N * K / 1e12, "TFLOP/s"
@@ -263,7 +276,8 @@ def run_kernel(args):
     fp8_gemm = bool(args.fp8) and name.startswith("gemm_") and name != "gemm_qkv"
     # e4m3 contractions: the measured bf16 burst peak times the nominal fp8/bf16 ratio (4.5 / 2.25)
     peak = (burst * (2.0 if fp8_gemm else 1.0)) if unit == "TFLOP/s" else hbm
-    print(json.dumps({"kernel": name + (" (e4m3)" if fp8_gemm else ""), "seq": S, "ms_median": ms, "ms_min": ts[0], "achieved": work / (ms / 1e3),
+    print(json.dumps({"kernel": name + (" (e4m3)" if fp8_gemm else "") + (" (folded norm)" if args.fold else ""),
+                      "seq": S, "ms_median": ms, "ms_min": ts[0], "achieved": work / (ms / 1e3),
                       "unit": unit, "peak": peak, "frac": work / (ms / 1e3) / peak,
                       "peak_source": f"{src} {'bf16_tflops' if unit == 'TFLOP/s' else 'hbm_gbs'} (burst)"
                                      + (" x 2 (nominal fp8/bf16)" if fp8_gemm else "")}),
@@ -282,6 +296,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--separate-norm", action="store_true",
+                    help="bf16: run each RMSNorm as its own kernel instead of folding it into the projections")
+    ap.add_argument("--fold", action="store_true",
+                    help="with --kernel: the projection as the folded-norm encode runs it (QKV and gate/up "
+                         "scale rows by the norm statistics, o and down emit them)")
     ap.add_argument("--eager", action="store_true",
                     help="launch every kernel from the host in the timed region instead of replaying a "
                          "CUDA graph of the encode")
@@ -315,7 +334,8 @@ def main():
     cfg = wl.model
     inp = W.gen_inputs(wl)
     S = inp["seq_len"]
-    enc = Q.Encoder(cfg, max_tokens=S, max_seqs=4, num_deepstack=wl.deepstack_levels, fp8=args.fp8)
+    enc = Q.Encoder(cfg, max_tokens=S, max_seqs=4, num_deepstack=wl.deepstack_levels, fp8=args.fp8,
+                    separate_norm=args.separate_norm)
     for l in range(cfg.num_layers):
         for name, shape, mean, sigma in W.layer_weight_specs(cfg, l):
             enc.load(name, W.gen_weight(wl.seed, name, shape, mean, sigma, device="cuda"))
@@ -423,10 +443,11 @@ def main():
     gu_flops = 2.0 * S * (2 * cfg.intermediate) * cfg.hidden
     gu_achieved = gu_flops / (gu_ms / gu_n / 1e3) / 1e12 if gu_n else 0.0
     # The denominator follows the clocks sampled over the timed region: the burst cuBLAS figure while
-    # the SM clock held its maximum, the power-capped sustained figure once it fell below.  e4m3
-    # contractions take the measured bf16 figure times the nominal fp8/bf16 dense ratio (4.5 / 2.25).
+    # the SM clock held its maximum with no power capping, the sustained figure (measured under the
+    # power cap) otherwise.  e4m3 contractions take the measured bf16 figure times the nominal
+    # fp8/bf16 dense ratio (4.5 / 2.25).
     at_max = bool(clk and clk.get("sm_mhz") and clk.get("sm_max_mhz")
-                  and clk["sm_mhz"] >= 0.97 * clk["sm_max_mhz"])
+                  and clk["sm_mhz"] >= 0.97 * clk["sm_max_mhz"] and "sw_power_cap" not in clk.get("reasons", []))
     base, base_name = (burst, "bf16_tflops") if at_max else (sustained, "bf16_tflops_sustained")
     f8 = 2.0 if args.fp8 else 1.0
     gu_peak = base * f8
@@ -442,14 +463,17 @@ def main():
                    "deepstack_levels": wl.deepstack_levels, "parallelism": f"replicas x{world}",
                    "l2": "no flush: each step streams 48.8 GB of weights, far above the 129 MB L2",
                    "launch": "eager (one host launch per kernel)" if graph is None
-                             else "CUDA graph of one encode, replayed once per step"},
+                             else "CUDA graph of one encode, replayed once per step",
+                   "rmsnorm": "quantising pass before each projection" if args.fp8
+                              else "separate pass before each projection" if args.separate_norm
+                              else "folded into the projections (statistics from the o/down epilogues)"},
         "pct_dense_bf16_peak": 100.0 * flops * args.steps / (ms / 1e3) / (base * 1e12),
         "tflops": flops * args.steps / (ms / 1e3) / 1e12,
         "roofline": {"kernel": "gemm_tcgen05 gate/up + SwiGLU" + (" (e4m3)" if args.fp8 else ""), "bound": "tensor",
                      "achieved": gu_achieved, "peak": gu_peak, "unit": "TFLOP/s", "frac": gu_achieved / gu_peak,
                      "peak_source": f"{peak_src} {base_name}"
-                                    + (" (SM clock at max through the timed region)" if at_max
-                                       else " (SM clock below max: power-capped)")
+                                    + (" (SM clock at max, no power capping in the timed region)" if at_max
+                                       else " (power capping or SM clock below max in the timed region)")
                                     + (" x 2 (nominal fp8/bf16)" if args.fp8 else ""),
                      "frac_of_burst": gu_achieved / (burst * f8),
                      "frac_of_sustained": gu_achieved / (sustained * f8),

@@ -86,6 +86,19 @@ typedef struct {
                                scale per output channel, activations to e4m3 with one
                                scale per token on every encode; attention stays bf16).
                                0: plain bf16.  The bf16 weights stay loaded. */
+    int32_t separate_norm;  /* bf16 only.  0 (default): the two RMSNorms of a layer run inside
+                               the projections that read them (page "... encoder.py",
+                               MiniMaxH3Qwen3VLRMSNorm before qkv_proj and gate_up_proj):
+                               h3enc_finalize_weights multiplies each norm weight into the
+                               K columns of those projections once; every encode then
+                               emits per-row sums of squares of the hidden state from the
+                               o_proj and down_proj epilogues (and one pass over the layer
+                               input), and the QKV and gate/up epilogues scale their rows
+                               by 1/sqrt(mean + rms_eps).  The normalised activation is
+                               never rounded to bf16 (the folded weights are).  1: a
+                               separate RMSNorm kernel writes the bf16 normalised rows
+                               before each of the two projections.  With linear_fp8 the
+                               norm always runs as its own quantising pass. */
 } h3enc_config;
 
 typedef struct h3enc h3enc;

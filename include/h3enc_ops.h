@@ -176,6 +176,42 @@ H3ENC_API h3enc_status h3enc_op_gemm_qkv_rope(const void *A, const void *W, void
                                     const void *w_k, float eps, const float *cos_tab, const float *sin_tab,
                                     void *workspace, int64_t workspace_bytes, int32_t *status, void *stream);
 
+/* RMSNorm folded into a projection (page "... encoder.py", MiniMaxH3Qwen3VLRMSNorm
+ * followed by the projection that reads its output; an algebraic rearrangement the
+ * encoder uses when h3enc_config.separate_norm == 0):
+ *   rmsnorm(x, g) W^T = diag(1 / sqrt(mean(x^2) + eps)) x (W diag(g))^T.
+ * Row statistics are sums of squares over slots of 128 columns, accumulated in fp32 in
+ * column order, stored slot-major: ss[s * rows + r] = sum_{c in [128 s, 128 s + 128)} x[r][c]^2.
+ *
+ * h3enc_op_row_sumsq: ss [cols/128, rows] fp32 of the bf16 matrix x [rows, cols];
+ * cols % 128 == 0, x 16-byte aligned. */
+H3ENC_API h3enc_status h3enc_op_row_sumsq(const void *x, int32_t rows, int32_t cols, float *ss, void *stream);
+
+/* h3enc_op_fold_cols: W[r][k] = bf16(W[r][k] * gamma[k]) in place (fp32 product rounded
+ * to nearest even), W bf16 [rows, cols], gamma bf16 [cols]; cols % 8 == 0, both
+ * 16-byte aligned. */
+H3ENC_API h3enc_status h3enc_op_fold_cols(void *W, int32_t rows, int32_t cols, const void *gamma, void *stream);
+
+/* h3enc_op_gemm with the folded norm: ss_in [K/128, M] (or NULL): the accumulator of row
+ * r is multiplied by 1/sqrt(sum_s ss_in[s][r] / K + eps) (slots added in order) before the
+ * epilogue; ss_out [N/128, M] (or NULL; STORE and RESIDUAL only): the row statistics of
+ * the bf16 output C, as h3enc_op_row_sumsq would give them.  epilogue: STORE,
+ * RESIDUAL or SWIGLU; other arguments as h3enc_op_gemm. */
+H3ENC_API h3enc_status h3enc_op_gemm_rms(const void *A, const void *W, void *C, int32_t M, int32_t N, int32_t K,
+                                         int32_t epilogue, const void *R, const float *ss_in, float *ss_out,
+                                         float eps, void *workspace, int64_t workspace_bytes, int32_t *status,
+                                         void *stream);
+
+/* h3enc_op_gemm_qkv_rope with the folded input norm: each row of A * W^T is first
+ * multiplied by 1/sqrt(sum_s ss_in[s][r] / K + in_eps) (ss_in [K/128, M], required), then
+ * the q/k RMSNorm (eps) and M-RoPE of h3enc_op_gemm_qkv_rope apply. */
+H3ENC_API h3enc_status h3enc_op_gemm_qkv_rope_rms(const void *A, const void *W, void *C, int32_t M, int32_t K,
+                                                  int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                                  const void *w_q, const void *w_k, float eps,
+                                                  const float *cos_tab, const float *sin_tab, const float *ss_in,
+                                                  float in_eps, void *workspace, int64_t workspace_bytes,
+                                                  int32_t *status, void *stream);
+
 /* Causal GQA attention over packed sequences (page "... encoder.py",
  * MiniMaxH3Qwen3VLTextAttention.forward: repeat_interleave of K/V, SDPA with
  * is_causal=True, scale 1/sqrt(d)).  Reads q/k/v from qkv [S, (nq+2nkv)*d]

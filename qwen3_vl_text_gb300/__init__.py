@@ -20,7 +20,8 @@ __all__ = [
     "h3enc_build_positions", "h3enc_aggregate_deepstack",
     "h3enc_op_gemm", "h3enc_op_gemm_workspace_bytes", "h3enc_op_gemm_trace_next", "h3enc_op_attention_trace_next", "h3enc_op_gemm_noalloc", "h3enc_op_gemm_noalloc_scratch_bytes", "h3enc_op_pack_gate_up", "h3enc_op_rmsnorm", "h3enc_op_gemm_fp8", "h3enc_op_quant_rows",
     "h3enc_op_rmsnorm_q8", "h3enc_op_wait_probe", "h3enc_op_rope_table",
-    "h3enc_op_gemm_qkv_rope", "h3enc_op_attention", "h3enc_op_embed", "h3enc_op_vis_rank", "Encoder",
+    "h3enc_op_gemm_qkv_rope", "h3enc_op_gemm_qkv_rope_rms", "h3enc_op_gemm_rms", "h3enc_op_row_sumsq",
+    "h3enc_op_fold_cols", "h3enc_op_attention", "h3enc_op_embed", "h3enc_op_vis_rank", "Encoder",
     "KERNEL_CLASSES",
 ]
 
@@ -45,7 +46,8 @@ class Config(ctypes.Structure):
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("intermediate", ctypes.c_int32),
                 ("vocab", ctypes.c_int32), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
                 ("mrope_section", ctypes.c_int32 * 3), ("max_tokens", ctypes.c_int32),
-                ("max_seqs", ctypes.c_int32), ("num_deepstack", ctypes.c_int32), ("linear_fp8", ctypes.c_int32)]
+                ("max_seqs", ctypes.c_int32), ("num_deepstack", ctypes.c_int32), ("linear_fp8", ctypes.c_int32),
+                ("separate_norm", ctypes.c_int32)]
 
 
 def _load():
@@ -91,6 +93,11 @@ _SIGS = {
     "h3enc_op_wait_probe": ([_P, ctypes.c_uint32, _I32, _P, _P], _I32),
     "h3enc_op_rmsnorm_q8": ([_P, _P, _P, _P, _I32, _I32, _F, _P], _I32),
     "h3enc_op_rope_table": ([_P, _I32, _I32, _F, ctypes.POINTER(_I32), _P, _P, _P], _I32),
+    "h3enc_op_gemm_qkv_rope_rms": ([_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _F, _P, _P, _P, _F, _P, _I64,
+                                    _P, _P], _I32),
+    "h3enc_op_gemm_rms": ([_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _F, _P, _I64, _P, _P], _I32),
+    "h3enc_op_row_sumsq": ([_P, _I32, _I32, _P, _P], _I32),
+    "h3enc_op_fold_cols": ([_P, _I32, _I32, _P, _P], _I32),
     "h3enc_op_gemm_qkv_rope": ([_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _F, _P, _P, _P, _I64, _P, _P],
                                _I32),
     "h3enc_op_attention": ([_P, _P, _I32, _I32, _I32, _I32, _P, _I32, _P], _I32),
@@ -356,6 +363,30 @@ def h3enc_op_gemm_qkv_rope(A, W, C, M, K, n_heads, n_kv_heads, head_dim, w_q, w_
                                              _ptr(workspace), wbytes, _ptr(status), _stream(stream)))
 
 
+def h3enc_op_gemm_qkv_rope_rms(A, W, C, M, K, n_heads, n_kv_heads, head_dim, w_q, w_k, eps, cos_tab, sin_tab,
+                               ss_in, in_eps, workspace=None, status=None, stream=None):
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return _check(lib.h3enc_op_gemm_qkv_rope_rms(_ptr(A), _ptr(W), _ptr(C), M, K, n_heads, n_kv_heads, head_dim,
+                                                 _ptr(w_q), _ptr(w_k), eps, _ptr(cos_tab), _ptr(sin_tab),
+                                                 _ptr(ss_in), in_eps, _ptr(workspace), wbytes, _ptr(status),
+                                                 _stream(stream)))
+
+
+def h3enc_op_gemm_rms(A, W, C, M, N, K, epilogue, R=None, ss_in=None, ss_out=None, eps=0.0, workspace=None,
+                      status=None, stream=None):
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return _check(lib.h3enc_op_gemm_rms(_ptr(A), _ptr(W), _ptr(C), M, N, K, epilogue, _ptr(R), _ptr(ss_in),
+                                        _ptr(ss_out), eps, _ptr(workspace), wbytes, _ptr(status), _stream(stream)))
+
+
+def h3enc_op_row_sumsq(x, rows, cols, ss, stream=None):
+    return _check(lib.h3enc_op_row_sumsq(_ptr(x), rows, cols, _ptr(ss), _stream(stream)))
+
+
+def h3enc_op_fold_cols(W, rows, cols, gamma, stream=None):
+    return _check(lib.h3enc_op_fold_cols(_ptr(W), rows, cols, _ptr(gamma), _stream(stream)))
+
+
 def h3enc_op_attention(qkv, o, S, n_heads, n_kv_heads, head_dim, cu_seqlens=None, stream=None):
     cu = _host_i32(cu_seqlens)
     n_seqs = len(cu) - 1 if cu is not None else 0
@@ -379,7 +410,8 @@ class Encoder:
     config attributes (num_layers, hidden, n_heads, n_kv_heads, head_dim,
     intermediate, vocab, rms_eps, rope_theta, mrope_section)."""
 
-    def __init__(self, model, max_tokens: int, max_seqs: int = 64, num_deepstack: int = 3, fp8: bool = False):
+    def __init__(self, model, max_tokens: int, max_seqs: int = 64, num_deepstack: int = 3, fp8: bool = False,
+                 separate_norm: bool = False):
         c = Config()
         c.num_layers, c.hidden, c.n_heads = model.num_layers, model.hidden, model.n_heads
         c.n_kv_heads, c.head_dim, c.intermediate = model.n_kv_heads, model.head_dim, model.intermediate
@@ -387,6 +419,7 @@ class Encoder:
         c.mrope_section = (ctypes.c_int32 * 3)(*model.mrope_section)
         c.max_tokens, c.max_seqs, c.num_deepstack = max_tokens, max_seqs, num_deepstack
         c.linear_fp8 = 1 if fp8 else 0
+        c.separate_norm = 1 if separate_norm else 0
         self.model = model
         self.handle = h3enc_create(c)
 

@@ -36,7 +36,15 @@ struct LayerW {
     bf16 *in_norm = nullptr, *post_norm = nullptr, *q_norm = nullptr, *k_norm = nullptr;
     CUtensorMap tm_qkv, tm_o, tm_gu, tm_down;
     uint32_t loaded = 0;
+    // RMSNorm folded into the projections: shards (bits 1 << T_Q, T_K, T_V, T_GATE, T_UP) whose
+    // arena rows already carry their norm weight; a norm reloaded while its projections are
+    // folded marks them stale until they are reloaded too
+    uint32_t folded = 0;
+    bool in_stale = false, post_stale = false;
 };
+
+constexpr uint32_t kQKVBits = (1u << T_Q) | (1u << T_K) | (1u << T_V);
+constexpr uint32_t kGUBits = (1u << T_GATE) | (1u << T_UP);
 
 thread_local std::string g_create_error;
 
@@ -64,6 +72,9 @@ struct h3enc {
     uint8_t *st_mask = nullptr;
     bf16 *st_ds = nullptr, *st_out = nullptr;
     CUtensorMap tm_y, tm_attn, tm_act;
+    // RMSNorm folded into the projections (bf16, separate_norm == 0): per-row sums of squares of
+    // the hidden state over slots of 128 columns, [hidden / 128][rows of the encode]
+    float *row_ss = nullptr;
     // online FP8 (linear_fp8): e4m3 copies of the four projections with per-row scales, e4m3
     // activations with per-token scales
     struct Layer8 {
@@ -158,6 +169,48 @@ cudaError_t run(h3enc *h, int cls, cudaStream_t st, F &&launch) {
     return e;
 }
 
+// bf16 encodes fold the two RMSNorms into the projections unless asked for separate passes;
+// the FP8 path quantises the norm's output and keeps its own pass.
+bool norm_folded(const h3enc_config &c) { return !c.linear_fp8 && !c.separate_norm; }
+
+// Multiply each layer's input_layernorm weight into the q/k/v rows and its
+// post_attention_layernorm weight into the gate/up rows (along K), for the shards not yet
+// folded.  A norm changed after its projections were folded cannot be applied to them.
+h3enc_status fold_norms(h3enc *h) {
+    const h3enc_config &c = h->cfg;
+    const int H = c.hidden, qr = c.n_heads * c.head_dim, kr = c.n_kv_heads * c.head_dim;
+    std::string stale;
+    for (int l = 0; l < c.num_layers; ++l) {
+        const LayerW &w = h->layers[l];
+        if (w.in_stale && (w.folded & kQKVBits))
+            stale += " layers." + std::to_string(l) + ": reload q/k/v_proj (input_layernorm changed)";
+        if (w.post_stale && (w.folded & kGUBits))
+            stale += " layers." + std::to_string(l) + ": reload gate/up_proj (post_attention_layernorm changed)";
+    }
+    if (!stale.empty())
+        return fail(h, H3ENC_ERR_MISSING_WEIGHTS,
+                    "norm weights changed after their projections were folded at finalize:%s", stale.c_str());
+    cudaError_t e = cudaSuccess;
+    for (auto &w : h->layers) {
+        const struct { int bit, r0, r1, blk, parity; const bf16 *g; bf16 *W; } shards[5] = {
+            {T_Q, 0, qr, 0, 0, w.in_norm, w.qkv},
+            {T_K, qr, qr + kr, 0, 0, w.in_norm, w.qkv},
+            {T_V, qr + kr, qr + 2 * kr, 0, 0, w.in_norm, w.qkv},
+            {T_GATE, 0, 2 * c.intermediate, 128, 0, w.post_norm, w.gu},   // packed: 128-row blocks
+            {T_UP, 0, 2 * c.intermediate, 128, 1, w.post_norm, w.gu},     // alternate gate / up
+        };
+        for (const auto &sh : shards) {
+            if (w.folded & (1u << sh.bit)) continue;
+            e = h3::launch_fold_cols(sh.W, H, sh.g, sh.r0, sh.r1, sh.blk, sh.parity, 0);
+            if (e != cudaSuccess) return cuda_fail(h, e, "norm fold");
+            w.folded |= 1u << sh.bit;
+        }
+        w.in_stale = w.post_stale = false;
+    }
+    e = cudaStreamSynchronize(0);
+    return e == cudaSuccess ? H3ENC_OK : cuda_fail(h, e, "norm fold");
+}
+
 h3enc_status validate_config(const h3enc_config *c) {
     if (!c) return fail(nullptr, H3ENC_ERR_INVALID_ARG, "config is NULL");
     if (c->num_layers < 1 || c->hidden < 1 || c->n_heads < 1 || c->n_kv_heads < 1 || c->intermediate < 1 ||
@@ -170,6 +223,8 @@ h3enc_status validate_config(const h3enc_config *c) {
         return fail(nullptr, H3ENC_ERR_INVALID_ARG, "config: negative mrope_section");
     if (c->linear_fp8 != 0 && c->linear_fp8 != 1)
         return fail(nullptr, H3ENC_ERR_INVALID_ARG, "config: linear_fp8 must be 0 or 1");
+    if (c->separate_norm != 0 && c->separate_norm != 1)
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "config: separate_norm must be 0 or 1");
     if (c->head_dim != 64 && c->head_dim != 128)
         return fail(nullptr, H3ENC_ERR_UNSUPPORTED, "config: head_dim %d not in {64, 128}", c->head_dim);
     if (c->n_heads % c->n_kv_heads)
@@ -367,7 +422,17 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         if (e != cudaSuccess) return cuda_fail(h, e, "visual embedding merge");
     }
     const bool f8 = c.linear_fp8 != 0;
+    const bool fold = norm_folded(c);
     const int AO = nq * d;
+    // folded RMSNorm: the projections read the hidden state itself and scale their rows by the
+    // 1/rms its producer's statistics give (here the layer input's, then the o/down epilogues')
+    CUtensorMap tm_h;
+    if (fold && le > lb) {
+        if (!h3::make_tmap_rows(&tm_h, out, S, H, h3::gemm_box_rows_a()))
+            return fail(h, H3ENC_ERR_INVALID_ARG, "out must be 16-byte aligned");
+        e = run(h, H3ENC_K_RMSNORM, st, [&] { return h3::launch_row_sumsq(out, S, H, h->row_ss, st); });
+        if (e != cudaSuccess) return cuda_fail(h, e, "row statistics");
+    }
     if (f8 && le > lb) {
         // the quantising passes clear the row maxima after use; start every encode from zeros
         e = cudaMemsetAsync(h->amax_attn, 0, 2 * align256((size_t)c.max_tokens * 4), st);
@@ -379,12 +444,15 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         NvtxRange layer_range(layer_name);
         LayerW &w = h->layers[l];
         h3enc::Layer8 *w8 = f8 ? &h->layers8[l] : nullptr;
-        // input_layernorm (FP8: its bf16 output quantised per token in the same kernel)
-        e = run(h, H3ENC_K_RMSNORM, st, [&] {
-            return f8 ? h3::launch_rmsnorm_q8(out, w.in_norm, h->y8, h->sy, S, H, c.rms_eps, st)
-                      : h3::launch_rmsnorm(out, w.in_norm, h->y, S, H, c.rms_eps, st);
-        });
-        if (e != cudaSuccess) return cuda_fail(h, e, "input_layernorm");
+        // input_layernorm (FP8: its bf16 output quantised per token in the same kernel; folded:
+        // inside the QKV projection)
+        if (!fold) {
+            e = run(h, H3ENC_K_RMSNORM, st, [&] {
+                return f8 ? h3::launch_rmsnorm_q8(out, w.in_norm, h->y8, h->sy, S, H, c.rms_eps, st)
+                          : h3::launch_rmsnorm(out, w.in_norm, h->y, S, H, c.rms_eps, st);
+            });
+            if (e != cudaSuccess) return cuda_fail(h, e, "input_layernorm");
+        }
         h3::GemmPlan p{};
         p.num_sms = h->num_sms;
         p.status = h->status;
@@ -394,7 +462,9 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         p.fp8 = f8;
         p.w_static = true;   // weights change only at load/finalize, never inside an encode
         // QKV projection with q_norm/k_norm and M-RoPE fused into the epilogue
-        p.tmA = f8 ? &h->tm_y8 : &h->tm_y;
+        p.tmA = f8 ? &h->tm_y8 : fold ? &tm_h : &h->tm_y;
+        p.ss_in = fold ? h->row_ss : nullptr;
+        p.norm_eps = c.rms_eps;
         p.tmW = f8 ? &w8->tm_qkv : &w.tm_qkv;
         p.sa = f8 ? h->sy : nullptr;
         p.sw = f8 ? w8->s_qkv : nullptr;
@@ -423,14 +493,20 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         p.sw = f8 ? w8->s_o : nullptr;
         p.N = H; p.K = AO; p.epi = h3::EPI_RESIDUAL;
         p.C = out; p.ldc = H; p.R = out;
+        p.ss_in = nullptr;
+        p.ss_out = fold ? h->row_ss : nullptr;   // statistics for the post-attention norm
         e = run(h, H3ENC_K_GEMM_O, st, [&] { return h3::launch_gemm(p, st); });
         if (e != cudaSuccess) return cuda_fail(h, e, "o_proj gemm");
-        e = run(h, H3ENC_K_RMSNORM, st, [&] {
-            return f8 ? h3::launch_rmsnorm_q8(out, w.post_norm, h->y8, h->sy, S, H, c.rms_eps, st)
-                      : h3::launch_rmsnorm(out, w.post_norm, h->y, S, H, c.rms_eps, st);
-        });
-        if (e != cudaSuccess) return cuda_fail(h, e, "post_attention_layernorm");
-        p.tmA = f8 ? &h->tm_y8 : &h->tm_y;
+        p.ss_out = nullptr;
+        if (!fold) {
+            e = run(h, H3ENC_K_RMSNORM, st, [&] {
+                return f8 ? h3::launch_rmsnorm_q8(out, w.post_norm, h->y8, h->sy, S, H, c.rms_eps, st)
+                          : h3::launch_rmsnorm(out, w.post_norm, h->y, S, H, c.rms_eps, st);
+            });
+            if (e != cudaSuccess) return cuda_fail(h, e, "post_attention_layernorm");
+        }
+        p.tmA = f8 ? &h->tm_y8 : fold ? &tm_h : &h->tm_y;
+        p.ss_in = fold ? h->row_ss : nullptr;
         p.tmW = f8 ? &w8->tm_gu : &w.tm_gu;
         p.sa = f8 ? h->sy : nullptr;
         p.sw = f8 ? w8->s_gu : nullptr;
@@ -449,6 +525,8 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         p.sa = f8 ? h->sact : nullptr;
         p.sw = f8 ? w8->s_down : nullptr;
         p.N = H; p.K = I; p.C = out; p.ldc = H; p.R = out;
+        p.ss_in = nullptr;
+        p.ss_out = fold && l + 1 < le ? h->row_ss : nullptr;   // statistics for the next input norm
         if (use_ds && l < nds) {
             p.epi = h3::EPI_RESIDUAL_DS;
             p.DS = ds + (size_t)l * n_vis * H;
@@ -514,9 +592,9 @@ h3enc_status h3enc_create(const h3enc_config *cfg, h3enc **out) {
                  b_cs = align256(T * (c.head_dim / 2) * 4), b_rank = align256(T * 4), b_stat = 256,
                  b_ids = align256(T * 4), b_pos = align256(3 * T * 4), b_mask = align256(T),
                  b_ds = align256((size_t)c.num_deepstack * T * H * 2), b_out = b_y,
-                 b_gemm = align256(h3::gemm_workspace_bytes(h->num_sms));
+                 b_gemm = align256(h3::gemm_workspace_bytes(h->num_sms)), b_ss = align256(T * (H / 128) * 4);
     const size_t wsz = b_y + b_qkv + b_attn + b_act + 2 * b_cs + b_rank + b_stat + b_ids + b_pos + b_mask + b_ds +
-                       b_out + b_gemm;
+                       b_out + b_gemm + b_ss;
     e = cudaMalloc(&h->ws, wsz);
     if (e != cudaSuccess) {
         cudaFree(h->arena);
@@ -540,6 +618,7 @@ h3enc_status h3enc_create(const h3enc_config *cfg, h3enc **out) {
     h->gemm_part = reinterpret_cast<float *>(p);
     h->gemm_flags = reinterpret_cast<uint32_t *>(p + h3::gemm_flags_offset(h->num_sms));
     p += b_gemm;
+    h->row_ss = reinterpret_cast<float *>(p); p += b_ss;
     e = cudaMemset(h->ws, 0, wsz);
     if (e != cudaSuccess) {
         h3enc_destroy(h);
@@ -633,7 +712,12 @@ h3enc_status h3enc_load_weights(h3enc *h, const char *name, const void *data, in
         } else {
             e = cudaMemcpy(dst, src, n * 2, kind);
         }
-        if (e == cudaSuccess) w.loaded |= 1u << which;
+        if (e == cudaSuccess) {
+            w.loaded |= 1u << which;
+            w.folded &= ~(1u << which);   // the arena holds the checkpoint's rows again
+            if (which == T_IN && (w.folded & kQKVBits)) w.in_stale = true;
+            if (which == T_POST && (w.folded & kGUBits)) w.post_stale = true;
+        }
     }
     if (e != cudaSuccess) return cuda_fail(h, e, name);
     h->finalized = false;
@@ -670,6 +754,10 @@ h3enc_status h3enc_finalize_weights(h3enc *h) {
     if (n_missing)
         return fail(h, H3ENC_ERR_MISSING_WEIGHTS, "weights not loaded: %d params: %s%s; fused shards missing:%s",
                     n_missing, missing.c_str(), n_missing > 40 ? ", ..." : "", shards.empty() ? " none" : shards.c_str());
+    if (norm_folded(c)) {
+        h3enc_status sf = fold_norms(h);
+        if (sf != H3ENC_OK) return sf;
+    }
     const uint32_t bw = (uint32_t)h3::gemm_box_rows_w();
     const size_t H = c.hidden, d = c.head_dim;
     for (auto &w : h->layers) {
@@ -857,11 +945,21 @@ int64_t h3enc_op_gemm_workspace_bytes(void) {
     return sms > 0 ? (int64_t)h3::gemm_workspace_bytes(sms) : -1;
 }
 
-h3enc_status h3enc_op_gemm(const void *A, const void *W, void *C, int32_t M, int32_t N, int32_t K, int32_t epilogue,
-                           const void *R, const void *DS, const int32_t *vis_rank, int32_t n_vis, void *workspace,
-                           int64_t workspace_bytes, int32_t *status, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// h3enc_op_gemm and h3enc_op_gemm_rms: the bf16 projection with optional folded-norm row
+// statistics in (ss_in) and out (ss_out).
+h3enc_status gemm_op(const void *A, const void *W, void *C, int32_t M, int32_t N, int32_t K, int32_t epilogue,
+                     const void *R, const void *DS, const int32_t *vis_rank, int32_t n_vis, const float *ss_in,
+                     float *ss_out, float norm_eps, void *workspace, int64_t workspace_bytes, int32_t *status,
+                     void *stream) {
     if (M < 0 || N <= 0 || K <= 0 || N % 256 || K % 8 || epilogue < 0 || epilogue > 3)
         return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm: bad sizes or epilogue");
+    if ((ss_in && K % 128) || (ss_out && epilogue == H3ENC_EPI_SWIGLU))
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm: row statistics need K %% 128 == 0 (in) and a stored "
+                                                    "output (out)");
     if (M == 0) return H3ENC_OK;
     if (!A || !W || !C || ((epilogue == H3ENC_EPI_RESIDUAL || epilogue == H3ENC_EPI_RESIDUAL_DS) && !R) ||
         (epilogue == H3ENC_EPI_RESIDUAL_DS && DS && !vis_rank))
@@ -880,6 +978,9 @@ h3enc_status h3enc_op_gemm(const void *A, const void *W, void *C, int32_t M, int
     p.n_vis = n_vis;
     p.status = status;
     p.num_sms = h3::device_num_sms();
+    p.ss_in = ss_in;
+    p.ss_out = ss_out;
+    p.norm_eps = norm_eps;
     if (workspace) {
         if (workspace_bytes < (int64_t)h3::gemm_workspace_bytes(p.num_sms) ||
             (reinterpret_cast<uintptr_t>(workspace) & 255))
@@ -891,6 +992,43 @@ h3enc_status h3enc_op_gemm(const void *A, const void *W, void *C, int32_t M, int
     }
     cudaError_t e = h3::launch_gemm(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "gemm launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+h3enc_status h3enc_op_gemm(const void *A, const void *W, void *C, int32_t M, int32_t N, int32_t K, int32_t epilogue,
+                           const void *R, const void *DS, const int32_t *vis_rank, int32_t n_vis, void *workspace,
+                           int64_t workspace_bytes, int32_t *status, void *stream) {
+    return gemm_op(A, W, C, M, N, K, epilogue, R, DS, vis_rank, n_vis, nullptr, nullptr, 0.f, workspace,
+                   workspace_bytes, status, stream);
+}
+
+h3enc_status h3enc_op_gemm_rms(const void *A, const void *W, void *C, int32_t M, int32_t N, int32_t K,
+                               int32_t epilogue, const void *R, const float *ss_in, float *ss_out, float eps,
+                               void *workspace, int64_t workspace_bytes, int32_t *status, void *stream) {
+    if (epilogue == H3ENC_EPI_RESIDUAL_DS)
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm_rms: epilogue must be STORE, RESIDUAL or SWIGLU");
+    return gemm_op(A, W, C, M, N, K, epilogue, R, nullptr, nullptr, 0, ss_in, ss_out, eps, workspace,
+                   workspace_bytes, status, stream);
+}
+
+h3enc_status h3enc_op_row_sumsq(const void *x, int32_t rows, int32_t cols, float *ss, void *stream) {
+    if (!x || !ss || rows < 0 || cols <= 0 || cols % 128 || (reinterpret_cast<uintptr_t>(x) & 15))
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "row_sumsq: bad args");
+    cudaError_t e = h3::launch_row_sumsq(static_cast<const bf16 *>(x), rows, cols, ss,
+                                         static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "row_sumsq launch");
+}
+
+h3enc_status h3enc_op_fold_cols(void *W, int32_t rows, int32_t cols, const void *gamma, void *stream) {
+    if (!W || !gamma || rows < 0 || cols <= 0 || cols % 8 || (reinterpret_cast<uintptr_t>(W) & 15) ||
+        (reinterpret_cast<uintptr_t>(gamma) & 15))
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "fold_cols: bad args");
+    cudaError_t e = h3::launch_fold_cols(static_cast<bf16 *>(W), cols, static_cast<const bf16 *>(gamma), 0, rows, 0,
+                                         0, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "fold_cols launch");
 }
 
 h3enc_status h3enc_op_gemm_trace_next(void *trace, int64_t trace_entries) {
@@ -995,11 +1133,17 @@ h3enc_status h3enc_op_rope_table(const int32_t *positions, int32_t S, int32_t he
     return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "rope_table launch");
 }
 
-h3enc_status h3enc_op_gemm_qkv_rope(const void *A, const void *W, void *C, int32_t M, int32_t K, int32_t n_heads,
-                                    int32_t n_kv_heads, int32_t head_dim, const void *w_q, const void *w_k, float eps,
-                                    const float *cos_tab, const float *sin_tab, void *workspace,
-                                    int64_t workspace_bytes, int32_t *status, void *stream) {
+}  // extern "C"
+
+namespace {
+
+h3enc_status qkv_rope_op(const void *A, const void *W, void *C, int32_t M, int32_t K, int32_t n_heads,
+                         int32_t n_kv_heads, int32_t head_dim, const void *w_q, const void *w_k, float eps,
+                         const float *cos_tab, const float *sin_tab, const float *ss_in, float in_eps,
+                         void *workspace, int64_t workspace_bytes, int32_t *status, void *stream) {
     const int64_t N = (int64_t)(n_heads + 2 * n_kv_heads) * head_dim;
+    if (ss_in && K % 128)
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm_qkv_rope: row statistics need K %% 128 == 0");
     if (M < 0 || K <= 0 || K % 8 || n_heads < 1 || n_kv_heads < 1 || (head_dim != 64 && head_dim != 128) ||
         N % 256 || !w_q || !w_k || !cos_tab || !sin_tab)
         return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm_qkv_rope: bad sizes or NULL operand");
@@ -1018,6 +1162,8 @@ h3enc_status h3enc_op_gemm_qkv_rope(const void *A, const void *W, void *C, int32
     p.wq = static_cast<const bf16 *>(w_q); p.wk = static_cast<const bf16 *>(w_k);
     p.cos_t = cos_tab; p.sin_t = sin_tab;
     p.head_dim = head_dim; p.nq = n_heads; p.nkv = n_kv_heads; p.eps = eps;
+    p.ss_in = ss_in;
+    p.norm_eps = in_eps;
     if (workspace) {
         if (workspace_bytes < (int64_t)h3::gemm_workspace_bytes(p.num_sms) ||
             (reinterpret_cast<uintptr_t>(workspace) & 255))
@@ -1028,6 +1174,28 @@ h3enc_status h3enc_op_gemm_qkv_rope(const void *A, const void *W, void *C, int32
     }
     cudaError_t e = h3::launch_gemm(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "gemm_qkv_rope launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+h3enc_status h3enc_op_gemm_qkv_rope(const void *A, const void *W, void *C, int32_t M, int32_t K, int32_t n_heads,
+                                    int32_t n_kv_heads, int32_t head_dim, const void *w_q, const void *w_k, float eps,
+                                    const float *cos_tab, const float *sin_tab, void *workspace,
+                                    int64_t workspace_bytes, int32_t *status, void *stream) {
+    return qkv_rope_op(A, W, C, M, K, n_heads, n_kv_heads, head_dim, w_q, w_k, eps, cos_tab, sin_tab, nullptr, 0.f,
+                       workspace, workspace_bytes, status, stream);
+}
+
+h3enc_status h3enc_op_gemm_qkv_rope_rms(const void *A, const void *W, void *C, int32_t M, int32_t K,
+                                        int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, const void *w_q,
+                                        const void *w_k, float eps, const float *cos_tab, const float *sin_tab,
+                                        const float *ss_in, float in_eps, void *workspace, int64_t workspace_bytes,
+                                        int32_t *status, void *stream) {
+    if (!ss_in) return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm_qkv_rope_rms: ss_in is NULL");
+    return qkv_rope_op(A, W, C, M, K, n_heads, n_kv_heads, head_dim, w_q, w_k, eps, cos_tab, sin_tab, ss_in, in_eps,
+                       workspace, workspace_bytes, status, stream);
 }
 
 h3enc_status h3enc_op_attention(const void *qkv, void *o, int32_t S, int32_t n_heads, int32_t n_kv_heads,

@@ -92,6 +92,12 @@ struct GemmArgs {
     float *row_amax;   // EPI_SWIGLU, optional: per-row max |bf16 output| (integer atomic max)
     int w_static;      // W is not written by earlier kernels of the stream: its first stages are
                        // fetched before the dependency wait
+    // RMSNorm folded into the projection: ss_in [K/128][M] row sums of squares of A (rows of the
+    // accumulator scaled by 1/sqrt(sum/K + norm_eps)); ss_out [N/128][M] the same sums of the
+    // bf16 output
+    const float *ss_in;
+    float *ss_out;
+    float norm_eps;
 };
 
 // Phase stamps of the optional timeline (h3enc_op_gemm_traced).
@@ -156,6 +162,21 @@ __device__ __forceinline__ int sk_part_index(const GemmArgs &g, int q, int t) {
 // 128 x 256 partial sits at float4 index ((col/32)*8 + (col%32)/4)*128 + r.
 __device__ __forceinline__ size_t part_f4(int r, int col) {
     return ((size_t)((col >> 5) * 8 + ((col & 31) >> 2)) << 7) + (size_t)r;
+}
+
+// 1/rms of row `row` of A from the slot sums of squares (slots of 128 columns, added in slot
+// order: the same value for every tile of the row).
+__device__ __forceinline__ float norm_rstd(const GemmArgs &g, int row) {
+    const int slots = g.K >> 7;
+    float s = 0.f;
+    for (int i0 = 0; i0 < slots; i0 += 16) {
+        float v[16];
+        #pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = i0 + i < slots ? __ldcg(g.ss_in + (size_t)(i0 + i) * g.M + row) : 0.f;
+        #pragma unroll
+        for (int i = 0; i < 16; ++i) s += v[i];
+    }
+    return 1.0f / sqrtf(s / (float)g.K + g.norm_eps);
 }
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
@@ -512,6 +533,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         return reinterpret_cast<const float4 *>(g.part) +
                                (size_t)(k == 0 ? slot_pa : 4 * (pa + k) + (int)rank) * (BM * BN / 4);
                     };
+                    // folded input norm: the 1/rms of rows [r0, r1), once per row, in the staging area
+                    // (idle until the data-parallel epilogues; barriers on both sides of its use)
+                    float *s_rn = reinterpret_cast<float *>(sC);
+                    if (g.ss_in) {
+                        for (int u = et; u < r1 - r0; u += EPI_THREADS) {
+                            const int row = m_blk * (2 * BM) + (int)rank * BM + r0 + u;
+                            s_rn[u] = row < g.M ? norm_rstd(g, row) : 1.f;
+                        }
+                        epi_bar_and(true);
+                    }
                     if constexpr (EPI == EPI_QKROPE) {
                         // four threads per (row, head): thread `sub` owns first-half columns
                         // [sub*d/8, (sub+1)*d/8) and their RoPE partners d/2 further on
@@ -548,6 +579,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                         dq4(a + i, sr, n_blk * BN + ca + i);
                                         dq4(b + i, sr, n_blk * BN + ca + half + i);
                                     }
+                                }
+                            }
+                            if (g.ss_in) {   // the folded input RMSNorm: 1/rms of this row of A
+                                const float rn = s_rn[r - r0];
+                                #pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    a[i] *= rn;
+                                    b[i] *= rn;
                                 }
                             }
                             __nv_bfloat16 *dst = g.C + (size_t)row * g.ldc + n_blk * BN + ca;
@@ -622,6 +661,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                 dq4(f, sr, n_blk * BN + c4);
                                 if constexpr (EPI == EPI_SWIGLU) dq4(up, sr, n_blk * BN + BN / 2 + c4);
                             }
+                            if (g.ss_in) {   // the folded input RMSNorm: 1/rms of this row of A
+                                const float rn = s_rn[r - r0];
+                                #pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    f[i] *= rn;
+                                    up[i] *= rn;
+                                }
+                            }
                             int col;
                             if constexpr (EPI == EPI_SWIGLU) {
                                 #pragma unroll
@@ -655,17 +702,56 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                 }
                             }
                         }
+                        if constexpr (EPI != EPI_SWIGLU) {
+                            if (g.ss_out) {
+                                // row statistics of the rows just stored: each (row, 128-column half)
+                                // re-read in column order once every epilogue warp's stores are done
+                                epi_bar_and(true);
+                                for (int u = et; u < nr * 2; u += EPI_THREADS) {
+                                    const int r = r0 + (u >> 1), hf = u & 1;
+                                    const int row = m_blk * (2 * BM) + (int)rank * BM + r;
+                                    if (row >= g.M) continue;
+                                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                                        g.C + (size_t)row * g.ldc + n_blk * BN + hf * (BN / 2));
+                                    float ssum = 0.f;
+                                    #pragma unroll 4
+                                    for (int i = 0; i < BN / 16; ++i) {
+                                        const uint4 v = __ldcg(src + i);
+                                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                                        #pragma unroll
+                                        for (int t = 0; t < 4; ++t) {
+                                            const float lo = bf16_lo(w4[t]), hi = bf16_hi(w4[t]);
+                                            ssum = fmaf(lo, lo, ssum);
+                                            ssum = fmaf(hi, hi, ssum);
+                                        }
+                                    }
+                                    g.ss_out[(size_t)(2 * n_blk + hf) * g.M + row] = ssum;
+                                }
+                            }
+                        }
                     }
+                    if (g.ss_in) epi_bar_and(true);   // s_rn is read no more (next tile, staging)
                 }
             }
             if (et == 0) stamp(g, TR_REDUCE_DONE);
         }
+        // the folded input RMSNorm: this thread's row scale, reused while the row block repeats
+        int rn_blk = -1;
+        float rn = 1.f;
+        auto scale32 = [&](uint32_t (&v)[32]) {
+            #pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * rn);
+        };
         for (int tile = pair; tile < g.dp_tiles; tile += npairs) {
             const int m_blk = tile % g.nm;
             const int n_blk = tile / g.nm;
             const int row0 = m_blk * (2 * BM) + (int)rank * BM + quarter * 32;   // the warp's first row
             const int row = row0 + lane;
             const bool live = row < g.M;
+            if (g.ss_in && m_blk != rn_blk) {   // its loads fly while the MMAs finish
+                rn = live ? norm_rstd(g, row) : 1.f;
+                rn_blk = m_blk;
+            }
             uint4 rpre[BN / 16];   // this thread's BN/2 residual columns
             if constexpr (EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_DS) {
                 // the residual does not depend on the accumulator: its loads fly while the MMAs finish
@@ -689,6 +775,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     tmem_ld_wait();
                     dq32(vg, row, live, n_blk * BN + c * 32);
                     dq32(vu, row, live, n_blk * BN + BN / 2 + c * 32);
+                    scale32(vg);
+                    scale32(vu);
                     float f[32];
                     #pragma unroll
                     for (int j = 0; j < 32; ++j) {
@@ -718,6 +806,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             tmem_ld32(taddr + cb + c * 32, v);
                             tmem_ld_wait();
                             dq32(v, row, live, n_blk * BN + cb + c * 32);
+                            scale32(v);
                             float f[32];
                             #pragma unroll
                             for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
@@ -732,6 +821,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         tmem_ld32(taddr + cb + c * 32, v);
                         tmem_ld_wait();
                         dq32(v, row, live, n_blk * BN + cb + c * 32);
+                        scale32(v);
                         #pragma unroll
                         for (int j = 0; j < 32; ++j) ss = fmaf(__uint_as_float(v[j]), __uint_as_float(v[j]), ss);
                     }
@@ -745,6 +835,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         tmem_ld_wait();
                         dq32(va, row, live, n_blk * BN + cb + c * 32);
                         dq32(vb, row, live, n_blk * BN + cb + half + c * 32);
+                        scale32(va);
+                        scale32(vb);
                         uint32_t oa[16], ob[16];
                         #pragma unroll
                         for (int i = 0; i < 16; ++i) oa[i] = ob[i] = 0u;   // rows past M: clipped by the store
@@ -786,6 +878,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         if (rank_ds >= g.n_vis) rank_ds = -1;  // count mismatch is reported by the rank scan
                     }
                 }
+                float ssum = 0.f;   // sum of squares of this thread's 128 bf16 outputs (ss_out)
                 #pragma unroll
                 for (int cc = 0; cc < BN / 64; ++cc) {
                     const int c = ehalf * (BN / 64) + cc;
@@ -794,6 +887,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     tmem_ld32(taddr + c * 32, v);
                     tmem_ld_wait();
                     dq32(v, row, live, col);
+                    scale32(v);
                     float f[32];
                     #pragma unroll
                     for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
@@ -817,8 +911,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             }
                         }
                     }
-                    store_chunk_f(f, col, row0);
+                    uint32_t pk[16];
+                    #pragma unroll
+                    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+                    if (g.ss_out) {   // squares of the stored bf16 values, in column order
+                        #pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float lo = bf16_lo(pk[i]), hi = bf16_hi(pk[i]);
+                            ssum = fmaf(lo, lo, ssum);
+                            ssum = fmaf(hi, hi, ssum);
+                        }
+                    }
+                    store_chunk(pk, col, row0);
                 }
+                if (g.ss_out && live) g.ss_out[(size_t)(2 * n_blk + ehalf) * g.M + row] = ssum;
             }
             release_acc();
         }
@@ -915,6 +1021,9 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     g.wq = p.wq; g.wk = p.wk; g.cos_t = p.cos_t; g.sin_t = p.sin_t;
     g.head_dim = p.head_dim; g.nq = p.nq; g.nkv = p.nkv; g.eps = p.eps;
     g.trace = p.trace;
+    g.ss_in = p.ss_in;
+    g.ss_out = p.ss_out;
+    g.norm_eps = p.norm_eps;
     const int tiles = g.nm * g.nn;
     int pairs = p.num_sms / 2 < max_pairs ? p.num_sms / 2 : max_pairs;   // all pairs co-resident
     if (pairs < 1) pairs = 1;
@@ -1001,6 +1110,9 @@ cudaError_t launch_gemm(const GemmPlan &p_in, cudaStream_t stream) {
     }
     if (p.epi == EPI_QKROPE &&
         ((p.head_dim != 64 && p.head_dim != 128) || !p.wq || !p.wk || !p.cos_t || !p.sin_t))
+        return cudaErrorInvalidValue;
+    // row statistics come in slots of 128 columns; only the stored (not SwiGLU) outputs emit them
+    if ((p.ss_in && p.K % 128) || (p.ss_out && (p.N % 128 || p.epi == EPI_SWIGLU || p.epi == EPI_QKROPE)))
         return cudaErrorInvalidValue;
     if (p.fp8) {
         // the scales are read as float4 groups of 4 columns

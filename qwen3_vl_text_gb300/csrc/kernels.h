@@ -46,7 +46,22 @@ struct GemmPlan {
     // true when no kernel earlier in the stream writes W (model weights): the weight half of the
     // first ring stages is fetched before waiting for the previous kernel
     bool w_static = false;
+    // RMSNorm folded into the projection (its weight pre-multiplied into W's columns).
+    // ss_in [K/128][M] (optional): per-row sums of squares of A over column slots of 128; every
+    // accumulator row is scaled by 1/sqrt(sum / K + norm_eps) before the epilogue.  ss_out
+    // [N/128][M] (optional; EPI_STORE, EPI_RESIDUAL, EPI_RESIDUAL_DS): the same sums over this
+    // GEMM's bf16 output, for the next projection.
+    const float *ss_in = nullptr;
+    float *ss_out = nullptr;
+    float norm_eps = 0.f;
 };
+// ss[s * rows + r] = sum of x[r][c]^2 over the 128 columns of slot s, accumulated in fp32 in
+// column order (x row-major [rows, cols], cols % 128 == 0).
+cudaError_t launch_row_sumsq(const bf16 *x, int rows, int cols, float *ss, cudaStream_t st);
+// W[r][k] = bf16(W[r][k] * gamma[k]) for rows r in [r0, r1) (with blk > 0: only rows whose
+// block r / blk has parity `parity`), W row-major [*, cols], cols % 8 == 0.
+cudaError_t launch_fold_cols(bf16 *W, int cols, const bf16 *gamma, int r0, int r1, int blk, int parity,
+                             cudaStream_t st);
 // Tensor map of a row-major bf16 matrix [rows, cols] read in boxes of
 // box_rows x 64 with 128-byte swizzle.  False if the driver refuses it.
 bool make_tmap_rows(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);

@@ -1,6 +1,8 @@
-// Memory-bound steps of the decoder layer: RMSNorm over the hidden size and the
-// M-RoPE cos/sin tables (the per-head q/k RMSNorm + rotary embedding runs in the
-// epilogue of the QKV projection, csrc/gemm.cu).
+// Memory-bound steps of the decoder layer: RMSNorm over the hidden size, the
+// pieces of the RMSNorm folded into the projections (row sums of squares of the
+// layer input, the norm weight multiplied into the weight columns once at
+// finalize) and the M-RoPE cos/sin tables (the per-head q/k RMSNorm + rotary
+// embedding runs in the epilogue of the QKV projection, csrc/gemm.cu).
 //
 // Page "vllm-omni vllm_omni/diffusion/models/minimax_h3/encoder.py":
 // MiniMaxH3Qwen3VLRMSNorm (fp32 variance and scaling) and
@@ -76,6 +78,53 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(const bf16 *__res
     }
 }
 
+// One thread per (row, slot of 128 columns): the slot's sum of squares in column order.  The
+// row statistics the projections fold the RMSNorm with (the same sums the residual GEMM
+// epilogues emit for their own output).
+__global__ void row_sumsq_kernel(const bf16 *__restrict__ x, int rows, int cols, float *ss) {
+    pdl_trigger();
+    pdl_wait();
+    const int slots = cols >> 7;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long long)rows * slots) return;
+    const int s = (int)(i / rows), r = (int)(i - (long long)s * rows);
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)r * cols + (size_t)s * 128);
+    float acc = 0.f;
+    #pragma unroll 4
+    for (int k = 0; k < 16; ++k) {
+        const uint4 v = src[k];
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+        #pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float a = bf16_lo(u[t]), b = bf16_hi(u[t]);
+            acc = fmaf(a, a, acc);
+            acc = fmaf(b, b, acc);
+        }
+    }
+    ss[(size_t)s * rows + r] = acc;
+}
+
+// One thread per 8 weights: W[r][k] = bf16(W[r][k] * gamma[k]) on the selected rows.
+__global__ void fold_cols_kernel(bf16 *W, int cols, const bf16 *__restrict__ gamma, int r0, int r1, int blk,
+                                 int parity) {
+    pdl_trigger();
+    pdl_wait();
+    const int per_row = cols >> 3;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long long)(r1 - r0) * per_row) return;
+    const int r = r0 + (int)(i / per_row), k8 = (int)(i % per_row);
+    if (blk > 0 && ((r / blk) & 1) != parity) return;
+    uint4 *w = reinterpret_cast<uint4 *>(W + (size_t)r * cols) + k8;
+    const uint4 g = reinterpret_cast<const uint4 *>(gamma)[k8];
+    const uint4 v = *w;
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w}, gg[4] = {g.x, g.y, g.z, g.w};
+    uint32_t o[4];
+    #pragma unroll
+    for (int t = 0; t < 4; ++t)
+        o[t] = pack_bf16x2(bf16_lo(u[t]) * bf16_lo(gg[t]), bf16_hi(u[t]) * bf16_hi(gg[t]));
+    *w = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // One thread per (token, frequency index j).
 __global__ void rope_table_kernel(const int32_t *__restrict__ pos, int S, const RopeParams rp, float *cos_t,
                                   float *sin_t) {
@@ -116,6 +165,25 @@ cudaError_t launch_rmsnorm(const bf16 *x, const bf16 *w, bf16 *y, int rows, int 
     cudaLaunchAttribute at[1];
     cudaLaunchConfig_t cfg = pdl_config(dim3(rows), dim3(NORM_THREADS), 0, st, at);
     return cudaLaunchKernelEx(&cfg, rmsnorm_kernel, x, w, y, cols, eps);
+}
+
+cudaError_t launch_row_sumsq(const bf16 *x, int rows, int cols, float *ss, cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    if (cols <= 0 || cols % 128) return cudaErrorInvalidValue;
+    const long long n = (long long)rows * (cols / 128);
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, at);
+    return cudaLaunchKernelEx(&cfg, row_sumsq_kernel, x, rows, cols, ss);
+}
+
+cudaError_t launch_fold_cols(bf16 *W, int cols, const bf16 *gamma, int r0, int r1, int blk, int parity,
+                             cudaStream_t st) {
+    if (r1 <= r0) return cudaSuccess;
+    if (cols <= 0 || cols % 8 || r0 < 0 || blk < 0) return cudaErrorInvalidValue;
+    const long long n = (long long)(r1 - r0) * (cols / 8);
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, at);
+    return cudaLaunchKernelEx(&cfg, fold_cols_kernel, W, cols, gamma, r0, r1, blk, parity);
 }
 
 cudaError_t launch_rope_table(const int32_t *positions, int S, const RopeParams &rp, float *cos_t, float *sin_t,

@@ -82,10 +82,12 @@ def oracle_embed(wl: W.Workload, cfg, ids: np.ndarray) -> np.ndarray:
     return bits_to_f32(W.gen_weight(wl.seed, W.embed_name(), (cfg.vocab, cfg.hidden), 0.0, 0.02, rows=ids))
 
 
-def make_encoder(wl: W.Workload, cfg, max_tokens: int, max_seqs: int = 64, fp8: bool = False):
+def make_encoder(wl: W.Workload, cfg, max_tokens: int, max_seqs: int = 64, fp8: bool = False,
+                 separate_norm: bool = False):
     import torch
     from qwen3_vl_text_gb300 import Encoder
-    enc = Encoder(cfg, max_tokens=max_tokens, max_seqs=max_seqs, num_deepstack=max(3, wl.deepstack_levels), fp8=fp8)
+    enc = Encoder(cfg, max_tokens=max_tokens, max_seqs=max_seqs, num_deepstack=max(3, wl.deepstack_levels), fp8=fp8,
+                  separate_norm=separate_norm)
     for l in range(cfg.num_layers):
         for name, shape, mean, sigma in W.layer_weight_specs(cfg, l):
             enc.load(name, W.gen_weight(wl.seed, name, shape, mean, sigma, device="cuda"))

@@ -83,10 +83,11 @@ def _check_layers_and_final(wl, cfg, enc, inp, per_layer=True):
         assert ok, f"layer {l}: " + msg
 
 
-def test_tiny_two_layer_model():
+@pytest.mark.parametrize("separate_norm", [False, True], ids=["folded_norm", "separate_norm"])
+def test_tiny_two_layer_model(separate_norm):
     wl = W.workload(0)
     cfg = wl.model
-    enc = make_encoder(wl, cfg, max_tokens=64)
+    enc = make_encoder(wl, cfg, max_tokens=64, separate_norm=separate_norm)
     try:
         _check_layers_and_final(wl, cfg, enc, W.gen_inputs(wl))
     finally:
@@ -125,11 +126,12 @@ def test_tiny_layer_capture_and_host_entry_match_device_encode():
         enc.close()
 
 
-def test_one_full_width_layer():
+@pytest.mark.parametrize("separate_norm", [False, True], ids=["folded_norm", "separate_norm"])
+def test_one_full_width_layer(separate_norm):
     wl = W.workload(1)
     cfg = wl.model
     inp = W.gen_inputs(wl)
-    enc = make_encoder(wl, cfg, max_tokens=inp["seq_len"])
+    enc = make_encoder(wl, cfg, max_tokens=inp["seq_len"], separate_norm=separate_norm)
     try:
         _check_layers_and_final(wl, cfg, enc, inp, per_layer=False)
         # one layer: the free run is the teacher-forced run; hold it to the per-layer bar
