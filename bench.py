@@ -129,9 +129,13 @@ class CpuOracleSample:
         import workloads as W
         self.O, self.wl, self.inp, self.layers = O, wl, inp, layers
         cfg = wl.model
-        self.x0 = O.bf16_bits_to_float(W.gen_weight(wl.seed, W.embed_name(), (cfg.vocab, cfg.hidden), 0.0, 0.02,
-                                                    rows=inp["input_ids"]))
-        self.ds = O.bf16_bits_to_float(inp["deepstack"])
+        if inp["input_ids"] is not None:
+            self.x0 = O.bf16_bits_to_float(W.gen_weight(wl.seed, W.embed_name(), (cfg.vocab, cfg.hidden), 0.0, 0.02,
+                                                        rows=inp["input_ids"]))
+        else:   # a hidden-state input (the one-layer workload)
+            self.x0 = O.bf16_bits_to_float(inp["inputs_embeds"])
+        self.ds = None if inp["deepstack"] is None else O.bf16_bits_to_float(inp["deepstack"])
+        self.mask = inp["visual_mask"] if inp["n_vis"] else None
         self.weights = [O.layer_weights_from_bits({n: W.gen_weight(wl.seed, n, s, m, sg)
                                                    for n, s, m, sg in W.layer_weight_specs(cfg, l)})
                         for l in range(layers)]
@@ -139,11 +143,57 @@ class CpuOracleSample:
     def run(self) -> float:
         t0 = time.perf_counter()
         self.O.forward(self.x0, self.inp["positions"], self.wl.model, lambda l: self.weights[l],
-                       self.inp["visual_mask"], self.ds, layers=range(self.layers))
+                       self.mask, self.ds, layers=range(self.layers))
         return time.perf_counter() - t0
 
 
 REF_LAYERS_PER_STEP = 4
+
+# the oracle timed on whole small workloads: (workload id, name)
+ORACLE_TIMED = ((0, "tiny_2layer_48tok"), (1, "one_full_layer_512tok"))
+
+
+def oracle_time(args):
+    """One workload through the CPU oracle in this process (its BLAS threads fixed by the caller's
+    environment): prints {"seconds": [...], "tokens": S}."""
+    import workloads as W
+    wl = W.workload(args.oracle_time)
+    inp = W.gen_inputs(wl)
+    sample = CpuOracleSample(wl, inp, wl.model.num_layers)
+    for _ in range(args.warm):
+        sample.run()
+    ts = [sample.run() for _ in range(args.reps)]
+    print(json.dumps({"seconds": ts, "tokens": int(inp["seq_len"])}), flush=True)
+    return 0
+
+
+def oracle_config_timings():
+    """The oracle on the tiny 2-layer workload and on one full-width layer at 512 tokens, with all
+    host cores and with one thread (BLAS threads set before numpy loads, so each runs in a child
+    process): median seconds, tokens/s and, for the full-width layer, GFLOP/s."""
+    import workloads as W
+    cores = os.cpu_count()
+    out = {"cores": cores}
+    for wid, name in ORACLE_TIMED:
+        wl = W.workload(wid)
+        inp = W.gen_inputs(wl)
+        flops = encode_flops(wl.model, inp["cu_seqlens"])
+        entry = {}
+        for label, threads, reps, warm in (("all_cores", cores, 3, 1), ("one_thread", 1, 1, 0)):
+            env = dict(os.environ, OMP_NUM_THREADS=str(threads), OPENBLAS_NUM_THREADS=str(threads),
+                       MKL_NUM_THREADS=str(threads))
+            r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-time", str(wid),
+                                "--reps", str(reps), "--warm", str(warm)],
+                               env=env, capture_output=True, text=True, timeout=600)
+            if r.returncode != 0:
+                raise RuntimeError("oracle timing failed: " + r.stderr[-400:])
+            d = json.loads(r.stdout.strip().splitlines()[-1])
+            ts = sorted(d["seconds"])
+            t = ts[len(ts) // 2]
+            entry[label] = {"threads": threads, "seconds": t, "tokens_per_s": d["tokens"] / t,
+                            "gflops": flops / t / 1e9}
+        out[name] = entry
+    return out
 
 
 def run_reference(args):
@@ -179,6 +229,7 @@ def run_reference(args):
 def run_kernel(args):
     """One kernel of the seq-1024 workload alone, device-timed (for ncu captures and tuning).
     Prints one JSON line with the average launch time and the achieved rate."""
+    import numpy as np
     import torch
 
     import qwen3_vl_text_gb300 as Q
@@ -244,12 +295,42 @@ def run_kernel(args):
         O_ = torch.empty(S, nq * d, dtype=torch.bfloat16, device=dev)
         fn = lambda: Q.h3enc_op_attention(X, O_, S, nq, nkv, d)
         work, unit = 4.0 * nq * d * S * (S + 1) / 2 / 1e12, "TFLOP/s"
-    elif name == "rmsnorm":
+    elif name == "rmsnorm":   # x read, y written, gamma read (algorithmic bytes)
         X = rnd("x", (S, H), 1.0)
         G = rnd("g", (H,), 1.0)
         Y = torch.empty_like(X)
         fn = lambda: Q.h3enc_op_rmsnorm(X, G, Y, S, H, 1e-6)
-        work, unit = 2.0 * S * H * 2 / 1e9, "GB/s"
+        work, unit = (2.0 * S * H * 2 + 2 * H) / 1e9, "GB/s"
+    elif name == "rmsnorm_q8":   # the FP8 path's norm: x read, e4m3 rows + scales written
+        X = rnd("x", (S, H), 1.0)
+        G = rnd("g", (H,), 1.0)
+        Y8 = torch.empty(S, H, dtype=torch.uint8, device=dev)
+        sc = torch.empty(S, dtype=torch.float32, device=dev)
+        fn = lambda: Q.h3enc_op_rmsnorm_q8(X, G, Y8, sc, S, H, 1e-6)
+        work, unit = (S * H * 2 + 2 * H + S * H + 4 * S) / 1e9, "GB/s"
+    elif name == "quant_rows":   # e4m3 quantisation of the SwiGLU output [S, I]: read bf16, write bytes
+        X = rnd("act", (S, I), 1.0)
+        Y8 = torch.empty(S, I, dtype=torch.uint8, device=dev)
+        sc = torch.empty(S, dtype=torch.float32, device=dev)
+        fn = lambda: Q.h3enc_op_quant_rows(X, S, I, Y8, sc)
+        work, unit = (S * I * 2 + S * I + 4 * S) / 1e9, "GB/s"
+    elif name == "row_sumsq":   # the folded norm's statistics of the layer input: x read, [H/128, S] written
+        X = rnd("x", (S, H), 1.0)
+        ss = torch.empty(H // 128, S, dtype=torch.float32, device=dev)
+        fn = lambda: Q.h3enc_op_row_sumsq(X, S, H, ss)
+        work, unit = (S * H * 2 + 4 * S * (H // 128)) / 1e9, "GB/s"
+    elif name == "embed":   # gather of S rows of the 151936 x H table: ids read, rows read and written
+        table = rnd("embed", (cfg.vocab, H))
+        ids = torch.from_numpy(np.random.default_rng(5).integers(0, cfg.vocab, S).astype(np.int32)).cuda()
+        Xo = torch.empty(S, H, dtype=torch.bfloat16, device=dev)
+        fn = lambda: Q.h3enc_op_embed(ids, table, cfg.vocab, H, Xo, S)
+        work, unit = (4 * S + 2.0 * S * H * 2) / 1e9, "GB/s"
+    elif name == "rope_table":   # positions read, fp32 cos/sin [S, d/2] written
+        pos = torch.arange(S, dtype=torch.int32, device=dev).repeat(3, 1).contiguous()
+        c = torch.empty(S, d // 2, device=dev)
+        s_ = torch.empty_like(c)
+        fn = lambda: Q.h3enc_op_rope_table(pos, S, d, cfg.rope_theta, cfg.mrope_section, c, s_)
+        work, unit = (3 * 4 * S + 2 * 4 * S * (d // 2)) / 1e9, "GB/s"
     else:
         raise SystemExit("unknown kernel " + name)
     stream = torch.cuda.current_stream()
@@ -278,6 +359,7 @@ def run_kernel(args):
     peak = (burst * (2.0 if fp8_gemm else 1.0)) if unit == "TFLOP/s" else hbm
     print(json.dumps({"kernel": name + (" (e4m3)" if fp8_gemm else "") + (" (folded norm)" if args.fold else ""),
                       "seq": S, "ms_median": ms, "ms_min": ts[0], "achieved": work / (ms / 1e3),
+                      "work_per_launch": work, "work_unit": "TFLOP" if unit == "TFLOP/s" else "GB",
                       "unit": unit, "peak": peak, "frac": work / (ms / 1e3) / peak,
                       "peak_source": f"{src} {'bf16_tflops' if unit == 'TFLOP/s' else 'hbm_gbs'} (burst)"
                                      + (" x 2 (nominal fp8/bf16)" if fp8_gemm else "")}),
@@ -289,7 +371,8 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--kernel", default=None,
                     help="time one kernel alone: gemm_qkv (with the fused q/k norm + M-RoPE), gemm_o, "
-                         "gemm_gate_up, gemm_down, attention, rmsnorm")
+                         "gemm_gate_up, gemm_down, attention, rmsnorm, rmsnorm_q8, quant_rows, row_sumsq, embed, "
+                         "rope_table")
     ap.add_argument("--seq", type=int, default=1024)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -298,6 +381,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--separate-norm", action="store_true",
                     help="bf16: run each RMSNorm as its own kernel instead of folding it into the projections")
+    ap.add_argument("--oracle-time", type=int, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--reps", type=int, default=3, help=argparse.SUPPRESS)
+    ap.add_argument("--warm", type=int, default=1, help=argparse.SUPPRESS)
     ap.add_argument("--fold", action="store_true",
                     help="with --kernel: the projection as the folded-norm encode runs it (QKV and gate/up "
                          "scale rows by the norm statistics, o and down emit them)")
@@ -310,6 +396,8 @@ def main():
                          "attention stays bf16.  Not the headline configuration, which is plain bf16.")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.oracle_time is not None:
+        return oracle_time(args)
     if args.kernel:
         return run_kernel(args)
     if args.impl == "reference":
@@ -405,17 +493,13 @@ def main():
     clk = clocks.stop()
     ms = e0.elapsed_time(e1)
     prof_gu = Q.h3enc_get_profile(enc.handle)[GEMM_GU_CLASS]
-    # per-kernel breakdown: the same steps again with an event pair around every launch
-    Q.h3enc_set_profiling(enc.handle, True)
-    for _ in range(args.steps):
-        step()
-    prof = Q.h3enc_get_profile(enc.handle)
-    Q.h3enc_set_profiling(enc.handle, False)
+    Q.h3enc_set_profiling_classes(enc.handle, [])
     value, ms = job_throughput(ms, S, args.steps, dist, "cuda")
     if enc.status() != 0:
         raise RuntimeError("device status after the timed region: " + Q.h3enc_last_error(enc.handle))
 
-    # end to end through the host-buffer entry point: pinned inputs in, result out, every step
+    # end to end through the host-buffer entry point: pinned inputs in, result out, every step.
+    # Right after the timed region and for as many steps, so both see the same power state.
     h_ids = torch.from_numpy(inp["input_ids"]).pin_memory()
     h_pos = torch.from_numpy(inp["positions"]).pin_memory()
     h_mask = torch.from_numpy(inp["visual_mask"]).pin_memory()
@@ -430,12 +514,19 @@ def main():
     if dist:
         dist.barrier()
     t0 = time.perf_counter()
-    e2e_steps = max(3, args.steps // 2)
+    e2e_steps = args.steps
     for _ in range(e2e_steps):
         host_step()
     e2e_value, e2e_ms = job_throughput((time.perf_counter() - t0) * 1e3, S, e2e_steps, dist, "cuda")
     h2d = (h_ids.numel() * 4 + h_pos.numel() * 4 + h_mask.numel() + h_ds.numel() * 2)
     d2h = h_out.numel() * 2
+
+    # per-kernel breakdown: the same steps again with an event pair around every launch
+    Q.h3enc_set_profiling(enc.handle, True)
+    for _ in range(args.steps):
+        step()
+    prof = Q.h3enc_get_profile(enc.handle)
+    Q.h3enc_set_profiling(enc.handle, False)
 
     burst, sustained, hbm, peak_src = _peaks()
     flops = encode_flops(cfg, inp["cu_seqlens"])
@@ -492,7 +583,8 @@ def main():
         line["cpu_baseline"] = {"value": S / per_encode, "unit": "tokens/s", "cores": os.cpu_count(),
                                 "kind": "oracle",
                                 "sample": f"first {args.cpu_layers} of 50 decoder layers at seq 1024, time scaled x"
-                                          f"{cfg.num_layers / args.cpu_layers:g}"}
+                                          f"{cfg.num_layers / args.cpu_layers:g}",
+                                "oracle_configs": oracle_config_timings()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
