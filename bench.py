@@ -374,6 +374,9 @@ def main():
                          "gemm_gate_up, gemm_down, attention, rmsnorm, rmsnorm_q8, quant_rows, row_sumsq, embed, "
                          "rope_table")
     ap.add_argument("--seq", type=int, default=1024)
+    ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=[2, 3, 4],
+                    help="2: 50-layer seq-1024 image layout (the headline); 3: seq-8192 video layout; "
+                         "4: 16 packed text prompts")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
@@ -418,12 +421,15 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
 
-    wl = W.workload(WORKLOAD_ID)
+    wl = W.workload(args.workload)
+    headline = args.workload == WORKLOAD_ID
     cfg = wl.model
     inp = W.gen_inputs(wl)
     S = inp["seq_len"]
-    enc = Q.Encoder(cfg, max_tokens=S, max_seqs=4, num_deepstack=wl.deepstack_levels, fp8=args.fp8,
-                    separate_norm=args.separate_norm)
+    cu = [int(x) for x in inp["cu_seqlens"]] if len(inp["cu_seqlens"]) > 2 else None
+    n_vis = inp["n_vis"]
+    enc = Q.Encoder(cfg, max_tokens=S, max_seqs=max(4, len(inp["cu_seqlens"]) - 1),
+                    num_deepstack=max(1, wl.deepstack_levels), fp8=args.fp8, separate_norm=args.separate_norm)
     for l in range(cfg.num_layers):
         for name, shape, mean, sigma in W.layer_weight_specs(cfg, l):
             enc.load(name, W.gen_weight(wl.seed, name, shape, mean, sigma, device="cuda"))
@@ -434,13 +440,13 @@ def main():
 
     ids = torch.from_numpy(inp["input_ids"]).cuda()
     pos = torch.from_numpy(inp["positions"]).cuda()
-    mask = torch.from_numpy(inp["visual_mask"]).cuda()
-    ds = W.bf16_bits_to_torch(inp["deepstack"]).cuda()
+    mask = torch.from_numpy(inp["visual_mask"]).cuda() if n_vis else None
+    ds = W.bf16_bits_to_torch(inp["deepstack"]).cuda() if inp["deepstack"] is not None else None
     out = torch.empty(S, cfg.hidden, dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
 
     def step():
-        enc.encode(ids, pos, out, visual_mask=mask, deepstack=ds, n_vis=inp["n_vis"], stream=stream)
+        enc.encode(ids, pos, out, visual_mask=mask, deepstack=ds, n_vis=n_vis, cu_seqlens=cu, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -456,13 +462,13 @@ def main():
         # once per step: the same kernels, launched by the graph instead of the host
         cap = torch.cuda.Stream()
         cap.wait_stream(stream)
-        enc.encode(ids, pos, out, visual_mask=mask, deepstack=ds, n_vis=inp["n_vis"], stream=cap)  # warm on cap
+        enc.encode(ids, pos, out, visual_mask=mask, deepstack=ds, n_vis=n_vis, cu_seqlens=cu, stream=cap)  # warm
         torch.cuda.synchronize()
         Q.h3enc_set_profiling_classes(enc.handle, [GEMM_GU_CLASS])   # drop the warm-up's event pairs
         n_cap = Q.h3enc_launch_count(enc.handle)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=cap):
-            enc.encode(ids, pos, out, visual_mask=mask, deepstack=ds, n_vis=inp["n_vis"], stream=cap)
+            enc.encode(ids, pos, out, visual_mask=mask, deepstack=ds, n_vis=n_vis, cu_seqlens=cu, stream=cap)
         launches_per_step = Q.h3enc_launch_count(enc.handle) - n_cap
         stream.wait_stream(cap)
         graph.replay()
@@ -502,13 +508,13 @@ def main():
     # Right after the timed region and for as many steps, so both see the same power state.
     h_ids = torch.from_numpy(inp["input_ids"]).pin_memory()
     h_pos = torch.from_numpy(inp["positions"]).pin_memory()
-    h_mask = torch.from_numpy(inp["visual_mask"]).pin_memory()
-    h_ds = W.bf16_bits_to_torch(inp["deepstack"]).pin_memory()
+    h_mask = torch.from_numpy(inp["visual_mask"]).pin_memory() if n_vis else None
+    h_ds = W.bf16_bits_to_torch(inp["deepstack"]).pin_memory() if ds is not None else None
     h_out = torch.empty(S, cfg.hidden, dtype=torch.bfloat16).pin_memory()
 
     def host_step():
-        Q.h3enc_encode_host(enc.handle, h_ids, h_pos, h_mask, h_ds, h_ds.shape[0], inp["n_vis"], None, S, h_out,
-                            stream)
+        Q.h3enc_encode_host(enc.handle, h_ids, h_pos, h_mask, h_ds, 0 if h_ds is None else h_ds.shape[0], n_vis, cu,
+                            S, h_out, stream)
 
     host_step()
     if dist:
@@ -518,7 +524,8 @@ def main():
     for _ in range(e2e_steps):
         host_step()
     e2e_value, e2e_ms = job_throughput((time.perf_counter() - t0) * 1e3, S, e2e_steps, dist, "cuda")
-    h2d = (h_ids.numel() * 4 + h_pos.numel() * 4 + h_mask.numel() + h_ds.numel() * 2)
+    h2d = (h_ids.numel() * 4 + h_pos.numel() * 4 + (0 if h_mask is None else h_mask.numel())
+           + (0 if h_ds is None else h_ds.numel() * 2))
     d2h = h_out.numel() * 2
 
     # per-kernel breakdown: the same steps again with an event pair around every launch
@@ -543,7 +550,8 @@ def main():
     f8 = 2.0 if args.fp8 else 1.0
     gu_peak = base * f8
     line = {
-        "metric": "encoded tokens/s, 50-layer seq-1024 encode" + (", online FP8 linears" if args.fp8 else ""),
+        "metric": (("encoded tokens/s, 50-layer seq-1024 encode" if headline else f"encoded tokens/s, {wl.name}")
+                   + (", online FP8 linears" if args.fp8 else "")),
         "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -568,7 +576,7 @@ def main():
                                     + (" x 2 (nominal fp8/bf16)" if args.fp8 else ""),
                      "frac_of_burst": gu_achieved / (burst * f8),
                      "frac_of_sustained": gu_achieved / (sustained * f8),
-                     "traffic": None if args.fp8 else GATE_UP_TRAFFIC_BYTES},
+                     "traffic": None if args.fp8 or not headline else GATE_UP_TRAFFIC_BYTES},
         "kernel_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
         "kernel_ms_note": "separate pass with an event pair around every launch",
         "gpu_launches": int(launches),
@@ -577,7 +585,7 @@ def main():
         "clocks": clk,
     }
     enc.close()
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.fp8:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.fp8 and headline:
         t = CpuOracleSample(wl, inp, args.cpu_layers).run()
         per_encode = t / args.cpu_layers * cfg.num_layers
         line["cpu_baseline"] = {"value": S / per_encode, "unit": "tokens/s", "cores": os.cpu_count(),
