@@ -19,3 +19,4 @@ on random weights, whose output has no independent value to compare with
 from .qwen3vl_text import *  # noqa: F401,F403
 from . import fp8  # noqa: F401  (online-FP8 linears)
 from . import frontend  # noqa: F401  (token ids -> positions, visual rows, DeepStack order)
+from . import vision  # noqa: F401  (the vision tower: visual embeddings and DeepStack features)

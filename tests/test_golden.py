@@ -93,3 +93,10 @@ def test_deepstack_order(case):
     want = [1000 + int(s[1:]) if s[0] == "i" else 2000 + int(s[1:]) for s in case["order"]]
     assert mask.tolist() == (kinds != 0).tolist()
     assert out[0, :, 0].tolist() == want and out[1, :, 0].tolist() == want
+
+
+@pytest.mark.parametrize("case", read_cases("vision_merge_order.txt"), ids=lambda c: c["case"])
+def test_vision_merge_order(case):
+    t, h, w = ints(case["grid"])
+    want = [[int(v) for v in p.split(",")] for p in case["patches"]]
+    assert O.vision.merge_order(t, h, w, int(case["merge"][0])).tolist() == want

@@ -36,6 +36,8 @@ __all__ = [
     "ModelConfig", "Workload", "MODELS", "WORKLOADS", "workload",
     "layer_weight_specs", "embed_name", "normal_bf16", "gen_weight",
     "gen_inputs", "bf16_bits_to_torch", "uniform_ints",
+    "VisionConfig", "VisionWorkload", "VISION_WORKLOADS", "vision_workload", "vision_weight_specs",
+    "gen_vision_inputs",
 ]
 
 _M32 = 0xFFFFFFFF
@@ -365,3 +367,113 @@ def gen_inputs(w: Workload) -> dict:
     else:
         out["deepstack"] = None
     return out
+
+
+# ---------------------------------------------------------------------------
+# vision tower (the producer of the visual embeddings and DeepStack features)
+# ---------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class VisionConfig:
+    """Sizes of the Qwen3-VL vision tower ("vllm-omni minimax_h3/encoder.py",
+    MiniMaxH3Qwen3VLVisionModel and the classes it builds).  The pages take them from
+    the checkpoint's config without printing them; the configurations below are
+    synthetic (random weights), sized for the kernels (widths multiples of 256)."""
+    depth: int
+    hidden: int
+    num_heads: int
+    intermediate: int
+    in_channels: int
+    patch_size: int
+    temporal_patch_size: int
+    spatial_merge_size: int
+    out_hidden: int
+    num_position_embeddings: int
+    deepstack_visual_indexes: tuple
+    ln_eps: float = 1e-6
+    rope_theta: float = 10000.0
+
+    @property
+    def head_dim(self) -> int:
+        return self.hidden // self.num_heads
+
+    @property
+    def patch_dim(self) -> int:
+        return self.in_channels * self.temporal_patch_size * self.patch_size * self.patch_size
+
+    @property
+    def merged_hidden(self) -> int:
+        return self.hidden * self.spatial_merge_size ** 2
+
+
+@dataclasses.dataclass(frozen=True)
+class VisionWorkload:
+    name: str
+    model: VisionConfig
+    seed: int
+    grids: tuple   # (t, h, w) patch grids, images and videos in sequence order
+
+
+VISION_TINY = VisionConfig(depth=3, hidden=256, num_heads=4, intermediate=512, in_channels=3, patch_size=4,
+                           temporal_patch_size=2, spatial_merge_size=2, out_hidden=256,
+                           num_position_embeddings=64, deepstack_visual_indexes=(0, 1))
+VISION_FULL = VisionConfig(depth=24, hidden=1024, num_heads=16, intermediate=4096, in_channels=3, patch_size=16,
+                           temporal_patch_size=2, spatial_merge_size=2, out_hidden=5120,
+                           num_position_embeddings=2304, deepstack_visual_indexes=(5, 11, 17))
+
+VISION_WORKLOADS = {
+    # 8 x 16 patches -> the 4 x 8 merged grid of the tiny text workload
+    0: VisionWorkload("vision-tiny-8x16", VISION_TINY, 2000, grids=((1, 8, 16),)),
+    # an image and a two-frame video of different sizes: several attention segments
+    1: VisionWorkload("vision-tiny-image-video", VISION_TINY, 2001, grids=((1, 12, 8), (2, 8, 8))),
+    # one 48 x 64-patch image -> the 24 x 32 merged grid of the seq-1024 workload
+    2: VisionWorkload("vision-image-48x64", VISION_FULL, 2002, grids=((1, 48, 64),)),
+}
+
+
+def vision_workload(i: int) -> VisionWorkload:
+    return VISION_WORKLOADS[i]
+
+
+def vision_weight_specs(cfg: VisionConfig):
+    """(HF name, shape, mean, sigma) of every vision-tower tensor.  Linear and
+    embedding weights and all biases ~ N(0, 0.02); LayerNorm weights ~ 1 + N(0, 0.1),
+    LayerNorm biases ~ N(0, 0.1)."""
+    p = "model.visual."
+    h, i, mh = cfg.hidden, cfg.intermediate, cfg.merged_hidden
+    specs = [
+        (p + "patch_embed.proj.weight", (h, cfg.in_channels, cfg.temporal_patch_size, cfg.patch_size,
+                                         cfg.patch_size), 0.0, 0.02),
+        (p + "patch_embed.proj.bias", (h,), 0.0, 0.02),
+        (p + "pos_embed.weight", (cfg.num_position_embeddings, h), 0.0, 0.02),
+    ]
+    for b in range(cfg.depth):
+        q = f"{p}blocks.{b}."
+        specs += [
+            (q + "norm1.weight", (h,), 1.0, 0.1), (q + "norm1.bias", (h,), 0.0, 0.1),
+            (q + "attn.qkv.weight", (3 * h, h), 0.0, 0.02), (q + "attn.qkv.bias", (3 * h,), 0.0, 0.02),
+            (q + "attn.proj.weight", (h, h), 0.0, 0.02), (q + "attn.proj.bias", (h,), 0.0, 0.02),
+            (q + "norm2.weight", (h,), 1.0, 0.1), (q + "norm2.bias", (h,), 0.0, 0.1),
+            (q + "mlp.linear_fc1.weight", (i, h), 0.0, 0.02), (q + "mlp.linear_fc1.bias", (i,), 0.0, 0.02),
+            (q + "mlp.linear_fc2.weight", (h, i), 0.0, 0.02), (q + "mlp.linear_fc2.bias", (h,), 0.0, 0.02),
+        ]
+    mergers = [("merger.", h)] + [(f"deepstack_merger_list.{j}.", mh)
+                                  for j in range(len(cfg.deepstack_visual_indexes))]
+    for m, norm_width in mergers:
+        q = p + m
+        specs += [
+            (q + "norm.weight", (norm_width,), 1.0, 0.1), (q + "norm.bias", (norm_width,), 0.0, 0.1),
+            (q + "linear_fc1.weight", (mh, mh), 0.0, 0.02), (q + "linear_fc1.bias", (mh,), 0.0, 0.02),
+            (q + "linear_fc2.weight", (cfg.out_hidden, mh), 0.0, 0.02),
+            (q + "linear_fc2.bias", (cfg.out_hidden,), 0.0, 0.02),
+        ]
+    return specs
+
+
+def gen_vision_inputs(w: VisionWorkload) -> dict:
+    """Pixel patches [n_patches, C*T*P*P] (bf16 bits, N(0, 1), flattened in (C, T, P, P)
+    order as the patch embedding views them), the grids, and the patch count."""
+    cfg = w.model
+    n = sum(t * h * ww for t, h, ww in w.grids)
+    return {"pixel_values": normal_bf16(w.seed, "pixel_values", (n, cfg.patch_dim), 0.0, 1.0),
+            "grid_thw": np.array(w.grids, dtype=np.int32).reshape(-1, 3), "n_patches": n}
