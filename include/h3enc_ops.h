@@ -25,8 +25,10 @@ enum {
     H3ENC_EPI_RESIDUAL = 1,    /* C = bf16(R + acc); R may equal C                (o_proj + residual) */
     H3ENC_EPI_SWIGLU = 2,      /* W packed by h3enc_op_pack_gate_up (N = 2*I rows):
                                   C[:, i] = bf16(silu(gate_i) * up_i), C has I columns (gate/up + SwiGLU) */
-    H3ENC_EPI_RESIDUAL_DS = 3  /* C = bf16(R + acc), then at rows with vis_rank[r] = j in [0, n_vis):
+    H3ENC_EPI_RESIDUAL_DS = 3, /* C = bf16(R + acc), then at rows with vis_rank[r] = j in [0, n_vis):
                                   C = bf16(C + DS[j])                             (down_proj + residual + DeepStack) */
+    H3ENC_EPI_GELU_TANH = 5,   /* C = bf16(gelu_tanh(acc + bias))                 (vision MLP fc1) */
+    H3ENC_EPI_GELU_ERF = 6     /* C = bf16(gelu(acc + bias)), exact erf form      (vision merger fc1) */
 };
 
 /* Projection GEMM on the tcgen05 tensor cores (page "vllm-omni ... encoder.py":
@@ -211,6 +213,56 @@ H3ENC_API h3enc_status h3enc_op_gemm_qkv_rope_rms(const void *A, const void *W, 
                                                   const float *cos_tab, const float *sin_tab, const float *ss_in,
                                                   float in_eps, void *workspace, int64_t workspace_bytes,
                                                   int32_t *status, void *stream);
+
+/* ---- vision tower kernels (page "... encoder.py", section "Qwen3-VL vision tower") ----
+ * The tower's patch order: per grid, frames, then the m x m blocks row-major, then the
+ * patches of a block row-major.  grid_thw: HOST int32 [n_grids, 3] (n_grids <= 64; rows and
+ * columns multiples of merge).
+ *
+ * h3enc_op_layernorm: y = bf16((x - mean) / sqrt(var + eps) * w + b) per row (nn.LayerNorm,
+ * biased variance, fp32); x, y [rows, cols] bf16, cols % 8 == 0, cols <= 8192. */
+H3ENC_API h3enc_status h3enc_op_layernorm(const void *x, const void *w, const void *b, void *y, int32_t rows,
+                                          int32_t cols, float eps, void *stream);
+
+/* h3enc_op_vision_pos_embed (fast_pos_embed_interpolate): out[k] = bf16 of the bilinear
+ * sample of the grid_side x grid_side table [grid_side^2, hidden] at patch k: the grid's
+ * h x w points evenly spaced from corner to corner (i * (G-1)/(h-1) in double, rounded
+ * to fp32), lower corner by truncation, upper clipped to G-1, fp32 weights and
+ * products summed corner by corner.  out [n_patches, hidden] bf16. */
+H3ENC_API h3enc_status h3enc_op_vision_pos_embed(const void *table, int32_t grid_side, int32_t hidden,
+                                                 const int32_t *grid_thw, int32_t n_grids, int32_t merge, void *out,
+                                                 void *stream);
+
+/* h3enc_op_vision_rope_table (rot_pos_emb): cos/sin [n_patches, head_dim/2] fp32 of the
+ * angles row * inv_freq[j] (j < head_dim/4) and column * inv_freq[j - head_dim/4] (the
+ * rest), inv_freq[j] = theta^(-2j/(head_dim/2)) rounded once to fp32; the pairs
+ * (j, j + head_dim/2) of q and k rotate by angle j as in h3enc_op_gemm_qkv_rope. */
+H3ENC_API h3enc_status h3enc_op_vision_rope_table(const int32_t *grid_thw, int32_t n_grids, int32_t merge,
+                                                  int32_t head_dim, float theta, float *cos_tab, float *sin_tab,
+                                                  void *stream);
+
+/* h3enc_op_gemm_bias: h3enc_op_gemm with bias [N] (bf16, 16-byte aligned) added to the
+ * accumulator; epilogue H3ENC_EPI_STORE (C = bf16(acc + bias)), H3ENC_EPI_RESIDUAL
+ * (C = bf16(R + acc + bias)), H3ENC_EPI_GELU_TANH or H3ENC_EPI_GELU_ERF.  Other arguments
+ * and requirements as h3enc_op_gemm. */
+H3ENC_API h3enc_status h3enc_op_gemm_bias(const void *A, const void *W, void *C, int32_t M, int32_t N, int32_t K,
+                                          int32_t epilogue, const void *R, const void *bias, void *workspace,
+                                          int64_t workspace_bytes, int32_t *status, void *stream);
+
+/* h3enc_op_gemm_qkv_rope_bias (the vision tower's attention input): qkv = A W^T + bias with
+ * W [3 * heads * head_dim, K] (q rows, k rows, v rows), then every q and k head rotated
+ * with the fp32 tables cos/sin [M, head_dim/2] (no per-head norm); v heads as they are. */
+H3ENC_API h3enc_status h3enc_op_gemm_qkv_rope_bias(const void *A, const void *W, void *C, int32_t M, int32_t K,
+                                                   int32_t heads, int32_t head_dim, const void *bias,
+                                                   const float *cos_tab, const float *sin_tab, void *workspace,
+                                                   int64_t workspace_bytes, int32_t *status, void *stream);
+
+/* h3enc_op_attention_bidir: as h3enc_op_attention with one kv head per q head and no
+ * causal mask: every query attends to every key of its segment (the tower's attention
+ * inside each frame, scaled_dot_product_attention with is_causal=False). */
+H3ENC_API h3enc_status h3enc_op_attention_bidir(const void *qkv, void *o, int32_t S, int32_t heads,
+                                                int32_t head_dim, const int32_t *cu_seqlens, int32_t n_seqs,
+                                                void *stream);
 
 /* Causal GQA attention over packed sequences (page "... encoder.py",
  * MiniMaxH3Qwen3VLTextAttention.forward: repeat_interleave of K/V, SDPA with

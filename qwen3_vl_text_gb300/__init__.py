@@ -14,6 +14,7 @@ import os
 
 __all__ = [
     "lib", "H3encError", "Config", "STATUS", "EPI_STORE", "EPI_RESIDUAL", "EPI_SWIGLU", "EPI_RESIDUAL_DS",
+    "EPI_GELU_TANH", "EPI_GELU_ERF",
     "h3enc_create", "h3enc_load_weights", "h3enc_finalize_weights", "h3enc_encode", "h3enc_encode_embeds", "h3enc_encode_multimodal",
     "h3enc_encode_host", "h3enc_set_layer_capture", "h3enc_get_status", "h3enc_last_error", "h3enc_destroy",
     "h3enc_set_profiling", "h3enc_set_profiling_classes", "h3enc_get_profile", "h3enc_launch_count", "h3enc_num_sms",
@@ -21,7 +22,10 @@ __all__ = [
     "h3enc_op_gemm", "h3enc_op_gemm_workspace_bytes", "h3enc_op_gemm_trace_next", "h3enc_op_attention_trace_next", "h3enc_op_gemm_noalloc", "h3enc_op_gemm_noalloc_scratch_bytes", "h3enc_op_pack_gate_up", "h3enc_op_rmsnorm", "h3enc_op_gemm_fp8", "h3enc_op_quant_rows",
     "h3enc_op_rmsnorm_q8", "h3enc_op_wait_probe", "h3enc_op_rope_table",
     "h3enc_op_gemm_qkv_rope", "h3enc_op_gemm_qkv_rope_rms", "h3enc_op_gemm_rms", "h3enc_op_row_sumsq",
-    "h3enc_op_fold_cols", "h3enc_op_attention", "h3enc_op_embed", "h3enc_op_vis_rank", "Encoder",
+    "h3enc_op_fold_cols", "h3enc_op_layernorm", "h3enc_op_vision_pos_embed", "h3enc_op_vision_rope_table",
+    "h3enc_op_gemm_bias", "h3enc_op_gemm_qkv_rope_bias", "h3enc_op_attention_bidir", "VisionConfig",
+    "h3vis_create", "h3vis_load_weights", "h3vis_finalize_weights", "h3vis_encode", "h3vis_get_status",
+    "h3vis_last_error", "h3vis_launch_count", "h3vis_destroy", "VisionEncoder", "h3enc_op_attention", "h3enc_op_embed", "h3enc_op_vis_rank", "Encoder",
     "KERNEL_CLASSES",
 ]
 
@@ -32,6 +36,7 @@ STATUS = {0: "OK", 1: "WARN_IGNORED", 2: "ERR_INVALID_ARG", 3: "ERR_SHAPE", 4: "
           5: "ERR_MISSING_WEIGHTS", 6: "ERR_UNSUPPORTED", 7: "ERR_CUDA", 8: "ERR_OOM",
           9: "ERR_DEVICE_TIMEOUT", 10: "ERR_DEVICE_BOUNDS"}
 EPI_STORE, EPI_RESIDUAL, EPI_SWIGLU, EPI_RESIDUAL_DS = 0, 1, 2, 3
+EPI_GELU_TANH, EPI_GELU_ERF = 5, 6
 KERNEL_CLASSES = ["prep", "rmsnorm", "gemm_qkv", "quant", "attention", "gemm_o", "gemm_gate_up", "gemm_down"]
 
 
@@ -48,6 +53,15 @@ class Config(ctypes.Structure):
                 ("mrope_section", ctypes.c_int32 * 3), ("max_tokens", ctypes.c_int32),
                 ("max_seqs", ctypes.c_int32), ("num_deepstack", ctypes.c_int32), ("linear_fp8", ctypes.c_int32),
                 ("separate_norm", ctypes.c_int32)]
+
+
+class VisionConfig(ctypes.Structure):
+    _fields_ = [("depth", ctypes.c_int32), ("hidden", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("intermediate", ctypes.c_int32), ("in_channels", ctypes.c_int32), ("patch_size", ctypes.c_int32),
+                ("temporal_patch_size", ctypes.c_int32), ("spatial_merge_size", ctypes.c_int32),
+                ("out_hidden", ctypes.c_int32), ("num_position_embeddings", ctypes.c_int32),
+                ("num_deepstack", ctypes.c_int32), ("deepstack_indexes", ctypes.c_int32 * 8),
+                ("ln_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("max_patches", ctypes.c_int32)]
 
 
 def _load():
@@ -103,6 +117,20 @@ _SIGS = {
     "h3enc_op_attention": ([_P, _P, _I32, _I32, _I32, _I32, _P, _I32, _P], _I32),
     "h3enc_op_embed": ([_P, _P, _I32, _I32, _P, _I32, _P, _P], _I32),
     "h3enc_op_vis_rank": ([_P, _I32, _I32, _P, _P, _P], _I32),
+    "h3enc_op_layernorm": ([_P, _P, _P, _P, _I32, _I32, _F, _P], _I32),
+    "h3enc_op_vision_pos_embed": ([_P, _I32, _I32, _P, _I32, _I32, _P, _P], _I32),
+    "h3enc_op_vision_rope_table": ([_P, _I32, _I32, _I32, _F, _P, _P, _P], _I32),
+    "h3enc_op_gemm_bias": ([_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _I64, _P, _P], _I32),
+    "h3enc_op_gemm_qkv_rope_bias": ([_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _I64, _P, _P], _I32),
+    "h3enc_op_attention_bidir": ([_P, _P, _I32, _I32, _I32, _P, _I32, _P], _I32),
+    "h3vis_create": ([ctypes.POINTER(VisionConfig), ctypes.POINTER(_P)], _I32),
+    "h3vis_load_weights": ([_P, ctypes.c_char_p, _P, _I32, ctypes.POINTER(_I64), _I32, _I32], _I32),
+    "h3vis_finalize_weights": ([_P], _I32),
+    "h3vis_encode": ([_P, _P, _I32, _P, _I32, _P, _P, _P], _I32),
+    "h3vis_get_status": ([_P], _I32),
+    "h3vis_last_error": ([_P], ctypes.c_char_p),
+    "h3vis_launch_count": ([_P], _I64),
+    "h3vis_destroy": ([_P], None),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -403,7 +431,140 @@ def h3enc_op_vis_rank(mask, S, n_vis, vis_rank, status=None, stream=None):
     return _check(lib.h3enc_op_vis_rank(_ptr(mask), S, n_vis, _ptr(vis_rank), _ptr(status), _stream(stream)))
 
 
-# ---------------------------------------------------------------- convenience wrapper
+def _vcheck(code, handle=None):
+    if code not in (0, 1):
+        msg = lib.h3vis_last_error(handle)
+        raise H3encError(code, msg.decode() if msg else "")
+    return code
+
+
+def h3enc_op_layernorm(x, w, b, y, rows, cols, eps, stream=None):
+    return _check(lib.h3enc_op_layernorm(_ptr(x), _ptr(w), _ptr(b), _ptr(y), rows, cols, eps, _stream(stream)))
+
+
+def _grids(grid_thw):
+    g = [int(v) for row in grid_thw for v in row]
+    return (ctypes.c_int32 * len(g))(*g), len(g) // 3
+
+
+def h3enc_op_vision_pos_embed(table, grid_side, hidden, grid_thw, merge, out, stream=None):
+    g, n = _grids(grid_thw)
+    return _check(lib.h3enc_op_vision_pos_embed(_ptr(table), grid_side, hidden, g, n, merge, _ptr(out),
+                                                _stream(stream)))
+
+
+def h3enc_op_vision_rope_table(grid_thw, merge, head_dim, theta, cos_tab, sin_tab, stream=None):
+    g, n = _grids(grid_thw)
+    return _check(lib.h3enc_op_vision_rope_table(g, n, merge, head_dim, theta, _ptr(cos_tab), _ptr(sin_tab),
+                                                 _stream(stream)))
+
+
+def h3enc_op_gemm_bias(A, W, C, M, N, K, epilogue, bias, R=None, workspace=None, status=None, stream=None):
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return _check(lib.h3enc_op_gemm_bias(_ptr(A), _ptr(W), _ptr(C), M, N, K, epilogue, _ptr(R), _ptr(bias),
+                                         _ptr(workspace), wbytes, _ptr(status), _stream(stream)))
+
+
+def h3enc_op_gemm_qkv_rope_bias(A, W, C, M, K, heads, head_dim, bias, cos_tab, sin_tab, workspace=None,
+                                status=None, stream=None):
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return _check(lib.h3enc_op_gemm_qkv_rope_bias(_ptr(A), _ptr(W), _ptr(C), M, K, heads, head_dim, _ptr(bias),
+                                                  _ptr(cos_tab), _ptr(sin_tab), _ptr(workspace), wbytes,
+                                                  _ptr(status), _stream(stream)))
+
+
+def h3enc_op_attention_bidir(qkv, o, S, heads, head_dim, cu_seqlens=None, stream=None):
+    cu = _host_i32(cu_seqlens)
+    n_seqs = len(cu) - 1 if cu is not None else 0
+    return _check(lib.h3enc_op_attention_bidir(_ptr(qkv), _ptr(o), S, heads, head_dim, cu, n_seqs, _stream(stream)))
+
+
+def h3vis_create(cfg: VisionConfig):
+    h = _P()
+    code = lib.h3vis_create(ctypes.byref(cfg), ctypes.byref(h))
+    if code != 0:
+        raise H3encError(code, lib.h3vis_last_error(None).decode())
+    return h
+
+
+def h3vis_load_weights(h, name: str, tensor, data_on_device: bool = True):
+    shape = (_I64 * tensor.dim())(*tensor.shape)
+    return _vcheck(lib.h3vis_load_weights(h, name.encode(), _ptr(tensor), 0, shape, tensor.dim(),
+                                          1 if data_on_device else 0), h)
+
+
+def h3vis_finalize_weights(h):
+    return _vcheck(lib.h3vis_finalize_weights(h), h)
+
+
+def h3vis_encode(h, pixel_values, n_patches, grid_thw, embeds_out, deepstack_out=None, stream=None):
+    g, n = _grids(grid_thw)
+    return _vcheck(lib.h3vis_encode(h, _ptr(pixel_values), n_patches, g, n, _ptr(embeds_out), _ptr(deepstack_out),
+                                    _stream(stream)), h)
+
+
+def h3vis_get_status(h):
+    return lib.h3vis_get_status(h)
+
+
+def h3vis_last_error(h) -> str:
+    m = lib.h3vis_last_error(h)
+    return m.decode() if m else ""
+
+
+def h3vis_launch_count(h) -> int:
+    return lib.h3vis_launch_count(h)
+
+
+def h3vis_destroy(h):
+    lib.h3vis_destroy(h)
+
+
+# ---------------------------------------------------------------- convenience wrappers
+
+class VisionEncoder:
+    """Owns one h3vis handle (the vision tower).  ``model`` is any object with the
+    vision config attributes (depth, hidden, num_heads, intermediate, in_channels,
+    patch_size, temporal_patch_size, spatial_merge_size, out_hidden,
+    num_position_embeddings, deepstack_visual_indexes, ln_eps, rope_theta)."""
+
+    def __init__(self, model, max_patches: int):
+        c = VisionConfig()
+        for f in ("depth", "hidden", "num_heads", "intermediate", "in_channels", "patch_size",
+                  "temporal_patch_size", "spatial_merge_size", "out_hidden", "num_position_embeddings",
+                  "ln_eps", "rope_theta"):
+            setattr(c, f, getattr(model, f))
+        idx = list(model.deepstack_visual_indexes)
+        c.num_deepstack = len(idx)
+        c.deepstack_indexes = (ctypes.c_int32 * 8)(*(idx + [0] * (8 - len(idx))))
+        c.max_patches = max_patches
+        self.model = model
+        self.handle = h3vis_create(c)
+
+    def load(self, name, tensor):
+        return h3vis_load_weights(self.handle, name, tensor, tensor.is_cuda)
+
+    def finalize(self):
+        return h3vis_finalize_weights(self.handle)
+
+    def encode(self, pixel_values, grid_thw, embeds_out, deepstack_out=None, stream=None):
+        return h3vis_encode(self.handle, pixel_values, int(pixel_values.shape[0]), grid_thw, embeds_out,
+                            deepstack_out, stream)
+
+    def status(self) -> int:
+        return h3vis_get_status(self.handle)
+
+    def close(self):
+        if self.handle:
+            h3vis_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
 
 class Encoder:
     """Owns one h3enc handle.  ``model`` is any object with the Qwen3-VL text

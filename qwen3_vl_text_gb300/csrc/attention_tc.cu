@@ -4,7 +4,9 @@
 // MiniMaxH3Qwen3VLTextAttention.forward: q head h reads kv head h / (nq/nkv)
 // (repeat_interleave), scaled_dot_product_attention(is_causal=True) with scale
 // 1/sqrt(d), output columns head-major.  Packed sequences (cu_seqlens) attend
-// only within themselves.
+// only within themselves.  The same kernel runs the vision tower's bidirectional
+// attention (MiniMaxH3Qwen3VLVisionAttention.forward: is_causal=False inside each
+// frame, one head per kv head) with the causal mask off.
 //
 // Work item = two query tiles of 128 rows (A = rows q0.., B = rows q0+128..) of one
 // head; both read the same key/value tiles of 128, so each K/V tile is staged once
@@ -53,6 +55,7 @@ struct AttnTcArgs {
     int pair_start[kMaxSeqs + 1];   // first tile-pair index of each sequence
     unsigned long long *trace;      // optional [grid][ATR_COUNT] timeline
     float *row_amax;                // optional [S]: atomic max of |output| per row (bf16 values, >= 0)
+    int causal;                     // 1: keys after the query are masked; 0: every key of the segment
 };
 
 // Timeline of one persistent CTA (h3enc_op_attention_trace_next): %globaltimer at
@@ -130,9 +133,16 @@ __device__ __forceinline__ AttnItem attn_item(const AttnTcArgs &a, int k) {
     it.seg0 = a.cu[lo];
     it.L = a.cu[lo + 1] - it.seg0;
     it.q0 = (pair_lin - a.pair_start[lo]) * (2 * TQ);
-    // key tiles of each query tile (tile B is empty when the sequence ends inside tile A)
-    it.nkt_a = (min(it.q0 + TQ, it.L) + TK - 1) / TK;
-    it.nkt_b = it.q0 + TQ < it.L ? (min(it.q0 + 2 * TQ, it.L) + TK - 1) / TK : 0;
+    // key tiles of each query tile (tile B is empty when the sequence ends inside tile A): up to
+    // the query's own position when causal, the whole segment otherwise
+    if (a.causal) {
+        it.nkt_a = (min(it.q0 + TQ, it.L) + TK - 1) / TK;
+        it.nkt_b = it.q0 + TQ < it.L ? (min(it.q0 + 2 * TQ, it.L) + TK - 1) / TK : 0;
+    } else {
+        const int all = (it.L + TK - 1) / TK;
+        it.nkt_a = all;
+        it.nkt_b = it.q0 + TQ < it.L ? all : 0;
+    }
     return it;
 }
 // The r-th item of CTA b among G persistent CTAs: rounds of G items, alternate rounds
@@ -345,13 +355,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(tS + 96, v3);
                     tmem_ld_wait();
                 }
-                // keys after the query masked (the diagonal tile only); row max of the raw scores
-                // (the scale is positive) as 8 independent chains
+                // keys after the query masked (causal: the diagonal tile only), else the keys past
+                // the segment's end (its last tile only); row max of the raw scores (the scale is
+                // positive) as 8 independent chains
                 const int key0 = j * TK;
-                if (key0 + TK - 1 > qtile0) {
+                if (a.causal) {
+                    if (key0 + TK - 1 > qtile0) {
+                        #pragma unroll
+                        for (int i = 0; i < TK; ++i)
+                            if (key0 + i > qpos) v[i] = __float_as_uint(-INFINITY);
+                    }
+                } else if (key0 + TK > w.L) {
                     #pragma unroll
                     for (int i = 0; i < TK; ++i)
-                        if (key0 + i > qpos) v[i] = __float_as_uint(-INFINITY);
+                        if (key0 + i >= w.L) v[i] = __float_as_uint(-INFINITY);
                 }
                 // (three-input maxima: chain u takes scores u, u + 8, ..., u + 120)
                 float mx[8];
@@ -500,7 +517,7 @@ thread_local unsigned long long *t_attn_trace = nullptr;
 void attention_trace_next(unsigned long long *trace) { t_attn_trace = trace; }
 int attention_trace_fields() { return ATR_COUNT; }
 cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, int d, const int32_t *cu_host,
-                             int n_seqs, int32_t *status, cudaStream_t st, float *row_amax) {
+                             int n_seqs, int32_t *status, cudaStream_t st, float *row_amax, bool causal) {
     if (S <= 0) return cudaSuccess;
     if (d != 64 && d != 128) return cudaErrorInvalidValue;
     AttnTcArgs args;   // per call: launches from several host threads do not share it
@@ -517,6 +534,7 @@ cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, i
     args.status = status;
     args.trace = t_attn_trace;
     args.row_amax = row_amax;
+    args.causal = causal ? 1 : 0;
     t_attn_trace = nullptr;
     int n = 0, pairs = 0;
     if (!cu_host) {

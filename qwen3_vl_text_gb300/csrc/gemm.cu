@@ -98,6 +98,7 @@ struct GemmArgs {
     const float *ss_in;
     float *ss_out;
     float norm_eps;
+    const __nv_bfloat16 *bias;   // optional [N], added to the accumulator (not with SWIGLU)
 };
 
 // Phase stamps of the optional timeline (h3enc_op_gemm_traced).
@@ -204,6 +205,11 @@ __device__ __forceinline__ bool epi_bar_and(bool v) {
 // silu(g) * u = g * u / (1 + e^-g), with the fast exponential and division intrinsics (a few
 // ulps of fp32, far below the bf16 rounding of the result); a very negative g gives 0.
 __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g * u, 1.0f + __expf(-g)); }
+// GELU of the vision tower: the tanh form in the blocks' MLP, the exact (erf) form in the mergers
+__device__ __forceinline__ float gelu_tanh(float x) {
+    return 0.5f * x * (1.0f + tanhf(0.7978845608028654f * (x + 0.044715f * x * x * x)));   // sqrt(2/pi)
+}
+__device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.0f + erff(x * 0.7071067811865476f)); }
 
 __device__ __forceinline__ void load_row32(const __nv_bfloat16 *p, float (&f)[32]) {
     const uint4 *q = reinterpret_cast<const uint4 *>(p);
@@ -415,6 +421,28 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 f[0] *= sr * sw.x; f[1] *= sr * sw.y; f[2] *= sr * sw.z; f[3] *= sr * sw.w;
             }
         };
+        // + bias[n0 .. n0 + 32) (the same 64 bytes for the whole warp: broadcast loads)
+        auto bias32 = [&](uint32_t (&v)[32], int n0) {
+            if (g.bias) {
+                const uint4 *b4 = reinterpret_cast<const uint4 *>(g.bias + n0);
+                #pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 bb = __ldg(b4 + q);
+                    const uint32_t w4[4] = {bb.x, bb.y, bb.z, bb.w};
+                    #pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        v[8 * q + 2 * t] = __float_as_uint(__uint_as_float(v[8 * q + 2 * t]) + bf16_lo(w4[t]));
+                        v[8 * q + 2 * t + 1] = __float_as_uint(__uint_as_float(v[8 * q + 2 * t + 1]) + bf16_hi(w4[t]));
+                    }
+                }
+            }
+        };
+        auto bias4 = [&](float *f, int n0) {
+            if (g.bias) {
+                const uint2 bb = *reinterpret_cast<const uint2 *>(g.bias + n0);
+                f[0] += bf16_lo(bb.x); f[1] += bf16_hi(bb.x); f[2] += bf16_lo(bb.y); f[3] += bf16_hi(bb.y);
+            }
+        };
         // data-parallel outputs leave through shared memory: the warp's 32 rows x 32 columns are
         // written to one of its two slots (row = lane, 64 bytes each) and stored by one TMA tile
         // store (rows past M are clipped); a slot is refilled once its store has read it
@@ -589,23 +617,36 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                     b[i] *= rn;
                                 }
                             }
+                            #pragma unroll
+                            for (int i = 0; i < 16; i += 4) {
+                                if (i < q4) {
+                                    bias4(a + i, n_blk * BN + ca + i);
+                                    bias4(b + i, n_blk * BN + ca + half + i);
+                                }
+                            }
                             __nv_bfloat16 *dst = g.C + (size_t)row * g.ldc + n_blk * BN + ca;
                             const bool is_q = head < g.nq, is_k = !is_q && head < g.nq + g.nkv;
                             if (is_q || is_k) {
-                                float ss = 0.f;
-                                #pragma unroll
-                                for (int i = 0; i < 16; ++i)
-                                    if (i < q4) ss = fmaf(a[i], a[i], fmaf(b[i], b[i], ss));
-                                ss += __shfl_xor_sync(gmask, ss, 1);
-                                ss += __shfl_xor_sync(gmask, ss, 2);
-                                const float rstd = 1.0f / sqrtf(ss / (float)d + g.eps);
+                                const bool qk_norm = g.wq != nullptr;   // the vision tower has none
+                                float rstd = 1.f;
+                                if (qk_norm) {
+                                    float ss = 0.f;
+                                    #pragma unroll
+                                    for (int i = 0; i < 16; ++i)
+                                        if (i < q4) ss = fmaf(a[i], a[i], fmaf(b[i], b[i], ss));
+                                    ss += __shfl_xor_sync(gmask, ss, 1);
+                                    ss += __shfl_xor_sync(gmask, ss, 2);
+                                    rstd = 1.0f / sqrtf(ss / (float)d + g.eps);
+                                }
                                 const __nv_bfloat16 *w = is_q ? g.wq : g.wk;
                                 const int jb = sub * q4;           // frequency index of a[0]
                                 #pragma unroll
                                 for (int i = 0; i < 16; ++i) {
                                     if (i < q4) {
-                                        const float ya = a[i] * rstd * __bfloat162float(w[jb + i]);
-                                        const float yb = b[i] * rstd * __bfloat162float(w[half + jb + i]);
+                                        const float ga = qk_norm ? __bfloat162float(w[jb + i]) : 1.f;
+                                        const float gb = qk_norm ? __bfloat162float(w[half + jb + i]) : 1.f;
+                                        const float ya = a[i] * rstd * ga;
+                                        const float yb = b[i] * rstd * gb;
                                         const float co = g.cos_t[(size_t)row * half + jb + i];
                                         const float si = g.sin_t[(size_t)row * half + jb + i];
                                         a[i] = ya * co - yb * si;
@@ -668,6 +709,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                     f[i] *= rn;
                                     up[i] *= rn;
                                 }
+                            }
+                            if constexpr (EPI != EPI_SWIGLU) bias4(f, n_blk * BN + c4);
+                            if constexpr (EPI == EPI_GELU_TANH || EPI == EPI_GELU_ERF) {
+                                #pragma unroll
+                                for (int i = 0; i < 4; ++i) f[i] = EPI == EPI_GELU_TANH ? gelu_tanh(f[i]) : gelu_erf(f[i]);
                             }
                             int col;
                             if constexpr (EPI == EPI_SWIGLU) {
@@ -807,6 +853,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             tmem_ld_wait();
                             dq32(v, row, live, n_blk * BN + cb + c * 32);
                             scale32(v);
+                            bias32(v, n_blk * BN + cb + c * 32);
                             float f[32];
                             #pragma unroll
                             for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
@@ -814,18 +861,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         }
                         continue;
                     }
-                    float ss = 0.f;
-                    #pragma unroll 1
-                    for (int c = 0; c < d / 32; ++c) {
-                        uint32_t v[32];
-                        tmem_ld32(taddr + cb + c * 32, v);
-                        tmem_ld_wait();
-                        dq32(v, row, live, n_blk * BN + cb + c * 32);
-                        scale32(v);
-                        #pragma unroll
-                        for (int j = 0; j < 32; ++j) ss = fmaf(__uint_as_float(v[j]), __uint_as_float(v[j]), ss);
+                    const bool qk_norm = g.wq != nullptr;   // the vision tower's q/k have no norm
+                    float rstd = 1.f;
+                    if (qk_norm) {
+                        float ss = 0.f;
+                        #pragma unroll 1
+                        for (int c = 0; c < d / 32; ++c) {
+                            uint32_t v[32];
+                            tmem_ld32(taddr + cb + c * 32, v);
+                            tmem_ld_wait();
+                            dq32(v, row, live, n_blk * BN + cb + c * 32);
+                            scale32(v);
+                            bias32(v, n_blk * BN + cb + c * 32);
+                            #pragma unroll
+                            for (int j = 0; j < 32; ++j) ss = fmaf(__uint_as_float(v[j]), __uint_as_float(v[j]), ss);
+                        }
+                        rstd = 1.0f / sqrtf(ss / (float)d + g.eps);
                     }
-                    const float rstd = 1.0f / sqrtf(ss / (float)d + g.eps);
                     const __nv_bfloat16 *w = is_q ? g.wq : g.wk;
                     #pragma unroll 1
                     for (int c = 0; c < half / 32; ++c) {
@@ -837,6 +889,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         dq32(vb, row, live, n_blk * BN + cb + half + c * 32);
                         scale32(va);
                         scale32(vb);
+                        bias32(va, n_blk * BN + cb + c * 32);
+                        bias32(vb, n_blk * BN + cb + half + c * 32);
                         uint32_t oa[16], ob[16];
                         #pragma unroll
                         for (int i = 0; i < 16; ++i) oa[i] = ob[i] = 0u;   // rows past M: clipped by the store
@@ -847,8 +901,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             for (int j = 0; j < 32; j += 4) {
                                 const float4 co = *reinterpret_cast<const float4 *>(cs + j);
                                 const float4 si = *reinterpret_cast<const float4 *>(sn + j);
-                                const uint2 wa = *reinterpret_cast<const uint2 *>(w + c * 32 + j);
-                                const uint2 wb = *reinterpret_cast<const uint2 *>(w + half + c * 32 + j);
+                                const uint2 wa = qk_norm ? *reinterpret_cast<const uint2 *>(w + c * 32 + j)
+                                                         : make_uint2(0x3F803F80u, 0x3F803F80u);   // bf16 1.0
+                                const uint2 wb = qk_norm ? *reinterpret_cast<const uint2 *>(w + half + c * 32 + j)
+                                                         : make_uint2(0x3F803F80u, 0x3F803F80u);
                                 const float ga[4] = {bf16_lo(wa.x), bf16_hi(wa.x), bf16_lo(wa.y), bf16_hi(wa.y)};
                                 const float gb[4] = {bf16_lo(wb.x), bf16_hi(wb.x), bf16_lo(wb.y), bf16_hi(wb.y)};
                                 const float cv[4] = {co.x, co.y, co.z, co.w}, sv[4] = {si.x, si.y, si.z, si.w};
@@ -888,9 +944,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     tmem_ld_wait();
                     dq32(v, row, live, col);
                     scale32(v);
+                    bias32(v, col);
                     float f[32];
                     #pragma unroll
                     for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+                    if constexpr (EPI == EPI_GELU_TANH || EPI == EPI_GELU_ERF) {
+                        #pragma unroll
+                        for (int j = 0; j < 32; ++j) f[j] = EPI == EPI_GELU_TANH ? gelu_tanh(f[j]) : gelu_erf(f[j]);
+                    }
                     if (live) {
                         if constexpr (EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_DS) {
                             #pragma unroll
@@ -1024,6 +1085,7 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     g.ss_in = p.ss_in;
     g.ss_out = p.ss_out;
     g.norm_eps = p.norm_eps;
+    g.bias = p.bias;
     const int tiles = g.nm * g.nn;
     int pairs = p.num_sms / 2 < max_pairs ? p.num_sms / 2 : max_pairs;   // all pairs co-resident
     if (pairs < 1) pairs = 1;
@@ -1109,8 +1171,10 @@ cudaError_t launch_gemm(const GemmPlan &p_in, cudaStream_t stream) {
         t_trace_next = nullptr;
     }
     if (p.epi == EPI_QKROPE &&
-        ((p.head_dim != 64 && p.head_dim != 128) || !p.wq || !p.wk || !p.cos_t || !p.sin_t))
+        ((p.head_dim != 64 && p.head_dim != 128) || (!p.wq != !p.wk) || !p.cos_t || !p.sin_t))
         return cudaErrorInvalidValue;
+    // a bias is read 32 columns at a time from 16-byte-aligned rows
+    if (p.bias && (p.epi == EPI_SWIGLU || (reinterpret_cast<uintptr_t>(p.bias) & 15))) return cudaErrorInvalidValue;
     // row statistics come in slots of 128 columns; only the stored (not SwiGLU) outputs emit them
     if ((p.ss_in && p.K % 128) || (p.ss_out && (p.N % 128 || p.epi == EPI_SWIGLU || p.epi == EPI_QKROPE)))
         return cudaErrorInvalidValue;
@@ -1132,6 +1196,8 @@ cudaError_t launch_gemm(const GemmPlan &p_in, cudaStream_t stream) {
         case EPI_SWIGLU: return launch_epi<EPI_SWIGLU, false>(p, stream);
         case EPI_RESIDUAL_DS: return launch_epi<EPI_RESIDUAL_DS, false>(p, stream);
         case EPI_QKROPE: return launch_epi<EPI_QKROPE, false>(p, stream);
+        case EPI_GELU_TANH: return launch_epi<EPI_GELU_TANH, false>(p, stream);
+        case EPI_GELU_ERF: return launch_epi<EPI_GELU_ERF, false>(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

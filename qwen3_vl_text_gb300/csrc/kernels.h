@@ -10,7 +10,8 @@ namespace h3 {
 
 using bf16 = __nv_bfloat16;
 
-enum { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_RESIDUAL_DS = 3, EPI_QKROPE = 4 };
+enum { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_RESIDUAL_DS = 3, EPI_QKROPE = 4,
+       EPI_GELU_TANH = 5, EPI_GELU_ERF = 6 };
 
 constexpr int kMaxSeqs = 1024;
 constexpr int kMaxDevices = 64;   // per-device launch caches
@@ -54,6 +55,10 @@ struct GemmPlan {
     const float *ss_in = nullptr;
     float *ss_out = nullptr;
     float norm_eps = 0.f;
+    // bias [N] (optional; every epilogue but SWIGLU): added to the accumulator before the fused
+    // op.  EPI_GELU_TANH / EPI_GELU_ERF store gelu(acc + bias).  EPI_QKROPE with wq = wk = NULL:
+    // no per-head norm, M-RoPE only (the vision tower's attention).
+    const bf16 *bias = nullptr;
 };
 // ss[s * rows + r] = sum of x[r][c]^2 over the 128 columns of slot s, accumulated in fp32 in
 // column order (x row-major [rows, cols], cols % 128 == 0).
@@ -109,7 +114,32 @@ cudaError_t launch_rope_table(const int32_t *positions, int S, const RopeParams 
 // row_amax (optional, [S] floats): each row's largest |bf16 output| is merged in with an
 // integer atomic max (the buffer must hold zeros or smaller values beforehand).
 cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, int d, const int32_t *cu_host,
-                             int n_seqs, int32_t *status, cudaStream_t st, float *row_amax = nullptr);
+                             int n_seqs, int32_t *status, cudaStream_t st, float *row_amax = nullptr,
+                             bool causal = true);
+
+// ---- vision tower (vision.cu)
+constexpr int kMaxVisionGrids = 64;
+// Patch grids of one vision encode, patches concatenated in the tower's order.
+struct VisionGrids {
+    int n, merge;
+    int first[kMaxVisionGrids];   // index of each grid's first patch
+    int h[kMaxVisionGrids], w[kMaxVisionGrids];
+};
+// thw host int32 [n_grids, 3]; false if a grid is empty or not divisible by the merge.
+bool make_vision_grids(VisionGrids *g, const int32_t *thw, int n_grids, int merge, int *n_patches);
+struct VisionRope {
+    float inv_freq[kMaxHalfDim];   // theta^(-2j/(d/2)), j < d/4
+};
+void make_vision_rope(VisionRope *r, int head_dim, float theta);
+// y = bf16((x - mean) / sqrt(var + eps) * w + b) per row; cols % 8 == 0, cols <= 8192.
+cudaError_t launch_layernorm(const bf16 *x, const bf16 *w, const bf16 *b, bf16 *y, int rows, int cols, float eps,
+                             cudaStream_t st);
+// out[k] = bilinear sample of the G x G table [G*G, D] at patch k (bf16), n patches.
+cudaError_t launch_pos_embed(const bf16 *table, int G, int D, const VisionGrids &gr, int n, bf16 *out,
+                             cudaStream_t st);
+// cos/sin [n, head_dim/2] of the 2-D rotary angles (row frequencies, then column frequencies).
+cudaError_t launch_vision_rope(const VisionGrids &gr, int n, int head_dim, const VisionRope &rp, float *cos_t,
+                               float *sin_t, cudaStream_t st);
 
 // ---- embedding gather, visual ranks, weight packing (embed.cu)
 cudaError_t launch_embed(const int32_t *ids, const bf16 *table, int vocab, int hidden, bf16 *out, int S,

@@ -14,7 +14,7 @@ def _declared():
     for f in os.listdir(os.path.join(ROOT, "include")):
         if f.endswith(".h"):
             text = open(os.path.join(ROOT, "include", f)).read()
-            names |= set(re.findall(r"^H3ENC_API\s+[\w\s\*]*?\b(h3enc_\w+)\s*\(", text, re.M))
+            names |= set(re.findall(r"^H3ENC_API\s+[\w\s\*]*?\b((?:h3enc|h3vis)_\w+)\s*\(", text, re.M))
     return names
 
 
