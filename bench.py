@@ -367,6 +367,117 @@ def run_kernel(args):
     return 0
 
 
+def vision_flops(cfg, grids) -> float:
+    """Algorithmic FLOPs of one vision encode: patch embedding, per block the four linears
+    (2 n (4 h^2 + 2 h I)) and bidirectional attention inside each frame (4 heads d L^2 per
+    frame of L patches), and the mergers (2 (n/m^2) 4h (4h + out) each)."""
+    h, I, m = cfg.hidden, cfg.intermediate, cfg.spatial_merge_size
+    n = sum(t * hh * w for t, hh, w in grids)
+    frames_sq = sum(t * (hh * w) ** 2 for t, hh, w in grids)
+    mh, nm = h * m * m, n // (m * m)
+    per_block = 2.0 * n * (4 * h * h + 2 * h * I) + 4.0 * cfg.num_heads * cfg.head_dim * frames_sq
+    mergers = (1 + len(cfg.deepstack_visual_indexes)) * 2.0 * nm * mh * (mh + cfg.out_hidden)
+    return 2.0 * n * cfg.patch_dim * h + cfg.depth * per_block + mergers
+
+
+def run_vision(args):
+    """The vision tower on one 48 x 64-patch image (the 24 x 32 merged grid of the seq-1024
+    text workload), device-timed like the encode; one JSON line."""
+    import torch
+
+    import qwen3_vl_text_gb300 as Q
+    import workloads as W
+    wl = W.vision_workload(2)
+    cfg = wl.model
+    inp = W.gen_vision_inputs(wl)
+    n = inp["n_patches"]
+    nm = n // cfg.spatial_merge_size ** 2
+    enc = Q.VisionEncoder(cfg, max_patches=n)
+    for name, shape, mean, sigma in W.vision_weight_specs(cfg):
+        enc.load(name, W.gen_weight(wl.seed, name, shape, mean, sigma, device="cuda"))
+    torch.cuda.synchronize()
+    enc.finalize()
+    px = W.bf16_bits_to_torch(inp["pixel_values"]).cuda()
+    emb = torch.empty(nm, cfg.out_hidden, dtype=torch.bfloat16, device="cuda")
+    ds = torch.empty(len(cfg.deepstack_visual_indexes), nm, cfg.out_hidden, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        enc.encode(px, wl.grids, emb, ds, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if enc.status() != 0:
+        raise RuntimeError("vision status after warm-up: " + Q.h3vis_last_error(enc.handle))
+    clocks = Clocks(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    time.sleep(0.5)
+    torch.cuda.synchronize()
+    n0 = Q.h3vis_launch_count(enc.handle)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    launches = Q.h3vis_launch_count(enc.handle) - n0
+    if enc.status() != 0:
+        raise RuntimeError("vision status after the timed region: " + Q.h3vis_last_error(enc.handle))
+    # end to end: pixels copied in from pinned host memory, embeddings and DeepStack features copied out
+    h_px = W.bf16_bits_to_torch(inp["pixel_values"]).pin_memory()
+    h_emb = torch.empty(emb.shape, dtype=torch.bfloat16).pin_memory()
+    h_ds = torch.empty(ds.shape, dtype=torch.bfloat16).pin_memory()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        px.copy_(h_px, non_blocking=True)
+        step()
+        h_emb.copy_(emb, non_blocking=True)
+        h_ds.copy_(ds, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3
+    burst, sustained, hbm, src = _peaks()
+    at_max = bool(clk and clk.get("sm_mhz") and clk.get("sm_max_mhz")
+                  and clk["sm_mhz"] >= 0.97 * clk["sm_max_mhz"] and "sw_power_cap" not in clk.get("reasons", []))
+    base, base_name = (burst, "bf16_tflops") if at_max else (sustained, "bf16_tflops_sustained")
+    flops = vision_flops(cfg, wl.grids)
+    tflops = flops * args.steps / (ms / 1e3) / 1e12
+    line = {
+        "metric": "vision tower: merged visual tokens/s, one 48x64-patch image", "value": nm * args.steps / (ms / 1e3),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded random-init weights and pixels)",
+        "config": {"workload": wl.name, "patches": n, "merged_tokens": nm, "depth": cfg.depth, "hidden": cfg.hidden,
+                   "heads": cfg.num_heads, "intermediate": cfg.intermediate, "deepstack": len(cfg.deepstack_visual_indexes),
+                   "l2": "no flush: each step streams 0.91 GB of weights, far above the 129 MB L2"},
+        "images_per_s": args.steps / (ms / 1e3), "tflops": tflops, "pct_dense_bf16_peak": 100.0 * tflops / base,
+        "roofline": {"kernel": "whole tower (all launches of one encode)", "bound": "tensor", "achieved": tflops,
+                     "peak": base, "unit": "TFLOP/s", "frac": tflops / base,
+                     "peak_source": f"{src} {base_name}", "traffic": None},
+        "gpu_launches": int(launches),
+        "e2e": {"value": nm * args.steps / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": int(h_px.numel() * 2),
+                "d2h_bytes_per_step": int((h_emb.numel() + h_ds.numel()) * 2)},
+        "clocks": clk,
+    }
+    enc.close()
+    if not args.no_cpu_baseline:
+        import oracle as O
+        ws = {nme[len("model.visual."):]: O.bf16_bits_to_float(W.gen_weight(wl.seed, nme, sh, mu, sg))
+              for nme, sh, mu, sg in W.vision_weight_specs(cfg)}
+        pxf = O.bf16_bits_to_float(inp["pixel_values"])
+        t0 = time.perf_counter()
+        O.vision.vision_forward(pxf, wl.grids, cfg, ws)
+        t = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": nm / t, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": "one whole tower forward on the same image"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--kernel", default=None,
@@ -384,6 +495,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--separate-norm", action="store_true",
                     help="bf16: run each RMSNorm as its own kernel instead of folding it into the projections")
+    ap.add_argument("--vision", action="store_true",
+                    help="time the vision tower on one 48x64-patch image instead of the text encode")
     ap.add_argument("--oracle-time", type=int, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--reps", type=int, default=3, help=argparse.SUPPRESS)
     ap.add_argument("--warm", type=int, default=1, help=argparse.SUPPRESS)
@@ -401,6 +514,8 @@ def main():
     args.warmup = max(3, args.warmup)
     if args.oracle_time is not None:
         return oracle_time(args)
+    if args.vision:
+        return run_vision(args)
     if args.kernel:
         return run_kernel(args)
     if args.impl == "reference":

@@ -61,6 +61,9 @@ constexpr int C_STAGE_BYTES = EPI_WARPS * 2 * C_SLOT_BYTES;   // 32 KB
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + C_STAGE_BYTES + 256;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
 constexpr int kMinStreamKBlocks = 4;             // smallest k-range a stream-K pair takes
+// cost of the stream-K partial exchange in k-block times (about 0.36 us each): behind
+// data-parallel tiles, and alone (measured: ~3 us and ~15 us of the launch)
+constexpr long long kSkFixupHidden = 8, kSkFixupExposed = 40;
 static_assert(BM * BN % 4 == 0, "partials are written as float4");
 
 struct GemmArgs {
@@ -1090,7 +1093,10 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     int pairs = p.num_sms / 2 < max_pairs ? p.num_sms / 2 : max_pairs;   // all pairs co-resident
     if (pairs < 1) pairs = 1;
     // full waves data-parallel; the k-blocks of a partial last wave spread over all pairs (stream-K),
-    // at least kMinStreamKBlocks per pair; when that leaves one tile per pair it stays data-parallel
+    // at least kMinStreamKBlocks per pair; when that leaves one tile per pair it stays data-parallel.
+    // The split is kept only where it shortens the launch (in k-block times): the pair's share of
+    // the tail plus the partial exchange (hidden behind the data-parallel tiles when there are
+    // some, exposed when the tail is all there is) against one more whole tile.
     const int left = tiles % pairs;
     int sk_pairs = 0;
     if (p.part && p.flags && left) {
@@ -1098,7 +1104,11 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
         long long ps = work / kMinStreamKBlocks;
         if (ps > pairs) ps = pairs;
         if (ps > EPI_THREADS) ps = EPI_THREADS;   // one polling thread per contributor
-        if (ps > left) sk_pairs = (int)ps;
+        if (ps > left) {
+            const long long full = tiles / pairs;
+            const long long sk_cost = full * g.nk + (work + ps - 1) / ps + (full ? kSkFixupHidden : kSkFixupExposed);
+            if (sk_cost < (full + 1) * g.nk) sk_pairs = (int)ps;
+        }
     }
     g.sk_pairs = sk_pairs;
     g.sk_work = (long long)left * g.nk;

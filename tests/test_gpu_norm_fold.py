@@ -156,8 +156,8 @@ def test_folded_norm_matches_norm_then_projection(case):
 
 @pytest.mark.parametrize("split", [False, True])
 def test_qkv_projection_with_folded_input_norm(split):
-    d, nq, nkv, K = 128, 64, 8, 512
-    M = 1024 if split else 300
+    d, nq, nkv = 128, 64, 8
+    M, K = (1024, 2048) if split else (300, 512)   # 160 tiles of 32 k-blocks: a stream-K tail
     N = (nq + 2 * nkv) * d
     A, a = _bf16(54, "A", (M, K))
     Wt, w = _bf16(55, "Wqkv", (N, K), sigma=0.05)

@@ -149,9 +149,9 @@ def _stream_k_shape(case, pairs):
     if case == "tail4":
         return 4 * 256 - 37, (pairs // 4 + 1) * 256, 2048
     if case == "span":
-        return 4 * 256 - 37, ((pairs + 40) // 4) * 256, 1280
+        return 4 * 256 - 37, ((pairs + 40) // 4) * 256, 5120
     if case == "nodp":
-        return 2 * 256 - 100, 8 * 256, 4096
+        return 2 * 256 - 100, 8 * 256, 8192
     return 2 * 256 - 100, 8 * 256, 256
 
 

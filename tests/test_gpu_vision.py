@@ -114,9 +114,10 @@ def test_gemm_bias_epilogues(epi, case):
     assert bad == 0, f"{bad} off, worst {worst}"
 
 
-@pytest.mark.parametrize("grid,split", [((1, 10, 30), False), ((1, 32, 32), True)])
+@pytest.mark.parametrize("grid,split", [((1, 10, 30), False), ((1, 32, 64), True)])
 def test_qkv_with_bias_and_2d_rotary(grid, split):
-    heads, d, K = 16, 64, 512
+    heads, d = 16, 64
+    K = 2048 if split else 512   # split: 96 tiles of 32 k-blocks, a stream-K tail
     M = grid[0] * grid[1] * grid[2]
     N = 3 * heads * d
     A, a = _bf16(78, "A", (M, K))
@@ -267,3 +268,22 @@ def test_tower_feeds_the_text_model():
                       O.round_to_bf16(np.stack(fbf)), storage=GPU_STORAGE)
     ok, msg = within(got, ref, refbf, 2e-2, 0.05)
     assert ok, msg
+
+
+@pytest.mark.slow
+def test_full_size_tower_on_the_48x64_image():
+    """The synthetic full-size tower (24 blocks, hidden 1024, 16 heads, DeepStack after
+    blocks 5, 11, 17) on one 48 x 64-patch image: every output against the oracle."""
+    w = W.vision_workload(2)
+    enc, inp = _tower(w)
+    try:
+        emb, ds = _run_tower(enc, w, inp)
+    finally:
+        enc.close()
+    m32, f32 = _oracle_tower(w, inp)
+    mbf, fbf = _oracle_tower(w, inp, storage=V.VISION_STORAGE_POINTS)
+    ok, msg = within(t2f(emb), m32, mbf, 2e-2, 0.05)
+    assert ok, "merged embeddings: " + msg
+    for j in range(len(f32)):
+        ok, msg = within(t2f(ds[j]), f32[j], fbf[j], 2e-2, 0.05)
+        assert ok, f"deepstack {j}: " + msg
