@@ -6,7 +6,8 @@
 // 1/sqrt(d), output columns head-major.  Packed sequences (cu_seqlens) attend
 // only within themselves.  The same kernel runs the vision tower's bidirectional
 // attention (MiniMaxH3Qwen3VLVisionAttention.forward: is_causal=False inside each
-// frame, one head per kv head) with the causal mask off.
+// frame, one head per kv head) with the causal mask off; there every item costs the same,
+// and the pair-items of a thin last round run as single query tiles instead.
 //
 // Work item = two query tiles of 128 rows (A = rows q0.., B = rows q0+128..) of one
 // head; both read the same key/value tiles of 128, so each K/V tile is staged once
@@ -50,6 +51,8 @@ struct AttnTcArgs {
     int k_col0, v_col0;
     float scale_log2;
     int n_seqs, total_pairs, n_items;
+    int n_whole;   // items [0, n_whole) are pairs of query tiles; each later pair-item is run as
+                   // two single-tile items (bidirectional mode, to fill a thin last round)
     int32_t *status;
     int cu[kMaxSeqs + 1];
     int pair_start[kMaxSeqs + 1];   // first tile-pair index of each sequence
@@ -121,8 +124,11 @@ __device__ __forceinline__ float ex2(float x) {
 struct AttnItem {
     int head, seg0, L, q0, nkt_a, nkt_b;
 };
-__device__ __forceinline__ AttnItem attn_item(const AttnTcArgs &a, int k) {
+__device__ __forceinline__ AttnItem attn_item(const AttnTcArgs &a, int k_in) {
     AttnItem it;
+    // past n_whole: item n_whole + 2j + h is tile h of pair-item n_whole + j on its own
+    const int split = k_in >= a.n_whole ? ((k_in - a.n_whole) & 1) + 1 : 0;   // 0 whole, 1 tile A, 2 tile B
+    const int k = split ? a.n_whole + ((k_in - a.n_whole) >> 1) : k_in;
     it.head = k % a.nq;                                   // heads fastest: one kv group's heads adjacent
     const int pair_lin = a.total_pairs - 1 - k / a.nq;    // heavy tile pairs first
     int lo = 0, hi = a.n_seqs - 1;
@@ -142,6 +148,10 @@ __device__ __forceinline__ AttnItem attn_item(const AttnTcArgs &a, int k) {
         const int all = (it.L + TK - 1) / TK;
         it.nkt_a = all;
         it.nkt_b = it.q0 + TQ < it.L ? all : 0;
+    }
+    if (split) {   // the host splits only pairs whose tile B exists
+        if (split == 2) it.q0 += TQ;
+        it.nkt_b = 0;
     }
     return it;
 }
@@ -559,8 +569,25 @@ cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, i
     args.n_seqs = n;
     args.total_pairs = pairs;
     args.n_items = pairs * nq;
+    args.n_whole = args.n_items;
     int sms = device_num_sms();
     if (sms <= 0) sms = 1;
+    if (!causal && args.n_items > sms) {
+        // bidirectional items all cost the same: when the last round would hold few pair-items,
+        // run them as single query tiles, twice as many and half as long (pairs with a tile B only)
+        const int I = args.n_items, rounds = (I + sms - 1) / sms, r = I - (rounds - 1) * sms;
+        bool ok = 2 * r <= sms;
+        for (int k = I - r; ok && k < I; ++k) {
+            const int pair_lin = pairs - 1 - k / nq;
+            int seg = 0;
+            while (seg + 1 < n && args.pair_start[seg + 1] <= pair_lin) ++seg;
+            ok = (pair_lin - args.pair_start[seg]) * 2 * TQ + TQ < args.cu[seg + 1] - args.cu[seg];
+        }
+        if (ok) {
+            args.n_whole = I - r;
+            args.n_items = I + r;
+        }
+    }
     const int grid = args.n_items < sms ? args.n_items : sms;   // persistent: one CTA per SM
     return d == 128 ? launch_tc<128>(tm, args, grid, st) : launch_tc<64>(tm, args, grid, st);
 }

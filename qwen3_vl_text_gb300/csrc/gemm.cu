@@ -208,9 +208,16 @@ __device__ __forceinline__ bool epi_bar_and(bool v) {
 // silu(g) * u = g * u / (1 + e^-g), with the fast exponential and division intrinsics (a few
 // ulps of fp32, far below the bf16 rounding of the result); a very negative g gives 0.
 __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g * u, 1.0f + __expf(-g)); }
-// GELU of the vision tower: the tanh form in the blocks' MLP, the exact (erf) form in the mergers
+// GELU of the vision tower: the tanh form in the blocks' MLP, the exact (erf) form in the mergers.
+// tanh from the hardware's approximate instruction (relative error about 2^-11, below the bf16
+// rounding of the output)
+__device__ __forceinline__ float tanh_hw(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ float gelu_tanh(float x) {
-    return 0.5f * x * (1.0f + tanhf(0.7978845608028654f * (x + 0.044715f * x * x * x)));   // sqrt(2/pi)
+    return 0.5f * x * (1.0f + tanh_hw(0.7978845608028654f * (x + 0.044715f * x * x * x)));   // sqrt(2/pi)
 }
 __device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.0f + erff(x * 0.7071067811865476f)); }
 

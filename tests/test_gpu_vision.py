@@ -137,9 +137,13 @@ def test_qkv_with_bias_and_2d_rotary(grid, split):
     assert bad == 0, f"{bad} off, worst {worst}"
 
 
-@pytest.mark.parametrize("cu", [[0, 96, 160, 224], [0, 1024, 2048], [0, 200]])
-def test_bidirectional_attention(cu):
-    heads, d = 4, 64
+@pytest.mark.parametrize("cu,heads", [([0, 96, 160, 224], 4), ([0, 1024, 2048], 4), ([0, 200], 4),
+                                      # more work items than SMs: the last round's pairs run as single
+                                      # query tiles; and the same with a pair that has no second tile
+                                      # in that range (the split is then refused)
+                                      ([0, 3072], 16), ([0, 100, 3172], 16)])
+def test_bidirectional_attention(cu, heads):
+    d = 64
     S = cu[-1]
     X, x = _bf16(81, "qkv", (S, 3 * heads * d), 0.0, 1.0)
     o = torch.empty(S, heads * d, dtype=torch.bfloat16, device="cuda")
