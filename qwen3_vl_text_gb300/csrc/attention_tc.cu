@@ -161,7 +161,7 @@ __device__ __forceinline__ int attn_item_index(int r, int b, int G) {
     return r * G + ((r & 1) ? G - 1 - b : b);
 }
 
-template <int D>
+template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ AttnTcArgs a) {
     using Lay = TcLayout<D>;
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the segment's end (its last tile only); row max of the raw scores (the scale is
                 // positive) as 8 independent chains
                 const int key0 = j * TK;
-                if (a.causal) {
+                if constexpr (CAUSAL) {
                     if (key0 + TK - 1 > qtile0) {
                         #pragma unroll
                         for (int i = 0; i < TK; ++i)
@@ -504,20 +504,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D>
+template <int D, bool CAUSAL>
 cudaError_t launch_tc(const CUtensorMap &tm, const AttnTcArgs &args, int grid, cudaStream_t st) {
     static std::atomic<bool> attr_of[kMaxDevices];   // per device: the shared-memory opt-in
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if (!attr_of[dev].load()) {
-        cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             TcLayout<D>::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel<D, CAUSAL>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, TcLayout<D>::SMEM);
         if (e != cudaSuccess) return e;
         attr_of[dev].store(true);
     }
     cudaLaunchAttribute at[1];
     cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(kThreads), TcLayout<D>::SMEM, st, at);
-    return cudaLaunchKernelEx(&cfg, attention_tc_kernel<D>, tm, args);
+    return cudaLaunchKernelEx(&cfg, attention_tc_kernel<D, CAUSAL>, tm, args);
 }
 
 thread_local unsigned long long *t_attn_trace = nullptr;
@@ -589,7 +589,8 @@ cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, i
         }
     }
     const int grid = args.n_items < sms ? args.n_items : sms;   // persistent: one CTA per SM
-    return d == 128 ? launch_tc<128>(tm, args, grid, st) : launch_tc<64>(tm, args, grid, st);
+    if (causal) return d == 128 ? launch_tc<128, true>(tm, args, grid, st) : launch_tc<64, true>(tm, args, grid, st);
+    return d == 128 ? launch_tc<128, false>(tm, args, grid, st) : launch_tc<64, false>(tm, args, grid, st);
 }
 
 }  // namespace h3
