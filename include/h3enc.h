@@ -257,8 +257,15 @@ H3ENC_API h3enc_status h3enc_set_profiling(h3enc *h, int32_t enable);
  * in mask (0 = off); launches of the other classes are still counted. */
 H3ENC_API h3enc_status h3enc_set_profiling_classes(h3enc *h, uint32_t mask);
 
-/* Synchronise and return per-class totals since the last reset:
- * ms[k], launches[k] for k < n (n <= H3ENC_K_COUNT).  Resets totals. */
+/* Restrict the profiling events to the launches of one decoder layer (0 <= layer <
+ * num_layers; -1, the default: every launch).  A sample of identical launches: an
+ * event between two launches stops the second from overlapping the first, so timing
+ * one layer's launches disturbs an encode far less than timing all of them. */
+H3ENC_API h3enc_status h3enc_set_profiling_layer(h3enc *h, int32_t layer);
+
+/* Synchronise and return per-class totals since the last reset: ms[k] and
+ * launches[k] (the number of timed launches) for k < n (n <= H3ENC_K_COUNT).
+ * Resets totals. */
 H3ENC_API h3enc_status h3enc_get_profile(h3enc *h, double *ms, int64_t *launches, int32_t n);
 
 /* Number of kernels this handle has launched since create. */

@@ -17,7 +17,7 @@ __all__ = [
     "EPI_GELU_TANH", "EPI_GELU_ERF",
     "h3enc_create", "h3enc_load_weights", "h3enc_finalize_weights", "h3enc_encode", "h3enc_encode_embeds", "h3enc_encode_multimodal",
     "h3enc_encode_host", "h3enc_set_layer_capture", "h3enc_get_status", "h3enc_last_error", "h3enc_destroy",
-    "h3enc_set_profiling", "h3enc_set_profiling_classes", "h3enc_get_profile", "h3enc_launch_count", "h3enc_num_sms",
+    "h3enc_set_profiling", "h3enc_set_profiling_classes", "h3enc_set_profiling_layer", "h3enc_get_profile", "h3enc_launch_count", "h3enc_num_sms",
     "h3enc_build_positions", "h3enc_aggregate_deepstack",
     "h3enc_op_gemm", "h3enc_op_gemm_workspace_bytes", "h3enc_op_gemm_trace_next", "h3enc_op_attention_trace_next", "h3enc_op_gemm_noalloc", "h3enc_op_gemm_noalloc_scratch_bytes", "h3enc_op_pack_gate_up", "h3enc_op_rmsnorm", "h3enc_op_gemm_fp8", "h3enc_op_quant_rows",
     "h3enc_op_rmsnorm_q8", "h3enc_op_wait_probe", "h3enc_op_rope_table",
@@ -87,6 +87,7 @@ _SIGS = {
     "h3enc_destroy": ([_P], None),
     "h3enc_set_profiling": ([_P, _I32], _I32),
     "h3enc_set_profiling_classes": ([_P, ctypes.c_uint32], _I32),
+    "h3enc_set_profiling_layer": ([_P, _I32], _I32),
     "h3enc_get_profile": ([_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I64), _I32], _I32),
     "h3enc_launch_count": ([_P], _I64),
     "h3enc_num_sms": ([_P], _I32),
@@ -288,6 +289,11 @@ def h3enc_set_profiling_classes(h, classes):
     for c in classes:
         mask |= 1 << KERNEL_CLASSES.index(c)
     return _check(lib.h3enc_set_profiling_classes(h, mask), h)
+
+
+def h3enc_set_profiling_layer(h, layer: int):
+    """Time only the given decoder layer's launches (-1: all)."""
+    return _check(lib.h3enc_set_profiling_layer(h, layer), h)
 
 
 def h3enc_get_profile(h):

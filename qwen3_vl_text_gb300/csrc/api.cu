@@ -93,6 +93,8 @@ struct h3enc {
     std::vector<void *> capture;
     bool prof = false;
     uint32_t prof_mask = 0;
+    int prof_layer = -1;   // time only this decoder layer's launches (-1: every launch)
+    int cur_layer = -1;    // the layer encode_core is issuing (-1 outside the layer loop)
     std::vector<cudaEvent_t> ev_pool;
     std::vector<int> ev_class;
     size_t ev_used = 0;
@@ -142,7 +144,7 @@ template <class F>
 cudaError_t run(h3enc *h, int cls, cudaStream_t st, F &&launch) {
     NvtxRange range(kClassName[cls]);
     size_t e0 = (size_t)-1;
-    if (h->prof && (h->prof_mask & (1u << cls))) {
+    if (h->prof && (h->prof_mask & (1u << cls)) && (h->prof_layer < 0 || h->prof_layer == h->cur_layer)) {
         if (h->ev_used + 2 > h->ev_pool.size()) {
             for (int i = 0; i < 256; ++i) {
                 cudaEvent_t ev;
@@ -163,9 +165,9 @@ cudaError_t run(h3enc *h, int cls, cudaStream_t st, F &&launch) {
         record_timing_event(h->ev_pool[e0 + 1], st);
         h->ev_class[e0] = cls;
         h->ev_used += 2;
+        h->launches[cls]++;   // timed launches of the class
     }
     h->launch_count++;
-    h->launches[cls]++;
     return e;
 }
 
@@ -438,7 +440,12 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         e = cudaMemsetAsync(h->amax_attn, 0, 2 * align256((size_t)c.max_tokens * 4), st);
         if (e != cudaSuccess) return cuda_fail(h, e, "FP8 row maxima clear");
     }
+    struct LayerMark {   // the layer being issued, for per-layer profiling; cleared on every exit
+        h3enc *h;
+        ~LayerMark() { h->cur_layer = -1; }
+    } mark{h};
     for (int l = lb; l < le; ++l) {
+        h->cur_layer = l;
         char layer_name[32];
         snprintf(layer_name, sizeof layer_name, "layer %d", l);
         NvtxRange layer_range(layer_name);
@@ -912,6 +919,12 @@ h3enc_status h3enc_set_profiling_classes(h3enc *h, uint32_t mask) {
         h->ms[k] = 0;
         h->launches[k] = 0;
     }
+    return H3ENC_OK;
+}
+
+h3enc_status h3enc_set_profiling_layer(h3enc *h, int32_t layer) {
+    if (!h || layer < -1 || layer >= h->cfg.num_layers) return fail(h, H3ENC_ERR_INVALID_ARG, "bad layer");
+    h->prof_layer = layer;
     return H3ENC_OK;
 }
 

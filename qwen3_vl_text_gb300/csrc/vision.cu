@@ -16,9 +16,9 @@ namespace h3 {
 
 namespace {
 
-constexpr int LN_THREADS = 256;
-constexpr int LN_VPT = 4;   // 4 x 8 values per thread -> cols <= 8192
+constexpr int LN_VPT = 4;   // 4 x 8 values per thread: cols <= 32 * threads
 
+template <int LN_THREADS>
 __device__ __forceinline__ float ln_block_sum(float v, float *red) {
     #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -32,7 +32,9 @@ __device__ __forceinline__ float ln_block_sum(float v, float *red) {
 }
 
 // One CTA per row, the row held in registers: mean, then the mean of the squared deviations,
-// then y = bf16((x - mean) / sqrt(var + eps) * w + b).
+// then y = bf16((x - mean) / sqrt(var + eps) * w + b).  128 threads up to 4096 columns (more
+// rows resident per SM), 256 above.
+template <int LN_THREADS>
 __global__ void __launch_bounds__(LN_THREADS) layernorm_kernel(const bf16 *__restrict__ x,
                                                                const bf16 *__restrict__ w,
                                                                const bf16 *__restrict__ b, bf16 *y, int cols,
@@ -60,7 +62,7 @@ __global__ void __launch_bounds__(LN_THREADS) layernorm_kernel(const bf16 *__res
             for (int k = 0; k < 8; ++k) s += f[i][k];
         }
     }
-    const float mean = ln_block_sum(s, red) / (float)cols;
+    const float mean = ln_block_sum<LN_THREADS>(s, red) / (float)cols;
     float q = 0.f;
     #pragma unroll
     for (int i = 0; i < LN_VPT; ++i) {
@@ -73,7 +75,7 @@ __global__ void __launch_bounds__(LN_THREADS) layernorm_kernel(const bf16 *__res
             }
         }
     }
-    const float rstd = 1.0f / sqrtf(ln_block_sum(q, red) / (float)cols + eps);
+    const float rstd = 1.0f / sqrtf(ln_block_sum<LN_THREADS>(q, red) / (float)cols + eps);
     const uint4 *wr = reinterpret_cast<const uint4 *>(w);
     const uint4 *br = reinterpret_cast<const uint4 *>(b);
     uint4 *yr = reinterpret_cast<uint4 *>(y + (size_t)row * cols);
@@ -205,10 +207,14 @@ void make_vision_rope(VisionRope *r, int head_dim, float theta) {
 cudaError_t launch_layernorm(const bf16 *x, const bf16 *w, const bf16 *b, bf16 *y, int rows, int cols, float eps,
                              cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
-    if (cols % 8 || cols > LN_THREADS * LN_VPT * 8) return cudaErrorInvalidValue;
+    if (cols % 8 || cols > 256 * LN_VPT * 8) return cudaErrorInvalidValue;
     cudaLaunchAttribute at[1];
-    cudaLaunchConfig_t cfg = pdl_config(dim3(rows), dim3(LN_THREADS), 0, st, at);
-    return cudaLaunchKernelEx(&cfg, layernorm_kernel, x, w, b, y, cols, eps);
+    if (cols <= 128 * LN_VPT * 8) {
+        cudaLaunchConfig_t cfg = pdl_config(dim3(rows), dim3(128), 0, st, at);
+        return cudaLaunchKernelEx(&cfg, layernorm_kernel<128>, x, w, b, y, cols, eps);
+    }
+    cudaLaunchConfig_t cfg = pdl_config(dim3(rows), dim3(256), 0, st, at);
+    return cudaLaunchKernelEx(&cfg, layernorm_kernel<256>, x, w, b, y, cols, eps);
 }
 
 cudaError_t launch_pos_embed(const bf16 *table, int G, int D, const VisionGrids &gr, int n, bf16 *out,

@@ -98,3 +98,29 @@ def test_profiled_graph_replays_time_the_gate_up_launches():
         assert enc.status() == 0, Q.h3enc_last_error(enc.handle)
     finally:
         enc.close()
+
+
+def test_profiling_one_layer_times_one_launch_per_encode():
+    wl = W.workload(0)
+    cfg = wl.model
+    inp = W.gen_inputs(wl)
+    S, H = inp["seq_len"], cfg.hidden
+    enc = make_encoder(wl, cfg, max_tokens=S)
+    try:
+        pos = torch.from_numpy(inp["positions"]).cuda()
+        x = W.bf16_bits_to_torch(W.normal_bf16(91, "graph_x", (S, H))).cuda()
+        out = torch.empty(S, H, dtype=torch.bfloat16, device="cuda")
+        Q.h3enc_set_profiling_classes(enc.handle, ["gemm_gate_up", "gemm_down"])
+        Q.h3enc_set_profiling_layer(enc.handle, cfg.num_layers - 1)
+        for _ in range(3):
+            Q.h3enc_encode_embeds(enc.handle, x, 0, cfg.num_layers, pos, None, None, 0, 0, None, S, out)
+        prof = Q.h3enc_get_profile(enc.handle)
+        assert prof["gemm_gate_up"][1] == 3 and prof["gemm_down"][1] == 3
+        assert prof["gemm_gate_up"][0] > 0 and prof["gemm_qkv"] == (0.0, 0)
+        with pytest.raises(Q.H3encError):
+            Q.h3enc_set_profiling_layer(enc.handle, cfg.num_layers)
+        Q.h3enc_set_profiling_layer(enc.handle, -1)
+        Q.h3enc_set_profiling_classes(enc.handle, [])
+        assert enc.status() == 0
+    finally:
+        enc.close()
