@@ -388,6 +388,9 @@ def run_vision(args):
     import qwen3_vl_text_gb300 as Q
     import workloads as W
     wl = W.vision_workload(2)
+    if args.images > 1:   # the same image size, several per encode (one attention segment each)
+        import dataclasses
+        wl = dataclasses.replace(wl, grids=wl.grids * args.images)
     cfg = wl.model
     inp = W.gen_vision_inputs(wl)
     n = inp["n_patches"]
@@ -447,14 +450,16 @@ def run_vision(args):
     flops = vision_flops(cfg, wl.grids)
     tflops = flops * args.steps / (ms / 1e3) / 1e12
     line = {
-        "metric": "vision tower: merged visual tokens/s, one 48x64-patch image", "value": nm * args.steps / (ms / 1e3),
+        "metric": ("vision tower: merged visual tokens/s, " + ("one 48x64-patch image" if args.images == 1
+                                                               else f"{args.images} 48x64-patch images per encode")),
+        "value": nm * args.steps / (ms / 1e3),
         "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded random-init weights and pixels)",
         "config": {"workload": wl.name, "patches": n, "merged_tokens": nm, "depth": cfg.depth, "hidden": cfg.hidden,
                    "heads": cfg.num_heads, "intermediate": cfg.intermediate, "deepstack": len(cfg.deepstack_visual_indexes),
                    "l2": "no flush: each step streams 0.91 GB of weights, far above the 129 MB L2"},
-        "images_per_s": args.steps / (ms / 1e3), "tflops": tflops, "pct_dense_bf16_peak": 100.0 * tflops / base,
+        "images_per_s": args.images * args.steps / (ms / 1e3), "tflops": tflops, "pct_dense_bf16_peak": 100.0 * tflops / base,
         "roofline": {"kernel": "whole tower (all launches of one encode)", "bound": "tensor", "achieved": tflops,
                      "peak": base, "unit": "TFLOP/s", "frac": tflops / base,
                      "peak_source": f"{src} {base_name}", "traffic": None},
@@ -464,7 +469,7 @@ def run_vision(args):
         "clocks": clk,
     }
     enc.close()
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and args.images == 1:
         import oracle as O
         ws = {nme[len("model.visual."):]: O.bf16_bits_to_float(W.gen_weight(wl.seed, nme, sh, mu, sg))
               for nme, sh, mu, sg in W.vision_weight_specs(cfg)}
@@ -474,6 +479,116 @@ def run_vision(args):
         t = time.perf_counter() - t0
         line["cpu_baseline"] = {"value": nm / t, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                                 "sample": "one whole tower forward on the same image"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_multimodal(args):
+    """The pages' whole multimodal encode per step: the vision tower on one 48x64-patch image,
+    then the 50-layer text encode of the seq-1024 prompt whose 768 image placeholders take the
+    tower's embeddings and whose first three layers take its DeepStack features."""
+    import torch
+
+    import qwen3_vl_text_gb300 as Q
+    import workloads as W
+    vw = W.vision_workload(2)
+    tw = W.workload(WORKLOAD_ID)
+    vcfg, cfg = vw.model, tw.model
+    vin, tin = W.gen_vision_inputs(vw), W.gen_inputs(tw)
+    S, n_vis = tin["seq_len"], tin["n_vis"]
+    venc = Q.VisionEncoder(vcfg, max_patches=vin["n_patches"])
+    for name, shape, mean, sigma in W.vision_weight_specs(vcfg):
+        venc.load(name, W.gen_weight(vw.seed, name, shape, mean, sigma, device="cuda"))
+    enc = Q.Encoder(cfg, max_tokens=S, max_seqs=4, num_deepstack=len(vcfg.deepstack_visual_indexes))
+    for l in range(cfg.num_layers):
+        for name, shape, mean, sigma in W.layer_weight_specs(cfg, l):
+            enc.load(name, W.gen_weight(tw.seed, name, shape, mean, sigma, device="cuda"))
+    enc.load(W.embed_name(), W.gen_weight(tw.seed, W.embed_name(), (cfg.vocab, cfg.hidden), 0.0, 0.02,
+                                          device="cuda"))
+    torch.cuda.synchronize()
+    venc.finalize()
+    enc.finalize()
+    ids_h = tin["input_ids"].copy()
+    ids_h[tin["visual_mask"] == 1] = 151655            # the image placeholder id
+    ids_h[tin["visual_mask"] == 0] %= 151655
+    ids = torch.from_numpy(ids_h).cuda()
+    pos = torch.from_numpy(tin["positions"]).cuda()
+    mask = torch.from_numpy(tin["visual_mask"]).cuda()
+    px = W.bf16_bits_to_torch(vin["pixel_values"]).cuda()
+    nds = len(vcfg.deepstack_visual_indexes)
+    emb = torch.empty(n_vis, cfg.hidden, dtype=torch.bfloat16, device="cuda")
+    ds = torch.empty(nds, n_vis, cfg.hidden, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(S, cfg.hidden, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        venc.encode(px, vw.grids, emb, ds, stream=stream)
+        Q.h3enc_encode_multimodal(enc.handle, ids, pos, mask, emb, ds, nds, n_vis, None, S, out, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if enc.status() != 0 or venc.status() != 0:
+        raise RuntimeError("device status after warm-up")
+    clocks = Clocks(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    time.sleep(0.5)
+    torch.cuda.synchronize()
+    l0 = Q.h3enc_launch_count(enc.handle) + Q.h3vis_launch_count(venc.handle)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    launches = Q.h3enc_launch_count(enc.handle) + Q.h3vis_launch_count(venc.handle) - l0
+    if enc.status() != 0 or venc.status() != 0:
+        raise RuntimeError("device status after the timed region")
+    # end to end: pixels, ids, positions and mask copied in from pinned memory, the output copied out
+    h_px = W.bf16_bits_to_torch(vin["pixel_values"]).pin_memory()
+    h_ids = torch.from_numpy(ids_h).pin_memory()
+    h_pos = torch.from_numpy(tin["positions"]).pin_memory()
+    h_mask = torch.from_numpy(tin["visual_mask"]).pin_memory()
+    h_out = torch.empty(S, cfg.hidden, dtype=torch.bfloat16).pin_memory()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        px.copy_(h_px, non_blocking=True)
+        ids.copy_(h_ids, non_blocking=True)
+        pos.copy_(h_pos, non_blocking=True)
+        mask.copy_(h_mask, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3
+    burst, sustained, hbm, src = _peaks()
+    at_max = bool(clk and clk.get("sm_mhz") and clk.get("sm_max_mhz")
+                  and clk["sm_mhz"] >= 0.97 * clk["sm_max_mhz"] and "sw_power_cap" not in clk.get("reasons", []))
+    base, base_name = (burst, "bf16_tflops") if at_max else (sustained, "bf16_tflops_sustained")
+    flops = encode_flops(cfg, tin["cu_seqlens"]) + vision_flops(vcfg, vw.grids)
+    tflops = flops * args.steps / (ms / 1e3) / 1e12
+    line = {
+        "metric": "multimodal encode (one 48x64-patch image + the seq-1024 prompt): encoded tokens/s",
+        "value": S * args.steps / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded random-init weights, pixels and ids)",
+        "config": {"workload": "vision-image-48x64 + " + tw.name, "seq_len": S, "visual_tokens": n_vis,
+                   "launch": "eager (one host launch per kernel)"},
+        "tflops": tflops, "pct_dense_bf16_peak": 100.0 * tflops / base,
+        "roofline": {"kernel": "whole step (vision tower + 50-layer text encode)", "bound": "tensor",
+                     "achieved": tflops, "peak": base, "unit": "TFLOP/s", "frac": tflops / base,
+                     "peak_source": f"{src} {base_name}", "traffic": None},
+        "gpu_launches": int(launches),
+        "e2e": {"value": S * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h_px.numel() * 2 + h_ids.numel() * 4 + h_pos.numel() * 4 + h_mask.numel()),
+                "d2h_bytes_per_step": int(h_out.numel() * 2)},
+        "clocks": clk,
+    }
+    venc.close()
+    enc.close()
     print(json.dumps(line), flush=True)
     return 0
 
@@ -497,6 +612,9 @@ def main():
                     help="bf16: run each RMSNorm as its own kernel instead of folding it into the projections")
     ap.add_argument("--vision", action="store_true",
                     help="time the vision tower on one 48x64-patch image instead of the text encode")
+    ap.add_argument("--images", type=int, default=1, help="with --vision: images per encode")
+    ap.add_argument("--multimodal", action="store_true",
+                    help="time the vision tower and the text encode together (one image + the seq-1024 prompt)")
     ap.add_argument("--oracle-time", type=int, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--reps", type=int, default=3, help=argparse.SUPPRESS)
     ap.add_argument("--warm", type=int, default=1, help=argparse.SUPPRESS)
@@ -516,6 +634,8 @@ def main():
         return oracle_time(args)
     if args.vision:
         return run_vision(args)
+    if args.multimodal:
+        return run_multimodal(args)
     if args.kernel:
         return run_kernel(args)
     if args.impl == "reference":
