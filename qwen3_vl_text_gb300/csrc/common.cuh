@@ -106,6 +106,10 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, const void *s
                  "r"(smem_u32(src)), "r"(x), "r"(y)
                  : "memory");
 }
+// Hint: bring the 128-byte line holding `p` into L2 (no register result, no fault on a valid address).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N of this thread's bulk groups still read their shared-memory source.
 template <int N>

@@ -818,6 +818,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     for (int i = 0; i < BN / 16; ++i) rpre[i] = src[i];
                 }
             }
+            if constexpr (EPI == EPI_QKROPE) {
+                // this row's cos/sin lines, pulled into L2 while the MMAs finish: by the time the
+                // accumulator is ready the streamed operands may have pushed them out
+                if (live && (n_blk * BN) / g.head_dim < g.nq + g.nkv) {
+                    const int bytes = (g.head_dim >> 1) * (int)sizeof(float);
+                    const char *cs = reinterpret_cast<const char *>(g.cos_t) + (size_t)row * bytes;
+                    const char *sn = reinterpret_cast<const char *>(g.sin_t) + (size_t)row * bytes;
+                    for (int off = ehalf * 128; off < bytes; off += 256) {
+                        prefetch_l2(cs + off);
+                        prefetch_l2(sn + off);
+                    }
+                }
+            }
             if (!wait_acc()) break;
             if (et == 0) stamp(g, TR_LAST_ACC);   // overwritten per tile: the last one stays
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
