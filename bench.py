@@ -751,10 +751,17 @@ def main():
     h_ds = W.bf16_bits_to_torch(inp["deepstack"]).pin_memory() if ds is not None else None
     h_out = torch.empty(S, cfg.hidden, dtype=torch.bfloat16).pin_memory()
 
+    host_stream = torch.cuda.Stream()   # a stream of its own: capturable, unlike the legacy default
+    Q.h3enc_set_graphs(enc.handle, graph is not None)   # --eager: the host entry runs eagerly too
+    torch.cuda.synchronize()
+
     def host_step():
         Q.h3enc_encode_host(enc.handle, h_ids, h_pos, h_mask, h_ds, 0 if h_ds is None else h_ds.shape[0], n_vis, cu,
-                            S, h_out, stream)
+                            S, h_out, host_stream)
 
+    # the entry point runs a new call shape eagerly once, captures it on the second call and
+    # replays the graph after that: both happen before the timed calls
+    host_step()
     host_step()
     if dist:
         dist.barrier()
@@ -821,7 +828,10 @@ def main():
         "kernel_ms_note": "separate pass with an event pair around every launch",
         "gpu_launches": int(launches),
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
+                "d2h_bytes_per_step": int(d2h),
+                "launch": "h3enc_encode_host: copies in, " + ("the call shape's CUDA graph replayed"
+                                                              if graph is not None else "eager launches")
+                          + ", copy out, sync"},
         "clocks": clk,
     }
     enc.close()

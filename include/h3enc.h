@@ -171,7 +171,16 @@ H3ENC_API h3enc_status h3enc_encode_embeds(h3enc *h, const void *inputs_embeds, 
 /* As h3enc_encode with HOST buffers (ids, positions, mask, deepstack, out):
  * copies the inputs to the handle's device staging buffers, encodes, copies
  * the result back and synchronises `stream`.  Host buffers may be pageable;
- * pinned buffers copy faster. */
+ * pinned buffers copy faster.
+ * CUDA graphs (h3enc_set_graphs, on by default): the encode reads and writes only
+ * the handle's own buffers here, so it is captured into a graph per call shape
+ * (seq_len, the cu_seqlens values, n_vis, num_deepstack, whether a mask is given)
+ * and replayed: the first call of a shape runs eagerly, the second captures and
+ * replays, later ones replay.  Up to 8 shapes are kept (least recently used
+ * dropped); loading or finalising weights drops them all.  Calls run eagerly
+ * while profiling or layer capture is on, on the legacy or per-thread default
+ * stream (NULL), or when `stream` is itself being captured.  The copies stay
+ * outside the graph. */
 H3ENC_API h3enc_status h3enc_encode_host(h3enc *h, const int32_t *input_ids, const int32_t *positions,
                                const uint8_t *visual_mask, const void *deepstack,
                                int32_t num_deepstack, int32_t n_vis, const int32_t *cu_seqlens,
@@ -268,8 +277,16 @@ H3ENC_API h3enc_status h3enc_set_profiling_layer(h3enc *h, int32_t layer);
  * Resets totals. */
 H3ENC_API h3enc_status h3enc_get_profile(h3enc *h, double *ms, int64_t *launches, int32_t n);
 
-/* Number of kernels this handle has launched since create. */
+/* Number of kernels this handle has launched since create (a graph replay counts
+ * the kernels it runs). */
 H3ENC_API int64_t h3enc_launch_count(const h3enc *h);
+
+/* enable (0 or 1): let h3enc_encode_host capture and replay CUDA graphs (default 1).
+ * Disabling drops the cached graphs. */
+H3ENC_API h3enc_status h3enc_set_graphs(h3enc *h, int32_t enable);
+
+/* Number of captured graphs the handle holds (0..8). */
+H3ENC_API int32_t h3enc_graph_count(const h3enc *h);
 
 /* Number of streaming multiprocessors the handle's kernels size their grids by. */
 H3ENC_API int32_t h3enc_num_sms(const h3enc *h);

@@ -18,6 +18,7 @@ __all__ = [
     "h3enc_create", "h3enc_load_weights", "h3enc_finalize_weights", "h3enc_encode", "h3enc_encode_embeds", "h3enc_encode_multimodal",
     "h3enc_encode_host", "h3enc_set_layer_capture", "h3enc_get_status", "h3enc_last_error", "h3enc_destroy",
     "h3enc_set_profiling", "h3enc_set_profiling_classes", "h3enc_set_profiling_layer", "h3enc_get_profile", "h3enc_launch_count", "h3enc_num_sms",
+    "h3enc_set_graphs", "h3enc_graph_count",
     "h3enc_build_positions", "h3enc_aggregate_deepstack",
     "h3enc_op_gemm", "h3enc_op_gemm_workspace_bytes", "h3enc_op_gemm_trace_next", "h3enc_op_attention_trace_next", "h3enc_op_gemm_noalloc", "h3enc_op_gemm_noalloc_scratch_bytes", "h3enc_op_pack_gate_up", "h3enc_op_rmsnorm", "h3enc_op_gemm_fp8", "h3enc_op_quant_rows",
     "h3enc_op_rmsnorm_q8", "h3enc_op_wait_probe", "h3enc_op_rope_table",
@@ -91,6 +92,8 @@ _SIGS = {
     "h3enc_get_profile": ([_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I64), _I32], _I32),
     "h3enc_launch_count": ([_P], _I64),
     "h3enc_num_sms": ([_P], _I32),
+    "h3enc_set_graphs": ([_P, _I32], _I32),
+    "h3enc_graph_count": ([_P], _I32),
     "h3enc_op_gemm": ([_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _I64, _P, _P], _I32),
     "h3enc_op_gemm_workspace_bytes": ([], _I64),
     "h3enc_op_gemm_trace_next": ([_P, _I64], _I32),
@@ -310,6 +313,15 @@ def h3enc_launch_count(h) -> int:
 
 def h3enc_num_sms(h) -> int:
     return lib.h3enc_num_sms(h)
+
+
+def h3enc_set_graphs(h, enable):
+    """Let h3enc_encode_host capture and replay one CUDA graph per call shape (default on)."""
+    _check(lib.h3enc_set_graphs(h, 1 if enable else 0), h)
+
+
+def h3enc_graph_count(h) -> int:
+    return lib.h3enc_graph_count(h)
 
 
 def h3enc_op_gemm(A, W, C, M, N, K, epilogue, R=None, DS=None, vis_rank=None, n_vis=0, workspace=None,

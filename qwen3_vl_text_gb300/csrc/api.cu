@@ -8,6 +8,7 @@
 // following MiniMaxH3Qwen3VLTextModel.forward and MiniMaxH3Qwen3VLTextDecoderLayer.
 // forward (page "vllm-omni vllm_omni/diffusion/models/minimax_h3/encoder.py").
 // The hidden state lives in the caller's output buffer for the whole encode.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -101,6 +102,28 @@ struct h3enc {
     double ms[H3ENC_K_COUNT] = {0};
     int64_t launches[H3ENC_K_COUNT] = {0};
     int64_t launch_count = 0;
+    // h3enc_encode_host's CUDA graphs: one per distinct call shape (every pointer the encode
+    // reads or writes is a staging or workspace buffer of the handle, fixed at create), replayed
+    // instead of issuing the launches again; least recently used beyond kMaxGraphs is dropped
+    struct Graph {
+        int S = 0, n_seqs = 0, n_vis = 0, nds = 0;
+        bool mask = false;
+        std::vector<int32_t> cu;
+        cudaGraphExec_t exec = nullptr;   // null until the shape's second call
+        bool failed = false;              // its capture failed: it runs eagerly
+        bool waits_ds = false;            // it holds a wait for the DeepStack copy
+        int64_t launches = 0;             // kernels one replay runs
+        uint64_t used = 0;
+    };
+    static constexpr size_t kMaxGraphs = 8;
+    std::vector<Graph> graphs;
+    uint64_t graph_tick = 0;
+    bool use_graphs = true;
+    // h3enc_encode_host's DeepStack copy runs on a stream of its own, so that it lands while
+    // the first layer computes; the encode waits for it just before the first DeepStack add
+    cudaStream_t copy_st = nullptr;
+    cudaEvent_t ds_fork = nullptr, ds_ready = nullptr;
+    bool ds_pending = false;   // set while encode_core is to wait for ds_ready
 };
 
 namespace {
@@ -390,6 +413,12 @@ h3enc_status finalize_fp8(h3enc *h) {
 }
 
 
+void drop_graphs(h3enc *h) {
+    for (auto &g : h->graphs)
+        if (g.exec) cudaGraphExecDestroy(g.exec);
+    h->graphs.clear();
+}
+
 h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int lb, int le, const int32_t *pos,
                          const uint8_t *mask, const bf16 *ds, int nds, int n_vis, const int32_t *cu, int n_seqs,
                          int S, bf16 *out, cudaStream_t st, const bf16 *visual_embeds = nullptr) {
@@ -535,6 +564,16 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         p.ss_in = nullptr;
         p.ss_out = fold && l + 1 < le ? h->row_ss : nullptr;   // statistics for the next input norm
         if (use_ds && l < nds) {
+            if (h->ds_pending) {   // the host entry's DeepStack copy, issued on its own stream
+                // (inside a capture the wait becomes an event-wait node on the copy's event)
+                cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+                e = cudaStreamIsCapturing(st, &cs);
+                if (e == cudaSuccess)
+                    e = cudaStreamWaitEvent(st, h->ds_ready,
+                                            cs == cudaStreamCaptureStatusActive ? cudaEventWaitExternal : 0);
+                if (e != cudaSuccess) return cuda_fail(h, e, "DeepStack copy wait");
+                h->ds_pending = false;
+            }
             p.epi = h3::EPI_RESIDUAL_DS;
             p.DS = ds + (size_t)l * n_vis * H;
             p.vis_rank = h->vis_rank;
@@ -653,6 +692,7 @@ h3enc_status h3enc_create(const h3enc_config *cfg, h3enc **out) {
 h3enc_status h3enc_load_weights(h3enc *h, const char *name, const void *data, int32_t dtype,
                                 const int64_t *shape, int32_t ndim, int32_t data_on_device) {
     if (!h || !name || !data || !shape || ndim < 1) return fail(h, H3ENC_ERR_INVALID_ARG, "NULL argument");
+    drop_graphs(h);   // a graph replays the weights as they were when it was captured
     const h3enc_config &c = h->cfg;
     if (strcmp(name, "lm_head.weight") == 0 || strcmp(name, "model.language_model.norm.weight") == 0 ||
         strncmp(name, "model.visual.", 13) == 0)
@@ -733,6 +773,7 @@ h3enc_status h3enc_load_weights(h3enc *h, const char *name, const void *data, in
 
 h3enc_status h3enc_finalize_weights(h3enc *h) {
     if (!h) return fail(h, H3ENC_ERR_INVALID_ARG, "NULL handle");
+    drop_graphs(h);
     const h3enc_config &c = h->cfg;
     std::string missing, shards;
     int n_missing = 0;
@@ -844,16 +885,118 @@ h3enc_status h3enc_encode_host(h3enc *h, const int32_t *input_ids, const int32_t
     if (!input_ids) return fail(h, H3ENC_ERR_INVALID_ARG, "input_ids is NULL");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t S = seq_len, H = h->cfg.hidden;
-    cudaError_t e = cudaMemcpyAsync(h->st_ids, input_ids, S * 4, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(h->st_pos, positions, 3 * S * 4, cudaMemcpyHostToDevice, st);
     const bool use_ds = num_deepstack > 0 && n_vis > 0;
+    cudaError_t e = cudaSuccess;
+    if (use_ds && !h->copy_st) {
+        e = cudaStreamCreateWithFlags(&h->copy_st, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ds_fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ds_ready, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(h, e, "copy stream");
+    }
+    // the DeepStack features (the bulk of the inputs) go first, on the copy stream, once the
+    // caller's earlier work on `stream` is done with the staging buffer
+    bool ds_waited = !use_ds;   // whether `stream` has been made to wait for that copy
+    if (use_ds) {
+        e = cudaEventRecord(h->ds_fork, st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h->copy_st, h->ds_fork, 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(h->st_ds, deepstack, (size_t)num_deepstack * n_vis * H * 2, cudaMemcpyHostToDevice,
+                                h->copy_st);
+        if (e == cudaSuccess) e = cudaEventRecord(h->ds_ready, h->copy_st);
+        if (e != cudaSuccess) return cuda_fail(h, e, "host-to-device copy");
+    }
+    // on every way out the host buffer is released only after the copy has read it
+    struct DsGuard {
+        h3enc *h;
+        const bool &waited;
+        ~DsGuard() {
+            h->ds_pending = false;
+            if (!waited) cudaStreamSynchronize(h->copy_st);
+        }
+    } ds_guard{h, ds_waited};
+    e = cudaMemcpyAsync(h->st_ids, input_ids, S * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h->st_pos, positions, 3 * S * 4, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess && visual_mask) e = cudaMemcpyAsync(h->st_mask, visual_mask, S, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess && use_ds)
-        e = cudaMemcpyAsync(h->st_ds, deepstack, (size_t)num_deepstack * n_vis * H * 2, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_fail(h, e, "host-to-device copy");
-    s = encode_core(h, h->st_ids, nullptr, 0, h->cfg.num_layers, h->st_pos, visual_mask ? h->st_mask : nullptr,
-                    use_ds ? h->st_ds : nullptr, num_deepstack, n_vis, cu_seqlens, n_seqs, seq_len, h->st_out, st);
-    if (s != H3ENC_OK) return s;
+    bool consumed = false;   // the last encode_core made `stream` wait for the DeepStack copy
+    auto encode = [&] {
+        h->ds_pending = use_ds;
+        const h3enc_status r = encode_core(h, h->st_ids, nullptr, 0, h->cfg.num_layers, h->st_pos,
+                                           visual_mask ? h->st_mask : nullptr, use_ds ? h->st_ds : nullptr,
+                                           num_deepstack, n_vis, cu_seqlens, n_seqs, seq_len, h->st_out, st);
+        consumed = use_ds && !h->ds_pending;
+        h->ds_pending = false;
+        return r;
+    };
+    // Graphs: the first call of a shape runs eagerly (and so makes every one-time kernel setup);
+    // the second captures the encode into a graph, which it and later calls of that shape replay.
+    // Eager when profiling or capturing layers (both change what an encode records), on the
+    // legacy or per-thread default stream (not capturable), when the caller's stream is itself
+    // being captured, or for a shape whose capture failed.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    const bool graphable = h->use_graphs && !h->prof && h->capture.empty() && st != nullptr &&
+                           st != cudaStreamLegacy && st != cudaStreamPerThread &&
+                           cudaStreamIsCapturing(st, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone;
+    h3enc::Graph *g = nullptr;
+    if (graphable) {
+        const int nseg = cu_seqlens ? n_seqs + 1 : 0;
+        for (auto &c : h->graphs)
+            if (c.S == seq_len && c.n_seqs == n_seqs && c.n_vis == n_vis && c.nds == num_deepstack &&
+                c.mask == (visual_mask != nullptr) && (int)c.cu.size() == nseg &&
+                std::equal(c.cu.begin(), c.cu.end(), cu_seqlens))
+                g = &c;
+        if (!g) {   // a new shape: remember it, run eagerly
+            if (h->graphs.size() >= h3enc::kMaxGraphs) {
+                auto lru = std::min_element(h->graphs.begin(), h->graphs.end(),
+                                            [](const h3enc::Graph &a, const h3enc::Graph &b) { return a.used < b.used; });
+                if (lru->exec) cudaGraphExecDestroy(lru->exec);
+                h->graphs.erase(lru);
+            }
+            h3enc::Graph ng;
+            ng.S = seq_len;
+            ng.n_seqs = n_seqs;
+            ng.n_vis = n_vis;
+            ng.nds = num_deepstack;
+            ng.mask = visual_mask != nullptr;
+            if (nseg) ng.cu.assign(cu_seqlens, cu_seqlens + nseg);
+            ng.used = ++h->graph_tick;
+            h->graphs.push_back(std::move(ng));
+        } else {
+            g->used = ++h->graph_tick;
+            if (!g->exec && !g->failed) {   // the second call of this shape: capture it
+                const int64_t before = h->launch_count;
+                bool ok = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
+                if (ok) {
+                    const h3enc_status cs = encode();
+                    cudaGraph_t graph = nullptr;
+                    ok = cudaStreamEndCapture(st, &graph) == cudaSuccess && cs == H3ENC_OK && graph;
+                    if (ok) ok = cudaGraphInstantiate(&g->exec, graph, 0) == cudaSuccess;
+                    g->waits_ds = consumed;
+                    if (graph) cudaGraphDestroy(graph);
+                }
+                g->launches = h->launch_count - before;
+                h->launch_count = before;   // counted when a replay runs them
+                if (!ok) {   // this shape stays eager; the eager run below reports any real error
+                    (void)cudaGetLastError();
+                    if (g->exec) cudaGraphExecDestroy(g->exec);
+                    g->exec = nullptr;
+                    g->failed = true;
+                    h->err.clear();
+                }
+            }
+            if (!g->exec) g = nullptr;
+        }
+    }
+    if (g) {
+        e = cudaGraphLaunch(g->exec, st);   // its wait node takes this call's DeepStack copy
+        if (e != cudaSuccess) return cuda_fail(h, e, "graph launch");
+        ds_waited = g->waits_ds;
+        h->launch_count += g->launches;
+    } else {
+        s = encode();
+        if (s != H3ENC_OK) return s;
+        ds_waited = consumed;
+    }
     e = cudaMemcpyAsync(out, h->st_out, S * H * 2, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(h, e, "device-to-host copy");
@@ -890,6 +1033,10 @@ const char *h3enc_last_error(const h3enc *h) { return h ? h->err.c_str() : g_cre
 
 void h3enc_destroy(h3enc *h) {
     if (!h) return;
+    drop_graphs(h);
+    if (h->copy_st) cudaStreamDestroy(h->copy_st);
+    if (h->ds_fork) cudaEventDestroy(h->ds_fork);
+    if (h->ds_ready) cudaEventDestroy(h->ds_ready);
     for (cudaEvent_t ev : h->ev_pool) cudaEventDestroy(ev);
     if (h->ws8) cudaFree(h->ws8);
     if (h->arena8) cudaFree(h->arena8);
@@ -949,6 +1096,21 @@ h3enc_status h3enc_get_profile(h3enc *h, double *ms, int64_t *launches, int32_t 
 }
 
 int64_t h3enc_launch_count(const h3enc *h) { return h ? h->launch_count : 0; }
+
+h3enc_status h3enc_set_graphs(h3enc *h, int32_t enable) {
+    if (!h) return fail(h, H3ENC_ERR_INVALID_ARG, "NULL handle");
+    if (enable != 0 && enable != 1) return fail(h, H3ENC_ERR_INVALID_ARG, "enable must be 0 or 1");
+    h->use_graphs = enable != 0;
+    if (!enable) drop_graphs(h);
+    return H3ENC_OK;
+}
+
+int32_t h3enc_graph_count(const h3enc *h) {
+    int32_t n = 0;
+    if (h)
+        for (const auto &g : h->graphs) n += g.exec != nullptr;
+    return n;
+}
 int32_t h3enc_num_sms(const h3enc *h) { return h ? h->num_sms : 0; }
 
 // ---------------------------------------------------------------- op-level entries

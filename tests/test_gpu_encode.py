@@ -126,6 +126,76 @@ def test_tiny_layer_capture_and_host_entry_match_device_encode():
         enc.close()
 
 
+def test_host_entry_graphs_replay_the_eager_encode():
+    """h3enc_encode_host on a stream of its own: the first call of a shape runs eagerly, the
+    second captures a CUDA graph, later calls replay it; every output is bit for bit the eager
+    one, new input values flow through a replay, a new packing is a new shape, and profiling,
+    disabling or reloading weights fall back to (or restart from) eager runs."""
+    wl = W.workload(0)
+    cfg = wl.model
+    inp = W.gen_inputs(wl)
+    S = inp["seq_len"]
+    enc = make_encoder(wl, cfg, max_tokens=64)
+    st = torch.cuda.Stream()
+    try:
+        ids = torch.from_numpy(inp["input_ids"]).pin_memory()
+        pos = torch.from_numpy(inp["positions"]).pin_memory()
+        mask = torch.from_numpy(inp["visual_mask"]).pin_memory()
+        ds = W.bf16_bits_to_torch(inp["deepstack"]).pin_memory()
+        h = enc.handle
+
+        def host(ids_, cu=None):
+            out = torch.empty(S, cfg.hidden, dtype=torch.bfloat16).pin_memory()
+            n0 = Q.h3enc_launch_count(h)
+            Q.h3enc_encode_host(h, ids_, pos, mask, ds, ds.shape[0], inp["n_vis"], cu, S, out, st)
+            return out, Q.h3enc_launch_count(h) - n0
+
+        Q.h3enc_set_graphs(h, False)
+        ref, n_eager = host(ids)
+        ref2, _ = host(ids)
+        assert torch.equal(ref, ref2) and n_eager > 0 and Q.h3enc_graph_count(h) == 0
+        Q.h3enc_set_graphs(h, True)
+        for call in range(4):
+            out, n = host(ids)
+            assert torch.equal(out, ref), call
+            assert n == n_eager, call                      # a replay counts the kernels it runs
+            assert Q.h3enc_graph_count(h) == (0 if call == 0 else 1), call
+        # other token ids through the same graph: equal to an eager run of them
+        ids_b = ((ids.to(torch.int64) * 7 + 3) % cfg.vocab).to(torch.int32).pin_memory()
+        out_b, _ = host(ids_b)
+        Q.h3enc_set_graphs(h, False)
+        want_b, _ = host(ids_b)
+        assert torch.equal(out_b, want_b) and not torch.equal(out_b, ref)
+        # two packed sequences: another shape, captured on its own second call
+        cu = [0, 20, S]
+        want_p, _ = host(ids, cu)
+        Q.h3enc_set_graphs(h, True)
+        for call in range(3):
+            out_p, _ = host(ids, cu)
+            assert torch.equal(out_p, want_p), call
+        assert Q.h3enc_graph_count(h) == 1 and not torch.equal(want_p, ref)
+        host(ids)
+        host(ids)
+        assert Q.h3enc_graph_count(h) == 2
+        # profiling on: eager runs, the cached graphs stay
+        Q.h3enc_set_profiling(h, True)
+        out, _ = host(ids)
+        assert torch.equal(out, ref) and Q.h3enc_graph_count(h) == 2
+        Q.h3enc_set_profiling(h, False)
+        # reloading a weight drops every graph; the handle is finalised again before the next encode
+        name, shape, mean, sigma = next(sp for sp in W.layer_weight_specs(cfg, 0) if "o_proj" in sp[0])
+        enc.load(name, W.gen_weight(wl.seed, name, shape, mean, sigma, device="cuda"))
+        assert Q.h3enc_graph_count(h) == 0
+        torch.cuda.synchronize()
+        enc.finalize()
+        for call in range(3):
+            out, _ = host(ids)
+            assert torch.equal(out, ref), call
+        assert Q.h3enc_graph_count(h) == 1
+    finally:
+        enc.close()
+
+
 @pytest.mark.parametrize("separate_norm", [False, True], ids=["folded_norm", "separate_norm"])
 def test_one_full_width_layer(separate_norm):
     wl = W.workload(1)
