@@ -339,18 +339,32 @@ def run_kernel(args):
     torch.cuda.synchronize()
     ts = []
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 256 MB > L2 between launches
+    timeline = args.timeline and (name.startswith("gemm_") or name == "attention")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    per_cta = 9 if name == "attention" else 11
+    trace = torch.zeros(sms * per_cta, dtype=torch.int64, device=dev) if timeline else None
+    traces = []
     for _ in range(args.steps):
         flush.zero_()
+        if timeline:
+            trace.zero_()
         # ~100 us of device sleep: the host enqueues the launch meanwhile, so the start event
         # fires with the launch already queued and the time is the kernel's, not the host's
         torch.cuda._sleep(200_000)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        if timeline:
+            if name == "attention":
+                Q.h3enc_op_attention_trace_next(trace, sms)
+            else:
+                Q.h3enc_op_gemm_trace_next(trace)
         e0.record(stream)
         fn()
         e1.record(stream)
         torch.cuda.synchronize()
         ts.append(e0.elapsed_time(e1))
+        if timeline:
+            traces.append(trace.view(sms, per_cta).cpu().numpy().copy())
     ts.sort()
     ms = ts[len(ts) // 2]
     burst, sustained, hbm, src = _peaks()
@@ -362,9 +376,40 @@ def run_kernel(args):
                       "work_per_launch": work, "work_unit": "TFLOP" if unit == "TFLOP/s" else "GB",
                       "unit": unit, "peak": peak, "frac": work / (ms / 1e3) / peak,
                       "peak_source": f"{src} {'bf16_tflops' if unit == 'TFLOP/s' else 'hbm_gbs'} (burst)"
-                                     + (" x 2 (nominal fp8/bf16)" if fp8_gemm else "")}),
+                                     + (" x 2 (nominal fp8/bf16)" if fp8_gemm else ""),
+                      **({"timeline": kernel_timeline(name, traces)} if timeline else {})}),
           flush=True)
     return 0
+
+
+def kernel_timeline(name, traces):
+    """Medians over the timed launches of the kernel's own per-CTA stamps (µs from the first
+    CTA's start; attention's middle stamps are SM cycles, reported as µs at each CTA's mean
+    rate between its ns stamps)."""
+    import numpy as np
+    rows = []
+    for t in traces:
+        t = t.astype(np.int64)
+        t = t[t[:, 0] > 0]
+        t0 = t[:, 0].min()
+        if name == "attention":
+            dur = (t[:, 6] - t[:, 0]) / 1e3
+            steps = t[:, 8].astype(np.float64)
+            rows.append({"span_us": float(((t[:, 6] - t0) / 1e3).max()),
+                         "cta_end_us_median": float(np.median((t[:, 6] - t0) / 1e3)),
+                         "key_tiles_per_cta_median": float(np.median(steps)),
+                         "us_per_key_tile_median": float(np.median(dur / np.maximum(steps, 1)))})
+        else:
+            rel = np.where(t > 0, (t - t0) / 1e3, np.nan)
+            leaders = ~np.isnan(rel[:, 4])   # the CTAs that issue the MMAs (one per pair)
+            rows.append({"span_us": float(np.nanmax(rel[:, 10])),
+                         "last_mma_us_median": float(np.nanmedian(rel[leaders, 4])) if leaders.any() else None,
+                         "last_mma_us_max": float(np.nanmax(rel[leaders, 4])) if leaders.any() else None,
+                         "last_tile_epilogue_us_median": float(np.nanmedian(rel[:, 5] - rel[:, 2])),
+                         "stream_k_reduce_done_us_max": (float(np.nanmax(rel[:, 9]))
+                                                         if not np.all(np.isnan(rel[:, 9])) else None)})
+    keys = rows[0].keys()
+    return {k: (None if any(r[k] is None for r in rows) else float(np.median([r[k] for r in rows]))) for k in keys}
 
 
 def vision_flops(cfg, grids) -> float:
@@ -608,6 +653,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--timeline", action="store_true",
+                    help="with --kernel gemm_* or attention: add the kernel's per-CTA phase timeline")
     ap.add_argument("--separate-norm", action="store_true",
                     help="bf16: run each RMSNorm as its own kernel instead of folding it into the projections")
     ap.add_argument("--vision", action="store_true",
