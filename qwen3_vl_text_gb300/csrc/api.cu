@@ -970,7 +970,9 @@ h3enc_status h3enc_encode_host(h3enc *h, const int32_t *input_ids, const int32_t
                     const h3enc_status cs = encode();
                     cudaGraph_t graph = nullptr;
                     ok = cudaStreamEndCapture(st, &graph) == cudaSuccess && cs == H3ENC_OK && graph;
-                    if (ok) ok = cudaGraphInstantiate(&g->exec, graph, 0) == cudaSuccess;
+                    cudaGraphExec_t exec = nullptr;
+                    if (ok) ok = cudaGraphInstantiate(&exec, graph, 0) == cudaSuccess && exec;
+                    if (ok) g->exec = exec;
                     g->waits_ds = consumed;
                     if (graph) cudaGraphDestroy(graph);
                 }
@@ -978,8 +980,6 @@ h3enc_status h3enc_encode_host(h3enc *h, const int32_t *input_ids, const int32_t
                 h->launch_count = before;   // counted when a replay runs them
                 if (!ok) {   // this shape stays eager; the eager run below reports any real error
                     (void)cudaGetLastError();
-                    if (g->exec) cudaGraphExecDestroy(g->exec);
-                    g->exec = nullptr;
                     g->failed = true;
                     h->err.clear();
                 }
