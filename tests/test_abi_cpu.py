@@ -78,3 +78,13 @@ def test_op_entries_validate_arguments(Q):
         Q.h3enc_op_attention(16, 16, 10, 4, 2, 64, [0, 4, 3, 10], stream=0)  # decreasing cu_seqlens
     with pytest.raises(Q.H3encError):
         Q.h3enc_op_pack_gate_up(16, 16, 16, 100, 64, stream=0)              # I % 128
+
+
+def test_handle_calls_reject_a_null_handle(Q):
+    """The graph, profiling and capture switches check their handle before touching CUDA."""
+    for call in (lambda: Q.h3enc_set_graphs(None, True), lambda: Q.h3enc_set_profiling(None, True),
+                 lambda: Q.h3enc_set_profiling_layer(None, 0)):
+        with pytest.raises(Q.H3encError) as e:
+            call()
+        assert e.value.code == 2
+    assert Q.h3enc_graph_count(None) == 0 and Q.h3enc_launch_count(None) == 0
