@@ -17,8 +17,10 @@
  *
  * Ownership: the caller owns every input/output buffer and the stream.  The
  * handle owns a copy of the weights (packed for the kernels) and a workspace
- * sized at create from max_tokens; encode calls allocate nothing and never
- * synchronise the host (h3enc_encode_host excepted).
+ * sized at create from max_tokens; encode calls allocate no device memory and
+ * never synchronise the host (h3enc_encode_host excepted: it synchronises, and
+ * makes a copy stream on its first DeepStack call and a CUDA graph per call
+ * shape).  A handle is used by one host thread at a time.
  *
  * Errors: every argument, shape and completeness error is detected on the
  * host before any launch and returned as a status (h3enc_last_error() has the
