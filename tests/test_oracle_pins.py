@@ -470,3 +470,113 @@ def test_fp8_layer_tracks_the_bf16_layer():
     ref = O.linear(x.astype(np.float64), w.astype(np.float64))
     e1 = np.linalg.norm(O.fp8.fp8_linear(x, w) - ref) / np.linalg.norm(ref)
     assert 5e-3 < e1 < 4e-2
+
+
+# ---------------------------------------------------------------- whole layer, hand-expanded
+
+def _hand_layer(x, w, pos, cfg, *, qk_norm="before_rope", swap_gate_up=False):
+    """One decoder layer written out element by element in float64 Python loops,
+    from page 1 (``MiniMaxH3Qwen3VLTextDecoderLayer.forward``,
+    ``MiniMaxH3Qwen3VLTextAttention.forward``, ``MiniMaxH3Qwen3VLTextMLP.forward``,
+    ``_apply_interleaved_mrope``, ``_rotate_half``): RMSNorm, q/k/v projections,
+    per-head q/k RMSNorm with their own weights, then rotate-half RoPE whose
+    frequency j is driven by position axis T, H or W, causal GQA softmax
+    attention, o_proj and residual; RMSNorm, ``down(silu(gate) * up)`` and
+    residual.  ``qk_norm`` ("before_rope", "after_rope", "none") and
+    ``swap_gate_up`` plant the mistakes this expansion must tell apart."""
+    s, hid = len(x), cfg.hidden
+    d, nq, nkv, half = cfg.head_dim, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim // 2
+    eps = cfg.rms_eps
+
+    def norm(vec, g):
+        r = math.sqrt(sum(t * t for t in vec) / len(vec) + eps)
+        return [vec[i] / r * g[i] for i in range(len(vec))]
+
+    def matvec(m, vec):
+        return [sum(m[r][c] * vec[c] for c in range(len(vec))) for r in range(len(m))]
+
+    sec = cfg.mrope_section
+    axis = []
+    for j in range(half):
+        if j % 3 == 1 and j < 3 * sec[1]:
+            axis.append(1)
+        elif j % 3 == 2 and j < 3 * sec[2]:
+            axis.append(2)
+        else:
+            axis.append(0)
+    inv = [float(np.float32(1.0 / cfg.rope_theta ** (2.0 * j / d))) for j in range(half)]
+
+    def rope(vec, t):
+        out = [0.0] * d
+        for j in range(half):
+            ang = float(np.float32(np.float32(pos[axis[j]][t]) * np.float32(inv[j])))
+            c, sn = math.cos(ang), math.sin(ang)
+            out[j] = vec[j] * c - vec[j + half] * sn
+            out[j + half] = vec[j + half] * c + vec[j] * sn
+        return out
+
+    def head_prep(vec, g, t):
+        if qk_norm == "before_rope":
+            return rope(norm(vec, g), t)
+        if qk_norm == "after_rope":
+            return norm(rope(vec, t), g)
+        return rope(vec, t)
+
+    wl = {k: v.tolist() for k, v in w.items()}
+    qs, ks, vs = [], [], []
+    for t in range(s):
+        y = norm(x[t], wl["input_layernorm"])
+        q, k, v = matvec(wl["q_proj"], y), matvec(wl["k_proj"], y), matvec(wl["v_proj"], y)
+        qs.append([head_prep(q[h * d:(h + 1) * d], wl["q_norm"], t) for h in range(nq)])
+        ks.append([head_prep(k[g * d:(g + 1) * d], wl["k_norm"], t) for g in range(nkv)])
+        vs.append([v[g * d:(g + 1) * d] for g in range(nkv)])
+    outs = []
+    for t in range(s):
+        attn = []
+        for h in range(nq):
+            g = h // (nq // nkv)
+            sc = [sum(qs[t][h][c] * ks[u][g][c] for c in range(d)) / math.sqrt(d) for u in range(t + 1)]
+            m = max(sc)
+            e = [math.exp(z - m) for z in sc]
+            tot = sum(e)
+            attn += [sum(e[u] / tot * vs[u][g][c] for u in range(t + 1)) for c in range(d)]
+        h1 = [x[t][i] + o for i, o in enumerate(matvec(wl["o_proj"], attn))]
+        y2 = norm(h1, wl["post_attention_layernorm"])
+        gate, up = matvec(wl["gate_proj"], y2), matvec(wl["up_proj"], y2)
+        if swap_gate_up:
+            gate, up = up, gate
+        act = [gi / (1.0 + math.exp(-gi)) * ui for gi, ui in zip(gate, up)]
+        outs.append([h1[i] + dn for i, dn in enumerate(matvec(wl["down_proj"], act))])
+    return np.array(outs)
+
+
+def test_three_token_layer_against_hand_expansion():
+    """A 3-token layer with non-zero gate and up weights, strongly non-uniform
+    q_norm / k_norm weights and positions that differ on every axis, against the
+    loop expansion above.  The same expansion with gate and up swapped, with the
+    q/k RMSNorm dropped, or with it applied after the rotation is far from the
+    oracle, so each of those mistakes in the oracle would fail here."""
+    from types import SimpleNamespace
+    cfg = SimpleNamespace(hidden=16, n_heads=4, n_kv_heads=2, head_dim=8, intermediate=12, rms_eps=1e-6,
+                          rope_theta=100.0, mrope_section=[2, 1, 1])
+    r = _rng(40)
+    nq_d, kv_d = cfg.n_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+    w = O.LayerWeights(
+        q_proj=r.standard_normal((nq_d, cfg.hidden)) * 0.4, k_proj=r.standard_normal((kv_d, cfg.hidden)) * 0.4,
+        v_proj=r.standard_normal((kv_d, cfg.hidden)) * 0.4, o_proj=r.standard_normal((cfg.hidden, nq_d)) * 0.3,
+        gate_proj=r.standard_normal((cfg.intermediate, cfg.hidden)) * 0.5,
+        up_proj=r.standard_normal((cfg.intermediate, cfg.hidden)) * 0.5,
+        down_proj=r.standard_normal((cfg.hidden, cfg.intermediate)) * 0.3,
+        q_norm=1.0 + 0.6 * r.standard_normal(cfg.head_dim), k_norm=1.0 + 0.6 * r.standard_normal(cfg.head_dim),
+        input_layernorm=1.0 + 0.2 * r.standard_normal(cfg.hidden),
+        post_attention_layernorm=1.0 + 0.2 * r.standard_normal(cfg.hidden))
+    x = r.standard_normal((3, cfg.hidden))
+    pos = np.array([[0, 3, 5], [0, 1, 7], [0, 4, 2]])       # (t, h, w) per token, all axes distinct
+    c, s = O.rope_cos_sin(pos, cfg.head_dim, cfg.rope_theta, cfg.mrope_section, F64)
+    got = O.decoder_layer(x, w, c, s, cfg)
+    want = _hand_layer(x, w, pos, cfg)
+    np.testing.assert_allclose(got, want, rtol=1e-9, atol=1e-10)
+    scale = np.linalg.norm(want - x)     # size of what the layer adds
+    for kw in ({"swap_gate_up": True}, {"qk_norm": "none"}, {"qk_norm": "after_rope"}):
+        wrong = _hand_layer(x, w, pos, cfg, **kw)
+        assert np.linalg.norm(wrong - want) > 1e-3 * scale, kw
