@@ -63,11 +63,13 @@ H3ENC_API h3enc_status h3enc_op_gemm_trace_next(void *trace, int64_t trace_entri
 
 /* Profiling aid: the next attention launch on this host thread (through
  * h3enc_op_attention or inside an encode) records a timeline per persistent CTA
- * (one per SM, at most one per work item; work items = heads * sum over
- * sequences of ceil(len / 256)).  CTA c writes 9 entries at trace[c * 9]:
- * 0 start and 6 end as %globaltimer ns; 1 set-up done, 2 first Q tiles landed,
- * 3 first score tile ready, 4 last P written, 5 last P V product done as SM
- * clock64 cycles; then 7 the SM id and 8 the number of key tiles processed.
+ * (one per SM, at most one per work item, or per CTA of a pair; work items =
+ * heads * sum over sequences of ceil(len / 256)).  Causal attention at head_dim
+ * 128 runs on CTA pairs: both CTAs of a pair run the same items.  CTA c writes 9
+ * entries at trace[c * 9]: 0 start and 6 end as %globaltimer ns; 1 set-up done,
+ * 2 first Q tiles landed (the MMA-issuing CTA only), 3 first score tile ready,
+ * 4 last P written, 5 last P V product done as SM clock64 cycles; then 7 the SM
+ * id and 8 the number of key tiles processed (by the CTA's pair, on pairs).
  * trace: device uint64 of at least 9 * ctas entries (ctas >= the SM count
  * covers every launch), alive until that launch has run. */
 H3ENC_API h3enc_status h3enc_op_attention_trace_next(void *trace, int64_t trace_entries, int32_t ctas);
@@ -98,8 +100,10 @@ H3ENC_API int64_t h3enc_op_gemm_workspace_bytes(void);
  * loads the library until the process exits.  The caller passes inputs and
  * outputs only; nothing is allocated or freed.
  *   - The first call on a device looks up the array's device address and clears
- *     its flags (a synchronous memset): make that first call before any stream
- *     capture.  Later calls only launch the kernel.
+ *     its flags with a memset queued on `stream` ahead of the kernel (no host or
+ *     device synchronisation).  While `stream` is being captured that first call
+ *     is refused (H3ENC_ERR_UNSUPPORTED): make it outside any capture.  Later
+ *     calls only launch the kernel.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents: calls that overlap on the GPU (other streams, other threads)
  *     race and corrupt each other's results; serialise them.

@@ -34,8 +34,10 @@ thread_local char g_error[256];
 
 // Device address of the scratch array on the current device.  The first call on
 // a device looks the address up (the host-side name is only a stand-in) and
-// zero-fills the flags; later calls return the cached address.
-h3enc_status scratch_for_current_device(unsigned char **out) {
+// zero-fills the flags with a memset ordered on the caller's stream (no device-wide
+// synchronisation); it refuses to run while that stream is being captured.  Later
+// calls return the cached address.
+h3enc_status scratch_for_current_device(cudaStream_t stream, unsigned char **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) {
@@ -48,6 +50,18 @@ h3enc_status scratch_for_current_device(unsigned char **out) {
     }
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     if (!g_scratch_addr[dev]) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        e = cudaStreamIsCapturing(stream, &cs);
+        if (e != cudaSuccess) {
+            snprintf(g_error, sizeof g_error, "gemm_noalloc: cannot query the stream: %s", cudaGetErrorString(e));
+            return H3ENC_ERR_CUDA;
+        }
+        if (cs != cudaStreamCaptureStatusNone) {
+            snprintf(g_error, sizeof g_error,
+                     "gemm_noalloc: the first call on device %d sets up the scratch array and cannot run "
+                     "inside a stream capture; make one call on this device before capturing", dev);
+            return H3ENC_ERR_UNSUPPORTED;
+        }
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_gemm_scratch);
         if (e != cudaSuccess || !p) {
@@ -56,8 +70,7 @@ h3enc_status scratch_for_current_device(unsigned char **out) {
         }
         // a flag equal to the epoch of a launch means "partial written": flags, epoch and counter
         // start from zero
-        e = cudaMemset(static_cast<unsigned char *>(p) + kFlagOffset, 0, kFlagWords * sizeof(uint32_t));
-        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        e = cudaMemsetAsync(static_cast<unsigned char *>(p) + kFlagOffset, 0, kFlagWords * sizeof(uint32_t), stream);
         if (e != cudaSuccess) {
             snprintf(g_error, sizeof g_error, "gemm_noalloc: clearing the flags failed: %s", cudaGetErrorString(e));
             return H3ENC_ERR_CUDA;
@@ -106,7 +119,7 @@ H3ENC_API h3enc_status h3enc_op_gemm_noalloc(const void *A, const void *W, void 
         return H3ENC_ERR_UNSUPPORTED;
     }
     unsigned char *scratch = nullptr;
-    h3enc_status s = scratch_for_current_device(&scratch);
+    h3enc_status s = scratch_for_current_device(static_cast<cudaStream_t>(stream), &scratch);
     if (s != H3ENC_OK) return s;
     CUtensorMap ta, tw;
     if (!h3::make_tmap_rows(&ta, A, M, K, h3::gemm_box_rows_a()) ||
