@@ -7,7 +7,7 @@ import pytest
 
 import oracle as O
 import workloads as W
-from _harness import GPU_STORAGE, bits_to_f32, make_encoder, oracle_embed, oracle_layer_getter, rel_l2, t2f, within
+from _harness import GPU_STORAGE, bits_to_f32, make_encoder, oracle_embed, oracle_layer_getter, rel_l2, t2f, parity
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -166,7 +166,7 @@ def test_fp8_encode_tiny_model_against_fp8_oracle():
     ref8 = O.forward(x0, inp["positions"], cfg, ws.__getitem__, inp["visual_mask"], dsf, fp8=True)
     ref8bf = O.forward(x0, inp["positions"], cfg, ws.__getitem__, inp["visual_mask"], dsf, fp8=True,
                        storage=GPU_STORAGE)
-    ok, msg = within(t2f(out8), ref8, ref8bf, 2e-2, 0.05)
+    ok, msg = parity("fp8 tiny encode", t2f(out8), ref8, ref8bf, 2e-2, 0.05)
     assert ok, "fp8 encode vs fp8 oracle: " + msg
     # the FP8 model departs from the bf16 one by its quantisation error, as the oracle's does
     ref = O.forward(x0, inp["positions"], cfg, ws.__getitem__, inp["visual_mask"], dsf)
@@ -198,7 +198,7 @@ def test_fp8_one_full_width_layer_against_fp8_oracle():
     w = oracle_layer_getter(wl, cfg)(0)
     ref8 = O.forward(x0, inp["positions"], cfg, lambda _: w, fp8=True)
     ref8bf = O.forward(x0, inp["positions"], cfg, lambda _: w, fp8=True, storage=GPU_STORAGE)
-    ok, msg = within(got, ref8, ref8bf, 5e-3)
+    ok, msg = parity("fp8 one full-width layer", got, ref8, ref8bf, 5e-3)
     assert ok, "fp8 layer vs fp8 oracle: " + msg
 
 
@@ -229,5 +229,5 @@ def test_fp8_packed_prompts_two_full_width_layers():
     ws = [get(l) for l in range(cfg.num_layers)]
     ref8 = O.forward(x0, inp["positions"], cfg, ws.__getitem__, cu_seqlens=cu, fp8=True)
     ref8bf = O.forward(x0, inp["positions"], cfg, ws.__getitem__, cu_seqlens=cu, fp8=True, storage=GPU_STORAGE)
-    ok, msg = within(got, ref8, ref8bf, 2e-2, 0.05)
+    ok, msg = parity("fp8 packed prompts, 2 layers", got, ref8, ref8bf, 2e-2, 0.05)
     assert ok, "fp8 packed prompts vs fp8 oracle: " + msg

@@ -8,7 +8,7 @@ import pytest
 
 import oracle as O
 import workloads as W
-from _harness import GPU_STORAGE, bits_to_f32, make_encoder, oracle_layer_getter, t2f, within
+from _harness import GPU_STORAGE, bits_to_f32, make_encoder, oracle_layer_getter, t2f, parity
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -79,5 +79,5 @@ def test_multimodal_encode_from_ids_against_oracle():
     dsf = bits_to_f32(ds_bits)
     ref = O.forward(x0, pos, cfg, ws.__getitem__, mask, dsf)
     refbf = O.forward(x0, pos, cfg, ws.__getitem__, mask, dsf, storage=GPU_STORAGE)
-    ok, msg = within(got, ref, refbf, 2e-2, 0.05)
+    ok, msg = parity("multimodal encode from ids", got, ref, refbf, 2e-2, 0.05)
     assert ok, msg
