@@ -422,7 +422,12 @@ def kernel_timeline(name, traces):
             rel = np.where(t > 0, (t - t0) / 1e3, np.nan)
             leaders = ~np.isnan(rel[:, 4])   # the CTAs that issue the MMAs (one per pair)
             rows.append({"span_us": float(np.nanmax(rel[:, 10])),
+                         "ready_us_median": float(np.nanmedian(rel[:, 1])),
+                         "first_mma_us_median": float(np.nanmedian(rel[leaders, 3])) if leaders.any() else None,
+                         "split_acc_ready_us_median": (float(np.nanmedian(rel[:, 6]))
+                                                       if not np.all(np.isnan(rel[:, 6])) else None),
                          "last_mma_us_median": float(np.nanmedian(rel[leaders, 4])) if leaders.any() else None,
+                         "last_mma_us_min": float(np.nanmin(rel[leaders, 4])) if leaders.any() else None,
                          "last_mma_us_max": float(np.nanmax(rel[leaders, 4])) if leaders.any() else None,
                          "last_tile_epilogue_us_median": float(np.nanmedian(rel[:, 5] - rel[:, 2])),
                          "stream_k_reduce_done_us_max": (float(np.nanmax(rel[:, 9]))

@@ -63,13 +63,11 @@ H3ENC_API h3enc_status h3enc_op_gemm_trace_next(void *trace, int64_t trace_entri
 
 /* Profiling aid: the next attention launch on this host thread (through
  * h3enc_op_attention or inside an encode) records a timeline per persistent CTA
- * (one per SM, at most one per work item, or per CTA of a pair; work items =
- * heads * sum over sequences of ceil(len / 256)).  Causal attention at head_dim
- * 128 runs on CTA pairs: both CTAs of a pair run the same items.  CTA c writes 9
- * entries at trace[c * 9]: 0 start and 6 end as %globaltimer ns; 1 set-up done,
- * 2 first Q tiles landed (the MMA-issuing CTA only), 3 first score tile ready,
- * 4 last P written, 5 last P V product done as SM clock64 cycles; then 7 the SM
- * id and 8 the number of key tiles processed (by the CTA's pair, on pairs).
+ * (one per SM, at most one per work item; work items = heads * sum over
+ * sequences of ceil(len / 256)).  CTA c writes 9 entries at trace[c * 9]:
+ * 0 start and 6 end as %globaltimer ns; 1 set-up done, 2 first Q tiles landed,
+ * 3 first score tile ready, 4 last P written, 5 last P V product done as SM
+ * clock64 cycles; then 7 the SM id and 8 the number of key tiles processed.
  * trace: device uint64 of at least 9 * ctas entries (ctas >= the SM count
  * covers every launch), alive until that launch has run. */
 H3ENC_API h3enc_status h3enc_op_attention_trace_next(void *trace, int64_t trace_entries, int32_t ctas);

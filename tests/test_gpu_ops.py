@@ -282,6 +282,7 @@ def test_qkv_projection_with_fused_norm_rope(d, nq, nkv, M, K, split):
     (64, 4, 1, [0, 1, 130, 131, 300]),
     (128, 16, 2, [0, 1024]),
     (128, 8, 8, [0, 77, 77, 333, 600]),
+    (128, 4, 1, [0, 1, 130, 131, 900]),
 ])
 def test_attention(d, nq, nkv, cu):
     S = cu[-1]
