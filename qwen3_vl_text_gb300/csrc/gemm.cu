@@ -64,11 +64,12 @@ constexpr int kMinStreamKBlocks = 4;             // smallest k-range a stream-K 
 // cost of the stream-K partial exchange in k-block times (about 0.36 us each): behind
 // data-parallel tiles, and alone (measured: ~3 us and ~15 us of the launch)
 constexpr long long kSkFixupHidden = 8, kSkFixupExposed = 40;
-// A bf16 launch of this many full waves or more runs unsplit.  Beside the split's exchange, its
+// A launch of this many full waves or more runs unsplit.  Beside the split's exchange, its
 // parts read k-ranges no other pair reads (cold, from DRAM) and its fix-up runs beside the
 // mainloop, which then loses about 6-17 us whatever the launch's length (per-CTA timelines at
 // seq 1024): more than a split saves at the end of a long launch (gate/up, ten and a half waves:
-// 303 us unsplit against 309 us split), less than it saves in the one- and two-wave projections.
+// 303 us unsplit against 309 us split in bf16, 166 against 176 us in e4m3), less than it saves
+// in the one- and two-wave projections.
 constexpr long long kSkMaxFullWaves = 8;
 static_assert(BM * BN % 4 == 0, "partials are written as float4");
 
@@ -1122,8 +1123,8 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     // at least kMinStreamKBlocks per pair; when that leaves one tile per pair it stays data-parallel.
     // The split is kept only where it shortens the launch (in k-block times): the pair's share of
     // the tail plus the partial exchange (hidden behind the data-parallel tiles when there are
-    // some, exposed when the tail is all there is) against one more whole tile; long bf16
-    // launches (kSkMaxFullWaves) run unsplit.
+    // some, exposed when the tail is all there is) against one more whole tile; long launches
+    // (kSkMaxFullWaves) run unsplit.
     const int left = tiles % pairs;
     int sk_pairs = 0;
     if (p.part && p.flags && left) {
@@ -1134,7 +1135,7 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
         if (ps > left) {
             const long long full = tiles / pairs;
             const long long sk_cost = full * g.nk + (work + ps - 1) / ps + (full ? kSkFixupHidden : kSkFixupExposed);
-            if (sk_cost < (full + 1) * g.nk && (F8 || full < kSkMaxFullWaves)) sk_pairs = (int)ps;
+            if (sk_cost < (full + 1) * g.nk && full < kSkMaxFullWaves) sk_pairs = (int)ps;
         }
     }
     g.sk_pairs = sk_pairs;
