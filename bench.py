@@ -268,18 +268,19 @@ def run_kernel(args):
         Wt = rnd("W", (cfg.qkv_out, H))
         G = rnd("g", (d,), 1.0)
         pos = torch.arange(S, dtype=torch.int32, device=dev).repeat(3, 1).contiguous()
-        c = torch.empty(S, d // 2, device=dev)
+        # the encoder's table layout: row-interleaved, rows padded to a multiple of 32
+        stride = (S + 31) // 32 * 32
+        c = torch.empty(stride * d // 2, device=dev)
         s_ = torch.empty_like(c)
-        Q.h3enc_op_rope_table(pos, S, d, cfg.rope_theta, cfg.mrope_section, c, s_)
+        Q.h3enc_op_rope_table_ex(pos, S, d, cfg.rope_theta, cfg.mrope_section, stride, c, s_)
         C = torch.empty(S, cfg.qkv_out, dtype=torch.bfloat16, device=dev)
         ws = torch.zeros(Q.h3enc_op_gemm_workspace_bytes(), dtype=torch.uint8, device=dev)
+        ss = None
         if args.fold:   # the input RMSNorm folded in: rows scaled by the statistics of A
             ss = torch.empty(H // 128, S, dtype=torch.float32, device=dev)
             Q.h3enc_op_row_sumsq(A, S, H, ss)
-            fn = lambda: Q.h3enc_op_gemm_qkv_rope_rms(A, Wt, C, S, H, nq, nkv, d, G, G, 1e-6, c, s_, ss, 1e-6,
-                                                      workspace=ws)
-        else:
-            fn = lambda: Q.h3enc_op_gemm_qkv_rope(A, Wt, C, S, H, nq, nkv, d, G, G, 1e-6, c, s_, workspace=ws)
+        fn = lambda: Q.h3enc_op_gemm_qkv_rope_ex(A, Wt, C, S, H, nq, nkv, d, G, G, 1e-6, c, s_, stride, ss_in=ss,
+                                                 in_eps=1e-6, workspace=ws)
         work, unit = 2.0 * S * cfg.qkv_out * H / 1e12, "TFLOP/s"
     elif name.startswith("gemm_"):
         shapes = {"gemm_o": (H, nq * d, Q.EPI_RESIDUAL),
@@ -344,6 +345,14 @@ def run_kernel(args):
         Xo = torch.empty(S, H, dtype=torch.bfloat16, device=dev)
         fn = lambda: Q.h3enc_op_embed(ids, table, cfg.vocab, H, Xo, S)
         work, unit = (4 * S + 2.0 * S * H * 2) / 1e9, "GB/s"
+    elif name == "layernorm":   # the vision tower's block norm: x [S, 1024] read, y written, w and b read
+        D = W.VISION_FULL.hidden
+        X = rnd("x", (S, D), 1.0)
+        G = rnd("g", (D,), 1.0)
+        B = rnd("b", (D,), 0.1)
+        Y = torch.empty_like(X)
+        fn = lambda: Q.h3enc_op_layernorm(X, G, B, Y, S, D, 1e-6)
+        work, unit = (2.0 * S * D * 2 + 2 * 2 * D) / 1e9, "GB/s"
     elif name == "rope_table":   # positions read, fp32 cos/sin [S, d/2] written
         pos = torch.arange(S, dtype=torch.int32, device=dev).repeat(3, 1).contiguous()
         c = torch.empty(S, d // 2, device=dev)
@@ -688,7 +697,7 @@ def main():
     ap.add_argument("--kernel", default=None,
                     help="time one kernel alone: gemm_qkv (with the fused q/k norm + M-RoPE), gemm_o, "
                          "gemm_gate_up, gemm_down, attention, rmsnorm, rmsnorm_q8, quant_rows, row_sumsq, embed, "
-                         "rope_table")
+                         "rope_table, layernorm (the vision tower's, 1024 columns; --seq 3072 for one 48x64 image)")
     ap.add_argument("--seq", type=int, default=1024)
     ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=[2, 3, 4],
                     help="2: 50-layer seq-1024 image layout (the headline); 3: seq-8192 video layout; "

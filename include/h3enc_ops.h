@@ -165,6 +165,18 @@ H3ENC_API h3enc_status h3enc_op_rope_table(const int32_t *positions, int32_t S, 
                                  const int32_t *section_host, float *cos_tab, float *sin_tab,
                                  void *stream);
 
+/* h3enc_op_rope_table with a choice of layout.  stride == 0: [S, head_dim/2] as above.
+ * stride >= S (head_dim % 8 == 0): row-interleaved, the layout the encoder uses,
+ *   cos_tab[((j/4) * stride + s) * 4 + j%4] = cos(ang(s, j))   (same for sin_tab),
+ * i.e. [head_dim/8][stride][4]: for each group of four frequencies the rows follow one
+ * another, so 32 consecutive rows read one group as 512 contiguous bytes.  Rows s >= S of
+ * the padding are not written.  Each table holds stride * head_dim/2 floats (16-byte
+ * aligned); a stride that is a multiple of 32 keeps every 32-row run on whole lines.
+ * INVALID_ARG for 0 < stride < S or head_dim % 8 with stride > 0. */
+H3ENC_API h3enc_status h3enc_op_rope_table_ex(const int32_t *positions, int32_t S, int32_t head_dim, float theta,
+                                    const int32_t *section_host, int32_t stride, float *cos_tab,
+                                    float *sin_tab, void *stream);
+
 /* QKV projection with the per-head q/k RMSNorm and M-RoPE fused into the GEMM
  * epilogue (page "... encoder.py", MiniMaxH3Qwen3VLTextAttention.forward: the
  * q/k/v projections, q_norm/k_norm over head_dim, then _apply_rotary_pos_emb):
@@ -205,6 +217,17 @@ H3ENC_API h3enc_status h3enc_op_gemm_rms(const void *A, const void *W, void *C, 
                                          int32_t epilogue, const void *R, const float *ss_in, float *ss_out,
                                          float eps, void *workspace, int64_t workspace_bytes, int32_t *status,
                                          void *stream);
+
+/* h3enc_op_gemm_qkv_rope reading tables of either layout of h3enc_op_rope_table_ex:
+ * cs_stride == 0 for [M, d/2], else the row-interleaved tables of that stride (>= M).
+ * ss_in (optional, NULL: none) and in_eps as for h3enc_op_gemm_qkv_rope_rms.  The output is
+ * the same, bit for bit, in both layouts; the row-interleaved one is faster (the epilogue's
+ * table loads are whole lines). */
+H3ENC_API h3enc_status h3enc_op_gemm_qkv_rope_ex(const void *A, const void *W, void *C, int32_t M, int32_t K,
+                                       int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, const void *w_q,
+                                       const void *w_k, float eps, const float *cos_tab, const float *sin_tab,
+                                       int32_t cs_stride, const float *ss_in, float in_eps, void *workspace,
+                                       int64_t workspace_bytes, int32_t *status, void *stream);
 
 /* h3enc_op_gemm_qkv_rope with the folded input norm: each row of A * W^T is first
  * multiplied by 1/sqrt(sum_s ss_in[s][r] / K + in_eps) (ss_in [K/128, M], required), then

@@ -21,7 +21,8 @@ __all__ = [
     "h3enc_set_graphs", "h3enc_graph_count",
     "h3enc_build_positions", "h3enc_aggregate_deepstack",
     "h3enc_op_gemm", "h3enc_op_gemm_workspace_bytes", "h3enc_op_gemm_trace_next", "h3enc_op_attention_trace_next", "h3enc_op_gemm_noalloc", "h3enc_op_gemm_noalloc_scratch_bytes", "h3enc_op_pack_gate_up", "h3enc_op_rmsnorm", "h3enc_op_gemm_fp8", "h3enc_op_quant_rows",
-    "h3enc_op_rmsnorm_q8", "h3enc_op_wait_probe", "h3enc_op_rope_table",
+    "h3enc_op_rmsnorm_q8", "h3enc_op_wait_probe", "h3enc_op_rope_table", "h3enc_op_rope_table_ex",
+    "h3enc_op_gemm_qkv_rope_ex",
     "h3enc_op_gemm_qkv_rope", "h3enc_op_gemm_qkv_rope_rms", "h3enc_op_gemm_rms", "h3enc_op_row_sumsq",
     "h3enc_op_fold_cols", "h3enc_op_layernorm", "h3enc_op_vision_pos_embed", "h3enc_op_vision_rope_table",
     "h3enc_op_gemm_bias", "h3enc_op_gemm_qkv_rope_bias", "h3enc_op_attention_bidir", "VisionConfig",
@@ -111,6 +112,9 @@ _SIGS = {
     "h3enc_op_wait_probe": ([_P, ctypes.c_uint32, _I32, _P, _P], _I32),
     "h3enc_op_rmsnorm_q8": ([_P, _P, _P, _P, _I32, _I32, _F, _P], _I32),
     "h3enc_op_rope_table": ([_P, _I32, _I32, _F, ctypes.POINTER(_I32), _P, _P, _P], _I32),
+    "h3enc_op_rope_table_ex": ([_P, _I32, _I32, _F, ctypes.POINTER(_I32), _I32, _P, _P, _P], _I32),
+    "h3enc_op_gemm_qkv_rope_ex": ([_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _F, _P, _P, _I32, _P, _F, _P,
+                                   _I64, _P, _P], _I32),
     "h3enc_op_gemm_qkv_rope_rms": ([_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _F, _P, _P, _P, _F, _P, _I64,
                                     _P, _P], _I32),
     "h3enc_op_gemm_rms": ([_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _F, _P, _I64, _P, _P], _I32),
@@ -399,6 +403,20 @@ def h3enc_op_rmsnorm(x, w, y, rows, cols, eps, stream=None):
 def h3enc_op_rope_table(positions, S, head_dim, theta, section, cos_tab, sin_tab, stream=None):
     return _check(lib.h3enc_op_rope_table(_ptr(positions), S, head_dim, theta, _host_i32(section), _ptr(cos_tab),
                                           _ptr(sin_tab), _stream(stream)))
+
+
+def h3enc_op_rope_table_ex(positions, S, head_dim, theta, section, stride, cos_tab, sin_tab, stream=None):
+    return _check(lib.h3enc_op_rope_table_ex(_ptr(positions), S, head_dim, theta, _host_i32(section), stride,
+                                             _ptr(cos_tab), _ptr(sin_tab), _stream(stream)))
+
+
+def h3enc_op_gemm_qkv_rope_ex(A, W, C, M, K, n_heads, n_kv_heads, head_dim, w_q, w_k, eps, cos_tab, sin_tab,
+                              cs_stride, ss_in=None, in_eps=0.0, workspace=None, status=None, stream=None):
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return _check(lib.h3enc_op_gemm_qkv_rope_ex(_ptr(A), _ptr(W), _ptr(C), M, K, n_heads, n_kv_heads, head_dim,
+                                                _ptr(w_q), _ptr(w_k), eps, _ptr(cos_tab), _ptr(sin_tab), cs_stride,
+                                                _ptr(ss_in), in_eps, _ptr(workspace), wbytes, _ptr(status),
+                                                _stream(stream)))
 
 
 def h3enc_op_gemm_qkv_rope(A, W, C, M, K, n_heads, n_kv_heads, head_dim, w_q, w_k, eps, cos_tab, sin_tab,

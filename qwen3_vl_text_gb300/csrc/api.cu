@@ -436,7 +436,9 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         e = cudaMemcpyAsync(out, embeds, (size_t)S * H * 2, cudaMemcpyDeviceToDevice, st);
         if (e != cudaSuccess) return cuda_fail(h, e, "input copy");
     }
-    e = run(h, H3ENC_K_PREP, st, [&] { return h3::launch_rope_table(pos, S, h->rope, h->cos_t, h->sin_t, st); });
+    // row-interleaved: the QKV epilogue's warps read them as whole lines
+    e = run(h, H3ENC_K_PREP, st,
+            [&] { return h3::launch_rope_table(pos, S, h->rope, h->cos_t, h->sin_t, st, h3::cs_stride(S)); });
     if (e != cudaSuccess) return cuda_fail(h, e, "rope table");
     const bool use_ds = nds > 0 && n_vis > 0;
     const bool use_ve = visual_embeds != nullptr && n_vis > 0;
@@ -506,7 +508,7 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
         p.sw = f8 ? w8->s_qkv : nullptr;
         p.N = h->qkv_out; p.K = H; p.epi = h3::EPI_QKROPE;
         p.C = h->qkv; p.ldc = h->qkv_out;
-        p.wq = w.q_norm; p.wk = w.k_norm; p.cos_t = h->cos_t; p.sin_t = h->sin_t;
+        p.wq = w.q_norm; p.wk = w.k_norm; p.cos_t = h->cos_t; p.sin_t = h->sin_t; p.cs_rows = h3::cs_stride(S);
         p.head_dim = d; p.nq = nq; p.nkv = nkv; p.eps = c.rms_eps;
         e = run(h, H3ENC_K_GEMM_QKV, st, [&] { return h3::launch_gemm(p, st); });
         if (e != cudaSuccess) return cuda_fail(h, e, "qkv gemm");
@@ -522,7 +524,7 @@ h3enc_status encode_core(h3enc *h, const int32_t *ids, const bf16 *embeds, int l
             });
             if (e != cudaSuccess) return cuda_fail(h, e, "attention output quantisation");
         }
-        p.wq = p.wk = nullptr; p.cos_t = p.sin_t = nullptr;
+        p.wq = p.wk = nullptr; p.cos_t = p.sin_t = nullptr; p.cs_rows = 0;
         p.tmA = f8 ? &h->tm_attn8 : &h->tm_attn;
         p.tmW = f8 ? &w8->tm_o : &w.tm_o;
         p.sa = f8 ? h->sattn : nullptr;
@@ -635,7 +637,7 @@ h3enc_status h3enc_create(const h3enc_config *cfg, h3enc **out) {
     const size_t T = c.max_tokens, H = c.hidden;
     const size_t b_y = align256(T * H * 2), b_qkv = align256(T * h->qkv_out * 2),
                  b_attn = align256(T * c.n_heads * c.head_dim * 2), b_act = align256(T * c.intermediate * 2),
-                 b_cs = align256(T * (c.head_dim / 2) * 4), b_rank = align256(T * 4), b_stat = 256,
+                 b_cs = align256((size_t)h3::cs_stride((int)T) * (c.head_dim / 2) * 4), b_rank = align256(T * 4), b_stat = 256,
                  b_ids = align256(T * 4), b_pos = align256(3 * T * 4), b_mask = align256(T),
                  b_ds = align256((size_t)c.num_deepstack * T * H * 2), b_out = b_y,
                  b_gemm = align256(h3::gemm_workspace_bytes(h->num_sms)), b_ss = align256(T * (H / 128) * 4);
@@ -1308,6 +1310,21 @@ h3enc_status h3enc_op_rope_table(const int32_t *positions, int32_t S, int32_t he
     return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "rope_table launch");
 }
 
+h3enc_status h3enc_op_rope_table_ex(const int32_t *positions, int32_t S, int32_t head_dim, float theta,
+                                    const int32_t *section_host, int32_t stride, float *cos_tab, float *sin_tab,
+                                    void *stream) {
+    if (stride == 0) return h3enc_op_rope_table(positions, S, head_dim, theta, section_host, cos_tab, sin_tab, stream);
+    if (!positions || !section_host || !cos_tab || !sin_tab || S < 0 || stride < S || head_dim < 8 ||
+        head_dim > 128 || head_dim % 8 || !(theta > 0.f) || (reinterpret_cast<uintptr_t>(cos_tab) & 15) ||
+        (reinterpret_cast<uintptr_t>(sin_tab) & 15))
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "rope_table_ex: bad args");
+    h3::RopeParams rp;
+    h3::make_rope_params(&rp, head_dim, theta, section_host);
+    cudaError_t e =
+        h3::launch_rope_table(positions, S, rp, cos_tab, sin_tab, static_cast<cudaStream_t>(stream), stride);
+    return e == cudaSuccess ? H3ENC_OK : cuda_fail(nullptr, e, "rope_table_ex launch");
+}
+
 }  // extern "C"
 
 namespace {
@@ -1315,8 +1332,12 @@ namespace {
 h3enc_status qkv_rope_op(const void *A, const void *W, void *C, int32_t M, int32_t K, int32_t n_heads,
                          int32_t n_kv_heads, int32_t head_dim, const void *w_q, const void *w_k, float eps,
                          const float *cos_tab, const float *sin_tab, const float *ss_in, float in_eps,
-                         void *workspace, int64_t workspace_bytes, int32_t *status, void *stream) {
+                         void *workspace, int64_t workspace_bytes, int32_t *status, void *stream,
+                         int32_t cs_stride = 0) {
     const int64_t N = (int64_t)(n_heads + 2 * n_kv_heads) * head_dim;
+    if (cs_stride && (cs_stride < M || (reinterpret_cast<uintptr_t>(cos_tab) & 15) ||
+                      (reinterpret_cast<uintptr_t>(sin_tab) & 15)))
+        return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm_qkv_rope: table stride below M or tables misaligned");
     if (ss_in && K % 128)
         return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm_qkv_rope: row statistics need K %% 128 == 0");
     if (M < 0 || K <= 0 || K % 8 || n_heads < 1 || n_kv_heads < 1 || (head_dim != 64 && head_dim != 128) ||
@@ -1335,7 +1356,7 @@ h3enc_status qkv_rope_op(const void *A, const void *W, void *C, int32_t M, int32
     p.status = status;
     p.num_sms = h3::device_num_sms();
     p.wq = static_cast<const bf16 *>(w_q); p.wk = static_cast<const bf16 *>(w_k);
-    p.cos_t = cos_tab; p.sin_t = sin_tab;
+    p.cos_t = cos_tab; p.sin_t = sin_tab; p.cs_rows = cs_stride;
     p.head_dim = head_dim; p.nq = n_heads; p.nkv = n_kv_heads; p.eps = eps;
     p.ss_in = ss_in;
     p.norm_eps = in_eps;
@@ -1371,6 +1392,16 @@ h3enc_status h3enc_op_gemm_qkv_rope_rms(const void *A, const void *W, void *C, i
     if (!ss_in) return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm_qkv_rope_rms: ss_in is NULL");
     return qkv_rope_op(A, W, C, M, K, n_heads, n_kv_heads, head_dim, w_q, w_k, eps, cos_tab, sin_tab, ss_in, in_eps,
                        workspace, workspace_bytes, status, stream);
+}
+
+h3enc_status h3enc_op_gemm_qkv_rope_ex(const void *A, const void *W, void *C, int32_t M, int32_t K,
+                                       int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, const void *w_q,
+                                       const void *w_k, float eps, const float *cos_tab, const float *sin_tab,
+                                       int32_t cs_stride, const float *ss_in, float in_eps, void *workspace,
+                                       int64_t workspace_bytes, int32_t *status, void *stream) {
+    if (cs_stride < 0) return fail(nullptr, H3ENC_ERR_INVALID_ARG, "gemm_qkv_rope_ex: negative table stride");
+    return qkv_rope_op(A, W, C, M, K, n_heads, n_kv_heads, head_dim, w_q, w_k, eps, cos_tab, sin_tab, ss_in, in_eps,
+                       workspace, workspace_bytes, status, stream, cs_stride);
 }
 
 h3enc_status h3enc_op_attention(const void *qkv, void *o, int32_t S, int32_t n_heads, int32_t n_kv_heads,

@@ -114,59 +114,78 @@ __global__ void __launch_bounds__(QT) quant_rows_amax_kernel(const bf16 *__restr
 }
 
 // RMSNorm of one row kept in registers (cols <= 8192), rounded to bf16, then quantised.
-constexpr int NQ_VPT = 4;   // 4 x 8 elements per thread -> cols <= 8192
-__global__ void __launch_bounds__(QT) rmsnorm_q8_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
-                                                        uint8_t *__restrict__ q, float *scale, int cols,
-                                                        float eps) {
+// 128 threads per row, each holding VPT 16-byte vectors of x and of the norm weight (both
+// loaded before the first reduction); the bf16 output overwrites x in place (packed, exact),
+// so the row costs 8 registers per vector and a 5120-wide row fits one wave of CTAs.
+constexpr int NQ_T = 128;
+template <int VPT>
+__global__ void __launch_bounds__(NQ_T) rmsnorm_q8_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
+                                                          uint8_t *__restrict__ q, float *scale, int cols,
+                                                          float eps) {
     pdl_trigger();
     pdl_wait();
-    __shared__ float red[QT / 32];
+    __shared__ float red[2][NQ_T / 32];
     const int row = blockIdx.x;
     const int nvec = cols >> 3;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)row * cols);
     const uint4 *wr = reinterpret_cast<const uint4 *>(w);
-    float f[NQ_VPT][8];
+    uint4 xv[VPT], gv[VPT];
+    #pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int idx = threadIdx.x + i * NQ_T;
+        xv[i] = idx < nvec ? xr[idx] : make_uint4(0u, 0u, 0u, 0u);
+        gv[i] = idx < nvec ? wr[idx] : make_uint4(0u, 0u, 0u, 0u);
+    }
     float ss = 0.f;
     #pragma unroll
-    for (int i = 0; i < NQ_VPT; ++i) {
-        const int idx = threadIdx.x + i * QT;
-        if (idx < nvec) {
-            unpack8(xr[idx], f[i]);
-            #pragma unroll
-            for (int k = 0; k < 8; ++k) ss = fmaf(f[i][k], f[i][k], ss);
-        }
+    for (int i = 0; i < VPT; ++i) {
+        float f[8];
+        unpack8(xv[i], f);
+        #pragma unroll
+        for (int k = 0; k < 8; ++k) ss = fmaf(f[k], f[k], ss);
     }
     #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    if (lane == 0) red[0][warp] = ss;
     __syncthreads();
     float tot = 0.f;
     #pragma unroll
-    for (int i = 0; i < QT / 32; ++i) tot += red[i];
+    for (int i = 0; i < NQ_T / 32; ++i) tot += red[0][i];
     const float rstd = 1.0f / sqrtf(tot / (float)cols + eps);
-    __syncthreads();   // red is reused by the max below
     float amax = 0.f;
     #pragma unroll
-    for (int i = 0; i < NQ_VPT; ++i) {
-        const int idx = threadIdx.x + i * QT;
-        if (idx < nvec) {
-            float g[8];
-            unpack8(wr[idx], g);
-            #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                f[i][k] = round_bf16(f[i][k] * rstd * g[k]);   // the norm's bf16 output
-                amax = fmaxf(amax, fabsf(f[i][k]));
-            }
+    for (int i = 0; i < VPT; ++i) {
+        float f[8], g[8];
+        unpack8(xv[i], f);
+        unpack8(gv[i], g);
+        uint32_t y[4];
+        #pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            const float a = round_bf16(f[k] * rstd * g[k]), b = round_bf16(f[k + 1] * rstd * g[k + 1]);
+            amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));   // the norm's bf16 output
+            y[k >> 1] = pack_bf16x2(a, b);
         }
+        xv[i] = make_uint4(y[0], y[1], y[2], y[3]);
     }
-    amax = block_max(amax, red);
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) red[1][warp] = amax;
+    __syncthreads();
+    amax = red[1][0];
+    #pragma unroll
+    for (int i = 1; i < NQ_T / 32; ++i) amax = fmaxf(amax, red[1][i]);
     const float inv = amax > 0.f ? __fdiv_rn(448.0f, amax) : 1.0f;
     if (threadIdx.x == 0) scale[row] = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
     uint2 *qr = reinterpret_cast<uint2 *>(q + (size_t)row * cols);
     #pragma unroll
-    for (int i = 0; i < NQ_VPT; ++i) {
-        const int idx = threadIdx.x + i * QT;
-        if (idx < nvec) qr[idx] = quant8(f[i], inv);
+    for (int i = 0; i < VPT; ++i) {
+        const int idx = threadIdx.x + i * NQ_T;
+        if (idx < nvec) {
+            float f[8];
+            unpack8(xv[i], f);
+            qr[idx] = quant8(f, inv);
+        }
     }
 }
 
@@ -193,10 +212,20 @@ cudaError_t launch_quant_rows_amax(const bf16 *x, int ldx, int rows, int cols, u
 cudaError_t launch_rmsnorm_q8(const bf16 *x, const bf16 *w, uint8_t *q, float *scale, int rows, int cols, float eps,
                               cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
-    if (cols % 8 || cols > QT * NQ_VPT * 8) return cudaErrorInvalidValue;
+    const int vpt = (cols / 8 + NQ_T - 1) / NQ_T;
+    if (cols % 8 || vpt < 1 || vpt > 8) return cudaErrorInvalidValue;
     cudaLaunchAttribute at[1];
-    cudaLaunchConfig_t cfg = pdl_config(dim3(rows), dim3(QT), 0, st, at);
-    return cudaLaunchKernelEx(&cfg, rmsnorm_q8_kernel, x, w, q, scale, cols, eps);
+    cudaLaunchConfig_t cfg = pdl_config(dim3(rows), dim3(NQ_T), 0, st, at);
+    switch (vpt) {
+        case 1: return cudaLaunchKernelEx(&cfg, rmsnorm_q8_kernel<1>, x, w, q, scale, cols, eps);
+        case 2: return cudaLaunchKernelEx(&cfg, rmsnorm_q8_kernel<2>, x, w, q, scale, cols, eps);
+        case 3: return cudaLaunchKernelEx(&cfg, rmsnorm_q8_kernel<3>, x, w, q, scale, cols, eps);
+        case 4: return cudaLaunchKernelEx(&cfg, rmsnorm_q8_kernel<4>, x, w, q, scale, cols, eps);
+        case 5: return cudaLaunchKernelEx(&cfg, rmsnorm_q8_kernel<5>, x, w, q, scale, cols, eps);
+        case 6: return cudaLaunchKernelEx(&cfg, rmsnorm_q8_kernel<6>, x, w, q, scale, cols, eps);
+        case 7: return cudaLaunchKernelEx(&cfg, rmsnorm_q8_kernel<7>, x, w, q, scale, cols, eps);
+        default: return cudaLaunchKernelEx(&cfg, rmsnorm_q8_kernel<8>, x, w, q, scale, cols, eps);
+    }
 }
 
 }  // namespace h3

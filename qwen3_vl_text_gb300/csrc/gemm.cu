@@ -94,6 +94,7 @@ struct GemmArgs {
     // EPI_QKROPE
     const __nv_bfloat16 *wq, *wk;
     const float *cos_t, *sin_t;
+    int cs_rows;       // 0: tables [M][head_dim/2]; > 0: [head_dim/8][cs_rows][4] (see cs_at)
     int head_dim, nq, nkv;
     float eps;
     unsigned long long *trace;   // optional [grid][TR_COUNT] %globaltimer stamps
@@ -177,6 +178,15 @@ __device__ __forceinline__ size_t part_f4(int r, int col) {
 
 // 1/rms of row `row` of A from the slot sums of squares (slots of 128 columns, added in slot
 // order: the same value for every tile of the row).
+// Element (row, j) of the rotary tables, j a multiple of 4: four consecutive frequencies are
+// one aligned float4 in either layout.  Row-interleaved ([d/8][cs_rows][4]) puts the same
+// four frequencies of consecutive rows side by side, so an epilogue warp (32 consecutive
+// rows, one per lane) reads whole lines instead of touching 32 lines per load.
+__device__ __forceinline__ size_t cs_at(const GemmArgs &g, int row, int j) {
+    return g.cs_rows ? ((size_t)(j >> 2) * g.cs_rows + row) * 4 + (j & 3)
+                     : (size_t)row * (g.head_dim >> 1) + j;
+}
+
 __device__ __forceinline__ float norm_rstd(const GemmArgs &g, int row) {
     const int slots = g.K >> 7;
     float s = 0.f;
@@ -658,16 +668,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                 const __nv_bfloat16 *w = is_q ? g.wq : g.wk;
                                 const int jb = sub * q4;           // frequency index of a[0]
                                 #pragma unroll
-                                for (int i = 0; i < 16; ++i) {
+                                for (int i = 0; i < 16; i += 4) {
                                     if (i < q4) {
-                                        const float ga = qk_norm ? __bfloat162float(w[jb + i]) : 1.f;
-                                        const float gb = qk_norm ? __bfloat162float(w[half + jb + i]) : 1.f;
-                                        const float ya = a[i] * rstd * ga;
-                                        const float yb = b[i] * rstd * gb;
-                                        const float co = g.cos_t[(size_t)row * half + jb + i];
-                                        const float si = g.sin_t[(size_t)row * half + jb + i];
-                                        a[i] = ya * co - yb * si;
-                                        b[i] = yb * co + ya * si;
+                                        const size_t ci = cs_at(g, row, jb + i);
+                                        const float4 co4 = *reinterpret_cast<const float4 *>(g.cos_t + ci);
+                                        const float4 si4 = *reinterpret_cast<const float4 *>(g.sin_t + ci);
+                                        const float cv[4] = {co4.x, co4.y, co4.z, co4.w};
+                                        const float sv[4] = {si4.x, si4.y, si4.z, si4.w};
+                                        #pragma unroll
+                                        for (int t = 0; t < 4; ++t) {
+                                            const float ga = qk_norm ? __bfloat162float(w[jb + i + t]) : 1.f;
+                                            const float gb = qk_norm ? __bfloat162float(w[half + jb + i + t]) : 1.f;
+                                            const float ya = a[i + t] * rstd * ga;
+                                            const float yb = b[i + t] * rstd * gb;
+                                            a[i + t] = ya * cv[t] - yb * sv[t];
+                                            b[i + t] = yb * cv[t] + ya * sv[t];
+                                        }
                                     }
                                 }
                             }
@@ -826,15 +842,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
             }
             if constexpr (EPI == EPI_QKROPE) {
-                // this row's cos/sin lines, pulled into L2 while the MMAs finish: by the time the
+                // the warp's cos/sin lines, pulled into L2 while the MMAs finish: by the time the
                 // accumulator is ready the streamed operands may have pushed them out
-                if (live && (n_blk * BN) / g.head_dim < g.nq + g.nkv) {
-                    const int bytes = (g.head_dim >> 1) * (int)sizeof(float);
-                    const char *cs = reinterpret_cast<const char *>(g.cos_t) + (size_t)row * bytes;
-                    const char *sn = reinterpret_cast<const char *>(g.sin_t) + (size_t)row * bytes;
-                    for (int off = ehalf * 128; off < bytes; off += 256) {
-                        prefetch_l2(cs + off);
-                        prefetch_l2(sn + off);
+                if ((n_blk * BN) / g.head_dim < g.nq + g.nkv) {
+                    const int half = g.head_dim >> 1;
+                    const float *tab = ehalf ? g.sin_t : g.cos_t;   // the two warps of a quarter split them
+                    if (g.cs_rows) {
+                        // group of four frequencies k: the warp's 32 rows are 512 contiguous bytes
+                        for (int li = lane; li < half; li += 32) {
+                            const int k = li >> 2, part = li & 3;
+                            if (row0 + 8 * part < g.M)
+                                prefetch_l2(tab + ((size_t)k * g.cs_rows + row0 + 8 * part) * 4);
+                        }
+                    } else if (live) {
+                        for (int off = 0; off < half; off += 32) prefetch_l2(tab + (size_t)row * half + off);
                     }
                 }
             }
@@ -925,12 +946,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         #pragma unroll
                         for (int i = 0; i < 16; ++i) oa[i] = ob[i] = 0u;   // rows past M: clipped by the store
                         if (live) {
-                            const float *cs = g.cos_t + (size_t)row * half + c * 32;
-                            const float *sn = g.sin_t + (size_t)row * half + c * 32;
                             #pragma unroll
                             for (int j = 0; j < 32; j += 4) {
-                                const float4 co = *reinterpret_cast<const float4 *>(cs + j);
-                                const float4 si = *reinterpret_cast<const float4 *>(sn + j);
+                                // row-interleaved tables: the warp's 32 rows load 512 contiguous bytes
+                                const size_t ci = cs_at(g, row, c * 32 + j);
+                                const float4 co = *reinterpret_cast<const float4 *>(g.cos_t + ci);
+                                const float4 si = *reinterpret_cast<const float4 *>(g.sin_t + ci);
                                 const uint2 wa = qk_norm ? *reinterpret_cast<const uint2 *>(w + c * 32 + j)
                                                          : make_uint2(0x3F803F80u, 0x3F803F80u);   // bf16 1.0
                                 const uint2 wb = qk_norm ? *reinterpret_cast<const uint2 *>(w + half + c * 32 + j)
@@ -1109,7 +1130,7 @@ cudaError_t launch_epi(const GemmPlan &p, cudaStream_t stream) {
     g.w_static = p.w_static ? 1 : 0;
     g.C = p.C; g.ldc = p.ldc; g.R = p.R; g.DS = p.DS; g.vis_rank = p.vis_rank; g.n_vis = p.n_vis;
     g.status = p.status;
-    g.wq = p.wq; g.wk = p.wk; g.cos_t = p.cos_t; g.sin_t = p.sin_t;
+    g.wq = p.wq; g.wk = p.wk; g.cos_t = p.cos_t; g.sin_t = p.sin_t; g.cs_rows = p.cs_rows;
     g.head_dim = p.head_dim; g.nq = p.nq; g.nkv = p.nkv; g.eps = p.eps;
     g.trace = p.trace;
     g.ss_in = p.ss_in;
@@ -1209,7 +1230,8 @@ cudaError_t launch_gemm(const GemmPlan &p_in, cudaStream_t stream) {
         t_trace_next = nullptr;
     }
     if (p.epi == EPI_QKROPE &&
-        ((p.head_dim != 64 && p.head_dim != 128) || (!p.wq != !p.wk) || !p.cos_t || !p.sin_t))
+        ((p.head_dim != 64 && p.head_dim != 128) || (!p.wq != !p.wk) || !p.cos_t || !p.sin_t ||
+         (p.cs_rows && p.cs_rows < p.M)))
         return cudaErrorInvalidValue;
     // a bias is read 32 columns at a time from 16-byte-aligned rows
     if (p.bias && (p.epi == EPI_SWIGLU || (reinterpret_cast<uintptr_t>(p.bias) & 15))) return cudaErrorInvalidValue;

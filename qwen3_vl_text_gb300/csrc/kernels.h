@@ -34,7 +34,8 @@ struct GemmPlan {
     uint32_t *flags;    // num_sms release flags, zero-filled once before first use
     // EPI_QKROPE: per-head RMSNorm of the q and k heads, then M-RoPE with the fp32 tables
     const bf16 *wq = nullptr, *wk = nullptr;
-    const float *cos_t = nullptr, *sin_t = nullptr;   // [M, head_dim/2]
+    const float *cos_t = nullptr, *sin_t = nullptr;   // [M, head_dim/2], or row-interleaved:
+    int cs_rows = 0;   // > 0: element (row, j) at ((j/4) * cs_rows + row) * 4 + j%4, cs_rows >= M
     int head_dim = 0, nq = 0, nkv = 0;
     float eps = 0.f;
     unsigned long long *trace = nullptr;   // optional per-CTA phase timeline (11 stamps per CTA)
@@ -106,8 +107,12 @@ struct RopeParams {
 };
 void make_rope_params(RopeParams *p, int head_dim, float theta, const int32_t section[3]);
 cudaError_t launch_rmsnorm(const bf16 *x, const bf16 *w, bf16 *y, int rows, int cols, float eps, cudaStream_t st);
+// Row stride of the row-interleaved rotary tables for n rows: whole 512-byte runs of 32 rows.
+inline int cs_stride(int n) { return (n + 31) & ~31; }
+// cos/sin [S, head_dim/2]; stride > 0: row-interleaved [head_dim/8][stride][4] (GemmPlan::cs_rows =
+// stride >= S, head_dim % 8 == 0; rows past S are not written).
 cudaError_t launch_rope_table(const int32_t *positions, int S, const RopeParams &rp, float *cos_t, float *sin_t,
-                              cudaStream_t st);
+                              cudaStream_t st, int stride = 0);
 
 
 // ---- attention on tcgen05 (attention_tc.cu)
@@ -137,9 +142,10 @@ cudaError_t launch_layernorm(const bf16 *x, const bf16 *w, const bf16 *b, bf16 *
 // out[k] = bilinear sample of the G x G table [G*G, D] at patch k (bf16), n patches.
 cudaError_t launch_pos_embed(const bf16 *table, int G, int D, const VisionGrids &gr, int n, bf16 *out,
                              cudaStream_t st);
-// cos/sin [n, head_dim/2] of the 2-D rotary angles (row frequencies, then column frequencies).
+// cos/sin [n, head_dim/2] of the 2-D rotary angles (row frequencies, then column frequencies);
+// stride > 0: row-interleaved [head_dim/8][stride][4] as launch_rope_table.
 cudaError_t launch_vision_rope(const VisionGrids &gr, int n, int head_dim, const VisionRope &rp, float *cos_t,
-                               float *sin_t, cudaStream_t st);
+                               float *sin_t, cudaStream_t st, int stride = 0);
 
 // ---- embedding gather, visual ranks, weight packing (embed.cu)
 cudaError_t launch_embed(const int32_t *ids, const bf16 *table, int vocab, int hidden, bf16 *out, int S,

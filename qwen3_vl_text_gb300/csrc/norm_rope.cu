@@ -125,15 +125,24 @@ __global__ void fold_cols_kernel(bf16 *W, int cols, const bf16 *__restrict__ gam
     *w = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// One thread per (token, frequency index j).
+// One thread per element i of the table, in either layout: row-major [S][d/2] (stride 0), or
+// row-interleaved [d/8][stride][4], i = ((j/4) stride + s) 4 + j%4 (padding rows s >= S skipped).
 __global__ void rope_table_kernel(const int32_t *__restrict__ pos, int S, const RopeParams rp, float *cos_t,
-                                  float *sin_t) {
+                                  float *sin_t, int stride) {
     pdl_trigger();
     pdl_wait();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= S * rp.half_dim) return;
-    const int s = i / rp.half_dim;
-    const int j = i - s * rp.half_dim;
+    if (i >= (stride ? stride : S) * rp.half_dim) return;
+    int s, j;
+    if (stride) {
+        const int grp = i / (4 * stride), rem = i - grp * 4 * stride;
+        s = rem >> 2;
+        j = 4 * grp + (rem & 3);
+        if (s >= S) return;
+    } else {
+        s = i / rp.half_dim;
+        j = i - s * rp.half_dim;
+    }
     const float p = (float)pos[rp.axis[j] * S + s];
     const float ang = __fmul_rn(p, rp.inv_freq[j]);
     float sn, cs;
@@ -187,12 +196,13 @@ cudaError_t launch_fold_cols(bf16 *W, int cols, const bf16 *gamma, int r0, int r
 }
 
 cudaError_t launch_rope_table(const int32_t *positions, int S, const RopeParams &rp, float *cos_t, float *sin_t,
-                              cudaStream_t st) {
+                              cudaStream_t st, int stride) {
     if (S <= 0) return cudaSuccess;
-    const int n = S * rp.half_dim;
+    if (stride && (rp.half_dim % 4 || stride < S)) return cudaErrorInvalidValue;
+    const int n = (stride ? stride : S) * rp.half_dim;
     cudaLaunchAttribute at[1];
     cudaLaunchConfig_t cfg = pdl_config(dim3((n + 255) / 256), dim3(256), 0, st, at);
-    return cudaLaunchKernelEx(&cfg, rope_table_kernel, positions, S, rp, cos_t, sin_t);
+    return cudaLaunchKernelEx(&cfg, rope_table_kernel, positions, S, rp, cos_t, sin_t, stride);
 }
 
 }  // namespace h3

@@ -95,6 +95,78 @@ __global__ void __launch_bounds__(LN_THREADS) layernorm_kernel(const bf16 *__res
     }
 }
 
+// One warp per row for rows of up to 2048 columns (the blocks' norms): VPT 16-byte vectors
+// of x, w and b per lane, all loaded before the first reduction; mean and variance by warp
+// shuffles alone.  Four rows per CTA, so a 3072 x 1024 activation is one wave of CTAs.
+constexpr int LNW_ROWS = 4;
+template <int VPT>
+__global__ void __launch_bounds__(32 * LNW_ROWS) layernorm_warp_kernel(const bf16 *__restrict__ x,
+                                                                       const bf16 *__restrict__ w,
+                                                                       const bf16 *__restrict__ b, bf16 *y,
+                                                                       int rows, int cols, float eps) {
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * LNW_ROWS + (threadIdx.x >> 5);
+    if (row >= rows) return;   // whole warps leave; no block-wide barrier follows
+    const int nvec = cols >> 3;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)row * cols);
+    const uint4 *wr = reinterpret_cast<const uint4 *>(w);
+    const uint4 *br = reinterpret_cast<const uint4 *>(b);
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    uint4 xv[VPT], wv[VPT], bv[VPT];
+    #pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int idx = lane + 32 * i;
+        const bool ok = idx < nvec;
+        xv[i] = ok ? xr[idx] : zero;
+        wv[i] = ok ? wr[idx] : zero;
+        bv[i] = ok ? br[idx] : zero;
+    }
+    float s = 0.f;
+    #pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const uint32_t u[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+        #pragma unroll
+        for (int k = 0; k < 4; ++k) s += bf16_lo(u[k]) + bf16_hi(u[k]);
+    }
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const float mean = s / (float)cols;
+    float q = 0.f;
+    #pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        if (lane + 32 * i < nvec) {
+            const uint32_t u[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+            #pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float d0 = bf16_lo(u[k]) - mean, d1 = bf16_hi(u[k]) - mean;
+                q = fmaf(d0, d0, q);
+                q = fmaf(d1, d1, q);
+            }
+        }
+    }
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+    const float rstd = 1.0f / sqrtf(q / (float)cols + eps);
+    uint4 *yr = reinterpret_cast<uint4 *>(y + (size_t)row * cols);
+    #pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int idx = lane + 32 * i;
+        if (idx < nvec) {
+            const uint32_t u[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+            const uint32_t wu[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+            const uint32_t bu[4] = {bv[i].x, bv[i].y, bv[i].z, bv[i].w};
+            uint32_t o[4];
+            #pragma unroll
+            for (int k = 0; k < 4; ++k)
+                o[k] = pack_bf16x2(fmaf((bf16_lo(u[k]) - mean) * rstd, bf16_lo(wu[k]), bf16_lo(bu[k])),
+                                   fmaf((bf16_hi(u[k]) - mean) * rstd, bf16_hi(wu[k]), bf16_hi(bu[k])));
+            yr[idx] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
 // The (row, column) of patch k of the concatenated grids, in the tower's order.
 __device__ __forceinline__ void patch_rc(const VisionGrids &gr, int k, int &grid, int &row, int &col) {
     grid = 0;
@@ -160,14 +232,24 @@ __global__ void pos_embed_kernel(const bf16 *__restrict__ table, int G, int D, c
 }
 
 // One thread per (patch, angle j < d/2): j < d/4 rotates by row * inv_freq[j], the rest by
-// column * inv_freq[j - d/4] (fp32 products); fp32 cos / sin.
+// column * inv_freq[j - d/4] (fp32 products); fp32 cos / sin, element i in either layout:
+// row-major [n][d/2] (stride 0), or row-interleaved [d/8][stride][4], i = ((j/4) stride + k) 4 + j%4.
 __global__ void vision_rope_kernel(const VisionGrids gr, int n, int half_dim, const VisionRope rp, float *cos_t,
-                                   float *sin_t) {
+                                   float *sin_t, int stride) {
     pdl_trigger();
     pdl_wait();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n * half_dim) return;
-    const int k = i / half_dim, j = i - k * half_dim;
+    if (i >= (stride ? stride : n) * half_dim) return;
+    int k, j;
+    if (stride) {
+        const int grp = i / (4 * stride), rem = i - grp * 4 * stride;
+        k = rem >> 2;
+        j = 4 * grp + (rem & 3);
+        if (k >= n) return;
+    } else {
+        k = i / half_dim;
+        j = i - k * half_dim;
+    }
     int grid, row, col;
     patch_rc(gr, k, grid, row, col);
     const int quarter = half_dim >> 1;
@@ -209,6 +291,14 @@ cudaError_t launch_layernorm(const bf16 *x, const bf16 *w, const bf16 *b, bf16 *
     if (rows <= 0) return cudaSuccess;
     if (cols % 8 || cols > 256 * LN_VPT * 8) return cudaErrorInvalidValue;
     cudaLaunchAttribute at[1];
+    if (cols <= 32 * 8 * 8) {   // a warp per row
+        const int vpt = (cols / 8 + 31) / 32;
+        cudaLaunchConfig_t cfg = pdl_config(dim3((rows + LNW_ROWS - 1) / LNW_ROWS), dim3(32 * LNW_ROWS), 0, st, at);
+        if (vpt <= 1) return cudaLaunchKernelEx(&cfg, layernorm_warp_kernel<1>, x, w, b, y, rows, cols, eps);
+        if (vpt <= 2) return cudaLaunchKernelEx(&cfg, layernorm_warp_kernel<2>, x, w, b, y, rows, cols, eps);
+        if (vpt <= 4) return cudaLaunchKernelEx(&cfg, layernorm_warp_kernel<4>, x, w, b, y, rows, cols, eps);
+        return cudaLaunchKernelEx(&cfg, layernorm_warp_kernel<8>, x, w, b, y, rows, cols, eps);
+    }
     if (cols <= 128 * LN_VPT * 8) {
         cudaLaunchConfig_t cfg = pdl_config(dim3(rows), dim3(128), 0, st, at);
         return cudaLaunchKernelEx(&cfg, layernorm_kernel<128>, x, w, b, y, cols, eps);
@@ -228,13 +318,14 @@ cudaError_t launch_pos_embed(const bf16 *table, int G, int D, const VisionGrids 
 }
 
 cudaError_t launch_vision_rope(const VisionGrids &gr, int n, int head_dim, const VisionRope &rp, float *cos_t,
-                               float *sin_t, cudaStream_t st) {
+                               float *sin_t, cudaStream_t st, int stride) {
     if (n <= 0) return cudaSuccess;
-    if (head_dim % 4 || head_dim / 2 > kMaxHalfDim) return cudaErrorInvalidValue;
-    const int total = n * (head_dim / 2);
+    if (head_dim % 4 || head_dim / 2 > kMaxHalfDim || (stride && (head_dim % 8 || stride < n)))
+        return cudaErrorInvalidValue;
+    const int total = (stride ? stride : n) * (head_dim / 2);
     cudaLaunchAttribute at[1];
     cudaLaunchConfig_t cfg = pdl_config(dim3((total + 255) / 256), dim3(256), 0, st, at);
-    return cudaLaunchKernelEx(&cfg, vision_rope_kernel, gr, n, head_dim / 2, rp, cos_t, sin_t);
+    return cudaLaunchKernelEx(&cfg, vision_rope_kernel, gr, n, head_dim / 2, rp, cos_t, sin_t, stride);
 }
 
 }  // namespace h3

@@ -151,6 +151,7 @@ cudaError_t gemm(h3vis *h, const CUtensorMap *tA, const CUtensorMap *tW, int M, 
     if (rope) {
         const int d = h->cfg.hidden / h->cfg.num_heads;
         p.cos_t = h->cos_t; p.sin_t = h->sin_t;
+        p.cs_rows = d % 8 == 0 ? h3::cs_stride(M) : 0;   // the tables' layout, as the encode writes them
         p.head_dim = d; p.nq = h->cfg.num_heads; p.nkv = h->cfg.num_heads;
     }
     ++h->launches;
@@ -220,7 +221,7 @@ h3enc_status h3vis_create(const h3vis_config *cfg, h3vis **out) {
     // workspace
     const size_t P = c.max_patches, d = H / c.num_heads;
     const size_t b_x = align256(P * H * 2), b_qkv = align256(P * 3 * H * 2),
-                 b_act = align256(P * (size_t)(I > H ? I : H) * 2), b_cs = align256(P * (d / 2) * 4),
+                 b_act = align256(P * (size_t)(I > H ? I : H) * 2), b_cs = align256((size_t)h3::cs_stride((int)P) * (d / 2) * 4),
                  b_gemm = align256(h3::gemm_workspace_bytes(h->num_sms)), b_st = 256;
     const size_t wsz = 3 * b_x + b_qkv + b_act + 2 * b_cs + b_gemm + b_st;
     e = cudaMalloc(&h->ws, wsz);
@@ -345,7 +346,9 @@ h3enc_status h3vis_encode(h3vis *h, const void *pixel_values, int32_t n_patches,
     VCHECK(h3::launch_pos_embed(h->pos, h->G, H, gr, n, h->x, st), "position embeddings");
     e = gemm(h, &tm_px, &h->tm_patch, n, H, pd, h3::EPI_RESIDUAL, h->x, H, h->x, h->patch_b, st);
     if (e != cudaSuccess) return vcuda(h, e, "patch embedding");
-    VCHECK(h3::launch_vision_rope(gr, n, d, h->rope, h->cos_t, h->sin_t, st), "rotary tables");
+    // row-interleaved (head_dim % 8 == 0): the QKV epilogue's warps read them as whole lines
+    VCHECK(h3::launch_vision_rope(gr, n, d, h->rope, h->cos_t, h->sin_t, st, d % 8 == 0 ? h3::cs_stride(n) : 0),
+           "rotary tables");
     for (int b = 0; b < c.depth; ++b) {
         const Block &k = h->blocks[b];
         VCHECK(h3::launch_layernorm(h->x, k.n1w, k.n1b, h->y, n, H, c.ln_eps, st), "norm1");

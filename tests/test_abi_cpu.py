@@ -78,6 +78,14 @@ def test_op_entries_validate_arguments(Q):
         Q.h3enc_op_attention(16, 16, 10, 4, 2, 64, [0, 4, 3, 10], stream=0)  # decreasing cu_seqlens
     with pytest.raises(Q.H3encError):
         Q.h3enc_op_pack_gate_up(16, 16, 16, 100, 64, stream=0)              # I % 128
+    with pytest.raises(Q.H3encError) as e:
+        Q.h3enc_op_rope_table_ex(16, 100, 128, 5e6, (24, 20, 20), 96, 16, 16, stream=0)   # stride < S
+    assert e.value.code == 2
+    with pytest.raises(Q.H3encError):
+        Q.h3enc_op_rope_table_ex(16, 10, 12, 5e6, (2, 2, 2), 32, 16, 16, stream=0)       # head_dim % 8
+    with pytest.raises(Q.H3encError) as e:                                              # table stride < M
+        Q.h3enc_op_gemm_qkv_rope_ex(16, 16, 16, 100, 512, 4, 2, 64, 16, 16, 1e-6, 16, 16, 64, stream=0)
+    assert e.value.code == 2
 
 
 def test_handle_calls_reject_a_null_handle(Q):

@@ -277,6 +277,61 @@ def test_qkv_projection_with_fused_norm_rope(d, nq, nkv, M, K, split):
     assert bad == 0, f"{bad} elements off, worst {worst}"
 
 
+@pytest.mark.parametrize("wl_id,extra", [(0, 0), (2, 32), (3, 0)])
+def test_rope_table_row_interleaved(wl_id, extra):
+    """The encoder's table layout, [d/8][stride][4]: the same values as the row-major table,
+    bit for bit, and the padding rows past S left alone."""
+    m = W.workload(wl_id).model
+    pos = W.gen_inputs(W.workload(wl_id))["positions"]
+    S, h = pos.shape[1], m.head_dim // 2
+    stride = (S + 31) // 32 * 32 + extra
+    P = torch.from_numpy(pos).cuda()
+    c = torch.empty(S, h, device="cuda")
+    s = torch.empty_like(c)
+    Q.h3enc_op_rope_table(P, S, m.head_dim, m.rope_theta, m.mrope_section, c, s)
+    ci = torch.full((h // 4, stride, 4), float("nan"), device="cuda")
+    si = torch.full_like(ci, float("nan"))
+    Q.h3enc_op_rope_table_ex(P, S, m.head_dim, m.rope_theta, m.mrope_section, stride, ci, si)
+    torch.cuda.synchronize()
+    for row_major, ilv in ((c, ci), (s, si)):
+        assert torch.equal(ilv[:, :S, :].permute(1, 0, 2).reshape(S, h), row_major)
+        assert torch.isnan(ilv[:, S:, :]).all()
+
+
+@pytest.mark.parametrize("M,K,split,folded", [(300, 512, False, False), (1024, 5120, True, False),
+                                              (1000, 2048, True, True), (97, 512, False, True)])
+def test_qkv_rope_row_interleaved_tables_bit_identical(M, K, split, folded):
+    """The QKV epilogue reads either table layout; the output is the same bit for bit (the
+    layout only changes which lines the loads touch)."""
+    d, nq, nkv = 128, 64, 8
+    N = (nq + 2 * nkv) * d
+    A, a = _bf16(26, "A", (M, K))
+    Wt, _ = _bf16(27, "Wqkv", (N, K), sigma=0.05)
+    Gq, _ = _bf16(28, "gq", (d,), 1.0, 0.1)
+    Gk, _ = _bf16(29, "gk", (d,), 1.0, 0.1)
+    pos = np.stack([np.arange(M) * 3, np.arange(M) * 5 + 1, np.arange(M) * 7 + 2]).astype(np.int32)
+    P = torch.from_numpy(pos).cuda()
+    c = torch.empty(M, d // 2, device="cuda")
+    s = torch.empty_like(c)
+    Q.h3enc_op_rope_table(P, M, d, 5e6, (24, 20, 20), c, s)
+    stride = (M + 31) // 32 * 32
+    ci = torch.empty(stride * d // 2, device="cuda")
+    si = torch.empty_like(ci)
+    Q.h3enc_op_rope_table_ex(P, M, d, 5e6, (24, 20, 20), stride, ci, si)
+    ss = None
+    if folded:
+        sq = a.astype(np.float32).reshape(M, K // 128, 128) ** 2
+        ss = torch.from_numpy(np.ascontiguousarray(sq.sum(axis=2, dtype=np.float32).T)).cuda()
+    outs = []
+    for cos_t, sin_t, cs in ((c, s, 0), (ci, si, stride)):
+        C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        Q.h3enc_op_gemm_qkv_rope_ex(A, Wt, C, M, K, nq, nkv, d, Gq, Gk, 1e-6, cos_t, sin_t, cs, ss_in=ss,
+                                    in_eps=1e-6, workspace=_workspace() if split else None)
+        outs.append(C)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+
+
 @pytest.mark.parametrize("d,nq,nkv,cu", [
     (64, 4, 2, [0, 48]),
     (64, 4, 1, [0, 1, 130, 131, 300]),

@@ -43,7 +43,7 @@ def _ws():
     return torch.zeros(Q.h3enc_op_gemm_workspace_bytes(), dtype=torch.uint8, device="cuda")
 
 
-@pytest.mark.parametrize("rows,cols", [(1, 256), (300, 1024), (77, 4096), (5, 8192)])
+@pytest.mark.parametrize("rows,cols", [(1, 256), (3, 72), (300, 1024), (33, 1536), (7, 2048), (77, 4096), (5, 8192)])
 def test_layernorm(rows, cols):
     X, x = _bf16(70, "x", (rows, cols), 0.3, 2.0)
     G, g = _bf16(71, "g", (cols,), 1.0, 0.1)
