@@ -9,9 +9,11 @@
 // frame, one head per kv head) with the causal mask off; there every item costs the same,
 // and the pair-items of a thin last round run as single query tiles instead.
 //
-// Work item = two query tiles of 128 rows (A = rows q0.., B = rows q0+128..) of one
-// head; both read the same key/value tiles of 128, so each K/V tile is staged once
-// for 256 query rows.  Persistent: one CTA per SM takes items heaviest first in
+// Work item = two query tiles of 128 rows that read the same key/value tiles, so each
+// K/V tile is staged once for 256 query rows: in causal attention with at least two q
+// heads per kv head, the same 128 rows (one tile of the sequence) of two q heads of one
+// kv group (A = head 2i, B = head 2i+1; both tiles need the same keys); otherwise two
+// consecutive tiles of one head (A = rows q0.., B = rows q0+128..).  Persistent: one CTA per SM takes items heaviest first in
 // alternating-direction rounds; TMEM, barriers and the K/V ring carry over from
 // item to item, and an item's epilogue overlaps the next item's first products.
 //   warp 0     TMA: Q_A and Q_B once, K and V tiles into a 2-stage ring (128-byte swizzle)
@@ -50,15 +52,16 @@ struct AttnTcArgs {
     int nq, group;
     int k_col0, v_col0;
     float scale_log2;
-    int n_seqs, total_pairs, n_items;
+    int n_seqs, total_pairs, n_items;   // "pairs": units of two query tiles (see head_pairs)
     int n_whole;   // items [0, n_whole) are pairs of query tiles; each later pair-item is run as
                    // two single-tile items (bidirectional mode, to fill a thin last round)
     int32_t *status;
     int cu[kMaxSeqs + 1];
-    int pair_start[kMaxSeqs + 1];   // first tile-pair index of each sequence
+    int pair_start[kMaxSeqs + 1];   // first unit of each sequence (a 128-row tile when head_pairs)
     unsigned long long *trace;      // optional [grid][ATR_COUNT] timeline
     float *row_amax;                // optional [S]: atomic max of |output| per row (bf16 values, >= 0)
     int causal;                     // 1: keys after the query are masked; 0: every key of the segment
+    int head_pairs;                 // 1: an item is one 128-row tile of two q heads of one kv group
 };
 
 // Timeline of one persistent CTA (h3enc_op_attention_trace_next): %globaltimer at
@@ -120,22 +123,39 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// One work item = (pair of query tiles, head); item k in heavy-first order.
+// One work item = (unit, head or head pair); item k in heavy-first order.  Tile A is head
+// `head`, rows q0..; tile B is head `head_b`, rows q0_b.. (nkt_b = 0: no tile B).
 struct AttnItem {
-    int head, seg0, L, q0, nkt_a, nkt_b;
+    int head, head_b, seg0, L, q0, q0_b, nkt_a, nkt_b;
 };
-__device__ __forceinline__ AttnItem attn_item(const AttnTcArgs &a, int k_in) {
-    AttnItem it;
-    // past n_whole: item n_whole + 2j + h is tile h of pair-item n_whole + j on its own
-    const int split = k_in >= a.n_whole ? ((k_in - a.n_whole) & 1) + 1 : 0;   // 0 whole, 1 tile A, 2 tile B
-    const int k = split ? a.n_whole + ((k_in - a.n_whole) >> 1) : k_in;
-    it.head = k % a.nq;                                   // heads fastest: one kv group's heads adjacent
-    const int pair_lin = a.total_pairs - 1 - k / a.nq;    // heavy tile pairs first
+__device__ __forceinline__ int seq_of_unit(const AttnTcArgs &a, int u) {
     int lo = 0, hi = a.n_seqs - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (a.pair_start[mid] <= pair_lin) lo = mid; else hi = mid - 1;
+        if (a.pair_start[mid] <= u) lo = mid; else hi = mid - 1;
     }
+    return lo;
+}
+__device__ __forceinline__ AttnItem attn_item(const AttnTcArgs &a, int k_in) {
+    AttnItem it;
+    if (a.head_pairs) {   // causal: heads (2i, 2i+1) share kv head and every key tile
+        const int hp = a.nq >> 1;
+        it.head = 2 * (k_in % hp);
+        it.head_b = it.head + 1;
+        const int tile_lin = a.total_pairs - 1 - k_in / hp;   // heavy tiles first
+        const int sq = seq_of_unit(a, tile_lin);
+        it.seg0 = a.cu[sq];
+        it.L = a.cu[sq + 1] - it.seg0;
+        it.q0 = it.q0_b = (tile_lin - a.pair_start[sq]) * TQ;
+        it.nkt_a = it.nkt_b = (min(it.q0 + TQ, it.L) + TK - 1) / TK;
+        return it;
+    }
+    // past n_whole: item n_whole + 2j + h is tile h of pair-item n_whole + j on its own
+    const int split = k_in >= a.n_whole ? ((k_in - a.n_whole) & 1) + 1 : 0;   // 0 whole, 1 tile A, 2 tile B
+    const int k = split ? a.n_whole + ((k_in - a.n_whole) >> 1) : k_in;
+    it.head = it.head_b = k % a.nq;                       // heads fastest: one kv group's heads adjacent
+    const int pair_lin = a.total_pairs - 1 - k / a.nq;    // heavy tile pairs first
+    const int lo = seq_of_unit(a, pair_lin);
     it.seg0 = a.cu[lo];
     it.L = a.cu[lo + 1] - it.seg0;
     it.q0 = (pair_lin - a.pair_start[lo]) * (2 * TQ);
@@ -153,6 +173,7 @@ __device__ __forceinline__ AttnItem attn_item(const AttnTcArgs &a, int k_in) {
         if (split == 2) it.q0 += TQ;
         it.nkt_b = 0;
     }
+    it.q0_b = it.q0 + TQ;
     return it;
 }
 // The r-th item of CTA b among G persistent CTAs: rounds of G items, alternate rounds
@@ -230,8 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(q_full, nq_tiles * Lay::Q_BYTES);
                 for (int t = 0; t < nq_tiles; ++t)
                     for (int c = 0; c < D / 64; ++c)
-                        tma_load_2d(sQ + t * Lay::Q_BYTES + c * Lay::ATOM, &tm, q_full, w.head * D + c * 64,
-                                    w.seg0 + w.q0 + t * TQ);
+                        tma_load_2d(sQ + t * Lay::Q_BYTES + c * Lay::ATOM, &tm, q_full,
+                                    (t ? w.head_b : w.head) * D + c * 64, w.seg0 + (t ? w.q0_b : w.q0));
                 for (int j = 0; j < n_kt; ++j, ++g) {
                     const int s = g & 1;
                     if (g >= 2 && !mbar_wait(&kv_empty[s], ((g >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
@@ -345,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const AttnItem w = attn_item(a, k);
             const int nkt = t == 0 ? w.nkt_a : w.nkt_b;
             if (nkt == 0) continue;
-            const int qtile0 = w.q0 + t * TQ;
+            const int qtile0 = t ? w.q0_b : w.q0;
             const int qpos = qtile0 + r_row;          // position inside the sequence
             float m_use = -INFINITY, l = 0.f;
             for (int j = 0; j < nkt; ++j, ++c) {
@@ -460,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const bool live = qpos < w.L;
-            bf16 *dst = a.o + (size_t)(w.seg0 + qpos) * a.ld_o + (size_t)w.head * D;
+            bf16 *dst = a.o + (size_t)(w.seg0 + qpos) * a.ld_o + (size_t)(t ? w.head_b : w.head) * D;
             float rmax = 0.f;   // largest |bf16 output| of this row's head
             #pragma unroll 1
             for (int cc = 0; cc < D / 32; ++cc) {
@@ -545,13 +566,16 @@ cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, i
     args.trace = t_attn_trace;
     args.row_amax = row_amax;
     args.causal = causal ? 1 : 0;
+    // causal with an even number of q heads per kv head: items are one tile of two heads
+    args.head_pairs = causal && args.group % 2 == 0 ? 1 : 0;
+    const int unit = args.head_pairs ? TQ : 2 * TQ;   // query rows per unit
     t_attn_trace = nullptr;
     int n = 0, pairs = 0;
     if (!cu_host) {
         args.cu[0] = 0;
         args.cu[1] = S;
         args.pair_start[0] = 0;
-        pairs = (S + 2 * TQ - 1) / (2 * TQ);
+        pairs = (S + unit - 1) / unit;
         n = 1;
     } else {
         args.cu[0] = 0;
@@ -560,7 +584,7 @@ cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, i
             if (len <= 0) continue;
             args.cu[n] = cu_host[i];
             args.pair_start[n] = pairs;
-            pairs += (len + 2 * TQ - 1) / (2 * TQ);
+            pairs += (len + unit - 1) / unit;
             ++n;
             args.cu[n] = cu_host[i + 1];
         }
@@ -568,7 +592,7 @@ cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, i
     if (n == 0) return cudaSuccess;
     args.n_seqs = n;
     args.total_pairs = pairs;
-    args.n_items = pairs * nq;
+    args.n_items = args.head_pairs ? pairs * (nq / 2) : pairs * nq;
     args.n_whole = args.n_items;
     int sms = device_num_sms();
     if (sms <= 0) sms = 1;
