@@ -599,101 +599,103 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         epi_bar_and(true);
                     }
                     if constexpr (EPI == EPI_QKROPE) {
-                        // four threads per (row, head): thread `sub` owns first-half columns
-                        // [sub*d/8, (sub+1)*d/8) and their RoPE partners d/2 further on
-                        const int d = g.head_dim, half = d >> 1, q4 = half >> 2, hpt = BN / d;
-                        const int sub = et & 3;
-                        const unsigned gmask = 0xFu << (lane & ~3);
-                        const int units = (r1 - r0) * hpt;
-                        for (int u = et >> 2; u < units; u += EPI_THREADS / 4) {
-                            const int r = r0 + u / hpt, hh = u % hpt;
-                            const int row = m_blk * (2 * BM) + (int)rank * BM + r;
-                            if (row >= g.M) continue;   // same row for the four threads
-                            const int head = (n_blk * BN) / d + hh;
-                            const int ca = hh * d + sub * q4;      // first-half column inside the tile
-                            float a[16], b[16];
-                            #pragma unroll
-                            for (int i = 0; i < 16; ++i) a[i] = b[i] = 0.f;
-                            for (int k = 0; k < nc; ++k) {
-                                const float4 *pk = slot_of(k);
-                                #pragma unroll
-                                for (int i = 0; i < 16; i += 4) {
-                                    if (i < q4) {
-                                        const float4 x = __ldcg(pk + part_f4(r, ca + i));
-                                        const float4 y = __ldcg(pk + part_f4(r, ca + half + i));
-                                        a[i] += x.x; a[i + 1] += x.y; a[i + 2] += x.z; a[i + 3] += x.w;
-                                        b[i] += y.x; b[i + 1] += y.y; b[i + 2] += y.z; b[i + 3] += y.w;
-                                    }
-                                }
-                            }
-                            if constexpr (F8) {
-                                const float sr = g.sa[row];
-                                #pragma unroll
-                                for (int i = 0; i < 16; i += 4) {
-                                    if (i < q4) {
-                                        dq4(a + i, sr, n_blk * BN + ca + i);
-                                        dq4(b + i, sr, n_blk * BN + ca + half + i);
-                                    }
-                                }
-                            }
-                            if (g.ss_in) {   // the folded input RMSNorm: 1/rms of this row of A
-                                const float rn = s_rn[r - r0];
-                                #pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    a[i] *= rn;
-                                    b[i] *= rn;
-                                }
-                            }
-                            #pragma unroll
-                            for (int i = 0; i < 16; i += 4) {
-                                if (i < q4) {
-                                    bias4(a + i, n_blk * BN + ca + i);
-                                    bias4(b + i, n_blk * BN + ca + half + i);
-                                }
-                            }
-                            __nv_bfloat16 *dst = g.C + (size_t)row * g.ldc + n_blk * BN + ca;
-                            const bool is_q = head < g.nq, is_k = !is_q && head < g.nq + g.nkv;
-                            if (is_q || is_k) {
-                                const bool qk_norm = g.wq != nullptr;   // the vision tower has none
-                                float rstd = 1.f;
-                                if (qk_norm) {
-                                    float ss = 0.f;
+                        // In chunks of up to 24 rows: (1) the contributors' partials summed in range
+                        // order into shared memory, consecutive threads on consecutive rows of one
+                        // float4 column group so that each warp load covers whole lines (loads
+                        // scattered over many lines cost the MMAs beside them shared-memory
+                        // bandwidth); (2) per (row, head) d/8 threads, thread `sub` owning
+                        // first-half columns [4 sub, 4 sub + 4) and their RoPE partners d/2 on
+                        constexpr int CH = 24, SROW = BN + 4;   // padded rows: no bank conflicts
+                        float *s_sum = reinterpret_cast<float *>(sC + 512);   // after s_rn (<= 128 floats)
+                        const int d = g.head_dim, half = d >> 1, hpt = BN / d;
+                        const int tpu = half >> 2;                      // 16 (d = 128) or 8 (d = 64)
+                        const int sub = et & (tpu - 1);
+                        const unsigned gmask = (tpu == 16 ? 0xFFFFu : 0xFFu) << (lane & (32 - tpu));
+                        #pragma unroll 1
+                        for (int c0 = r0; c0 < r1; c0 += CH) {
+                            const int nch = min(CH, r1 - c0);
+                            #pragma unroll 1
+                            for (int u = et; u < nch * (BN / 4); u += EPI_THREADS) {
+                                const int rr = u % nch, c4 = (u / nch) * 4;
+                                const size_t i4 = part_f4(c0 + rr, c4);
+                                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                                for (int k0 = 0; k0 < nc; k0 += 8) {
+                                    float4 x[8];
                                     #pragma unroll
-                                    for (int i = 0; i < 16; ++i)
-                                        if (i < q4) ss = fmaf(a[i], a[i], fmaf(b[i], b[i], ss));
-                                    ss += __shfl_xor_sync(gmask, ss, 1);
-                                    ss += __shfl_xor_sync(gmask, ss, 2);
-                                    rstd = 1.0f / sqrtf(ss / (float)d + g.eps);
-                                }
-                                const __nv_bfloat16 *w = is_q ? g.wq : g.wk;
-                                const int jb = sub * q4;           // frequency index of a[0]
-                                #pragma unroll
-                                for (int i = 0; i < 16; i += 4) {
-                                    if (i < q4) {
-                                        const size_t ci = cs_at(g, row, jb + i);
-                                        const float4 co4 = *reinterpret_cast<const float4 *>(g.cos_t + ci);
-                                        const float4 si4 = *reinterpret_cast<const float4 *>(g.sin_t + ci);
-                                        const float cv[4] = {co4.x, co4.y, co4.z, co4.w};
-                                        const float sv[4] = {si4.x, si4.y, si4.z, si4.w};
-                                        #pragma unroll
-                                        for (int t = 0; t < 4; ++t) {
-                                            const float ga = qk_norm ? __bfloat162float(w[jb + i + t]) : 1.f;
-                                            const float gb = qk_norm ? __bfloat162float(w[half + jb + i + t]) : 1.f;
-                                            const float ya = a[i + t] * rstd * ga;
-                                            const float yb = b[i + t] * rstd * gb;
-                                            a[i + t] = ya * cv[t] - yb * sv[t];
-                                            b[i + t] = yb * cv[t] + ya * sv[t];
+                                    for (int k = 0; k < 8; ++k)
+                                        if (k0 + k < nc) x[k] = __ldcg(slot_of(k0 + k) + i4);
+                                    #pragma unroll
+                                    for (int k = 0; k < 8; ++k) {
+                                        if (k0 + k < nc) {
+                                            acc.x += x[k].x; acc.y += x[k].y; acc.z += x[k].z; acc.w += x[k].w;
                                         }
                                     }
                                 }
-                            }
-                            #pragma unroll
-                            for (int i = 0; i < 16; i += 2) {
-                                if (i < q4) {
-                                    *reinterpret_cast<uint32_t *>(dst + i) = pack_bf16x2(a[i], a[i + 1]);
-                                    *reinterpret_cast<uint32_t *>(dst + half + i) = pack_bf16x2(b[i], b[i + 1]);
+                                if constexpr (F8) {   // the e4m3 scales of row and column
+                                    const int row = m_blk * (2 * BM) + (int)rank * BM + c0 + rr;
+                                    float f[4] = {acc.x, acc.y, acc.z, acc.w};
+                                    dq4(f, row < g.M ? g.sa[row] : 0.f, n_blk * BN + c4);
+                                    acc = make_float4(f[0], f[1], f[2], f[3]);
                                 }
+                                *reinterpret_cast<float4 *>(s_sum + rr * SROW + c4) = acc;
                             }
+                            epi_bar_and(true);
+                            #pragma unroll 1
+                            for (int u = et / tpu; u < nch * hpt; u += EPI_THREADS / tpu) {
+                                const int rr = u / hpt, hh = u % hpt;
+                                const int r = c0 + rr;
+                                const int row = m_blk * (2 * BM) + (int)rank * BM + r;
+                                if (row >= g.M) continue;   // same row for the unit's threads
+                                const int head = (n_blk * BN) / d + hh;
+                                const int jb = 4 * sub;                 // frequency index of a[0]
+                                const int ca = hh * d + jb;             // first-half column inside the tile
+                                const float4 sa4 = *reinterpret_cast<const float4 *>(s_sum + rr * SROW + ca);
+                                const float4 sb4 = *reinterpret_cast<const float4 *>(s_sum + rr * SROW + ca + half);
+                                float a[4] = {sa4.x, sa4.y, sa4.z, sa4.w}, b[4] = {sb4.x, sb4.y, sb4.z, sb4.w};
+                                if (g.ss_in) {   // the folded input RMSNorm: 1/rms of this row of A
+                                    const float rn = s_rn[r - r0];
+                                    #pragma unroll
+                                    for (int i = 0; i < 4; ++i) {
+                                        a[i] *= rn;
+                                        b[i] *= rn;
+                                    }
+                                }
+                                bias4(a, n_blk * BN + ca);
+                                bias4(b, n_blk * BN + ca + half);
+                                __nv_bfloat16 *dst = g.C + (size_t)row * g.ldc + n_blk * BN + ca;
+                                const bool is_q = head < g.nq, is_k = !is_q && head < g.nq + g.nkv;
+                                if (is_q || is_k) {
+                                    const bool qk_norm = g.wq != nullptr;   // the vision tower has none
+                                    float rstd = 1.f;
+                                    if (qk_norm) {
+                                        float ss = 0.f;
+                                        #pragma unroll
+                                        for (int i = 0; i < 4; ++i) ss = fmaf(a[i], a[i], fmaf(b[i], b[i], ss));
+                                        for (int o = 1; o < tpu; o <<= 1) ss += __shfl_xor_sync(gmask, ss, o);
+                                        rstd = 1.0f / sqrtf(ss / (float)d + g.eps);
+                                    }
+                                    const __nv_bfloat16 *w = is_q ? g.wq : g.wk;
+                                    const size_t ci = cs_at(g, row, jb);
+                                    const float4 co4 = *reinterpret_cast<const float4 *>(g.cos_t + ci);
+                                    const float4 si4 = *reinterpret_cast<const float4 *>(g.sin_t + ci);
+                                    const float cv[4] = {co4.x, co4.y, co4.z, co4.w};
+                                    const float sv[4] = {si4.x, si4.y, si4.z, si4.w};
+                                    #pragma unroll
+                                    for (int i = 0; i < 4; ++i) {
+                                        const float ga = qk_norm ? __bfloat162float(w[jb + i]) : 1.f;
+                                        const float gb = qk_norm ? __bfloat162float(w[half + jb + i]) : 1.f;
+                                        const float ya = a[i] * rstd * ga;
+                                        const float yb = b[i] * rstd * gb;
+                                        a[i] = ya * cv[i] - yb * sv[i];
+                                        b[i] = yb * cv[i] + ya * sv[i];
+                                    }
+                                }
+                                *reinterpret_cast<uint2 *>(dst) =
+                                    make_uint2(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]));
+                                *reinterpret_cast<uint2 *>(dst + half) =
+                                    make_uint2(pack_bf16x2(b[0], b[1]), pack_bf16x2(b[2], b[3]));
+                            }
+                            epi_bar_and(true);   // s_sum is rewritten by the next chunk
                         }
                     } else {
                         // consecutive threads take consecutive rows of one float4 column group
