@@ -479,9 +479,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             uint8_t *slot = cslots + (cstores & 1) * C_SLOT_BYTES;
             if (lane == 0) bulk_wait_read<1>();
             __syncwarp();
+            // 64-byte swizzle (as the tensor map): 16-byte unit q of row r at unit q ^ ((r >> 1) & 3),
+            // so the warp's four stores are bank-conflict free
             uint4 *dst = reinterpret_cast<uint4 *>(slot + lane * 64);
+            const int sw = (lane >> 1) & 3;
             #pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            for (int q = 0; q < 4; ++q) dst[q ^ sw] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0 && row0 < g.M) {   // a box wholly past the last row is not issued
@@ -833,14 +836,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 rn = live ? norm_rstd(g, row) : 1.f;
                 rn_blk = m_blk;
             }
-            uint4 rpre[BN / 16];   // this thread's BN/2 residual columns
+            uint4 rpre[BN / 16];   // the warp's 32 rows x BN/2 residual columns, 16 bytes per lane per load
             if constexpr (EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_DS) {
-                // the residual does not depend on the accumulator: its loads fly while the MMAs finish
-                if (live) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(g.R + (size_t)row * g.ldc + n_blk * BN +
-                                                                       ehalf * (BN / 2));
-                    #pragma unroll
-                    for (int i = 0; i < BN / 16; ++i) rpre[i] = src[i];
+                // the residual does not depend on the accumulator: its loads fly while the MMAs finish.
+                // Load i covers rows 2i, 2i + 1 of the warp (lanes 0-15, 16-31), 256 bytes each: whole
+                // lines (a lane per row would touch 32 lines per load and take L1 data-path time from
+                // the MMAs); the chunk loop below turns them into rows through the staging slot
+                #pragma unroll
+                for (int i = 0; i < BN / 16; ++i) {
+                    const int rr = row0 + 2 * i + (lane >> 4);
+                    rpre[i] = rr < g.M ? *(reinterpret_cast<const uint4 *>(g.R + (size_t)rr * g.ldc + n_blk * BN +
+                                                                           ehalf * (BN / 2)) + (lane & 15))
+                                       : make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             if constexpr (EPI == EPI_QKROPE) {
@@ -1005,11 +1012,34 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         #pragma unroll
                         for (int j = 0; j < 32; ++j) f[j] = EPI == EPI_GELU_TANH ? gelu_tanh(f[j]) : gelu_erf(f[j]);
                     }
+                    uint4 rrow[4];   // this row's residual in the chunk's 32 columns
+                    if constexpr (EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_DS) {
+                        {
+                            // the lanes holding the chunk's 16-byte units write them into the staging slot
+                            // this chunk's output will use (same swizzle), then each lane reads its row
+                            uint8_t *slot = cslots + (cstores & 1) * C_SLOT_BYTES;
+                            if (lane == 0) bulk_wait_read<1>();
+                            __syncwarp();
+                            if (((lane & 15) >> 2) == cc) {
+                                const int u = lane & 3;
+                                #pragma unroll
+                                for (int i = 0; i < BN / 16; ++i) {
+                                    const int rr = 2 * i + (lane >> 4);
+                                    *reinterpret_cast<uint4 *>(slot + rr * 64 + ((u ^ ((rr >> 1) & 3)) * 16)) = rpre[i];
+                                }
+                            }
+                            __syncwarp();
+                            #pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                rrow[q] = *reinterpret_cast<const uint4 *>(slot + lane * 64 + ((q ^ ((lane >> 1) & 3)) * 16));
+                            __syncwarp();   // read before store_chunk writes this chunk's output over it
+                        }
+                    }
                     if (live) {
                         if constexpr (EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_DS) {
                             #pragma unroll
                             for (int i = 0; i < 4; ++i) {
-                                const uint4 rv = rpre[cc * 4 + i];
+                                const uint4 rv = rrow[i];
                                 f[8 * i + 0] += bf16_lo(rv.x); f[8 * i + 1] += bf16_hi(rv.x);
                                 f[8 * i + 2] += bf16_lo(rv.y); f[8 * i + 3] += bf16_hi(rv.y);
                                 f[8 * i + 4] += bf16_lo(rv.z); f[8 * i + 5] += bf16_hi(rv.z);
@@ -1081,6 +1111,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Output map for the epilogue's tile stores: bf16 [rows, ld] row-major, boxes of 32 x 32, no swizzle.
+// The epilogue's output map: 32 x 32 boxes staged in 64-byte-swizzled shared memory.
 bool make_tmap_c(CUtensorMap *m, void *ptr, uint64_t rows, uint64_t ld) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn || rows == 0 || ld == 0 || (ld * 2) % 16 != 0 || (reinterpret_cast<uintptr_t>(ptr) & 15)) return false;
@@ -1089,7 +1120,8 @@ bool make_tmap_c(CUtensorMap *m, void *ptr, uint64_t rows, uint64_t ld) {
     cuuint32_t box[2] = {32, 32};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
