@@ -28,7 +28,7 @@ WORKLOAD_ID = 2
 GEMM_GU_CLASS = "gemm_gate_up"
 # DRAM bytes (read + write) of one gate/up launch at seq 1024, from an ncu capture of this
 # kernel source (dram__bytes_read.sum + dram__bytes_write.sum).
-GATE_UP_TRAFFIC_BYTES = 619.0e6
+GATE_UP_TRAFFIC_BYTES = 609.4e6
 # NVIDIA's dense (no 2:4 sparsity) bf16 tensor rate for one GB300, TFLOP/s: context for the
 # measured peaks, which are the denominators of the fractions.
 NOMINAL_DENSE_BF16_TFLOPS = 2250.0
