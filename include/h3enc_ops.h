@@ -289,6 +289,18 @@ H3ENC_API h3enc_status h3enc_op_attention_bidir(const void *qkv, void *o, int32_
                                                 int32_t head_dim, const int32_t *cu_seqlens, int32_t n_seqs,
                                                 void *stream);
 
+/* h3enc_op_attention_bidir with a workspace (h3enc_op_attention_workspace_bytes(head_dim)
+ * bytes, 16-byte aligned, zero-filled once before its first use; calls sharing it must not
+ * overlap on the GPU).  When the persistent kernel's last round of work items would leave
+ * most SMs idle, those items are cut into up to 8 ranges of their keys; each range writes
+ * its unnormalised output, running maximum and sum to the workspace and the range that
+ * finishes last merges them in range order (the same result on every run).  The output
+ * equals the plain call's up to fp32 rounding.  0 from the size query: head_dim not 64/128. */
+H3ENC_API int64_t h3enc_op_attention_workspace_bytes(int32_t head_dim);
+H3ENC_API h3enc_status h3enc_op_attention_bidir_ws(const void *qkv, void *o, int32_t S, int32_t heads,
+                                                   int32_t head_dim, const int32_t *cu_seqlens, int32_t n_seqs,
+                                                   void *workspace, int64_t workspace_bytes, void *stream);
+
 /* Causal GQA attention over packed sequences (page "... encoder.py",
  * MiniMaxH3Qwen3VLTextAttention.forward: repeat_interleave of K/V, SDPA with
  * is_causal=True, scale 1/sqrt(d)).  Reads q/k/v from qkv [S, (nq+2nkv)*d]

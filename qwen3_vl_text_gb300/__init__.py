@@ -26,6 +26,7 @@ __all__ = [
     "h3enc_op_gemm_qkv_rope", "h3enc_op_gemm_qkv_rope_rms", "h3enc_op_gemm_rms", "h3enc_op_row_sumsq",
     "h3enc_op_fold_cols", "h3enc_op_layernorm", "h3enc_op_vision_pos_embed", "h3enc_op_vision_rope_table",
     "h3enc_op_gemm_bias", "h3enc_op_gemm_qkv_rope_bias", "h3enc_op_attention_bidir", "VisionConfig",
+    "h3enc_op_attention_bidir_ws", "h3enc_op_attention_workspace_bytes",
     "h3vis_create", "h3vis_load_weights", "h3vis_finalize_weights", "h3vis_encode", "h3vis_get_status",
     "h3vis_last_error", "h3vis_launch_count", "h3vis_destroy", "VisionEncoder", "h3enc_op_attention", "h3enc_op_embed", "h3enc_op_vis_rank", "Encoder",
     "KERNEL_CLASSES",
@@ -131,6 +132,8 @@ _SIGS = {
     "h3enc_op_gemm_bias": ([_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _I64, _P, _P], _I32),
     "h3enc_op_gemm_qkv_rope_bias": ([_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _I64, _P, _P], _I32),
     "h3enc_op_attention_bidir": ([_P, _P, _I32, _I32, _I32, _P, _I32, _P], _I32),
+    "h3enc_op_attention_bidir_ws": ([_P, _P, _I32, _I32, _I32, _P, _I32, _P, _I64, _P], _I32),
+    "h3enc_op_attention_workspace_bytes": ([_I32], _I64),
     "h3vis_create": ([ctypes.POINTER(VisionConfig), ctypes.POINTER(_P)], _I32),
     "h3vis_load_weights": ([_P, ctypes.c_char_p, _P, _I32, ctypes.POINTER(_I64), _I32, _I32], _I32),
     "h3vis_finalize_weights": ([_P], _I32),
@@ -513,6 +516,18 @@ def h3enc_op_attention_bidir(qkv, o, S, heads, head_dim, cu_seqlens=None, stream
     cu = _host_i32(cu_seqlens)
     n_seqs = len(cu) - 1 if cu is not None else 0
     return _check(lib.h3enc_op_attention_bidir(_ptr(qkv), _ptr(o), S, heads, head_dim, cu, n_seqs, _stream(stream)))
+
+
+def h3enc_op_attention_workspace_bytes(head_dim):
+    return int(lib.h3enc_op_attention_workspace_bytes(head_dim))
+
+
+def h3enc_op_attention_bidir_ws(qkv, o, S, heads, head_dim, workspace, cu_seqlens=None, stream=None):
+    cu = _host_i32(cu_seqlens)
+    n_seqs = len(cu) - 1 if cu is not None else 0
+    wbytes = workspace.numel() * workspace.element_size()
+    return _check(lib.h3enc_op_attention_bidir_ws(_ptr(qkv), _ptr(o), S, heads, head_dim, cu, n_seqs,
+                                                  _ptr(workspace), wbytes, _stream(stream)))
 
 
 def h3vis_create(cfg: VisionConfig):

@@ -33,6 +33,7 @@
 // previous P V product is awaited only before a rescale.  Every wait is bounded.
 #include <atomic>
 #include <cmath>
+#include <utility>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -45,6 +46,7 @@ constexpr int TQ = 128;
 constexpr int TK = 128;
 constexpr int kThreads = 64 + 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kMaxKeyRanges = 8;           // key ranges a split pair-item is cut into, at most
 
 struct AttnTcArgs {
     bf16 *o;
@@ -54,7 +56,11 @@ struct AttnTcArgs {
     float scale_log2;
     int n_seqs, total_pairs, n_items;   // "pairs": units of two query tiles (see head_pairs)
     int n_whole;   // items [0, n_whole) are pairs of query tiles; each later pair-item is run as
-                   // two single-tile items (bidirectional mode, to fill a thin last round)
+                   // two single-tile items, or (ks > 0) as ks items over consecutive key ranges
+                   // (bidirectional mode, to fill a thin last round)
+    int ks;                         // key ranges per split pair-item (0: split into single tiles)
+    float *split_ws;                // ks > 0: [unit][tile][D + 2][128] fp32: O, m, l of each range
+    int *split_cnt;                 // ks > 0: [split pair-item][tile][quarter] arrivals, 0 between launches
     int32_t *status;
     int cu[kMaxSeqs + 1];
     int pair_start[kMaxSeqs + 1];   // first unit of each sequence (a 128-row tile when head_pairs)
@@ -127,6 +133,8 @@ __device__ __forceinline__ float ex2(float x) {
 // `head`, rows q0..; tile B is head `head_b`, rows q0_b.. (nkt_b = 0: no tile B).
 struct AttnItem {
     int head, head_b, seg0, L, q0, q0_b, nkt_a, nkt_b;
+    int kt0;    // first key tile
+    int unit;   // >= 0: key-range unit (k - n_whole) of a split pair-item; -1: whole item
 };
 __device__ __forceinline__ int seq_of_unit(const AttnTcArgs &a, int u) {
     int lo = 0, hi = a.n_seqs - 1;
@@ -136,8 +144,11 @@ __device__ __forceinline__ int seq_of_unit(const AttnTcArgs &a, int u) {
     }
     return lo;
 }
+template <bool CAUSAL>
 __device__ __forceinline__ AttnItem attn_item(const AttnTcArgs &a, int k_in) {
     AttnItem it;
+    it.kt0 = 0;
+    it.unit = -1;
     if (a.head_pairs) {   // causal: heads (2i, 2i+1) share kv head and every key tile
         const int hp = a.nq >> 1;
         it.head = 2 * (k_in % hp);
@@ -150,9 +161,11 @@ __device__ __forceinline__ AttnItem attn_item(const AttnTcArgs &a, int k_in) {
         it.nkt_a = it.nkt_b = (min(it.q0 + TQ, it.L) + TK - 1) / TK;
         return it;
     }
-    // past n_whole: item n_whole + 2j + h is tile h of pair-item n_whole + j on its own
-    const int split = k_in >= a.n_whole ? ((k_in - a.n_whole) & 1) + 1 : 0;   // 0 whole, 1 tile A, 2 tile B
-    const int k = split ? a.n_whole + ((k_in - a.n_whole) >> 1) : k_in;
+    // past n_whole: item n_whole + 2j + h is tile h of pair-item n_whole + j on its own, or with
+    // key ranges (ks > 0) item n_whole + ks j + r is key range r of pair-item n_whole + j
+    const int past = CAUSAL ? -1 : k_in - a.n_whole;   // the host splits bidirectional items only
+    const int split = past >= 0 && a.ks == 0 ? (past & 1) + 1 : 0;   // 0 whole, 1 tile A, 2 tile B
+    const int k = past < 0 ? k_in : a.ks ? a.n_whole + past / a.ks : a.n_whole + (past >> 1);
     it.head = it.head_b = k % a.nq;                       // heads fastest: one kv group's heads adjacent
     const int pair_lin = a.total_pairs - 1 - k / a.nq;    // heavy tile pairs first
     const int lo = seq_of_unit(a, pair_lin);
@@ -161,7 +174,7 @@ __device__ __forceinline__ AttnItem attn_item(const AttnTcArgs &a, int k_in) {
     it.q0 = (pair_lin - a.pair_start[lo]) * (2 * TQ);
     // key tiles of each query tile (tile B is empty when the sequence ends inside tile A): up to
     // the query's own position when causal, the whole segment otherwise
-    if (a.causal) {
+    if (CAUSAL) {
         it.nkt_a = (min(it.q0 + TQ, it.L) + TK - 1) / TK;
         it.nkt_b = it.q0 + TQ < it.L ? (min(it.q0 + 2 * TQ, it.L) + TK - 1) / TK : 0;
     } else {
@@ -172,6 +185,14 @@ __device__ __forceinline__ AttnItem attn_item(const AttnTcArgs &a, int k_in) {
     if (split) {   // the host splits only pairs whose tile B exists
         if (split == 2) it.q0 += TQ;
         it.nkt_b = 0;
+    }
+    if (past >= 0 && a.ks) {   // key tiles [kt0, kt1) of the whole segment (bidirectional only)
+        const int r = past % a.ks, all = it.nkt_a;
+        it.kt0 = r * all / a.ks;
+        const int n = (r + 1) * all / a.ks - it.kt0;
+        it.nkt_a = n;
+        it.nkt_b = it.nkt_b ? n : 0;
+        it.unit = past;
     }
     it.q0_b = it.q0 + TQ;
     return it;
@@ -242,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int r = 0, it = 0; ok; ++r, ++it) {
                 const int k = attn_item_index(r, b, G);
                 if (k >= a.n_items) break;
-                const AttnItem w = attn_item(a, k);
+                const AttnItem w = attn_item<CAUSAL>(a, k);
                 const int kvh = w.head / a.group;
                 const int n_kt = w.nkt_b > w.nkt_a ? w.nkt_b : w.nkt_a;
                 steps += n_kt;
@@ -256,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < n_kt; ++j, ++g) {
                     const int s = g & 1;
                     if (g >= 2 && !mbar_wait(&kv_empty[s], ((g >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
-                    const int y = w.seg0 + j * TK;
+                    const int y = w.seg0 + ((CAUSAL ? 0 : w.kt0) + j) * TK;   // key ranges: bidirectional only
                     mbar_arrive_expect_tx(&k_full[s], Lay::KV_BYTES);
                     for (int c = 0; c < D / 64; ++c)
                         tma_load_2d(sK + s * Lay::KV_BYTES + c * Lay::ATOM, &tm, &k_full[s],
@@ -322,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int r = 0, it = 0; ok; ++r, ++it) {
                 const int k = attn_item_index(r, b, G);
                 if (k >= a.n_items) break;
-                const AttnItem w = attn_item(a, k);
+                const AttnItem w = attn_item<CAUSAL>(a, k);
                 const int n_kt = w.nkt_b > w.nkt_a ? w.nkt_b : w.nkt_a;
                 if (!mbar_wait(q_full, it & 1, abort_flag)) { ok = false; break; }
                 if (it == 0) astamp_clk(a, ATR_Q);
@@ -363,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; good; ++r) {
             const int k = attn_item_index(r, b, G);
             if (k >= a.n_items) break;
-            const AttnItem w = attn_item(a, k);
+            const AttnItem w = attn_item<CAUSAL>(a, k);
             const int nkt = t == 0 ? w.nkt_a : w.nkt_b;
             if (nkt == 0) continue;
             const int qtile0 = t ? w.q0_b : w.q0;
@@ -389,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // keys after the query masked (causal: the diagonal tile only), else the keys past
                 // the segment's end (its last tile only); row max of the raw scores (the scale is
                 // positive) as 8 independent chains
-                const int key0 = j * TK;
+                const int key0 = ((CAUSAL ? 0 : w.kt0) + j) * TK;
                 if constexpr (CAUSAL) {
                     if (key0 + TK - 1 > qtile0) {
                         #pragma unroll
@@ -479,9 +500,88 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!good) break;
             if (threadIdx.x == 64) astamp_clk(a, ATR_O);
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
             const bool live = qpos < w.L;
             bf16 *dst = a.o + (size_t)(w.seg0 + qpos) * a.ld_o + (size_t)(t ? w.head_b : w.head) * D;
+            if constexpr (!CAUSAL) {
+                if (w.unit >= 0) {
+                    // one key range of a split pair-item: its unnormalised O, running max and sum go
+                    // to the workspace (consecutive lanes on consecutive floats); the warp whose range
+                    // is the last to arrive for these 32 rows merges the ranges in range order
+                    const size_t stride = (size_t)(D + 2) * 128;
+                    float *mine = a.split_ws + (size_t)(w.unit * 2 + t) * stride;
+                    #pragma unroll 1
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t v[32];
+                        tmem_ld32(tO + cc * 32, v);
+                        tmem_ld_wait();
+                        #pragma unroll
+                        for (int i = 0; i < 32; ++i) mine[(size_t)(cc * 32 + i) * 128 + r_row] = __uint_as_float(v[i]);
+                    }
+                    mine[(size_t)D * 128 + r_row] = m_use;
+                    mine[(size_t)(D + 1) * 128 + r_row] = l;
+                    __threadfence();
+                    __syncwarp();
+                    const int r_unit = w.unit % a.ks;
+                    int *cnt = a.split_cnt + ((w.unit / a.ks) * 2 + t) * 4 + quarter;
+                    int prior = 0;
+                    if (lane == 0) prior = atomicAdd(cnt, 1);
+                    prior = __shfl_sync(0xffffffffu, prior, 0);
+                    if (prior == a.ks - 1) {
+                        __threadfence();
+                        if (lane == 0) *cnt = 0;   // zero again for the next launch
+                        const float *first = a.split_ws + (size_t)((w.unit - r_unit) * 2 + t) * stride;
+                        float mx = -INFINITY;
+                        for (int i = 0; i < a.ks; ++i)
+                            mx = fmaxf(mx, __ldcg(first + (size_t)i * 2 * stride + (size_t)D * 128 + r_row));
+                        float f[kMaxKeyRanges], lsum = 0.f;
+                        #pragma unroll
+                        for (int i = 0; i < kMaxKeyRanges; ++i) {
+                            f[i] = 0.f;
+                            if (i < a.ks) {
+                                const float *u = first + (size_t)i * 2 * stride;
+                                f[i] = ex2(__ldcg(u + (size_t)D * 128 + r_row) - mx);
+                                lsum += __ldcg(u + (size_t)(D + 1) * 128 + r_row) * f[i];
+                            }
+                        }
+                        const float inv_s = lsum > 0.f ? 1.f / lsum : 0.f;
+                        float rmax_s = 0.f;
+                        #pragma unroll 1
+                        for (int cc = 0; cc < D / 32; ++cc) {
+                            float o[32];
+                            #pragma unroll
+                            for (int k = 0; k < 32; ++k) o[k] = 0.f;
+                            #pragma unroll
+                            for (int i = 0; i < kMaxKeyRanges; ++i) {
+                                if (i < a.ks) {
+                                    const float *u = first + (size_t)i * 2 * stride + (size_t)(cc * 32) * 128 + r_row;
+                                    #pragma unroll
+                                    for (int k = 0; k < 32; ++k) o[k] += __ldcg(u + (size_t)k * 128) * f[i];
+                                }
+                            }
+                            if (live) {
+                                uint4 *d4 = reinterpret_cast<uint4 *>(dst + cc * 32);
+                                #pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    uint4 uu;
+                                    uu.x = pack_bf16x2(o[8 * q + 0] * inv_s, o[8 * q + 1] * inv_s);
+                                    uu.y = pack_bf16x2(o[8 * q + 2] * inv_s, o[8 * q + 3] * inv_s);
+                                    uu.z = pack_bf16x2(o[8 * q + 4] * inv_s, o[8 * q + 5] * inv_s);
+                                    uu.w = pack_bf16x2(o[8 * q + 6] * inv_s, o[8 * q + 7] * inv_s);
+                                    d4[q] = uu;
+                                    const uint32_t uw[4] = {uu.x, uu.y, uu.z, uu.w};
+                                    #pragma unroll
+                                    for (int k = 0; k < 4; ++k)
+                                        rmax_s = fmaxf(rmax_s, fmaxf(fabsf(bf16_lo(uw[k])), fabsf(bf16_hi(uw[k]))));
+                                }
+                            }
+                        }
+                        if (live && a.row_amax)
+                            atomicMax(reinterpret_cast<int *>(a.row_amax + w.seg0 + qpos), __float_as_int(rmax_s));
+                    }
+                    continue;
+                }
+            }
+            const float inv = l > 0.f ? 1.f / l : 0.f;
             float rmax = 0.f;   // largest |bf16 output| of this row's head
             #pragma unroll 1
             for (int cc = 0; cc < D / 32; ++cc) {
@@ -547,8 +647,13 @@ thread_local unsigned long long *t_attn_trace = nullptr;
 
 void attention_trace_next(unsigned long long *trace) { t_attn_trace = trace; }
 int attention_trace_fields() { return ATR_COUNT; }
+size_t attention_workspace_bytes(int num_sms, int d) {
+    return (size_t)num_sms * 2 * (d + 2) * 128 * sizeof(float) + (size_t)num_sms * 8 * sizeof(int);
+}
+
 cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, int d, const int32_t *cu_host,
-                             int n_seqs, int32_t *status, cudaStream_t st, float *row_amax, bool causal) {
+                             int n_seqs, int32_t *status, cudaStream_t st, float *row_amax, bool causal,
+                             void *workspace, size_t workspace_bytes) {
     if (S <= 0) return cudaSuccess;
     if (d != 64 && d != 128) return cudaErrorInvalidValue;
     AttnTcArgs args;   // per call: launches from several host threads do not share it
@@ -566,6 +671,9 @@ cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, i
     args.trace = t_attn_trace;
     args.row_amax = row_amax;
     args.causal = causal ? 1 : 0;
+    args.ks = 0;
+    args.split_ws = nullptr;
+    args.split_cnt = nullptr;
     // causal with an even number of q heads per kv head: items are one tile of two heads
     args.head_pairs = causal && args.group % 2 == 0 ? 1 : 0;
     const int unit = args.head_pairs ? TQ : 2 * TQ;   // query rows per unit
@@ -598,18 +706,43 @@ cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, i
     if (sms <= 0) sms = 1;
     if (!causal && args.n_items > sms) {
         // bidirectional items all cost the same: when the last round would hold few pair-items,
-        // run them as single query tiles, twice as many and half as long (pairs with a tile B only)
+        // cut each into ks ranges of its keys (a workspace holds the ranges' partial results, merged
+        // by whichever range finishes last), or without a workspace run them as single query tiles,
+        // twice as many and half as long (pairs with a tile B only)
         const int I = args.n_items, rounds = (I + sms - 1) / sms, r = I - (rounds - 1) * sms;
-        bool ok = 2 * r <= sms;
-        for (int k = I - r; ok && k < I; ++k) {
+        auto seg_of = [&](int k) {
             const int pair_lin = pairs - 1 - k / nq;
             int seg = 0;
             while (seg + 1 < n && args.pair_start[seg + 1] <= pair_lin) ++seg;
-            ok = (pair_lin - args.pair_start[seg]) * 2 * TQ + TQ < args.cu[seg + 1] - args.cu[seg];
+            return std::make_pair(seg, pair_lin);
+        };
+        if (workspace && workspace_bytes >= attention_workspace_bytes(sms, d) &&
+            !(reinterpret_cast<uintptr_t>(workspace) & 15) && r < sms) {
+            int ks = sms / r < kMaxKeyRanges ? sms / r : kMaxKeyRanges;
+            for (int k = I - r; ks >= 2 && k < I; ++k) {
+                const int seg = seg_of(k).first;
+                const int all = (args.cu[seg + 1] - args.cu[seg] + TK - 1) / TK;
+                if (all < ks) ks = all;
+            }
+            if (ks >= 2) {
+                args.ks = ks;
+                args.n_whole = I - r;
+                args.n_items = I - r + r * ks;
+                args.split_ws = static_cast<float *>(workspace);
+                args.split_cnt = reinterpret_cast<int *>(static_cast<char *>(workspace) +
+                                                         (size_t)sms * 2 * (d + 2) * 128 * sizeof(float));
+            }
         }
-        if (ok) {
-            args.n_whole = I - r;
-            args.n_items = I + r;
+        if (!args.ks) {
+            bool ok = 2 * r <= sms;
+            for (int k = I - r; ok && k < I; ++k) {
+                const auto sp = seg_of(k);
+                ok = (sp.second - args.pair_start[sp.first]) * 2 * TQ + TQ < args.cu[sp.first + 1] - args.cu[sp.first];
+            }
+            if (ok) {
+                args.n_whole = I - r;
+                args.n_items = I + r;
+            }
         }
     }
     const int grid = args.n_items < sms ? args.n_items : sms;   // persistent: one CTA per SM

@@ -118,9 +118,13 @@ cudaError_t launch_rope_table(const int32_t *positions, int S, const RopeParams 
 // ---- attention on tcgen05 (attention_tc.cu)
 // row_amax (optional, [S] floats): each row's largest |bf16 output| is merged in with an
 // integer atomic max (the buffer must hold zeros or smaller values beforehand).
+// workspace (optional, bidirectional only; attention_workspace_bytes, zero-filled once before
+// first use, calls sharing it must not overlap on the GPU): lets a thin last round of items be
+// cut along the keys instead of into single query tiles.
 cudaError_t launch_attention(const bf16 *qkv, bf16 *o, int S, int nq, int nkv, int d, const int32_t *cu_host,
                              int n_seqs, int32_t *status, cudaStream_t st, float *row_amax = nullptr,
-                             bool causal = true);
+                             bool causal = true, void *workspace = nullptr, size_t workspace_bytes = 0);
+size_t attention_workspace_bytes(int num_sms, int d);
 
 // ---- vision tower (vision.cu)
 constexpr int kMaxVisionGrids = 64;

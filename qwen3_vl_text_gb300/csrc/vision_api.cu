@@ -59,6 +59,7 @@ struct h3vis {
     bf16 *x = nullptr, *y = nullptr, *qkv = nullptr, *attn = nullptr, *act = nullptr;
     float *cos_t = nullptr, *sin_t = nullptr, *part = nullptr;
     uint32_t *flags = nullptr;
+    void *attn_ws = nullptr;   // attention's key-range partials (a thin last round of items)
     int32_t *status = nullptr;
     CUtensorMap tm_y, tm_attn, tm_act, tm_y4, tm_act4;
     h3::VisionRope rope;
@@ -222,8 +223,9 @@ h3enc_status h3vis_create(const h3vis_config *cfg, h3vis **out) {
     const size_t P = c.max_patches, d = H / c.num_heads;
     const size_t b_x = align256(P * H * 2), b_qkv = align256(P * 3 * H * 2),
                  b_act = align256(P * (size_t)(I > H ? I : H) * 2), b_cs = align256((size_t)h3::cs_stride((int)P) * (d / 2) * 4),
-                 b_gemm = align256(h3::gemm_workspace_bytes(h->num_sms)), b_st = 256;
-    const size_t wsz = 3 * b_x + b_qkv + b_act + 2 * b_cs + b_gemm + b_st;
+                 b_gemm = align256(h3::gemm_workspace_bytes(h->num_sms)), b_st = 256,
+                 b_aw = align256(h3::attention_workspace_bytes(h->num_sms, (int)d));
+    const size_t wsz = 3 * b_x + b_qkv + b_act + 2 * b_cs + b_gemm + b_st + b_aw;
     e = cudaMalloc(&h->ws, wsz);
     if (e == cudaSuccess) e = cudaMemset(h->ws, 0, wsz);
     if (e != cudaSuccess) {
@@ -241,6 +243,8 @@ h3enc_status h3vis_create(const h3vis_config *cfg, h3vis **out) {
     h->part = reinterpret_cast<float *>(w);
     h->flags = reinterpret_cast<uint32_t *>(w + h3::gemm_flags_offset(h->num_sms));
     w += b_gemm;
+    h->attn_ws = w;
+    w += b_aw;
     h->status = reinterpret_cast<int32_t *>(w);
     const uint32_t ba = (uint32_t)h3::gemm_box_rows_a();
     if (!h3::make_tmap_rows(&h->tm_y, h->y, P, H, ba) || !h3::make_tmap_rows(&h->tm_attn, h->attn, P, H, ba) ||
@@ -355,7 +359,8 @@ h3enc_status h3vis_encode(h3vis *h, const void *pixel_values, int32_t n_patches,
         e = gemm(h, &h->tm_y, &k.tm_qkv, n, 3 * H, H, h3::EPI_QKROPE, h->qkv, 3 * H, nullptr, k.qkv_b, st, true);
         if (e != cudaSuccess) return vcuda(h, e, "qkv");
         VCHECK(h3::launch_attention(h->qkv, h->attn, n, heads, heads, d, cu.data(), (int)cu.size() - 1, h->status,
-                                    st, nullptr, false), "attention");
+                                    st, nullptr, false, h->attn_ws, h3::attention_workspace_bytes(h->num_sms, d)),
+               "attention");
         e = gemm(h, &h->tm_attn, &k.tm_proj, n, H, H, h3::EPI_RESIDUAL, h->x, H, h->x, k.proj_b, st);
         if (e != cudaSuccess) return vcuda(h, e, "proj");
         VCHECK(h3::launch_layernorm(h->x, k.n2w, k.n2b, h->y, n, H, c.ln_eps, st), "norm2");
@@ -517,6 +522,30 @@ h3enc_status h3enc_op_attention_bidir(const void *qkv, void *o, int32_t S, int32
     cudaError_t e = h3::launch_attention(static_cast<const bf16 *>(qkv), static_cast<bf16 *>(o), S, heads, heads,
                                          head_dim, cu_seqlens, cu_seqlens ? n_seqs : 0, nullptr,
                                          static_cast<cudaStream_t>(stream), nullptr, false);
+    return e == cudaSuccess ? H3ENC_OK : H3ENC_ERR_CUDA;
+}
+
+int64_t h3enc_op_attention_workspace_bytes(int32_t head_dim) {
+    if (head_dim != 64 && head_dim != 128) return 0;
+    return (int64_t)h3::attention_workspace_bytes(h3::device_num_sms(), head_dim);
+}
+
+h3enc_status h3enc_op_attention_bidir_ws(const void *qkv, void *o, int32_t S, int32_t heads, int32_t head_dim,
+                                         const int32_t *cu_seqlens, int32_t n_seqs, void *workspace,
+                                         int64_t workspace_bytes, void *stream) {
+    if (!qkv || !o || S < 0 || heads < 1 || (head_dim != 64 && head_dim != 128) || !workspace ||
+        workspace_bytes < h3enc_op_attention_workspace_bytes(head_dim) || (reinterpret_cast<uintptr_t>(workspace) & 15))
+        return H3ENC_ERR_INVALID_ARG;
+    if (cu_seqlens) {
+        if (n_seqs < 1 || n_seqs > h3::kMaxSeqs || cu_seqlens[0] != 0 || cu_seqlens[n_seqs] != S)
+            return H3ENC_ERR_INVALID_ARG;
+        for (int i = 0; i < n_seqs; ++i)
+            if (cu_seqlens[i + 1] < cu_seqlens[i]) return H3ENC_ERR_INVALID_ARG;
+    }
+    cudaError_t e = h3::launch_attention(static_cast<const bf16 *>(qkv), static_cast<bf16 *>(o), S, heads, heads,
+                                         head_dim, cu_seqlens, cu_seqlens ? n_seqs : 0, nullptr,
+                                         static_cast<cudaStream_t>(stream), nullptr, false, workspace,
+                                         (size_t)workspace_bytes);
     return e == cudaSuccess ? H3ENC_OK : H3ENC_ERR_CUDA;
 }
 

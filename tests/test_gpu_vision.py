@@ -138,18 +138,41 @@ def test_qkv_with_bias_and_2d_rotary(grid, split):
     assert bad == 0, f"{bad} off, worst {worst}"
 
 
-@pytest.mark.parametrize("cu,heads", [([0, 96, 160, 224], 4), ([0, 1024, 2048], 4), ([0, 200], 4),
-                                      # more work items than SMs: the last round's pairs run as single
-                                      # query tiles; and the same with a pair that has no second tile
-                                      # in that range (the split is then refused)
-                                      ([0, 3072], 16), ([0, 100, 3172], 16)])
-def test_bidirectional_attention(cu, heads):
-    d = 64
+def _bidir_case(cu, heads, d, workspace=None):
     S = cu[-1]
     X, x = _bf16(81, "qkv", (S, 3 * heads * d), 0.0, 1.0)
     o = torch.empty(S, heads * d, dtype=torch.bfloat16, device="cuda")
-    Q.h3enc_op_attention_bidir(X, o, S, heads, d, cu)
+    if workspace is None:
+        Q.h3enc_op_attention_bidir(X, o, S, heads, d, cu)
+    else:
+        Q.h3enc_op_attention_bidir_ws(X, o, S, heads, d, workspace, cu)
     torch.cuda.synchronize()
+    return X, x, o
+
+
+@pytest.mark.parametrize("cu,heads,d,ws", [([0, 96, 160, 224], 4, 64, False), ([0, 1024, 2048], 4, 64, False),
+                                           ([0, 200], 4, 64, False),
+                                           # more work items than SMs: the last round's pairs run as single
+                                           # query tiles; and the same with a pair that has no second tile
+                                           # in that range (the split is then refused)
+                                           ([0, 3072], 16, 64, False), ([0, 100, 3172], 16, 64, False),
+                                           # with a workspace the last round's pairs are cut along the keys
+                                           # instead: one segment, two frames, a short segment that limits
+                                           # the number of ranges, head_dim 128
+                                           ([0, 3072], 16, 64, True), ([0, 1536, 3072], 16, 64, True),
+                                           ([0, 384, 4736], 9, 64, True), ([0, 3072], 16, 128, True)])
+def test_bidirectional_attention(cu, heads, d, ws):
+    S = cu[-1]
+    workspace = None
+    if ws:
+        workspace = torch.zeros(Q.h3enc_op_attention_workspace_bytes(d), dtype=torch.uint8, device="cuda")
+    X, x, o = _bidir_case(cu, heads, d, workspace)
+    if ws:   # the merge is in range order: the same bits on a second call (counters back at zero)
+        o2 = torch.empty_like(o)
+        Q.h3enc_op_attention_bidir_ws(X, o2, S, heads, d, workspace, cu)
+        torch.cuda.synchronize()
+        assert torch.equal(o, o2)
+        assert not workspace[-(torch.cuda.get_device_properties(0).multi_processor_count * 32):].any()
     q = x[:, :heads * d].reshape(S, heads, d).astype(np.float64)
     k = x[:, heads * d:2 * heads * d].reshape(S, heads, d).astype(np.float64)
     v = x[:, 2 * heads * d:].reshape(S, heads, d).astype(np.float64)
