@@ -86,6 +86,10 @@ def test_op_entries_validate_arguments(Q):
     with pytest.raises(Q.H3encError) as e:                                              # table stride < M
         Q.h3enc_op_gemm_qkv_rope_ex(16, 16, 16, 100, 512, 4, 2, 64, 16, 16, 1e-6, 16, 16, 64, stream=0)
     assert e.value.code == 2
+    assert Q.h3enc_op_attention_workspace_bytes(96) == 0                                # head_dim not 64/128
+    with pytest.raises(Q.H3encError) as e:                                              # no workspace
+        Q._check(Q.lib.h3enc_op_attention_bidir_ws(16, 16, 256, 4, 64, None, 0, None, 1 << 30, None))
+    assert e.value.code == 2
 
 
 def test_handle_calls_reject_a_null_handle(Q):
