@@ -290,8 +290,8 @@ H3ENC_API h3enc_status h3enc_op_attention_bidir(const void *qkv, void *o, int32_
                                                 void *stream);
 
 /* h3enc_op_attention_bidir with a workspace (h3enc_op_attention_workspace_bytes(head_dim)
- * bytes, 16-byte aligned, zero-filled once before its first use; calls sharing it must not
- * overlap on the GPU).  When the persistent kernel's last round of work items would leave
+ * bytes, 16-byte aligned, zero-filled once before its first use and again after a call whose
+ * device status reported a timeout; calls sharing it must not overlap on the GPU).  When the persistent kernel's last round of work items would leave
  * most SMs idle, those items are cut into up to 8 ranges of their keys; each range writes
  * its unnormalised output, running maximum and sum to the workspace and the range that
  * finishes last merges them in range order (the same result on every run).  The output

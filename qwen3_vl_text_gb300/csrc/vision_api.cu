@@ -399,7 +399,11 @@ h3enc_status h3vis_get_status(h3vis *h) {
     e = cudaMemcpy(&st, h->status, 4, cudaMemcpyDeviceToHost);
     if (e == cudaSuccess) e = cudaMemset(h->status, 0, 4);
     if (e != cudaSuccess) return vcuda(h, e, "status read");
-    if (st & 1) return vfail(h, H3ENC_ERR_DEVICE_TIMEOUT, "a bounded device wait ran out");
+    if (st & 1) {
+        // an aborted attention launch may leave key-range arrival counts behind: start them again
+        if (h->attn_ws) cudaMemset(h->attn_ws, 0, h3::attention_workspace_bytes(h->num_sms, h->cfg.hidden / h->cfg.num_heads));
+        return vfail(h, H3ENC_ERR_DEVICE_TIMEOUT, "a bounded device wait ran out");
+    }
     return st ? vfail(h, H3ENC_ERR_CUDA, "device status 0x%x", st) : H3ENC_OK;
 }
 
