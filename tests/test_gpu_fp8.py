@@ -56,8 +56,10 @@ def test_quant_rows_bit_exact(rows, cols):
     assert np.array_equal(q.cpu().numpy(), _e4m3_bytes(qr))
 
 
-def test_rmsnorm_q8_matches_norm_then_quantise():
-    rows, cols = 129, 5120
+@pytest.mark.parametrize("rows,cols", [(129, 5120), (7, 256), (3, 1000), (33, 2048), (2, 3072), (2, 4096),
+                                       (2, 6144), (2, 7168), (5, 8192)])
+def test_rmsnorm_q8_matches_norm_then_quantise(rows, cols):
+    """Every register-tile width of the norm pass (8 to 64 values per thread), ragged too."""
     X, x = _bf16(71, "x", (rows, cols), sigma=2.0)
     G, g = _bf16(72, "g", (cols,), 1.0, 0.1)
     q = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
